@@ -1,0 +1,378 @@
+"""Pins of the CPU oracle against things other than itself: worked examples,
+closed forms, invariants, brute force on tiny inputs, special cases that
+reduce to plain dense computations, fp64 finite differences and an
+independent autograd derivation.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16(a):
+    """Round an fp32 array to bf16 values (kept as fp32), round to nearest even."""
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _layer(n, d, f, e, k, gate="softmax", bias=False, shared=0, seed=0, wscale=0.3):
+    r = _rng(seed)
+    p = {
+        "x": _bf16(r.standard_normal((n, d))),
+        "w_gate": _bf16(r.standard_normal((e, d)) * wscale),
+        "w1": _bf16(r.standard_normal((e, f, d)) * wscale),
+        "w3": _bf16(r.standard_normal((e, f, d)) * wscale),
+        "w2": _bf16(r.standard_normal((e, d, f)) * wscale),
+        "bias": (r.standard_normal(e).astype(np.float32) * 0.5) if bias else None,
+        "shared": None,
+    }
+    if shared:
+        p["shared"] = (_bf16(r.standard_normal((shared, d)) * wscale),
+                       _bf16(r.standard_normal((shared, d)) * wscale),
+                       _bf16(r.standard_normal((d, shared)) * wscale))
+    return p
+
+
+# ---------------------------------------------------------------- router ---
+def test_router_worked_examples():
+    ex = json.load(open(os.path.join(GOLD, "router_worked_examples.json")))
+    for c in ex["cases"]:
+        lg = np.array(c["logits"], dtype=np.float32)
+        bias = None if c["bias"] is None else np.array(c["bias"], dtype=np.float32)
+        idx, g = O.route(lg, bias, c["k"], c["gate"])
+        assert idx.tolist() == c["idx"], c["name"]
+        np.testing.assert_allclose(g, np.array(c["g"]), rtol=2e-7, atol=0, err_msg=c["name"])
+
+
+@pytest.mark.parametrize("e,k", [(8, 2), (16, 4), (64, 8), (5, 5)])
+def test_topk_matches_bruteforce(e, k):
+    r = _rng(e * 10 + k)
+    keys = r.standard_normal((200, e)).astype(np.float32)
+    keys[:50] = np.round(keys[:50])                     # many exact ties
+    keys[50:60, 0] = -0.0
+    keys[50:60, 1] = 0.0
+    keys[60:65, 2] = np.nan
+    keys[65:70] = np.nan                                  # a whole row of NaN
+    np.testing.assert_array_equal(O.topk_select(keys, k), O.topk_select_bruteforce(keys, k))
+
+
+def test_topk_zero_gate_picks_first_k_with_equal_weights():
+    # W_g = 0 -> every logit is 0 -> experts 0..K-1, each weight exactly 1/K
+    x = np.ones((7, 16), dtype=np.float32)
+    lg = O.gate_logits(x, np.zeros((8, 16), dtype=np.float32))
+    for gate in ("softmax", "sigmoid"):
+        idx, g = O.route(lg, None, 4, gate)
+        assert (idx == np.arange(4)).all()
+        assert (g == np.float32(0.25)).all()
+
+
+def test_gate_weights_sum_to_one():
+    r = _rng(3)
+    lg = (r.standard_normal((500, 32)) * 3).astype(np.float32)
+    for gate in ("softmax", "sigmoid"):
+        idx, g = O.route(lg, None, 6, gate)
+        s = g.astype(np.float64).sum(axis=1)
+        assert np.abs(s - 1.0).max() <= 4 * np.finfo(np.float32).eps
+
+
+def test_softmax_renorm_equals_softmax_over_selected():
+    # full-softmax then renorm == softmax restricted to the selected logits
+    r = _rng(4)
+    lg = (r.standard_normal((300, 16)) * 2).astype(np.float32)
+    idx, g = O.route(lg, None, 3, "softmax")
+    sel = np.take_along_axis(lg.astype(np.float64), idx.astype(np.int64), axis=1)
+    ref = np.exp(sel - sel.max(axis=1, keepdims=True))
+    ref /= ref.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(g, ref, rtol=1e-6, atol=1e-7)
+
+
+def test_bias_changes_selection_not_weights():
+    r = _rng(5)
+    lg = r.standard_normal((100, 8)).astype(np.float32)
+    bias = np.array([5, 0, 0, 0, 0, 0, 0, -5], dtype=np.float32)
+    idx, g = O.route(lg, bias, 2, "sigmoid")
+    assert (idx[:, 0] == 0).all() and not (idx == 7).any()
+    s = 1 / (1 + np.exp(-np.take_along_axis(lg.astype(np.float64), idx.astype(np.int64), axis=1)))
+    np.testing.assert_allclose(g, s / s.sum(axis=1, keepdims=True), rtol=1e-6)
+
+
+# ------------------------------------------------ histogram / permutation ---
+@pytest.mark.parametrize("n,e,k", [(256, 8, 2), (300, 64, 8), (1, 4, 4), (50, 16, 1)])
+def test_histogram_offsets_permutation_invariants(n, e, k):
+    r = _rng(n + e)
+    lg = r.standard_normal((n, e)).astype(np.float32)
+    lg[:, 0] += 1.0                                        # skew
+    idx, _ = O.route(lg, None, k, "softmax")
+    counts = O.histogram(idx, e)
+    off = O.exclusive_offsets(counts)
+    assert counts.sum() == n * k and off[0] == 0 and off[-1] == n * k
+    roc, cor = O.permutation(idx, e)
+    assert sorted(roc.tolist()) == list(range(n * k))      # bijection
+    assert (cor[roc] == np.arange(n * k)).all()            # inverse maps
+    flat = idx.reshape(-1)
+    for ex in range(e):
+        rows = np.arange(off[ex], off[ex + 1])
+        assert (flat[cor[rows]] == ex).all()               # expert-major
+        toks = cor[rows] // k
+        assert (np.diff(toks) > 0).all()                   # ascending token
+    # same order as a library stable sort by expert of the copies
+    assert (cor == np.argsort(flat, kind="stable")).all()
+
+
+# --------------------------------------------------------------- forward ---
+@pytest.mark.parametrize("gate,bias,shared", [("softmax", False, 0), ("sigmoid", True, 24)])
+def test_forward_matches_dense_bruteforce(gate, bias, shared):
+    p = _layer(40, 16, 24, 6, 2, gate, bias, shared, seed=7)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, p["bias"], 2, gate)
+    out, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"], dtype=np.float64)
+    ref = O.moe_forward_dense_bruteforce(p["x"], idx, g, p["w1"], p["w3"], p["w2"], p["shared"])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    out32, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"])
+    assert np.linalg.norm(out32 - ref) / np.linalg.norm(ref) < 1e-5
+
+
+def test_forward_single_expert_is_dense_swiglu():
+    # E = 1, K = 1: the layer is a plain SwiGLU FFN (torch fp64 matmuls)
+    p = _layer(33, 16, 40, 1, 1, seed=8)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, None, 1, "softmax")
+    assert (g == 1).all()
+    out, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], dtype=np.float64)
+    x = torch.from_numpy(p["x"]).double()
+    a1 = x @ torch.from_numpy(p["w1"][0]).double().T
+    a3 = x @ torch.from_numpy(p["w3"][0]).double().T
+    ref = (torch.nn.functional.silu(a1) * a3) @ torch.from_numpy(p["w2"][0]).double().T
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_forward_all_tokens_one_expert():
+    p = _layer(20, 8, 16, 5, 1, gate="sigmoid", seed=9)
+    bias = np.array([0, 0, 0, 1e4, 0], dtype=np.float32)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, bias, 1, "sigmoid")
+    assert (idx == 3).all() and (g == 1).all()
+    counts = O.histogram(idx, 5)
+    assert counts.tolist() == [0, 0, 0, 20, 0]
+    out, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], dtype=np.float64)
+    ref = O.swiglu_expert(p["x"], p["w1"][3], p["w3"][3], p["w2"][3], np.float64)[0]
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_k_equals_e_is_soft_moe():
+    # softmax with K = E: every expert weighted by its full-softmax probability
+    p = _layer(16, 8, 12, 4, 4, seed=10)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, None, 4, "softmax")
+    out, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], dtype=np.float64)
+    probs = torch.softmax(torch.from_numpy(lg).double(), dim=1).numpy()
+    ref = np.zeros_like(out)
+    for e in range(4):
+        ref += probs[:, e:e + 1] * O.swiglu_expert(p["x"], p["w1"][e], p["w3"][e], p["w2"][e], np.float64)[0]
+    np.testing.assert_allclose(out, ref, rtol=1e-6, atol=1e-7)
+
+
+# -------------------------------------------------------------- backward ---
+def _loss_and_grads(p, dy, gate, k, idx_frozen=None, dtype=np.float64):
+    lg = O.gate_logits(p["x"], p["w_gate"], dtype)
+    if idx_frozen is None:
+        idx = O.topk_select(O.selection_keys(lg.astype(np.float32), p["bias"]), k)
+    else:
+        idx = idx_frozen
+    g = O.gate_weights(lg, idx, gate, dtype)
+    out, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"], dtype=dtype)
+    loss = float((out * dy).sum())
+    return loss, idx, lg, g, saved
+
+
+@pytest.mark.parametrize("gate,shared", [("softmax", 0), ("sigmoid", 6)])
+def test_backward_finite_differences(gate, shared):
+    n, d, f, e, k = 16, 8, 16, 4, 2
+    p = _layer(n, d, f, e, k, gate, bias=(gate == "sigmoid"), shared=shared, seed=11, wscale=0.5)
+    for key in ("x", "w_gate", "w1", "w3", "w2"):
+        p[key] = p[key].astype(np.float64)
+    if shared:
+        p["shared"] = tuple(a.astype(np.float64) for a in p["shared"])
+    dy = _rng(12).standard_normal((n, d))
+    loss, idx, lg, g, saved = _loss_and_grads(p, dy, gate, k)
+    keys = np.sort(O.selection_keys(lg.astype(np.float32), p["bias"]), axis=1)
+    assert (keys[:, -k] - keys[:, -k - 1]).min() > 1e-3      # routing margin >> h
+    gr = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved,
+                        gate, p["shared"], dtype=np.float64)
+    h = 1e-6
+    r = _rng(13)
+    targets = [("x", "dx"), ("w_gate", "dw_gate"), ("w1", "dw1"), ("w3", "dw3"), ("w2", "dw2")]
+    if shared:
+        targets += [(("shared", 0), "dws1"), (("shared", 1), "dws3"), (("shared", 2), "dws2")]
+    for src, gname in targets:
+        arr = p[src] if isinstance(src, str) else p["shared"][src[1]]
+        for _ in range(6):
+            pos = tuple(int(r.integers(s)) for s in arr.shape)
+            old = arr[pos]
+            arr[pos] = old + h
+            lp = _loss_and_grads(p, dy, gate, k, idx)[0]
+            arr[pos] = old - h
+            lm = _loss_and_grads(p, dy, gate, k, idx)[0]
+            arr[pos] = old
+            fd = (lp - lm) / (2 * h)
+            an = gr[gname][pos]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (gname, pos, fd, an)
+
+
+def _torch_layer_restatement(x, w_gate, w1, w3, w2, bias, k, gate, shared):
+    """The page's single-GPU MoE layer forward written with torch ops
+    (fp64 CPU), used only to get gradients from autograd."""
+    logits = x @ w_gate.T
+    routing = logits + (bias if bias is not None else 0)
+    _, topk_idx = routing.topk(k, dim=-1)
+    if gate == "sigmoid":
+        gw = torch.sigmoid(logits.gather(-1, topk_idx))
+    else:
+        gw = torch.softmax(logits, dim=-1).gather(-1, topk_idx)
+    gw = gw / gw.sum(-1, keepdim=True)
+    out = torch.zeros_like(x)
+    for e in range(w1.shape[0]):
+        mask = topk_idx == e
+        if not mask.any():
+            continue
+        tok, kk = mask.nonzero(as_tuple=True)
+        xs = x[tok]
+        y = (torch.nn.functional.silu(xs @ w1[e].T) * (xs @ w3[e].T)) @ w2[e].T
+        out = out.index_add(0, tok, y * gw[tok, kk].unsqueeze(-1))
+    if shared is not None:
+        out = out + (torch.nn.functional.silu(x @ shared[0].T) * (x @ shared[1].T)) @ shared[2].T
+    return out, topk_idx
+
+
+@pytest.mark.parametrize("gate,shared", [("softmax", 0), ("sigmoid", 10)])
+def test_backward_matches_autograd(gate, shared):
+    n, d, f, e, k = 24, 12, 20, 6, 3
+    p = _layer(n, d, f, e, k, gate, bias=(gate == "sigmoid"), shared=shared, seed=14, wscale=0.4)
+    dy = _rng(15).standard_normal((n, d))
+    lg = O.gate_logits(p["x"], p["w_gate"], np.float64)
+    idx = O.topk_select(O.selection_keys(lg.astype(np.float32), p["bias"]), k)
+    g = O.gate_weights(lg, idx, gate, np.float64)
+    out, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"], dtype=np.float64)
+    gr = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, gate,
+                        p["shared"], dtype=np.float64)
+    T = {key: torch.tensor(p[key], dtype=torch.float64, requires_grad=True)
+         for key in ("x", "w_gate", "w1", "w3", "w2")}
+    sh = None
+    if shared:
+        sh = tuple(torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in p["shared"])
+    b = None if p["bias"] is None else torch.tensor(p["bias"], dtype=torch.float64)
+    tout, tidx = _torch_layer_restatement(T["x"], T["w_gate"], T["w1"], T["w3"], T["w2"], b, k, gate, sh)
+    assert np.array_equal(np.sort(tidx.numpy(), 1), np.sort(idx, 1))
+    np.testing.assert_allclose(tout.detach().numpy(), out, rtol=1e-10, atol=1e-12)
+    (tout * torch.from_numpy(dy)).sum().backward()
+    for key, gname in [("x", "dx"), ("w_gate", "dw_gate"), ("w1", "dw1"), ("w3", "dw3"), ("w2", "dw2")]:
+        np.testing.assert_allclose(gr[gname], T[key].grad.numpy(), rtol=1e-9, atol=1e-10, err_msg=gname)
+    if shared:
+        for i, gname in enumerate(("dws1", "dws3", "dws2")):
+            np.testing.assert_allclose(gr[gname], sh[i].grad.numpy(), rtol=1e-9, atol=1e-10)
+
+
+def test_backward_unused_expert_has_zero_grad():
+    p = _layer(10, 8, 8, 4, 1, gate="sigmoid", seed=16)
+    bias = np.array([1e4, 0, 0, 0], dtype=np.float32)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, bias, 1, "sigmoid")
+    out, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"])
+    gr = O.moe_backward(np.ones_like(out), p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"],
+                        saved, "sigmoid")
+    for e in (1, 2, 3):
+        assert not gr["dw1"][e].any() and not gr["dw3"][e].any() and not gr["dw2"][e].any()
+    # K = 1 with renorm: g == 1 regardless of the logit, so the router gets no gradient
+    assert not gr["dlogits"].any()
+
+
+# ------------------------------------------------- balancing / monitoring ---
+def test_bias_update_worked_example():
+    ex = json.load(open(os.path.join(GOLD, "bias_update_worked_example.json")))
+    counts = np.array(ex["counts"], dtype=np.int32)
+    b0 = np.array(ex["bias_in"], dtype=np.float32)
+    np.testing.assert_array_equal(O.load_stat(counts), np.array(ex["load_stat"], dtype=np.float32))
+    np.testing.assert_allclose(O.update_bias(counts, b0, ex["gamma"], 0),
+                               np.array(ex["mode0_bias_out"], dtype=np.float32), rtol=3e-7, atol=0)  # fp32 products: a few ulp
+    np.testing.assert_allclose(O.update_bias(counts, b0, ex["gamma"], 1),
+                               np.array(ex["mode1_bias_out"], dtype=np.float32), rtol=1e-7, atol=0)
+
+
+def test_bias_update_balanced_and_empty():
+    b = np.full(4, 0.5, dtype=np.float32)
+    assert (O.update_bias(np.array([2, 2, 2, 2]), b) == b).all()   # exactly balanced: no step
+    assert (O.update_bias(np.zeros(4, dtype=np.int32), b) == b).all()
+
+
+def test_aux_loss_closed_forms():
+    # W_g = 0: P = 1/E everywhere, the top-K mask picks experts 0..K-1: loss = K
+    lg = np.zeros((64, 8), dtype=np.float32)
+    idx = O.topk_select(lg, 2)
+    assert O.aux_loss(lg, idx, 8) == pytest.approx(2.0, abs=1e-12)
+    # K = 1 with perfectly uniform hard routing and uniform probabilities: loss = 1
+    idx1 = (np.arange(64) % 8).reshape(64, 1)
+    assert O.aux_loss(lg, idx1, 8) == pytest.approx(1.0, abs=1e-12)
+
+
+def test_monitor_stats_hand_example():
+    h = [np.array([0.5, 0.3, 0.2, 0.0]), np.array([0.3, 0.3, 0.3, 0.1])]
+    st = O.monitor_stats(h)
+    recent = np.array([0.4, 0.3, 0.25, 0.05])
+    assert st["min_load"] == pytest.approx(0.05)
+    assert st["cold_experts"] == 1                      # 0.05 < 0.3/4
+    assert st["entropy"] == pytest.approx(-sum(r * math.log(r + 1e-9) for r in recent))
+
+
+# ---------------------------------------------------------------- MXFP8 ---
+def test_e4m3_table_and_rounding():
+    t = json.load(open(os.path.join(GOLD, "e4m3_table.json")))
+    for code, val in t["codes"].items():
+        got = O.e4m3_decode(np.array([int(code, 16)]))[0]
+        assert got == val and np.signbit(got) == np.signbit(val), code
+    for code in t["nan_codes"]:
+        assert np.isnan(O.e4m3_decode(np.array([int(code, 16)]))[0])
+    for v, code in t["round_cases"]:
+        assert int(O.e4m3_encode(np.array([v]))[0]) == int(code, 16), v
+
+
+def test_e4m3_roundtrip_all_codes_and_nearest():
+    codes = np.arange(256)
+    vals = O.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    assert (O.e4m3_encode(vals[finite]) == codes[finite]).all()
+    # brute force: every encoded value is a nearest representable value
+    grid = np.unique(vals[finite])
+    r = _rng(17)
+    xs = np.concatenate([r.standard_normal(2000) * 50, r.standard_normal(2000) * 0.01])
+    enc = O.e4m3_decode(O.e4m3_encode(xs))
+    clipped = np.clip(xs, -448, 448)
+    best = np.abs(grid[None, :] - clipped[:, None]).min(axis=1)
+    assert np.allclose(np.abs(enc - clipped), best, rtol=0, atol=0)
+
+
+def test_mx_scale_is_the_unique_power_of_two():
+    r = _rng(18)
+    amax = np.abs(r.standard_normal(500)) * 10.0 ** r.integers(-20, 20, 500)
+    ex = O.e8m0_scale_exponent(amax)
+    for a, e in zip(amax, ex):
+        # brute force over exponents: the one with 2^8 <= amax / 2^e < 2^9
+        cands = [j for j in range(-127, 128) if 256 <= a / 2.0 ** j < 512]
+        assert cands == [e]
+
+
+def test_mx_quantize_group_aware_blocks():
+    r = _rng(19)
+    x = r.standard_normal((70, 3))
+    codes, scales, starts = O.mx_quantize(x, axis=0, group_starts=[0, 40, 45])
+    assert starts == [0, 32, 40, 45]
+    deq = O.mx_dequantize(codes, scales, starts, axis=0)
+    assert np.abs(deq - x).max() <= np.abs(x).max() * 2 ** -3
