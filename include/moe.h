@@ -1,0 +1,248 @@
+/*
+ * moe.h - C ABI of libmoe, a single-GPU dropless Mixture-of-Experts layer
+ * (forward and backward) written as hand-made CUDA kernels for sm_103a.
+ *
+ * What the layer computes is the single-device MoE layer of "LLM
+ * Infrastructure Engineering 08: MoE Training Engineering" (quant67):
+ *   §4.1 / §4.3  router: logits = x W_g^T (fp32, §12.7); top-K selection;
+ *                softmax (then renormalised over the K selected) or sigmoid
+ *                of the selected logits renormalised to sum 1;
+ *   §6.3         DeepSeek-V3 bias-adjusted selection: top-K ranks
+ *                logits + route_bias, weights use the unbiased logits;
+ *   §9           SwiGLU experts y = w2(silu(w1 x) * w3 x) (no bias), every
+ *                token copy computed (dropless: no capacity, no drop, no pad,
+ *                "Accelerating Dropless MoE Training in JAX with NVIDIA
+ *                Transformer Engine" ¶2-¶3), results weighted and summed back
+ *                per token; shared expert added to every token (§5 formula);
+ *                load statistics and update_balance_bias;
+ *   §12.5        dispatch as a sort of token copies by destination, combine
+ *                as unsort + weighted sum over K.
+ * The backward is the exact derivative of that forward (§11.3: experts that
+ * received no token get zero weight gradient; the route bias gets none).
+ *
+ * Conventions (all entry points):
+ *  - Every pointer is device memory owned by the caller unless stated; the
+ *    library allocates nothing and frees nothing.  bf16 buffers are passed as
+ *    void* and hold IEEE bfloat16 values, row-major.
+ *  - Notation: N = n_tok, D = d_model, F = d_ff, E = n_exp, K = top_k,
+ *    R = N*K rows of the permuted (expert-major) buffers, Fs = d_ff_shared.
+ *  - Weights use the nn.Linear layout: W_g [E,D]; w1, w3 [E,F,D];
+ *    w2 [E,D,F]; shared ws1, ws3 [Fs,D], ws2 [D,Fs].
+ *  - Buffers must be 16-byte aligned; D, F and Fs must be multiples of 64;
+ *    1 <= K <= min(E, 32); E <= 1024; R < 2^31.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work: no host synchronisation and no host read of device data,
+ *    so a sequence of calls can be captured in a CUDA graph.
+ *  - Errors the host can detect (bad sizes, null or misaligned pointers,
+ *    workspace too small) return a status before anything is enqueued.
+ *    Errors found on the device (an expert index out of range, a bounded
+ *    wait that timed out) set bits in the status word at the start of the
+ *    workspace; read it with moe_get_device_status.
+ *  - Workspace: `ws` must hold moe_workspace_size() bytes and be cleared once
+ *    with moe_workspace_init.  One workspace must not be used by two calls
+ *    that may run concurrently.
+ */
+#ifndef RAGGED_GROUPED_GEMM_GB300_MOE_H
+#define RAGGED_GROUPED_GEMM_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, size out of range */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE = 5        /* device status word reports an error */
+} moe_status_t;
+
+/* Device status bits (moe_get_device_status). */
+#define MOE_DEV_TIMEOUT 1      /* a bounded wait inside a kernel ran out */
+#define MOE_DEV_BAD_INDEX 2    /* an expert index outside [0, E) */
+#define MOE_DEV_BAD_OFFSETS 4  /* the histogram did not sum to N*K */
+
+/* Layer description; the pages' MoELayer(d_model, d_ff, n_experts, top_k,
+ * n_shared, use_bias_balance) constructor (§9). */
+typedef struct {
+  int32_t n_tok;       /* N: tokens in the batch (B*T) */
+  int32_t d_model;     /* D */
+  int32_t d_ff;        /* F: routed expert hidden size */
+  int32_t n_exp;       /* E: routed experts */
+  int32_t top_k;       /* K */
+  int32_t gate;        /* 0: softmax top-K renorm (§4.1); 1: sigmoid renorm (§4.3) */
+  int32_t use_bias;    /* 1: select on logits + route_bias (§6.3) */
+  int32_t n_shared;    /* 0 or 1 shared expert (§5) */
+  int32_t d_ff_shared; /* Fs */
+  int32_t precision;   /* 0: bf16 operands, fp32 accumulation (only value implemented) */
+} moe_desc_t;
+
+/* Expert weights (all bf16, nn.Linear layout, see above).  ws1/ws3/ws2 are
+ * ignored when n_shared == 0. */
+typedef struct {
+  const void* w1;
+  const void* w3;
+  const void* w2;
+  const void* ws1;
+  const void* ws3;
+  const void* ws2;
+} moe_expert_weights_t;
+
+/* Activations the forward writes for the backward (bf16).  a1 = x_e w1_e^T,
+ * a3 = x_e w3_e^T, h = silu(a1) * a3, per permuted row [R,F]; the shared
+ * expert's a1s, a3s, hs are [N,Fs].  a1/a3/a1s/a3s may be NULL for an
+ * inference-only forward; h (and hs with a shared expert) are required. */
+typedef struct {
+  void* a1;
+  void* a3;
+  void* h;
+  void* a1s;
+  void* a3s;
+  void* hs;
+} moe_ffn_saved_t;
+
+/* Everything the backward reads from the forward (all written by the
+ * forward entry points, see each). */
+typedef struct {
+  const void* x;               /* [N,D] bf16 layer input */
+  const void* x_perm;          /* [R,D] bf16 from moe_permute */
+  const float* logits;         /* [N,E] fp32 from moe_route */
+  const int32_t* topk_idx;     /* [N,K] */
+  const float* topk_w;         /* [N,K] */
+  const int32_t* offsets;      /* [E+1] */
+  const int32_t* row_of_copy;  /* [R] */
+  const int32_t* copy_of_row;  /* [R] */
+  const void* a1;              /* [R,F] */
+  const void* a3;              /* [R,F] */
+  const void* h;               /* [R,F] */
+  const void* y_perm;          /* [R,D] from moe_grouped_ffn */
+  const void* a1s;             /* [N,Fs] */
+  const void* a3s;             /* [N,Fs] */
+  const void* hs;              /* [N,Fs] */
+} moe_fwd_state_t;
+
+/* Gradients written by moe_backward (fp32 unless stated).  dg and dlogits
+ * may be NULL; the shared gradients are ignored when n_shared == 0. */
+typedef struct {
+  void* dx;          /* [N,D] bf16: input gradient (experts + router) */
+  float* dw_gate;    /* [E,D] */
+  float* dw1;        /* [E,F,D] (zero for experts with no token) */
+  float* dw3;        /* [E,F,D] */
+  float* dw2;        /* [E,D,F] */
+  float* dws1;       /* [Fs,D] */
+  float* dws3;       /* [Fs,D] */
+  float* dws2;       /* [D,Fs] */
+  float* dg;         /* [N,K] d loss / d topk_w */
+  float* dlogits;    /* [N,K] d loss / d logits at the selected experts (0 elsewhere) */
+} moe_grads_t;
+
+/* Library and ABI identification. */
+MOE_API int32_t moe_abi_version(void);
+MOE_API const char* moe_status_string(moe_status_t s);
+
+/* Bytes of workspace the forward calls (route, permute, grouped_ffn,
+ * combine) and the backward call need for `d`.  fwd_bytes <= bwd_bytes; a
+ * workspace of bwd_bytes serves every call.  Either output may be NULL. */
+MOE_API moe_status_t moe_workspace_size(const moe_desc_t* d, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/* Clear the device status word at the start of `ws` (enqueued on stream). */
+MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then copy the two device status words (bits, site)
+ * to `status_host[0..1]`.  The only call that blocks the host. */
+MOE_API moe_status_t moe_get_device_status(const void* ws, int32_t* status_host, void* stream);
+
+/* Router (§4.1, §4.3, §6.3, §9 step 1) and expert histogram (§9 step 4,
+ * §12.5 bincount):
+ *   logits[N,E] (fp32 out) = x[N,D] (bf16) * w_gate[E,D]^T  (tensor cores,
+ *                            fp32 accumulation);
+ *   topk_idx[N,K] (out)    = the K experts with the largest
+ *                            logits + bias (bias [E] fp32, NULL when the layer
+ *                            has none), sorted by rank; equal keys: lower
+ *                            expert index first; -0.0 == +0.0; NaN lowest;
+ *   topk_w[N,K] (fp32 out) = renormalised gate weights (softmax over all E
+ *                            then p_sel/sum p_sel, or sigmoid(l_sel)/sum);
+ *   counts[E] (int32 out)  = copies routed to each expert;
+ *   offsets[E+1] (out)     = exclusive prefix sum of counts.
+ * Needs the forward workspace. */
+MOE_API moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias,
+                       float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* The same selection, weights, histogram and offsets from given fp32
+ * logits [N,E] (input).  Used when logits come from elsewhere. */
+MOE_API moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, const float* bias,
+                                   int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch (§12.5 sort by destination; §9 mask/nonzero order): a stable
+ * counting sort of the copies c = t*K+k by expert, ascending token inside
+ * an expert.  row_of_copy[c] (out) is the permuted row of copy c;
+ * copy_of_row[r] (out) its inverse; x_perm[r,:] (out, bf16 [R,D]) =
+ * x[copy_of_row[r]/K,:].  Rows of expert e are offsets[e]..offsets[e+1]-1.
+ * `offsets` comes from moe_route.  Needs the forward workspace. */
+MOE_API moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                         int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Ragged grouped SwiGLU FFN (§9 Expert; grouped GEMM of "Accelerating
+ * Dropless MoE Training in JAX with NVIDIA Transformer Engine" ¶5): for every
+ * expert e and its rows r in [offsets[e], offsets[e+1]):
+ *   a1 = x_perm[r] w1_e^T, a3 = x_perm[r] w3_e^T, h[r] = silu(a1) * a3,
+ *   y_perm[r] = h[r] w2_e^T  (bf16 out [R,D], unweighted).
+ * Both GEMMs run as one persistent tcgen05 launch each over all experts,
+ * reading the group sizes from `offsets` on the device.  With a shared
+ * expert the same FFN of ws1/ws3/ws2 runs over x (all N tokens) into
+ * y_shared [N,D] (bf16 out); y_shared is ignored otherwise.  `saved`
+ * receives the activations (see moe_ffn_saved_t). */
+MOE_API moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
+                             const moe_expert_weights_t* w, const moe_ffn_saved_t* saved, void* y_perm,
+                             void* y_shared, void* ws, size_t ws_bytes, void* stream);
+
+/* Combine (§9 index_add_ of weighted outputs plus shared expert; §12.5
+ * unsort + K-sum): out[t] = sum_{k<K} topk_w[t,k] * y_perm[row_of_copy[t*K+k]]
+ * + y_shared[t] (y_shared NULL: no shared term), summed in fp32 in rank
+ * order, stored bf16 [N,D].  A token-major gather, so deterministic. */
+MOE_API moe_status_t moe_combine(const moe_desc_t* d, const void* y_perm, const int32_t* row_of_copy, const float* topk_w,
+                         const void* y_shared, void* out, void* stream);
+
+/* Backward of the layer for the upstream gradient dy [N,D] (bf16 input):
+ * combine backward (dYw = g*dY per permuted row, dg = <dY, y_perm>), grouped
+ * data-gradient GEMM through w2 with the SwiGLU derivative fused in its
+ * epilogue, grouped data-gradient GEMM through w1|w3, grouped weight-gradient
+ * GEMMs (contraction over each expert's ragged rows, fp32 out, zero for
+ * empty experts), the shared expert's backward, the router logit gradient
+ * (softmax-renorm: g_k (dg_k - sum_j g_j dg_j); sigmoid-renorm:
+ * s_k (1-s_k)/S (dg_k - sum_j g_j dg_j); no gradient to route_bias), the
+ * router weight gradient dw_gate = dlogits^T x and the input gradient
+ * dx = sum_k dx_perm + dlogits W_g (+ shared).  Needs the backward workspace. */
+MOE_API moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
+                          const moe_fwd_state_t* st, const void* dy, const moe_grads_t* g, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* Online route-bias update (§9 update_balance_bias, §6.3), in place on
+ * bias[E] (fp32) from counts[E] of the last batch, load_stat = counts/sum:
+ *   mode 0 (listing): bias -= gamma * sign(load_stat - 1/E) * max(load_stat, 1e-6)
+ *   mode 1 (prose):   bias -= gamma * sign(load_stat - 1/E)
+ * in fp32 with every operation rounded separately.  An empty batch leaves
+ * the bias unchanged. */
+MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
+                             void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAGGED_GROUPED_GEMM_GB300_MOE_H */

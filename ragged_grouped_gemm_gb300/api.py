@@ -1,0 +1,238 @@
+"""Python binding of libmoe: one function per C entry point, same names.
+
+Each function only marshals arguments (checks device, dtype, contiguity and
+shape; passes ``data_ptr()`` and the current CUDA stream) and raises
+:class:`MoEError` on a non-OK status.  All computation happens in the CUDA
+kernels of libmoe.so.  :class:`MoELayer` owns the buffers of one layer and
+calls the entry points in forward/backward order.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from .inputs import MoEConfig
+
+BF16, F32, I32 = torch.bfloat16, torch.float32, torch.int32
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        lib = _lib.load()
+        super().__init__(f"{fn}: {lib.moe_status_string(code).decode()} (status {code})")
+        self.code = code
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MoEError(fn, code)
+
+
+def _p(t: torch.Tensor | None, dtype=None, shape=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(stream)
+
+
+def make_desc(cfg: MoEConfig) -> _lib.MoeDesc:
+    return _lib.MoeDesc(cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k,
+                        1 if cfg.gate == "sigmoid" else 0, 1 if cfg.use_bias else 0,
+                        cfg.n_shared, cfg.d_ff_shared if cfg.n_shared else 0,
+                        0 if cfg.precision == "bf16" else 1)
+
+
+# --------------------------------------------------------------- entry points
+def moe_workspace_size(desc: _lib.MoeDesc) -> tuple[int, int]:
+    f, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("moe_workspace_size", _lib.load().moe_workspace_size(ctypes.byref(desc), ctypes.byref(f), ctypes.byref(b)))
+    return f.value, b.value
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check("moe_workspace_init", _lib.load().moe_workspace_init(_p(ws, name="ws"), ws.numel() * ws.element_size(),
+                                                                _s(stream)))
+
+
+def moe_get_device_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:
+    out = (ctypes.c_int32 * 2)()
+    _check("moe_get_device_status", _lib.load().moe_get_device_status(_p(ws, name="ws"), out, _s(stream)))
+    return out[0], out[1]
+
+
+def moe_route(desc, x, w_gate, bias, logits, topk_idx, topk_w, counts, offsets, ws, stream=None):
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    _check("moe_route", _lib.load().moe_route(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(w_gate, BF16, (e, d), "w_gate"),
+        _p(bias, F32, (e,), "bias"), _p(logits, F32, (n, e), "logits"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(topk_w, F32, (n, k), "topk_w"), _p(counts, I32, (e,), "counts"), _p(offsets, I32, (e + 1,), "offsets"),
+        _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_route_from_logits(desc, logits, bias, topk_idx, topk_w, counts, offsets, ws, stream=None):
+    n, e, k = desc.n_tok, desc.n_exp, desc.top_k
+    _check("moe_route_from_logits", _lib.load().moe_route_from_logits(
+        ctypes.byref(desc), _p(logits, F32, (n, e), "logits"), _p(bias, F32, (e,), "bias"),
+        _p(topk_idx, I32, (n, k), "topk_idx"), _p(topk_w, F32, (n, k), "topk_w"), _p(counts, I32, (e,), "counts"),
+        _p(offsets, I32, (e + 1,), "offsets"), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_permute(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, x_perm, ws, stream=None):
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_permute", _lib.load().moe_permute(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(offsets, I32, (e + 1,), "offsets"), _p(row_of_copy, I32, (r,), "row_of_copy"),
+        _p(copy_of_row, I32, (r,), "copy_of_row"), _p(x_perm, BF16, (r, d), "x_perm"), _p(ws, name="ws"),
+        ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_grouped_ffn(desc, x_perm, offsets, x, w1, w3, w2, ws1, ws3, ws2, a1, a3, h, a1s, a3s, hs, y_perm,
+                    y_shared, ws, stream=None):
+    n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
+    r, fs = n * k, desc.d_ff_shared
+    sh = desc.n_shared
+    w = _lib.MoeExpertWeights(_p(w1, BF16, (e, f, d), "w1"), _p(w3, BF16, (e, f, d), "w3"),
+                              _p(w2, BF16, (e, d, f), "w2"),
+                              _p(ws1, BF16, (fs, d), "ws1") if sh else None,
+                              _p(ws3, BF16, (fs, d), "ws3") if sh else None,
+                              _p(ws2, BF16, (d, fs), "ws2") if sh else None)
+    sv = _lib.MoeFfnSaved(_p(a1, BF16, (r, f), "a1"), _p(a3, BF16, (r, f), "a3"), _p(h, BF16, (r, f), "h"),
+                          _p(a1s, BF16, (n, fs), "a1s") if sh else None,
+                          _p(a3s, BF16, (n, fs), "a3s") if sh else None,
+                          _p(hs, BF16, (n, fs), "hs") if sh else None)
+    _check("moe_grouped_ffn", _lib.load().moe_grouped_ffn(
+        ctypes.byref(desc), _p(x_perm, BF16, (r, d), "x_perm"), _p(offsets, I32, (e + 1,), "offsets"),
+        _p(x, BF16, (n, d), "x") if sh else None, ctypes.byref(w), ctypes.byref(sv),
+        _p(y_perm, BF16, (r, d), "y_perm"), _p(y_shared, BF16, (n, d), "y_shared") if sh else None,
+        _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_combine(desc, y_perm, row_of_copy, topk_w, y_shared, out, stream=None):
+    n, d, k = desc.n_tok, desc.d_model, desc.top_k
+    r = n * k
+    _check("moe_combine", _lib.load().moe_combine(
+        ctypes.byref(desc), _p(y_perm, BF16, (r, d), "y_perm"), _p(row_of_copy, I32, (r,), "row_of_copy"),
+        _p(topk_w, F32, (n, k), "topk_w"), _p(y_shared, BF16, (n, d), "y_shared"), _p(out, BF16, (n, d), "out"),
+        _s(stream)))
+
+
+def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, stream=None):
+    """``weights``: w1, w3, w2 (+ ws1, ws3, ws2); ``state``: the fields of
+    moe_fwd_state_t; ``grads``: the fields of moe_grads_t (dg, dlogits optional)."""
+    n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
+    r, fs, sh = n * k, desc.d_ff_shared, desc.n_shared
+    w = _lib.MoeExpertWeights(_p(weights["w1"], BF16, (e, f, d), "w1"), _p(weights["w3"], BF16, (e, f, d), "w3"),
+                              _p(weights["w2"], BF16, (e, d, f), "w2"),
+                              _p(weights.get("ws1"), BF16, (fs, d), "ws1") if sh else None,
+                              _p(weights.get("ws3"), BF16, (fs, d), "ws3") if sh else None,
+                              _p(weights.get("ws2"), BF16, (d, fs), "ws2") if sh else None)
+    S = state
+    st = _lib.MoeFwdState(
+        _p(S["x"], BF16, (n, d), "x"), _p(S["x_perm"], BF16, (r, d), "x_perm"), _p(S["logits"], F32, (n, e), "logits"),
+        _p(S["topk_idx"], I32, (n, k), "topk_idx"), _p(S["topk_w"], F32, (n, k), "topk_w"),
+        _p(S["offsets"], I32, (e + 1,), "offsets"), _p(S["row_of_copy"], I32, (r,), "row_of_copy"),
+        _p(S["copy_of_row"], I32, (r,), "copy_of_row"), _p(S["a1"], BF16, (r, f), "a1"), _p(S["a3"], BF16, (r, f), "a3"),
+        _p(S["h"], BF16, (r, f), "h"), _p(S["y_perm"], BF16, (r, d), "y_perm"),
+        _p(S.get("a1s"), BF16, (n, fs), "a1s") if sh else None, _p(S.get("a3s"), BF16, (n, fs), "a3s") if sh else None,
+        _p(S.get("hs"), BF16, (n, fs), "hs") if sh else None)
+    G = grads
+    gr = _lib.MoeGrads(
+        _p(G["dx"], BF16, (n, d), "dx"), _p(G["dw_gate"], F32, (e, d), "dw_gate"), _p(G["dw1"], F32, (e, f, d), "dw1"),
+        _p(G["dw3"], F32, (e, f, d), "dw3"), _p(G["dw2"], F32, (e, d, f), "dw2"),
+        _p(G.get("dws1"), F32, (fs, d), "dws1") if sh else None, _p(G.get("dws3"), F32, (fs, d), "dws3") if sh else None,
+        _p(G.get("dws2"), F32, (d, fs), "dws2") if sh else None,
+        _p(G.get("dg"), F32, (n, k), "dg"), _p(G.get("dlogits"), F32, (n, k), "dlogits"))
+    _check("moe_backward", _lib.load().moe_backward(
+        ctypes.byref(desc), _p(w_gate, BF16, (e, d), "w_gate"), ctypes.byref(w), ctypes.byref(st),
+        _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_update_bias(desc, counts, bias, gamma: float, mode: int = 0, stream=None):
+    _check("moe_update_bias", _lib.load().moe_update_bias(
+        ctypes.byref(desc), _p(counts, I32, (desc.n_exp,), "counts"), _p(bias, F32, (desc.n_exp,), "bias"),
+        ctypes.c_float(gamma), mode, _s(stream)))
+
+
+# --------------------------------------------------------------- layer runner
+class MoELayer:
+    """Buffers of one layer plus the forward / backward call sequences.
+
+    ``params``: x-independent tensors from :func:`inputs.make_layer` on the GPU
+    (w_gate, w1, w3, w2, bias, and ws1, ws3, ws2 with a shared expert).
+    """
+
+    def __init__(self, cfg: MoEConfig, params: dict, train: bool = True, device="cuda"):
+        self.cfg = cfg
+        self.desc = make_desc(cfg)
+        self.p = params
+        self.train = train
+        n, d, f, e, k = cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k
+        r, fs = cfg.rows, cfg.d_ff_shared
+        z = lambda *s, dt=BF16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+        self.buf = {
+            "logits": z(n, e, dt=F32), "topk_idx": z(n, k, dt=I32), "topk_w": z(n, k, dt=F32),
+            "counts": z(e, dt=I32), "offsets": z(e + 1, dt=I32), "row_of_copy": z(r, dt=I32),
+            "copy_of_row": z(r, dt=I32), "x_perm": z(r, d), "h": z(r, f), "y_perm": z(r, d), "out": z(n, d),
+            "a1": z(r, f) if train else None, "a3": z(r, f) if train else None,
+        }
+        if cfg.n_shared:
+            self.buf.update(hs=z(n, fs), y_shared=z(n, d), a1s=z(n, fs) if train else None,
+                            a3s=z(n, fs) if train else None)
+        else:
+            self.buf.update(hs=None, y_shared=None, a1s=None, a3s=None)
+        fwd_b, bwd_b = moe_workspace_size(self.desc)
+        self.ws = torch.empty((bwd_b if train else fwd_b) + 256, dtype=torch.uint8, device=device)
+        moe_workspace_init(self.ws)
+        self.grads = None
+        if train:
+            self.grads = {"dx": z(n, d), "dw_gate": z(e, d, dt=F32), "dw1": z(e, f, d, dt=F32),
+                          "dw3": z(e, f, d, dt=F32), "dw2": z(e, d, f, dt=F32), "dg": z(n, k, dt=F32),
+                          "dlogits": z(n, k, dt=F32)}
+            if cfg.n_shared:
+                self.grads.update(dws1=z(fs, d, dt=F32), dws3=z(fs, d, dt=F32), dws2=z(d, fs, dt=F32))
+        self.x = None
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        b, p = self.buf, self.p
+        self.x = x
+        moe_route(self.desc, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
+                  b["offsets"], self.ws, stream)
+        moe_permute(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"],
+                    self.ws, stream)
+        moe_grouped_ffn(self.desc, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
+                        p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
+                        b["y_perm"], b["y_shared"], self.ws, stream)
+        moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
+        return b["out"]
+
+    def backward(self, dy: torch.Tensor, stream=None) -> dict:
+        b = self.buf
+        state = {key: b[key] for key in ("x_perm", "logits", "topk_idx", "topk_w", "offsets", "row_of_copy",
+                                         "copy_of_row", "a1", "a3", "h", "y_perm", "a1s", "a3s", "hs")}
+        state["x"] = self.x
+        moe_backward(self.desc, self.p["w_gate"], self.p, state, dy, self.grads, self.ws, stream)
+        return self.grads
+
+    def update_bias(self, gamma: float = 1e-3, mode: int = 0, stream=None):
+        moe_update_bias(self.desc, self.buf["counts"], self.p["bias"], gamma, mode, stream)
+
+    def device_status(self) -> tuple[int, int]:
+        return moe_get_device_status(self.ws)

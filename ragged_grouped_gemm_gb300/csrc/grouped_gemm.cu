@@ -1,0 +1,622 @@
+// Persistent, warp-specialised tcgen05 grouped GEMM for sm_103a.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: one lane streams A/B k-blocks into a ring of
+//               shared-memory stages (128-byte swizzle), signalled by
+//               mbarriers with transaction counts.
+//   warp 1      TMEM owner and MMA issuer: one lane issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into a
+//               double-buffered fp32 accumulator in tensor memory and commits
+//               stage releases and accumulator hand-offs to mbarriers.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31 = tile rows), apply the fused epilogue and store.
+// The accumulator is double-buffered, so the epilogue of tile i overlaps the
+// main loop of tile i+1.  Tiles are walked in a persistent loop; for the
+// ragged-M form the tile list is derived on the device from the group
+// offsets (prefix of per-group 128-row tile counts), so a launch needs no
+// host-side knowledge of the group sizes.
+//
+// Shared-memory operand layouts (both 1024-byte aligned per stage):
+//   K-major : rows of 64 bf16 (128 B), 8-row swizzle atoms of 1024 B;
+//             descriptor SBO = 1024, advance 32 B per K=16 step.
+//   MN-major: per 64-wide MN atom a region of 64 K-rows x 128 B;
+//             descriptor LBO = 8192 (next MN atom), SBO = 1024 (next 8 K-rows),
+//             advance 2048 B per K=16 step.
+#include "grouped_gemm.cuh"
+#include "sm100_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 1024;
+constexpr int kABytes = BM * BK * 2;   // 16 KB
+
+struct KParams {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  const int32_t* offsets;
+  int32_t num_groups;
+  int32_t m_size;
+  int32_t n_size;
+  int32_t kb0, kb1;
+  int32_t b_dual_n;
+  int32_t b_3d;
+  int32_t tile_n;
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+  int64_t ld_out;
+  int64_t group_stride_out;
+  int32_t* status;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStageBytes = (BM + BN) * BK * 2;
+  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  // stages | barriers (2S+5) | tmem base, abort | offsets[G+1] | prefix[G+1]
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kMiscOff = kBarOff + (2 * kStages + 5) * 8;
+  static constexpr int kOffOff = kMiscOff + 16;
+  static constexpr size_t smem_bytes(int groups) {
+    return 1024 + kOffOff + 2 * 4 * (groups + 1);
+  }
+};
+
+struct Tile {
+  int g, mt, nt;
+  int row0;        // ragged M: first permuted row of the tile; ragged K: first row of the group
+  int rows_valid;  // ragged M: valid rows of the tile
+  int k_rows;      // ragged K: rows of the group (contraction length)
+  int num_kb;
+};
+
+template <bool RAGGED_K, int BN>
+__device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const int* s_off, const int* s_pre) {
+  Tile t;
+  if (!RAGGED_K) {
+    const int total_m = s_pre[p.num_groups];
+    t.nt = tile / total_m;
+    const int rem = tile - t.nt * total_m;
+    int lo = 0, hi = p.num_groups;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= rem) lo = mid; else hi = mid;
+    }
+    t.g = lo;
+    t.mt = rem - s_pre[lo];
+    t.row0 = s_off[lo] + t.mt * BM;
+    t.rows_valid = min(BM, s_off[lo + 1] - t.row0);
+    t.k_rows = 0;
+    t.num_kb = p.kb0 + p.kb1;
+  } else {
+    const int mtiles = (p.m_size + BM - 1) / BM;
+    const int ntiles = (p.n_size + BN - 1) / BN;
+    const int per_g = mtiles * ntiles;
+    t.g = tile / per_g;
+    const int rem = tile - t.g * per_g;
+    t.mt = rem / ntiles;
+    t.nt = rem - t.mt * ntiles;
+    t.row0 = s_off[t.g];
+    t.k_rows = s_off[t.g + 1] - s_off[t.g];
+    t.rows_valid = min(BM, p.m_size - t.mt * BM);
+    t.num_kb = (t.k_rows + BK - 1) / BK;
+  }
+  return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float sigmoidf_fast(float a) { return 1.0f / (1.0f + __expf(-a)); }
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<BN>;
+  constexpr bool RAGGED_K = A_MN;
+  constexpr int S = C::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  int* s_off = reinterpret_cast<int*>(smem + C::kOffOff);
+  int* s_pre = s_off + (p.num_groups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.num_groups;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  // group offsets and (ragged M) the prefix of per-group 128-row tile counts
+  for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = p.offsets[i];
+  __syncthreads();
+  if (!RAGGED_K && warp == 0) {
+    const int per = (G + 31) / 32;
+    const int lo = lane * per;
+    const int hi = min(G, lo + per);
+    int sum = 0;
+    for (int g = lo; g < hi; ++g) sum += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+    for (int g = lo; g < hi; ++g) {
+      s_pre[g] = run;
+      run += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    }
+    if (lane == 31) s_pre[G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  int total_tiles;
+  if (!RAGGED_K) {
+    const int ntiles = (p.n_size + p.tile_n - 1) / p.tile_n;
+    total_tiles = s_pre[G] * ntiles;
+  } else {
+    total_tiles = G * ((p.m_size + BM - 1) / BM) * ((p.n_size + BN - 1) / BN);
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
+          uint8_t* sA = smem + s * C::kStageBytes;
+          uint8_t* sB = sA + kABytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          if (!RAGGED_K) {
+            const int src = (kb < p.kb0) ? 0 : 1;
+            const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
+            tma_load_2d(sA, &p.tmA[src], &full[s], k0, t.row0);
+            if (!B_MN) {
+              if (p.b_dual_n) {
+                const int f0 = t.nt * (BN / 2);
+                tma_load_3d(sB, &p.tmB[0], &full[s], k0, f0, t.g);
+                tma_load_3d(sB + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
+              } else if (p.b_3d) {
+                tma_load_3d(sB, &p.tmB[src], &full[s], k0, t.nt * BN, t.g);
+              } else {
+                tma_load_2d(sB, &p.tmB[src], &full[s], k0, t.nt * BN);
+              }
+            } else {
+#pragma unroll
+              for (int a = 0; a < BN / 64; ++a) {
+                if (p.b_3d) tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
+                else tma_load_2d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0);
+              }
+            }
+          } else {
+            const int r = t.row0 + kb * BK;
+            const int m0 = t.mt * BM;
+            tma_load_2d(sA, &p.tmA[0], &full[s], m0, r);
+            tma_load_2d(sA + 8192, &p.tmA[0], &full[s], m0 + 64, r);
+#pragma unroll
+            for (int a = 0; a < BN / 64; ++a)
+              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], t.nt * BN + 64 * a, r);
+          }
+        }
+      }
+      // Wait (bounded) for every stage's last armed load so that no copy is
+      // still landing in shared memory when the CTA exits.
+      for (int s = 0; s < S; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t last = s + S * ((it - 1 - s) / S);
+          mbar_wait_drain(&full[s], (last / S) & 1u);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
+      const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+      const uint32_t buf = tcount & 1u;
+      const uint32_t aph = (tcount >> 1) & 1u;
+      if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 300 + s)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* sA = smem + s * C::kStageBytes;
+        uint8_t* sB = sA + kABytes;
+        int nkk = BK / 16;
+        if (RAGGED_K) {
+          const int rv = min(BK, t.k_rows - kb * BK);
+          if (rv < BK) {
+            // Rows past the group's end belong to the next expert: zero them
+            // up to the next multiple of 16 and skip the empty K=16 steps.
+            nkk = (rv + 15) / 16;
+            const int zrows = nkk * 16 - rv;
+            if (zrows > 0) {
+              const int nreg = 2 + BN / 64;
+              const int per_reg = zrows * 8;  // 16-byte chunks
+              const uint4 z = make_uint4(0, 0, 0, 0);
+              for (int i = lane; i < nreg * per_reg; i += 32) {
+                const int reg = i / per_reg;
+                const int j = i - reg * per_reg;
+                uint8_t* base = (reg < 2) ? (sA + reg * 8192) : (sB + (reg - 2) * 8192);
+                *reinterpret_cast<uint4*>(base + rv * 128 + j * 16) = z;
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(sA);
+          const uint32_t b_base = smem_u32(sB);
+          for (int kk = 0; kk < nkk; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (t.num_kb > 0) tc_commit(&tfull[buf]);
+        else mbar_arrive(&tfull[buf]);
+      }
+      __syncwarp();
+    }
+    // every MMA issued by this CTA has completed before TMEM is released
+    if (lane == 0) {
+      tc_commit(mma_done);
+      mbar_wait_drain(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    uint32_t tcount = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
+      const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+      const uint32_t buf = tcount & 1u;
+      const uint32_t aph = (tcount >> 1) & 1u;
+      if (!mbar_wait_bounded(&tfull[buf], aph, s_abort, p.status, 400)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const bool row_ok = r < t.rows_valid;
+      if (EPI == EPI_BF16 || EPI == EPI_F32) {
+        int64_t grow;
+        char* obase = static_cast<char*>(p.out0);
+        if (!RAGGED_K) {
+          grow = t.row0 + r;
+        } else {
+          grow = static_cast<int64_t>(t.mt) * BM + r;
+          obase += static_cast<int64_t>(t.g) * p.group_stride_out * (EPI == EPI_F32 ? 4 : 2);
+        }
+        const bool zero = RAGGED_K && t.num_kb == 0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          uint32_t v[16];
+          if (!zero) {
+            tmem_ld_32x32b_x16(tb + c, v);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0u;
+          }
+          const int col = t.nt * BN + c;
+          if (row_ok && col < p.n_size) {
+            const int nvalid = min(16, p.n_size - col);
+            if (EPI == EPI_F32) {
+              float* dst = reinterpret_cast<float*>(obase) + grow * p.ld_out + col;
+              if (nvalid == 16 && (p.ld_out & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  reinterpret_cast<uint4*>(dst)[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              } else {
+                for (int j = 0; j < nvalid; ++j) dst[j] = __uint_as_float(v[j]);
+              }
+            } else {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(obase) + grow * p.ld_out + col;
+              uint32_t w[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              if (nvalid == 16) {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              } else {
+                for (int j = 0; j < nvalid; ++j) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_FWD) {
+        const int64_t grow = t.row0 + r;
+        const int f0 = t.nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 16) {
+          uint32_t u[16], v[16];
+          tmem_ld_32x32b_x16(tb + c, u);
+          tmem_ld_32x32b_x16(tb + BN / 2 + c, v);
+          tmem_wait_ld();
+          const int col = f0 + c;
+          if (row_ok && col < p.n_size) {
+            uint32_t hw[8], aw[8], bw[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float a0 = __uint_as_float(u[2 * j]), a1 = __uint_as_float(u[2 * j + 1]);
+              const float b0 = __uint_as_float(v[2 * j]), b1 = __uint_as_float(v[2 * j + 1]);
+              hw[j] = pack_bf16x2(a0 * sigmoidf_fast(a0) * b0, a1 * sigmoidf_fast(a1) * b1);
+              aw[j] = pack_bf16x2(a0, a1);
+              bw[j] = pack_bf16x2(b0, b1);
+            }
+            const int64_t off = grow * p.ld_out + col;
+            uint4* h = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + off);
+            h[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            h[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            if (p.out1) {
+              uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out1) + off);
+              d[0] = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+              d[1] = make_uint4(aw[4], aw[5], aw[6], aw[7]);
+            }
+            if (p.out2) {
+              uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out2) + off);
+              d[0] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+              d[1] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+            }
+          }
+        }
+      } else {  // EPI_SWIGLU_BWD
+        const int64_t grow = t.row0 + r;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          uint32_t u[16];
+          tmem_ld_32x32b_x16(tb + c, u);
+          tmem_wait_ld();
+          const int col = t.nt * BN + c;
+          if (row_ok && col < p.n_size) {
+            const int64_t off = grow * p.ld_out + col;
+            const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.in0) + off);
+            const uint4* pb = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.in1) + off);
+            const uint4 a01 = pa[0], a23 = pa[1], b01 = pb[0], b23 = pb[1];
+            const uint32_t aw[8] = {a01.x, a01.y, a01.z, a01.w, a23.x, a23.y, a23.z, a23.w};
+            const uint32_t bw[8] = {b01.x, b01.y, b01.z, b01.w, b23.x, b23.y, b23.z, b23.w};
+            uint32_t d1[8], d3[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float o1[2], o3[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float dh = __uint_as_float(u[2 * j + h]);
+                const float a1 = h ? bf16hi(aw[j]) : bf16lo(aw[j]);
+                const float a3 = h ? bf16hi(bw[j]) : bf16lo(bw[j]);
+                const float sg = sigmoidf_fast(a1);
+                o3[h] = dh * a1 * sg;
+                o1[h] = dh * a3 * sg * (1.0f + a1 * (1.0f - sg));
+              }
+              d1[j] = pack_bf16x2(o1[0], o1[1]);
+              d3[j] = pack_bf16x2(o3[0], o3[1]);
+            }
+            uint4* q1 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + off);
+            uint4* q3 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out1) + off);
+            q1[0] = make_uint4(d1[0], d1[1], d1[2], d1[3]);
+            q1[1] = make_uint4(d1[4], d1[5], d1[6], d1[7]);
+            q3[0] = make_uint4(d3[0], d3[1], d3[2], d3[3]);
+            q3[1] = make_uint4(d3[4], d3[5], d3[6], d3[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ host
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle and zero fill out of bounds.
+// 2-D when op.groups == 1: dims {cols, rows}; else 3-D {cols, rows, groups}.
+bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t box_rows) {
+  EncodeFn enc = get_encode_fn();
+  if (!enc || !op.ptr) return false;
+  if ((reinterpret_cast<uintptr_t>(op.ptr) & 15u) != 0 || (op.ld * 2) % 16 != 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows),
+                        static_cast<cuuint64_t>(op.groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(op.ld) * 2, static_cast<cuuint64_t>(op.group_stride) * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t rank = op.groups > 1 ? 3 : 2;
+  if (rank == 3 && (op.group_stride * 2) % 16 != 0) return false;
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(op.ptr), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_impl(const KParams& kp, int grid, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  const size_t smem = C::smem_bytes(kp.num_groups);
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(C::smem_bytes(kMaxGroups)));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  kern<<<grid, kThreads, smem, stream>>>(kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  });
+  return n;
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.num_groups < 1 || a.num_groups > kMaxGroups || !a.offsets || !a.out0 || a.n_size <= 0)
+    return cudaErrorInvalidValue;
+  if (a.block_n != 256 && !(a.block_n == 32 && !a.b_mn && !a.a_mn && a.epi == EPI_F32))
+    return cudaErrorInvalidValue;
+  if (a.ragged_k != a.a_mn) return cudaErrorInvalidValue;  // the two forms this kernel implements
+  const int BN = a.block_n;
+  KParams kp{};
+  kp.offsets = a.offsets;
+  kp.num_groups = a.num_groups;
+  kp.m_size = a.m_size;
+  kp.n_size = a.n_size;
+  kp.b_dual_n = a.b_dual_n ? 1 : 0;
+  kp.tile_n = a.b_dual_n ? BN / 2 : BN;
+  kp.out0 = a.out0;
+  kp.out1 = a.out1;
+  kp.out2 = a.out2;
+  kp.in0 = a.in0;
+  kp.in1 = a.in1;
+  kp.ld_out = a.ld_out;
+  kp.group_stride_out = a.group_stride_out;
+  kp.status = a.status;
+
+  int64_t tiles_ub = 0;
+  if (!a.ragged_k) {
+    if (a.max_rows <= 0) return cudaSuccess;
+    kp.kb0 = (a.k0 + BK - 1) / BK;
+    kp.kb1 = (a.k1 + BK - 1) / BK;
+    if (kp.kb0 <= 0) return cudaErrorInvalidValue;
+    const int nsrc = kp.kb1 > 0 ? 2 : 1;
+    for (int s = 0; s < nsrc; ++s) {
+      if (!make_map(&kp.tmA[s], a.a[s], 64, BM)) return cudaErrorInvalidValue;
+      if (!a.b_mn) {
+        if (!make_map(&kp.tmB[s], a.b[s], 64, a.b_dual_n ? BN / 2 : BN)) return cudaErrorInvalidValue;
+      } else {
+        if (!make_map(&kp.tmB[s], a.b[s], 64, 64)) return cudaErrorInvalidValue;
+      }
+    }
+    if (a.b_dual_n) {
+      if (a.b_mn || !make_map(&kp.tmB[1], a.b[1], 64, BN / 2)) return cudaErrorInvalidValue;
+    }
+    if (nsrc == 1) {
+      kp.tmA[1] = kp.tmA[0];
+      if (!a.b_dual_n) kp.tmB[1] = kp.tmB[0];
+    }
+    kp.b_3d = a.b[0].groups > 1 ? 1 : 0;
+    const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
+    tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+  } else {
+    if (a.m_size <= 0) return cudaSuccess;
+    if (!make_map(&kp.tmA[0], a.a[0], 64, 64) || !make_map(&kp.tmB[0], a.b[0], 64, 64))
+      return cudaErrorInvalidValue;
+    kp.tmA[1] = kp.tmA[0];
+    kp.tmB[1] = kp.tmB[0];
+    kp.b_3d = 0;
+    tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + BN - 1) / BN);
+  }
+  if (tiles_ub <= 0) return cudaSuccess;
+  const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
+
+  if (BN == 32) return launch_impl<32, false, false, EPI_F32>(kp, grid, stream);
+  if (!a.a_mn && !a.b_mn) {
+    switch (a.epi) {
+      case EPI_BF16: return launch_impl<256, false, false, EPI_BF16>(kp, grid, stream);
+      case EPI_F32: return launch_impl<256, false, false, EPI_F32>(kp, grid, stream);
+      case EPI_SWIGLU_FWD: return launch_impl<256, false, false, EPI_SWIGLU_FWD>(kp, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (!a.a_mn && a.b_mn) {
+    switch (a.epi) {
+      case EPI_BF16: return launch_impl<256, false, true, EPI_BF16>(kp, grid, stream);
+      case EPI_SWIGLU_BWD: return launch_impl<256, false, true, EPI_SWIGLU_BWD>(kp, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (a.a_mn && a.b_mn && a.epi == EPI_F32) return launch_impl<256, true, true, EPI_F32>(kp, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,71 @@
+// Host-side interface of the persistent tcgen05 grouped GEMM.
+//
+// One launch computes, for every group g of a ragged problem,
+//   C_g = A_g * B_g^T       (A_g: [m_g, K], B_g: [N, K], fp32 accumulation)
+// where the ragged dimension is either M (forward and data-gradient GEMMs:
+// the rows of expert g in the expert-major permuted buffers) or K (weight
+// gradients: the contraction runs over the rows of expert g).  Group sizes
+// are read on the device from an offsets array, so no host synchronisation
+// and no padding is needed ("Accelerating Dropless MoE Training in JAX with
+// NVIDIA Transformer Engine", ¶5-¶6: grouped GEMM over ragged tensors in a
+// single call, with shapes not known on the CPU).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+enum EpiKind : int {
+  EPI_BF16 = 0,        // out0[row, col] = bf16(acc)
+  EPI_F32 = 1,         // out0[row, col] = acc
+  EPI_SWIGLU_FWD = 2,  // acc = [a1 | a3] -> out0 = h = silu(a1) * a3, out1 = a1, out2 = a3 (bf16)
+  EPI_SWIGLU_BWD = 3,  // acc = dh; in0 = a1, in1 = a3 -> out0 = da1, out1 = da3 (bf16)
+};
+
+// One operand source: a bf16 matrix in global memory.
+//   K-major A: [rows, K] row-major (rows = permuted rows), ld = K.
+//   K-major B: per group [N, K] row-major, groups stacked with group_stride.
+//   MN-major A/B: [K_rows, MN] row-major (the contraction runs over rows).
+struct Operand {
+  const void* ptr = nullptr;
+  int64_t rows = 0;          // per group for stacked weights
+  int64_t cols = 0;
+  int64_t ld = 0;            // elements between consecutive rows
+  int64_t groups = 1;        // >1: a stack of matrices (3-D tensor map)
+  int64_t group_stride = 0;  // elements between consecutive matrices
+};
+
+struct GemmArgs {
+  bool a_mn = false;          // A stored MN-major (weight gradients)
+  bool b_mn = false;          // B stored MN-major (data gradients)
+  bool ragged_k = false;      // contraction over the group's rows
+  int block_n = 256;          // 256, or 32 for narrow N (router logits)
+  EpiKind epi = EPI_BF16;
+  Operand a[2];               // a[1]: second half of a split contraction
+  Operand b[2];               // b[1]: second contraction half, or W3 half of the N tile
+  bool b_dual_n = false;      // N tile = [b[0] rows | b[1] rows] (fused W1|W3)
+  int k0 = 0, k1 = 0;         // ragged M: contraction length of source 0 and 1
+  const int32_t* offsets = nullptr;  // device, [num_groups + 1]
+  int num_groups = 1;
+  int64_t max_rows = 0;       // upper bound of offsets[num_groups] (grid sizing)
+  int m_size = 0;             // ragged K: rows of each C_g
+  int n_size = 0;             // columns of C (f extent for EPI_SWIGLU_FWD)
+  void* out0 = nullptr;
+  void* out1 = nullptr;
+  void* out2 = nullptr;
+  const void* in0 = nullptr;
+  const void* in1 = nullptr;
+  int64_t ld_out = 0;
+  int64_t group_stride_out = 0;
+  int32_t* status = nullptr;  // device status words
+};
+
+// Enqueue the grouped GEMM on `stream`.  Returns cudaSuccess or the first
+// CUDA error (tensor-map encoding failures map to cudaErrorInvalidValue).
+cudaError_t launch_grouped_gemm(const GemmArgs& args, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,434 @@
+// C ABI of libmoe (declared in include/moe.h): argument validation,
+// workspace layout, and the launch sequence of each entry point.
+#include "moe.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "grouped_gemm.cuh"
+#include "moe_kernels.cuh"
+
+namespace {
+
+using moe::GemmArgs;
+using moe::Operand;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, fwd_end = 0;
+  size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
+};
+
+WsLayout layout(const moe_desc_t& d) {
+  WsLayout L;
+  const size_t N = d.n_tok, D = d.d_model, F = d.d_ff, E = d.n_exp, K = d.top_k;
+  const size_t R = N * K, Fs = d.n_shared ? d.d_ff_shared : 0;
+  const size_t nch = moe::permute_num_chunks(d.n_tok);
+  size_t o = 0;
+  L.status = o; o += kAlign;
+  L.dense_off = o; o += kAlign;
+  L.blk_counts = o; o = align_up(o + nch * E * 4);
+  L.blk_base = o; o = align_up(o + nch * E * 4);
+  L.fwd_end = o;
+  L.dl = o; o = align_up(o + R * 4);
+  L.dg = o; o = align_up(o + R * 4);
+  L.dyw = o; o = align_up(o + R * D * 2);  // also holds dx_perm
+  L.da1 = o; o = align_up(o + R * F * 2);
+  L.da3 = o; o = align_up(o + R * F * 2);
+  L.da1s = o; o = align_up(o + N * Fs * 2);
+  L.da3s = o; o = align_up(o + N * Fs * 2);
+  L.dxs = o; o = align_up(o + (Fs ? N * D * 2 : 0));
+  L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_exp, d.d_model) * 4);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_desc(const moe_desc_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->n_tok < 0 || d->d_model <= 0 || d->d_ff <= 0 || d->n_exp <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->top_k > d->n_exp || d->top_k > 32 || d->n_exp > 1024) return MOE_ERR_INVALID_ARG;
+  if (d->d_model % 64 || d->d_ff % 64) return MOE_ERR_INVALID_ARG;
+  if (d->gate != 0 && d->gate != 1) return MOE_ERR_INVALID_ARG;
+  if (d->use_bias != 0 && d->use_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared != 0 && d->n_shared != 1) return d->n_shared > 1 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (d->d_ff_shared <= 0 || d->d_ff_shared % 64)) return MOE_ERR_INVALID_ARG;
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->n_tok) * d->top_k >= (int64_t{1} << 31)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_desc_t& d, void* ws, size_t ws_bytes, bool bwd) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  const WsLayout L = layout(d);
+  if (ws_bytes < (bwd ? L.total : L.fwd_end)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                          \
+  do {                                         \
+    const moe_status_t s_ = (expr);            \
+    if (s_ != MOE_OK) return s_;               \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+bool all16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return false;
+  return true;
+}
+
+// A K-major activation [rows, cols] (row-major, ld = cols).
+Operand act(const void* p, int64_t rows, int64_t cols) {
+  Operand o;
+  o.ptr = p;
+  o.rows = rows;
+  o.cols = cols;
+  o.ld = cols;
+  o.groups = 1;
+  o.group_stride = rows * cols;
+  return o;
+}
+// A stack of `groups` weight matrices [rows, cols] each.
+Operand wstack(const void* p, int64_t groups, int64_t rows, int64_t cols) {
+  Operand o = act(p, rows, cols);
+  o.groups = groups;
+  o.group_stride = rows * cols;
+  return o;
+}
+
+// SwiGLU FFN of one "expert set": GEMM1 (fused w1|w3 with SwiGLU epilogue)
+// then GEMM2, over `groups` ragged row groups of `a_in` [rows, D].
+moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, const int32_t* offsets,
+                      const void* w1, const void* w3, const void* w2, void* h, void* a1, void* a3, void* y,
+                      int32_t* status, cudaStream_t st) {
+  GemmArgs g1;
+  g1.epi = moe::EPI_SWIGLU_FWD;
+  g1.a[0] = act(a_in, rows, D);
+  g1.b[0] = wstack(w1, groups, F, D);
+  g1.b[1] = wstack(w3, groups, F, D);
+  g1.b_dual_n = true;
+  g1.k0 = D;
+  g1.offsets = offsets;
+  g1.num_groups = groups;
+  g1.max_rows = rows;
+  g1.n_size = F;
+  g1.out0 = h;
+  g1.out1 = a1;
+  g1.out2 = a3;
+  g1.ld_out = F;
+  g1.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g1, st));
+  GemmArgs g2;
+  g2.epi = moe::EPI_BF16;
+  g2.a[0] = act(h, rows, F);
+  g2.b[0] = wstack(w2, groups, D, F);
+  g2.k0 = F;
+  g2.offsets = offsets;
+  g2.num_groups = groups;
+  g2.max_rows = rows;
+  g2.n_size = D;
+  g2.out0 = y;
+  g2.ld_out = D;
+  g2.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g2, st));
+  return MOE_OK;
+}
+
+// Backward of one expert set: dgrad through w2 with the SwiGLU derivative,
+// weight gradient of w2, dgrad through w1|w3, weight gradients of w1, w3.
+moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, const void* a3, const void* h,
+                          int64_t rows, int D, int F, int groups, const int32_t* offsets, const void* w1,
+                          const void* w3, const void* w2, void* da1, void* da3, void* dx_rows, float* dw1,
+                          float* dw3, float* dw2, int32_t* status, cudaStream_t st) {
+  GemmArgs g;
+  g.epi = moe::EPI_SWIGLU_BWD;
+  g.b_mn = true;
+  g.a[0] = act(dyw, rows, D);
+  g.b[0] = wstack(w2, groups, D, F);  // B[n=f, k=d], f contiguous
+  g.k0 = D;
+  g.offsets = offsets;
+  g.num_groups = groups;
+  g.max_rows = rows;
+  g.n_size = F;
+  g.in0 = a1;
+  g.in1 = a3;
+  g.out0 = da1;
+  g.out1 = da3;
+  g.ld_out = F;
+  g.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+
+  GemmArgs w;
+  w.epi = moe::EPI_F32;
+  w.a_mn = w.b_mn = w.ragged_k = true;
+  w.offsets = offsets;
+  w.num_groups = groups;
+  w.max_rows = rows;
+  w.status = status;
+  // dW2_e [D,F] = dYw_e^T h_e
+  w.a[0] = act(dyw, rows, D);
+  w.b[0] = act(h, rows, F);
+  w.m_size = D;
+  w.n_size = F;
+  w.out0 = dw2;
+  w.ld_out = F;
+  w.group_stride_out = static_cast<int64_t>(D) * F;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+
+  // dx_rows = da1 w1_e + da3 w3_e (the dYw buffer may be reused as dx_rows)
+  GemmArgs d;
+  d.epi = moe::EPI_BF16;
+  d.b_mn = true;
+  d.a[0] = act(da1, rows, F);
+  d.a[1] = act(da3, rows, F);
+  d.b[0] = wstack(w1, groups, F, D);  // B[n=d, k=f], d contiguous
+  d.b[1] = wstack(w3, groups, F, D);
+  d.k0 = F;
+  d.k1 = F;
+  d.offsets = offsets;
+  d.num_groups = groups;
+  d.max_rows = rows;
+  d.n_size = D;
+  d.out0 = dx_rows;
+  d.ld_out = D;
+  d.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(d, st));
+
+  // dW1_e [F,D] = da1_e^T x_e, dW3_e = da3_e^T x_e
+  w.a[0] = act(da1, rows, F);
+  w.b[0] = act(a_in, rows, D);
+  w.m_size = F;
+  w.n_size = D;
+  w.out0 = dw1;
+  w.ld_out = D;
+  w.group_stride_out = static_cast<int64_t>(F) * D;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  w.a[0] = act(da3, rows, F);
+  w.out0 = dw3;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device status error";
+  }
+  return "unknown";
+}
+
+moe_status_t moe_workspace_size(const moe_desc_t* d, size_t* fwd_bytes, size_t* bwd_bytes) {
+  MOE_TRY(check_desc(d));
+  const WsLayout L = layout(*d);
+  if (fwd_bytes) *fwd_bytes = L.fwd_end;
+  if (bwd_bytes) *bwd_bytes = L.total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kAlign || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status_t moe_get_device_status(const void* ws, int32_t* status_host, void* stream) {
+  if (!ws || !status_host) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  MOE_CUDA(cudaMemcpy(status_host, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+static moe_status_t route_tail(const moe_desc_t* d, const float* logits, const float* bias, int32_t* topk_idx,
+                               float* topk_w, int32_t* counts, int32_t* offsets, int32_t* status, cudaStream_t st) {
+  moe::RouteShape rs{d->n_tok, d->n_exp, d->top_k, d->gate};
+  MOE_CUDA(moe::launch_topk(rs, logits, d->use_bias ? bias : nullptr, topk_idx, topk_w, counts, status, st));
+  MOE_CUDA(moe::launch_offsets(counts, d->n_exp, static_cast<int64_t>(d->n_tok) * d->top_k, offsets, status, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias, float* logits,
+                       int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, void* ws,
+                       size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!all16({x, w_gate, logits}) || !topk_idx || !topk_w || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (d->use_bias && !bias) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* dense = at<int32_t>(ws, L.dense_off);
+  MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
+  if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+  MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
+  GemmArgs g;
+  g.epi = moe::EPI_F32;
+  g.block_n = d->n_exp <= 32 ? 32 : 256;
+  g.a[0] = act(x, d->n_tok, d->d_model);
+  g.b[0] = wstack(w_gate, 1, d->n_exp, d->d_model);
+  g.k0 = d->d_model;
+  g.offsets = dense;
+  g.num_groups = 1;
+  g.max_rows = d->n_tok;
+  g.n_size = d->n_exp;
+  g.out0 = logits;
+  g.ld_out = d->n_exp;
+  g.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+  return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, status, st);
+}
+
+moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, const float* bias,
+                                   int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!logits || !topk_idx || !topk_w || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (d->use_bias && !bias) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
+  if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+  return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, at<int32_t>(ws, L.status), st);
+}
+
+moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                         int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
+                         void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!all16({x, x_perm}) || !topk_idx || !offsets || !row_of_copy || !copy_of_row) return MOE_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  MOE_CUDA(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, at<int32_t>(ws, L.blk_counts),
+                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row,
+                                    at<int32_t>(ws, L.status), st));
+  MOE_CUDA(moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
+                             const moe_expert_weights_t* w, const moe_ffn_saved_t* saved, void* y_perm,
+                             void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!w || !saved || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!all16({x_perm, w->w1, w->w3, w->w2, saved->h, y_perm})) return MOE_ERR_INVALID_ARG;
+  if ((saved->a1 && !aligned16(saved->a1)) || (saved->a3 && !aligned16(saved->a3))) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared) {
+    if (!all16({x, w->ws1, w->ws3, w->ws2, saved->hs, y_shared})) return MOE_ERR_INVALID_ARG;
+    if ((saved->a1s && !aligned16(saved->a1s)) || (saved->a3s && !aligned16(saved->a3s)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  MOE_TRY(ffn_pair(x_perm, R, d->d_model, d->d_ff, d->n_exp, offsets, w->w1, w->w3, w->w2, saved->h, saved->a1,
+                   saved->a3, y_perm, status, st));
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
+    MOE_TRY(ffn_pair(x, d->n_tok, d->d_model, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2, saved->hs,
+                     saved->a1s, saved->a3s, y_shared, status, st));
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_desc_t* d, const void* y_perm, const int32_t* row_of_copy, const float* topk_w,
+                         const void* y_shared, void* out, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (!all16({y_perm, out}) || !row_of_copy || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_combine(d->n_tok, d->d_model, d->top_k, y_perm, row_of_copy, topk_w, y_shared, out,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
+                          const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                          size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, true));
+  if (!w || !s || !g) return MOE_ERR_INVALID_ARG;
+  if (!all16({w_gate, w->w1, w->w3, w->w2, s->x, s->x_perm, s->a1, s->a3, s->h, s->y_perm, dy, g->dx, g->dw_gate,
+              g->dw1, g->dw3, g->dw2}))
+    return MOE_ERR_INVALID_ARG;
+  if (!s->logits || !s->topk_idx || !s->topk_w || !s->offsets || !s->row_of_copy || !s->copy_of_row)
+    return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && !all16({w->ws1, w->ws3, w->ws2, s->a1s, s->a3s, s->hs, g->dws1, g->dws3, g->dws2}))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  const int N = d->n_tok, D = d->d_model, F = d->d_ff, E = d->n_exp, K = d->top_k;
+  const int64_t R = static_cast<int64_t>(N) * K;
+  if (N == 0) {
+    MOE_CUDA(cudaMemsetAsync(g->dw_gate, 0, sizeof(float) * E * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw1, 0, sizeof(float) * E * F * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw3, 0, sizeof(float) * E * F * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw2, 0, sizeof(float) * E * F * D, st));
+    if (d->n_shared) {
+      const size_t fs = d->d_ff_shared;
+      MOE_CUDA(cudaMemsetAsync(g->dws1, 0, sizeof(float) * fs * D, st));
+      MOE_CUDA(cudaMemsetAsync(g->dws3, 0, sizeof(float) * fs * D, st));
+      MOE_CUDA(cudaMemsetAsync(g->dws2, 0, sizeof(float) * fs * D, st));
+    }
+    return MOE_OK;
+  }
+  int32_t* status = at<int32_t>(ws, L.status);
+  float* dl = g->dlogits ? g->dlogits : at<float>(ws, L.dl);
+  float* dg = g->dg ? g->dg : at<float>(ws, L.dg);
+  void* dyw = at<void>(ws, L.dyw);
+  void* da1 = at<void>(ws, L.da1);
+  void* da3 = at<void>(ws, L.da3);
+
+  MOE_CUDA(moe::launch_combine_bwd(N, D, K, d->gate, dy, s->y_perm, s->row_of_copy, s->topk_w, s->logits, E,
+                                   s->topk_idx, dyw, dg, dl, st));
+  // routed experts; dx_perm overwrites dYw once its last reader is done
+  MOE_TRY(ffn_pair_bwd(dyw, s->x_perm, s->a1, s->a3, s->h, R, D, F, E, s->offsets, w->w1, w->w3, w->w2, da1, da3,
+                       dyw, g->dw1, g->dw3, g->dw2, status, st));
+  void* dxs = nullptr;
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, N, st));
+    dxs = at<void>(ws, L.dxs);
+    MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
+                         at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st));
+  }
+  MOE_CUDA(moe::launch_dwgate(E, D, s->offsets, s->copy_of_row, dl, s->x_perm, at<float>(ws, L.dwg), g->dw_gate,
+                              st));
+  MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
+                             void* stream) {
+  MOE_TRY(check_desc(d));
+  if (!counts || !bias || (mode != 0 && mode != 1)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      moe::launch_update_bias(counts, d->n_exp, bias, gamma, mode, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,619 @@
+// Memory-bound kernels of the dropless MoE layer: router top-K with
+// renormalised gate weights and the expert histogram, the exclusive scan of
+// the histogram, the route-bias update, the stable expert-major permutation
+// (maps and 16-byte vectorised row scatter), the gate-weighted combine, and
+// the backward counterparts (combine backward with the router logit
+// gradient, router weight gradient, unpermute-sum of the input gradient).
+//
+// Sources: "LLM Infrastructure Engineering 08: MoE Training Engineering"
+// (quant67): §4.1 softmax top-K gate, §4.3 sigmoid gate with renormalisation,
+// §6.3 bias-adjusted selection and online bias update, §9 simplified MoE
+// layer (gate, loop over experts, index_add_, shared expert, load
+// statistics, update_balance_bias), §12.5 sort by destination / bincount /
+// unsort and K-sum.
+#include "moe_kernels.cuh"
+#include "sm100_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kChunkTok = 128;  // tokens per chunk of the permute
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// Total order of the selection keys: larger value first, equal values by
+// lower expert index, -0.0 == +0.0, NaN below every number.  The key 0 is
+// reserved for "removed".
+__device__ __forceinline__ unsigned long long make_key(float v, int e) {
+  uint32_t u;
+  if (v != v) {
+    u = 0u;                                  // NaN: lowest
+  } else {
+    if (v == 0.0f) v = 0.0f;                 // -0.0 -> +0.0
+    u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ top-K
+// One warp per token; expert e lives in lane e % 32, slot e / 32.
+template <int PL>
+__global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __restrict__ logits,
+                                                   const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w, int32_t* __restrict__ counts) {
+  extern __shared__ int s_hist[];
+  const int E = s.n_exp, K = s.top_k;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t < s.n_tok) {
+    float lg[PL];
+    unsigned long long key[PL];
+    const float* row = logits + static_cast<int64_t>(t) * E;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) {
+        lg[j] = row[e];
+        const float kv = bias ? __fadd_rn(lg[j], bias[e]) : lg[j];
+        key[j] = make_key(kv, e);
+      } else {
+        lg[j] = -INFINITY;
+        key[j] = 0ull;
+      }
+    }
+    int my_e = -1;
+    float my_l = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      unsigned long long best = key[0];
+#pragma unroll
+      for (int j = 1; j < PL; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(kFull, best, o);
+        best = other > best ? other : best;
+      }
+      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+      float le = 0.0f;
+#pragma unroll
+      for (int j = 0; j < PL; ++j) {
+        if (lane + 32 * j == e) {
+          key[j] = 0ull;
+          le = lg[j];
+        }
+      }
+      le = __shfl_sync(kFull, le, e & 31);
+      if (lane == k) {
+        my_e = e;
+        my_l = le;
+      }
+    }
+    float sel;
+    if (s.gate == 0) {
+      // p = softmax over all E in fp32, then p_sel / sum(p_sel)
+      float m = lg[0];
+#pragma unroll
+      for (int j = 1; j < PL; ++j) m = fmaxf(m, lg[j]);
+      m = warp_max(m);
+      float z = 0.0f;
+#pragma unroll
+      for (int j = 0; j < PL; ++j)
+        if (lane + 32 * j < E) z += expf(lg[j] - m);
+      z = warp_sum(z);
+      sel = (lane < K) ? expf(my_l - m) / z : 0.0f;
+    } else {
+      sel = (lane < K) ? 1.0f / (1.0f + expf(-my_l)) : 0.0f;
+    }
+    const float tot = warp_sum(sel);
+    if (lane < K) {
+      topk_idx[static_cast<int64_t>(t) * K + lane] = my_e;
+      topk_w[static_cast<int64_t>(t) * K + lane] = sel / tot;
+      atomicAdd(&s_hist[my_e], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    if (s_hist[i]) atomicAdd(&counts[i], s_hist[i]);
+}
+
+// ------------------------------------------------------------ offsets scan
+__global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E, long long expected,
+                                                       int32_t* __restrict__ offsets, int32_t* status) {
+  __shared__ int warp_tot[32];
+  const int i = threadIdx.x;
+  const int lane = i & 31, w = i >> 5;
+  const int c = i < E ? counts[i] : 0;
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = warp_tot[lane];
+    int inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(kFull, inc, d);
+      if (lane >= d) inc += u;
+    }
+    warp_tot[lane] = inc - v;
+  }
+  __syncthreads();
+  const int val = incl + warp_tot[w];
+  if (i < E) offsets[i + 1] = val;
+  if (i == 0) offsets[0] = 0;
+  if (i == E - 1 && static_cast<long long>(val) != expected && status) atomicOr(status, DEV_BAD_OFFSETS);
+}
+
+// ------------------------------------------------------------ bias update
+__global__ void update_bias_kernel(const int32_t* __restrict__ counts, int E, float* __restrict__ bias, float gamma,
+                                   int mode, float target) {
+  __shared__ long long s_total;
+  if (threadIdx.x == 0) {
+    long long tot = 0;
+    for (int e = 0; e < E; ++e) tot += counts[e];
+    s_total = tot;
+  }
+  __syncthreads();
+  if (s_total == 0) return;  // empty batch: leave the bias unchanged
+  const float total = static_cast<float>(s_total);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float ls = __fdiv_rn(static_cast<float>(counts[e]), total);
+    const float diff = __fsub_rn(ls, target);
+    const float sgn = diff > 0.0f ? 1.0f : (diff < 0.0f ? -1.0f : 0.0f);
+    float step = __fmul_rn(gamma, sgn);
+    if (mode == 0) step = __fmul_rn(step, fmaxf(ls, 1e-6f));
+    bias[e] = __fsub_rn(bias[e], step);
+  }
+}
+
+// ------------------------------------------------------------ permutation
+__global__ void __launch_bounds__(256) block_hist_kernel(int n_tok, int E, int K, const int32_t* __restrict__ idx,
+                                                         int32_t* __restrict__ block_counts, int32_t* status) {
+  extern __shared__ int s_h[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_h[i] = 0;
+  __syncthreads();
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunkTok * K;
+  const int64_t c1 = min(static_cast<int64_t>(n_tok) * K, c0 + static_cast<int64_t>(kChunkTok) * K);
+  for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+    const int e = idx[c];
+    if (e >= 0 && e < E) atomicAdd(&s_h[e], 1);
+    else if (status) atomicOr(status, DEV_BAD_INDEX);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    block_counts[static_cast<int64_t>(blockIdx.x) * E + i] = s_h[i];
+}
+
+__global__ void block_base_kernel(int nchunks, int E, const int32_t* __restrict__ offsets,
+                                  const int32_t* __restrict__ block_counts, int32_t* __restrict__ block_base) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  int run = offsets[e];
+  for (int ch = 0; ch < nchunks; ++ch) {
+    block_base[static_cast<int64_t>(ch) * E + e] = run;
+    run += block_counts[static_cast<int64_t>(ch) * E + e];
+  }
+}
+
+// One warp per chunk of tokens; copies are visited in copy order c = t*K+k,
+// (32/K) tokens per step, so each expert's rows come out in ascending token
+// order (ties of a repeated expert inside one token by ascending k).
+__global__ void __launch_bounds__(32) scatter_maps_kernel(int n_tok, int E, int K, const int32_t* __restrict__ idx,
+                                                          const int32_t* __restrict__ block_base,
+                                                          int32_t* __restrict__ row_of_copy,
+                                                          int32_t* __restrict__ copy_of_row) {
+  extern __shared__ int s_base[];
+  const int lane = threadIdx.x;
+  for (int i = lane; i < E; i += 32) s_base[i] = block_base[static_cast<int64_t>(blockIdx.x) * E + i];
+  __syncwarp();
+  const int t_begin = blockIdx.x * kChunkTok;
+  const int t_end = min(n_tok, t_begin + kChunkTok);
+  const int tpi = 32 / K;
+  for (int t0 = t_begin; t0 < t_end; t0 += tpi) {
+    const int t = t0 + lane / K;
+    const int k = lane - (lane / K) * K;
+    const bool active = (lane < tpi * K) && (t < t_end);
+    const int64_t c = static_cast<int64_t>(t) * K + k;
+    const int e = active ? idx[c] : -1;
+    const bool ok = active && e >= 0 && e < E;
+    const unsigned am = __ballot_sync(kFull, ok);
+    if (ok) {
+      const unsigned m = __match_any_sync(am, e);
+      const int leader = __ffs(m) - 1;
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      int base = 0;
+      if (lane == leader) {
+        base = s_base[e];
+        s_base[e] = base + __popc(m);
+      }
+      base = __shfl_sync(am, base, leader);
+      const int pos = base + rank;
+      row_of_copy[c] = pos;
+      copy_of_row[pos] = static_cast<int32_t>(c);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, int K, const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ row_of_copy,
+                                                           uint4* __restrict__ x_perm) {
+  __shared__ int s_rows[32];
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < K) s_rows[threadIdx.x] = row_of_copy[static_cast<int64_t>(t) * K + threadIdx.x];
+    __syncthreads();
+    const uint4* src = x + static_cast<int64_t>(t) * d8;
+    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
+      const uint4 v = src[i];
+      for (int k = 0; k < K; ++k) x_perm[static_cast<int64_t>(s_rows[k]) * d8 + i] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------ combine
+__global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, const uint4* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ row_of_copy,
+                                                      const float* __restrict__ topk_w,
+                                                      const uint4* __restrict__ y_shared, uint4* __restrict__ out) {
+  __shared__ int s_rows[32];
+  __shared__ float s_w[32];
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < K) {
+      s_rows[threadIdx.x] = row_of_copy[static_cast<int64_t>(t) * K + threadIdx.x];
+      s_w[threadIdx.x] = topk_w[static_cast<int64_t>(t) * K + threadIdx.x];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int k = 0; k < K; ++k) {
+        float y[8];
+        unpack8(y_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], y);
+        const float w = s_w[k];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, y[j], acc[j]);
+      }
+      if (y_shared) {
+        float y[8];
+        unpack8(y_shared[static_cast<int64_t>(t) * d8 + i], y);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += y[j];
+      }
+      out[static_cast<int64_t>(t) * d8 + i] = pack8(acc);
+    }
+  }
+}
+
+// ------------------------------------------------------------ combine backward
+constexpr int kMaxK = 32;
+
+__global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int K, int gate, int E,
+                                                          const uint4* __restrict__ dy,
+                                                          const uint4* __restrict__ y_perm,
+                                                          const int32_t* __restrict__ row_of_copy,
+                                                          const float* __restrict__ topk_w,
+                                                          const float* __restrict__ logits,
+                                                          const int32_t* __restrict__ topk_idx,
+                                                          uint4* __restrict__ dyw, float* __restrict__ dg_out,
+                                                          float* __restrict__ dl_out) {
+  __shared__ int s_rows[kMaxK];
+  __shared__ float s_w[kMaxK];
+  __shared__ float s_part[8][kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < K) {
+      s_rows[threadIdx.x] = row_of_copy[static_cast<int64_t>(t) * K + threadIdx.x];
+      s_w[threadIdx.x] = topk_w[static_cast<int64_t>(t) * K + threadIdx.x];
+    }
+    __syncthreads();
+    float part[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) part[k] = 0.0f;
+    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
+      float g8[8];
+      unpack8(dy[static_cast<int64_t>(t) * d8 + i], g8);
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        if (k < K) {
+          const int64_t r = s_rows[k];
+          float y[8], o[8];
+          unpack8(y_perm[r * d8 + i], y);
+          const float w = s_w[k];
+          float acc = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc = fmaf(g8[j], y[j], acc);
+            o[j] = w * g8[j];
+          }
+          part[k] += acc;
+          dyw[r * d8 + i] = pack8(o);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      if (k < K) {
+        const float v = warp_sum(part[k]);
+        if (lane == 0) s_part[warp][k] = v;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float dgk = 0.0f, gk = 0.0f, lk = 0.0f;
+      if (lane < K) {
+        for (int w = 0; w < 8; ++w) dgk += s_part[w][lane];
+        gk = s_w[lane];
+        if (gate == 1) lk = logits[static_cast<int64_t>(t) * E + topk_idx[static_cast<int64_t>(t) * K + lane]];
+      }
+      const float inner = warp_sum(lane < K ? gk * dgk : 0.0f);
+      float dl = 0.0f;
+      if (gate == 0) {
+        dl = gk * (dgk - inner);
+      } else {
+        const float sg = (lane < K) ? 1.0f / (1.0f + expf(-lk)) : 0.0f;
+        const float ssum = warp_sum(sg);
+        dl = (lane < K) ? sg * (1.0f - sg) / ssum * (dgk - inner) : 0.0f;
+      }
+      if (lane < K) {
+        if (dg_out) dg_out[static_cast<int64_t>(t) * K + lane] = dgk;
+        dl_out[static_cast<int64_t>(t) * K + lane] = dl;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ router weight gradient
+__global__ void __launch_bounds__(256) dwgate_kernel(int E, int d8, int splits, const int32_t* __restrict__ offsets,
+                                                     const int32_t* __restrict__ copy_of_row,
+                                                     const float* __restrict__ dl, const uint4* __restrict__ x_perm,
+                                                     float* __restrict__ out) {
+  const int e = blockIdx.x;
+  const int s = blockIdx.z;
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;
+  if (i >= d8) return;
+  const int lo = offsets[e], hi = offsets[e + 1];
+  const int64_t len = hi - lo;
+  const int r0 = lo + static_cast<int>(len * s / splits);
+  const int r1 = lo + static_cast<int>(len * (s + 1) / splits);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r = r0; r < r1; ++r) {
+    const float w = dl[copy_of_row[r]];
+    float x[8];
+    unpack8(x_perm[static_cast<int64_t>(r) * d8 + i], x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, x[j], acc[j]);
+  }
+  float4* dst = reinterpret_cast<float4*>(out + (static_cast<int64_t>(e) * splits + s) * d8 * 8) + 2 * i;
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+__global__ void reduce_splits_kernel(int E, int d, int splits, const float* __restrict__ partial,
+                                     float* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(E) * d;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i / d, c = i - e * d;
+    float acc = 0.0f;
+    for (int s = 0; s < splits; ++s) acc += partial[(e * splits + s) * d + c];
+    out[i] = acc;
+  }
+}
+
+// ------------------------------------------------------------ unpermute-sum of dx
+__global__ void __launch_bounds__(256) unpermute_dx_kernel(int n_tok, int d8, int K, const uint4* __restrict__ dx_perm,
+                                                           const int32_t* __restrict__ row_of_copy,
+                                                           const float* __restrict__ dl,
+                                                           const int32_t* __restrict__ topk_idx,
+                                                           const uint4* __restrict__ w_gate,
+                                                           const uint4* __restrict__ dx_shared,
+                                                           uint4* __restrict__ dx) {
+  __shared__ int s_rows[32];
+  __shared__ int s_e[32];
+  __shared__ float s_dl[32];
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < K) {
+      const int64_t c = static_cast<int64_t>(t) * K + threadIdx.x;
+      s_rows[threadIdx.x] = row_of_copy[c];
+      s_e[threadIdx.x] = topk_idx[c];
+      s_dl[threadIdx.x] = dl ? dl[c] : 0.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int k = 0; k < K; ++k) {
+        float v[8];
+        unpack8(dx_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += v[j];
+      }
+      if (w_gate && dl) {
+        for (int k = 0; k < K; ++k) {
+          float v[8];
+          unpack8(w_gate[static_cast<int64_t>(s_e[k]) * d8 + i], v);
+          const float w = s_dl[k];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, v[j], acc[j]);
+        }
+      }
+      if (dx_shared) {
+        float v[8];
+        unpack8(dx_shared[static_cast<int64_t>(t) * d8 + i], v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += v[j];
+      }
+      dx[static_cast<int64_t>(t) * d8 + i] = pack8(acc);
+    }
+  }
+}
+
+__global__ void dense_offsets_kernel(int32_t* dst, int n) {
+  if (threadIdx.x == 0) {
+    dst[0] = 0;
+    dst[1] = n;
+  }
+}
+
+int grid_for_tokens(int n_tok) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int g = sms > 0 ? sms * 8 : 1024;
+  return n_tok < g ? (n_tok > 0 ? n_tok : 1) : g;
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* bias, int32_t* topk_idx,
+                        float* topk_w, int32_t* counts, int32_t* status, cudaStream_t st) {
+  (void)status;
+  if (s.n_tok <= 0) return cudaSuccess;
+  const int blocks = (s.n_tok + 7) / 8;
+  const size_t smem = static_cast<size_t>(s.n_exp) * sizeof(int);
+  const int pl = (s.n_exp + 31) / 32;
+#define MOE_TOPK(P) topk_kernel<P><<<blocks, 256, smem, st>>>(s, logits, bias, topk_idx, topk_w, counts)
+  if (pl <= 1) MOE_TOPK(1);
+  else if (pl <= 2) MOE_TOPK(2);
+  else if (pl <= 4) MOE_TOPK(4);
+  else if (pl <= 8) MOE_TOPK(8);
+  else if (pl <= 16) MOE_TOPK(16);
+  else if (pl <= 32) MOE_TOPK(32);
+  else return cudaErrorInvalidValue;
+#undef MOE_TOPK
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
+                           int32_t* status, cudaStream_t st) {
+  if (n_exp > 1024) return cudaErrorInvalidValue;
+  offsets_kernel<<<1, 1024, 0, st>>>(counts, n_exp, static_cast<long long>(expected_total), offsets, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_update_bias(const int32_t* counts, int n_exp, float* bias, float gamma, int mode,
+                               cudaStream_t st) {
+  const float target = static_cast<float>(1.0 / static_cast<double>(n_exp));
+  update_bias_kernel<<<1, 256, 0, st>>>(counts, n_exp, bias, gamma, mode, target);
+  return cudaGetLastError();
+}
+
+int permute_num_chunks(int n_tok) { return (n_tok + kChunkTok - 1) / kChunkTok; }
+
+cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
+                                int32_t* block_counts, int32_t* block_base, int32_t* row_of_copy,
+                                int32_t* copy_of_row, int32_t* status, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  const int nch = permute_num_chunks(n_tok);
+  const size_t smem = static_cast<size_t>(n_exp) * sizeof(int);
+  block_hist_kernel<<<nch, 256, smem, st>>>(n_tok, n_exp, top_k, topk_idx, block_counts, status);
+  block_base_kernel<<<(n_exp + 255) / 256, 256, 0, st>>>(nch, n_exp, offsets, block_counts, block_base);
+  scatter_maps_kernel<<<nch, 32, smem, st>>>(n_tok, n_exp, top_k, topk_idx, block_base, row_of_copy, copy_of_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, const int32_t* row_of_copy,
+                                void* x_perm, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  permute_rows_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(x),
+                                                              row_of_copy, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, const int32_t* row_of_copy,
+                           const float* topk_w, const void* y_shared, void* out, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  combine_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(y_perm),
+                                                         row_of_copy, topk_w, static_cast<const uint4*>(y_shared),
+                                                         static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void* dy, const void* y_perm,
+                               const int32_t* row_of_copy, const float* topk_w, const float* logits, int n_exp,
+                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  if (top_k > kMaxK) return cudaErrorInvalidValue;
+  combine_bwd_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
+      n_tok, d / 8, top_k, gate, n_exp, static_cast<const uint4*>(dy), static_cast<const uint4*>(y_perm),
+      row_of_copy, topk_w, logits, topk_idx, static_cast<uint4*>(dyw), dg, dl);
+  return cudaGetLastError();
+}
+
+// Row splits of the router weight gradient: enough blocks for about two per
+// SM of a 152-SM part.  Independent of the device so that workspace sizes are.
+static int dwgate_splits(int n_exp, int d) {
+  const int colblocks = (d / 8 + 255) / 256;
+  const int base = n_exp * colblocks;
+  int s = (304 + base - 1) / base;
+  return s < 1 ? 1 : (s > 64 ? 64 : s);
+}
+
+size_t dwgate_partial_floats(int n_exp, int d) {
+  const int s = dwgate_splits(n_exp, d);
+  return s > 1 ? static_cast<size_t>(n_exp) * s * d : 0;
+}
+
+cudaError_t launch_dwgate(int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row, const float* dl,
+                          const void* x_perm, float* partial, float* dw_gate, cudaStream_t st) {
+  const int s = dwgate_splits(n_exp, d);
+  const int d8 = d / 8;
+  dim3 grid(n_exp, (d8 + 255) / 256, s);
+  float* dst = s > 1 ? partial : dw_gate;
+  if (s > 1 && !partial) return cudaErrorInvalidValue;
+  dwgate_kernel<<<grid, 256, 0, st>>>(n_exp, d8, s, offsets, copy_of_row, dl, static_cast<const uint4*>(x_perm),
+                                      dst);
+  if (s > 1) reduce_splits_kernel<<<256, 256, 0, st>>>(n_exp, d, s, partial, dw_gate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm, const int32_t* row_of_copy,
+                                const float* dl, const int32_t* topk_idx, const void* w_gate,
+                                const void* dx_shared, void* dx, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  unpermute_dx_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
+      n_tok, d / 8, top_k, static_cast<const uint4*>(dx_perm), row_of_copy, dl, topk_idx,
+      static_cast<const uint4*>(w_gate), static_cast<const uint4*>(dx_shared), static_cast<uint4*>(dx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_offsets(int32_t* dst, int n, cudaStream_t st) {
+  dense_offsets_kernel<<<1, 32, 0, st>>>(dst, n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,55 @@
+// Launchers of the memory-bound kernels of the MoE layer (router top-K,
+// histogram, scan, permute, combine and their backward counterparts).
+// All launches are asynchronous on the given stream and read group sizes
+// only on the device.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+struct RouteShape {
+  int n_tok, n_exp, top_k;
+  int gate;      // 0 softmax, 1 sigmoid
+};
+
+// Per-token top-K over fp32 keys (logits + bias), renormalised weights from
+// the unbiased logits, and the expert histogram (counts must be zeroed).
+cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* bias, int32_t* topk_idx,
+                        float* topk_w, int32_t* counts, int32_t* status, cudaStream_t st);
+// offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]; checks the total.
+cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
+                           int32_t* status, cudaStream_t st);
+// Route-bias update from the histogram (mode 0: listing form, 1: +-gamma).
+cudaError_t launch_update_bias(const int32_t* counts, int n_exp, float* bias, float gamma, int mode,
+                               cudaStream_t st);
+
+// Token chunking of the permute: block_counts/block_base are
+// [num_chunks(n_tok), n_exp] int32 scratch.
+int permute_num_chunks(int n_tok);
+cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
+                                int32_t* block_counts, int32_t* block_base, int32_t* row_of_copy,
+                                int32_t* copy_of_row, int32_t* status, cudaStream_t st);
+// x_perm[row_of_copy[t*K+k]] = x[t] (bf16 rows of d elements).
+cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, const int32_t* row_of_copy,
+                                void* x_perm, cudaStream_t st);
+// out[t] = sum_k g[t,k] * y_perm[row_of_copy[t*K+k]] (+ y_shared[t]), fp32 sum, bf16 store.
+cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, const int32_t* row_of_copy,
+                           const float* topk_w, const void* y_shared, void* out, cudaStream_t st);
+// dYw[row] = bf16(g * dY[t]); dg[t,k] = <dY[t], y_perm[row]>; dl[t,k] = router logit gradient.
+cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void* dy, const void* y_perm,
+                               const int32_t* row_of_copy, const float* topk_w, const float* logits, int n_exp,
+                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st);
+// dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r] (fp32).
+size_t dwgate_partial_floats(int n_exp, int d);
+cudaError_t launch_dwgate(int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row, const float* dl,
+                          const void* x_perm, float* partial, float* dw_gate, cudaStream_t st);
+// dx[t] = sum_k dx_perm[row(t,k)] + sum_k dl[t,k] * W_g[idx[t,k]] (+ dx_shared[t]); bf16 out.
+cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm, const int32_t* row_of_copy,
+                                const float* dl, const int32_t* topk_idx, const void* w_gate,
+                                const void* dx_shared, void* dx, cudaStream_t st);
+// dst[0] = 0, dst[1] = n (device offsets of a single dense group).
+cudaError_t launch_dense_offsets(int32_t* dst, int n, cudaStream_t st);
+
+}  // namespace moe
