@@ -1,0 +1,368 @@
+"""Benchmark of the dropless MoE layer (forward + backward) on GB300.
+
+One step = one pass of the whole hot path over one batch: router (gate GEMM,
+top-K, histogram, scan), permute, grouped SwiGLU FFN, combine, then the
+backward (combine backward, grouped data and weight gradients, router
+gradient, input gradient).  Default workload: the Mixtral-8x7B-shaped layer
+(N=4096 tokens, D=4096, F=14336, E=8, K=2, softmax gate), synthetic seeded
+inputs.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica on its own tokens (the layer has no exchange step on one
+GPU per replica), timing is max over ranks and `value` counts all ranks'
+tokens.  `--impl reference` times the CPU oracle on the machine's host cores on a
+bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s fwd+bwd (grouped-GEMM TFLOP/s, % peak reported alongside), 1 GB300"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--sample", type=int, default=0, help="oracle token sample (0: automatic)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def flops(cfg) -> dict:
+    """Algorithmic FLOPs of one step: 6DF per routed copy forward and 12DF
+    backward (no padding, empty experts cost nothing), the same per token for
+    the shared expert, 2DE / 4DE per token for the router."""
+    n, k, d, f, e = cfg.n_tok, cfg.top_k, cfg.d_model, cfg.d_ff, cfg.n_exp
+    fs = cfg.d_ff_shared * cfg.n_shared
+    return {"ffn_fwd": 6 * n * k * d * f + 6 * n * d * fs, "router_fwd": 2 * n * d * e,
+            "ffn_bwd": 12 * n * k * d * f + 12 * n * d * fs, "router_bwd": 4 * n * d * e}
+
+
+def launches_per_step(cfg) -> int:
+    """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
+    from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
+    fwd = 4 + 4 + 2 + 1          # route: dense offsets, gate GEMM, top-K, scan; permute: 3 map kernels + rows;
+    if cfg.n_shared:             # grouped FFN: GEMM1, GEMM2; combine
+        fwd += 3
+    bwd = 1 + 5 + 1              # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3; unpermute-sum
+    if cfg.n_shared:
+        bwd += 6
+    splits = -(-304 // (cfg.n_exp * (-(-cfg.d_model // 8 // 256))))
+    bwd += 2 if min(max(splits, 1), 64) > 1 else 1   # router weight gradient (+ split reduction)
+    return fwd + bwd
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [line for line in out.splitlines() if line.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a stored ncu capture, or None when absent or
+    when the kernel source has changed since the capture."""
+    path = os.path.join(PROFILES, "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(f"{kernel}@{workload}")
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "ragged_grouped_gemm_gb300", "csrc", rec["source"])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_step_sample(cfg, host, sample_idx, dy_host):
+    """Forward + backward of the CPU oracle on a token sample (its own routing)."""
+    import oracle as O
+    x = host["x"][sample_idx]
+    dy = dy_host[sample_idx]
+    shared = (host["ws1"], host["ws3"], host["ws2"]) if cfg.n_shared else None
+    lg = O.gate_logits(x, host["w_gate"])
+    idx, g = O.route(lg, host.get("bias"), cfg.top_k, cfg.gate)
+    out, saved = O.moe_forward(x, lg, idx, g, host["w1"], host["w3"], host["w2"], shared)
+    O.moe_backward(dy, x, lg, idx, g, host["w_gate"], host["w1"], host["w3"], host["w2"], saved, cfg.gate, shared)
+    return out
+
+
+def time_oracle(cfg, sample: int, steps: int = 1):
+    import numpy as np
+    import torch
+
+    from ragged_grouped_gemm_gb300.inputs import make_dy, make_layer, sample_tokens
+    p = make_layer(cfg, "cpu")
+    host = {k: (v.float().numpy() if v is not None else None) for k, v in p.items()}
+    dy = make_dy(cfg, "cpu").float().numpy()
+    del p
+    idx = sample_tokens(cfg.n_tok, sample).numpy()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle_step_sample(cfg, host, idx, dy)
+        times.append(time.perf_counter() - t0)
+    del torch, np
+    return len(idx), times
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from ragged_grouped_gemm_gb300 import api
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_dy, make_layer
+
+    cfg = CONFIGS[args.workload]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    p = make_layer(cfg, dev)
+    dy = make_dy(cfg, dev)
+    layer = api.MoELayer(cfg, p, train=True, device=dev)
+    b, d, ws = layer.buf, layer.desc, layer.ws
+    x = p["x"]
+    names = ["route", "permute", "grouped_ffn", "combine", "backward"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record()
+        mark(0)
+        api.moe_route(d, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
+                      b["offsets"], ws)
+        mark(1)
+        api.moe_permute(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], ws)
+        mark(2)
+        api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"), p.get("ws3"),
+                            p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"], b["y_perm"],
+                            b["y_shared"], ws)
+        mark(3)
+        api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
+        mark(4)
+        layer.x = x
+        layer.backward(dy)
+        mark(5)
+        if cfg.use_bias:
+            layer.update_bias(1e-3, 0)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bits, site = layer.device_status()
+    if bits:
+        raise RuntimeError(f"device status {bits} at site {site}")
+
+    # --- device-timed fwd+bwd steps (inputs resident in HBM)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0.record()
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1)
+    per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                for j, n in enumerate(names)}
+
+    # --- forward-only steps
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    f0.record()
+    for _ in range(args.steps):
+        layer.forward(x)
+    f1.record()
+    torch.cuda.synchronize()
+    ms_fwd = f0.elapsed_time(f1)
+
+    # --- end to end through the public API with pinned host buffers
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hout = torch.empty(b["out"].shape, dtype=b["out"].dtype).pin_memory()
+    dx_dev, ddy_dev = torch.empty_like(x), torch.empty_like(dy)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        dx_dev.copy_(hx, non_blocking=True)
+        ddy_dev.copy_(hdy, non_blocking=True)
+        layer.forward(dx_dev)
+        layer.backward(ddy_dev)
+        hout.copy_(b["out"], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    bits, site = layer.device_status()
+    if bits:
+        raise RuntimeError(f"device status {bits} at site {site}")
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms, ms_fwd, ms_e2e = max_over_ranks(ms), max_over_ranks(ms_fwd), max_over_ranks(ms_e2e)
+    return cfg, ms, ms_fwd, ms_e2e, per_call, clk.summary(), hx.numel() * 2 + hdy.numel() * 2, hout.numel() * 2
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS
+    cfg = CONFIGS[args.workload]
+    tokens_per_step = cfg.n_tok
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample = args.sample or 64
+        n, times = time_oracle(cfg, sample, steps=args.warmup + args.steps)
+        t = times[args.warmup:] if len(times) > args.warmup else times
+        sec = statistics.mean(t)
+        val = n / sec
+        cores = os.cpu_count()
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * tokens_per_step / n,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "config": {"workload": f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} "
+                                                f"F={cfg.d_ff} E={cfg.n_exp} K={cfg.top_k} {cfg.gate}",
+                                                "sample_tokens": n},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    cfg, ms, ms_fwd, ms_e2e, per_call, clocks, h2d, d2h = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    fl = flops(cfg)
+    peaks = measured_peaks()
+    step_s = ms / 1e3 / args.steps
+    tok_s = world * tokens_per_step / step_s
+    ffn_s = per_call["grouped_ffn"] / 1e3
+    ffn_tflops = fl["ffn_fwd"] / ffn_s / 1e12
+    bwd_s = per_call["backward"] / 1e3
+    peak = peaks["bf16_tflops_sustained"]
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} F={cfg.d_ff} E={cfg.n_exp} "
+                               f"K={cfg.top_k} {cfg.gate}, fwd+bwd",
+                   "l2": "no flush: the 2.8 GB of expert weights streamed every step exceed the 126 MB L2",
+                   "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 dY=9"},
+        "fwd_tokens_per_s": world * tokens_per_step * args.steps / (ms_fwd / 1e3),
+        "grouped_ffn_tflops": ffn_tflops,
+        "backward_tflops": (fl["ffn_bwd"] + fl["router_bwd"]) / bwd_s / 1e12,
+        "per_call_ms": per_call,
+        "roofline": {"bound": "tensor", "kernel": "moe_grouped_ffn (GEMM1 w1|w3+SwiGLU, GEMM2 w2)",
+                     "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s", "frac": ffn_tflops / peak,
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained",
+                     "traffic": recorded_traffic("grouped_ffn", cfg.name)},
+        "e2e": {"value": world * tokens_per_step * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step(cfg) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        sample = args.sample or 64
+        n, times = time_oracle(cfg, sample, steps=1)
+        line["cpu_baseline"] = {"value": n / times[0], "unit": "tokens/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -47,7 +47,6 @@ struct KParams {
   int32_t n_size;
   int32_t kb0, kb1;
   int32_t b_dual_n;
-  int32_t b_3d;
   int32_t tile_n;
   void* out0;
   void* out1;
@@ -219,22 +218,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int src = (kb < p.kb0) ? 0 : 1;
             const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
             tma_load_2d(sA, &p.tmA[src], &full[s], k0, t.row0);
+            // B maps of the ragged-M form are always 3-D: {cols, rows, group}
             if (!B_MN) {
               if (p.b_dual_n) {
                 const int f0 = t.nt * (BN / 2);
                 tma_load_3d(sB, &p.tmB[0], &full[s], k0, f0, t.g);
                 tma_load_3d(sB + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
-              } else if (p.b_3d) {
-                tma_load_3d(sB, &p.tmB[src], &full[s], k0, t.nt * BN, t.g);
               } else {
-                tma_load_2d(sB, &p.tmB[src], &full[s], k0, t.nt * BN);
+                tma_load_3d(sB, &p.tmB[src], &full[s], k0, t.nt * BN, t.g);
               }
             } else {
 #pragma unroll
-              for (int a = 0; a < BN / 64; ++a) {
-                if (p.b_3d) tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
-                else tma_load_2d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0);
-              }
+              for (int a = 0; a < BN / 64; ++a)
+                tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
             }
           } else {
             const int r = t.row0 + kb * BK;
@@ -491,8 +487,9 @@ EncodeFn get_encode_fn() {
 }
 
 // bf16 tensor map with 128-byte swizzle and zero fill out of bounds.
-// 2-D when op.groups == 1: dims {cols, rows}; else 3-D {cols, rows, groups}.
-bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t box_rows) {
+// rank3 == false: 2-D {cols, rows} (op.groups must be 1);
+// rank3 == true : 3-D {cols, rows, groups} (also for a single group).
+bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t box_rows, bool rank3) {
   EncodeFn enc = get_encode_fn();
   if (!enc || !op.ptr) return false;
   if ((reinterpret_cast<uintptr_t>(op.ptr) & 15u) != 0 || (op.ld * 2) % 16 != 0) return false;
@@ -501,8 +498,9 @@ bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t b
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(op.ld) * 2, static_cast<cuuint64_t>(op.group_stride) * 2};
   cuuint32_t box[3] = {box_cols, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  const cuuint32_t rank = op.groups > 1 ? 3 : 2;
-  if (rank == 3 && (op.group_stride * 2) % 16 != 0) return false;
+  if (!rank3 && op.groups != 1) return false;
+  const cuuint32_t rank = rank3 ? 3 : 2;
+  if (rank == 3 && ((op.group_stride * 2) % 16 != 0 || op.group_stride < op.rows * op.ld)) return false;
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(op.ptr), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -570,30 +568,28 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (kp.kb0 <= 0) return cudaErrorInvalidValue;
     const int nsrc = kp.kb1 > 0 ? 2 : 1;
     for (int s = 0; s < nsrc; ++s) {
-      if (!make_map(&kp.tmA[s], a.a[s], 64, BM)) return cudaErrorInvalidValue;
+      if (!make_map(&kp.tmA[s], a.a[s], 64, BM, false)) return cudaErrorInvalidValue;
       if (!a.b_mn) {
-        if (!make_map(&kp.tmB[s], a.b[s], 64, a.b_dual_n ? BN / 2 : BN)) return cudaErrorInvalidValue;
+        if (!make_map(&kp.tmB[s], a.b[s], 64, a.b_dual_n ? BN / 2 : BN, true)) return cudaErrorInvalidValue;
       } else {
-        if (!make_map(&kp.tmB[s], a.b[s], 64, 64)) return cudaErrorInvalidValue;
+        if (!make_map(&kp.tmB[s], a.b[s], 64, 64, true)) return cudaErrorInvalidValue;
       }
     }
     if (a.b_dual_n) {
-      if (a.b_mn || !make_map(&kp.tmB[1], a.b[1], 64, BN / 2)) return cudaErrorInvalidValue;
+      if (a.b_mn || nsrc != 1 || !make_map(&kp.tmB[1], a.b[1], 64, BN / 2, true)) return cudaErrorInvalidValue;
     }
     if (nsrc == 1) {
       kp.tmA[1] = kp.tmA[0];
       if (!a.b_dual_n) kp.tmB[1] = kp.tmB[0];
     }
-    kp.b_3d = a.b[0].groups > 1 ? 1 : 0;
     const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
     tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
   } else {
     if (a.m_size <= 0) return cudaSuccess;
-    if (!make_map(&kp.tmA[0], a.a[0], 64, 64) || !make_map(&kp.tmB[0], a.b[0], 64, 64))
+    if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
       return cudaErrorInvalidValue;
     kp.tmA[1] = kp.tmA[0];
     kp.tmB[1] = kp.tmB[0];
-    kp.b_3d = 0;
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + BN - 1) / BN);
   }
   if (tiles_ub <= 0) return cudaSuccess;
