@@ -78,6 +78,8 @@ def test_full_size_sampled(name):
         cur.append(t)
         cur_e |= es
     groups.append(cur)
+    got = {k: [] for k in ("out", "dx", "dg", "dlogits")}
+    want = {k: [] for k in got}
     for grp in groups:
         grp = np.array(grp)
         used = np.unique(idx[grp])
@@ -86,11 +88,17 @@ def test_full_size_sampled(name):
         w1, w3, w2 = _experts(p["w1"], used), _experts(p["w3"], used), _experts(p["w2"], used)
         o, saved = O.moe_forward(x[grp], lgc, ic, g[grp], w1, w3, w2, shared)
         rg = O.moe_backward(dyh[grp], x[grp], lgc, ic, g[grp], wg[used], w1, w3, w2, saved, cfg.gate, shared)
-        assert rel(np32(out)[grp], o) < BF16_TOL
-        assert rel(np32(gr["dx"])[grp], rg["dx"]) < BF16_TOL
-        assert rel(np32(gr["dg"])[grp], rg["dg"]) < BF16_TOL
-        dl_ref = np.take_along_axis(rg["dlogits"], ic.astype(np.int64), axis=1)
-        assert rel(np32(gr["dlogits"])[grp], dl_ref) < BF16_TOL
+        got["out"].append(np32(out)[grp])
+        want["out"].append(o)
+        got["dx"].append(np32(gr["dx"])[grp])
+        want["dx"].append(rg["dx"])
+        got["dg"].append(np32(gr["dg"])[grp])
+        want["dg"].append(rg["dg"])
+        got["dlogits"].append(np32(gr["dlogits"])[grp])
+        want["dlogits"].append(np.take_along_axis(rg["dlogits"], ic.astype(np.int64), axis=1))
+    # one normwise error over the whole sample (the groups only bound the oracle's memory)
+    for key in got:
+        assert rel(np.concatenate(got[key]), np.concatenate(want[key])) < BF16_TOL, key
 
     # ---- weight gradients of the most loaded expert (K=1 sub-problem of its rows)
     counts = O.histogram(idx, cfg.n_exp)
