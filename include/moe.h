@@ -241,6 +241,29 @@ MOE_API moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const
 MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
                              void* stream);
 
+/* moe_permute without a workspace (no counterpart in the pages; an addition
+ * of this library for callers that cannot allocate).  Same inputs, outputs
+ * and results as moe_permute, for callers that cannot give the library any
+ * device memory of its own: for example a plugin that its host application
+ * calls with nothing but input and output buffers and no allocator, or a
+ * loop running under a fixed memory budget reserved up front, where a new
+ * allocation is not allowed (cudaMalloc may block and synchronise the GPU).
+ * The per-chunk tables moe_permute keeps in the workspace live here in one
+ * fixed 512 KiB device array inside the library, resident on every GPU that
+ * loads it until the process exits.  Limit: ceil(n_tok/128) * n_exp must not
+ * exceed 65536; larger sizes return MOE_ERR_WORKSPACE before anything is
+ * enqueued.  The call allocates nothing.  The first call on each device looks
+ * up the array's device address (with that device current) and caches it,
+ * so make that first call before any stream capture.  All calls share the
+ * one array (it keeps the last call's contents; every call rewrites the
+ * parts it reads): calls whose work may overlap on the GPU race with each
+ * other and must be serialised, e.g. issued on one stream.  Expert indices
+ * outside [0, E) are skipped without a device status report (there is no
+ * workspace to hold one). */
+MOE_API moe_status_t moe_permute_noalloc(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
+                                         const int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row,
+                                         void* x_perm, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

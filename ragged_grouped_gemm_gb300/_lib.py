@@ -62,6 +62,7 @@ SIGNATURES = {
                              ctypes.POINTER(MoeFwdState), c_vp, ctypes.POINTER(MoeGrads), c_vp, ctypes.c_size_t,
                              c_vp]),
     "moe_update_bias": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, ctypes.c_float, c_i32, c_vp]),
+    "moe_permute_noalloc": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
 }
 
 _LIB = None

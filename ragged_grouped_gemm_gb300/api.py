@@ -104,6 +104,17 @@ def moe_permute(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, x_perm, ws
         ws.numel() * ws.element_size(), _s(stream)))
 
 
+def moe_permute_noalloc(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, x_perm, stream=None):
+    """moe_permute for callers that cannot provide a workspace (see moe.h):
+    the chunk tables live in a fixed device array inside the library."""
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_permute_noalloc", _lib.load().moe_permute_noalloc(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(offsets, I32, (e + 1,), "offsets"), _p(row_of_copy, I32, (r,), "row_of_copy"),
+        _p(copy_of_row, I32, (r,), "copy_of_row"), _p(x_perm, BF16, (r, d), "x_perm"), _s(stream)))
+
+
 def moe_grouped_ffn(desc, x_perm, offsets, x, w1, w3, w2, ws1, ws3, ws2, a1, a3, h, a1s, a3s, hs, y_perm,
                     y_shared, ws, stream=None):
     n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
