@@ -41,6 +41,8 @@ constexpr int kABytes = BM * BK * 2;   // 16 KB
 struct KParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  CUtensorMap tmC;       // fp32 output map {n, m, group}, used when c_tma != 0
+  int32_t c_tma;
   const int32_t* offsets;
   int32_t num_groups;
   int32_t m_size;
@@ -64,8 +66,11 @@ struct Cfg {
   static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  // stages | barriers (2S+5) | tmem base, abort | offsets[G+1] | prefix[G+1]
-  static constexpr int kBarOff = kStages * kStageBytes;
+  // stages | epilogue staging (4 warps x 32x32 fp32) | barriers (2S+5) |
+  // tmem base, abort | offsets[G+1] | prefix[G+1]
+  static constexpr int kEpiOff = kStages * kStageBytes;
+  static constexpr int kEpiBytes = 4 * 4096;
+  static constexpr int kBarOff = kEpiOff + kEpiBytes;
   static constexpr int kMiscOff = kBarOff + (2 * kStages + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr size_t smem_bytes(int groups) {
@@ -344,6 +349,38 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           obase += static_cast<int64_t>(t.g) * p.group_stride_out * (EPI == EPI_F32 ? 4 : 2);
         }
         const bool zero = RAGGED_K && t.num_kb == 0;
+        if (EPI == EPI_F32 && p.c_tma) {
+          // Stage this warp's 32 rows x 32 columns in shared memory (128-byte
+          // swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7)) and write
+          // them with one TMA tensor store; the map clips rows and columns
+          // outside the output.
+          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 4096;
+          const uint32_t stg_addr = smem_u32(stg);
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t v[32];
+            if (!zero) {
+              tmem_ld_32x32b_x32(tb + c, v);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0u;
+            }
+            if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(stg_addr + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                           v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (RAGGED_K) tma_store_3d(&p.tmC, stg, t.nt * BN + c, t.mt * BM + q * 32, t.g);
+              else tma_store_3d(&p.tmC, stg, t.nt * BN + c, t.row0 + q * 32, 0);
+              bulk_commit_group();
+            }
+          }
+        } else
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           uint32_t v[16];
@@ -459,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
+    if (EPI == EPI_F32 && lane == 0) bulk_wait_group0();   // every TMA store of this warp has landed
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -505,6 +544,22 @@ bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t b
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// fp32 output map {n, m, groups} with a 32x32 box and 128-byte swizzle, for
+// the TMA-store epilogue.  False when the layout is not TMA-compatible.
+bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_t groups, int64_t ld,
+                      int64_t group_stride) {
+  EncodeFn enc = get_encode_fn();
+  if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  if ((ld * 4) % 16 != 0 || (group_stride * 4) % 16 != 0 || group_stride < m * ld) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(group_stride) * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
@@ -593,6 +648,13 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + BN - 1) / BN);
   }
   if (tiles_ub <= 0) return cudaSuccess;
+  // fp32 outputs go through TMA stores when every tile's rows either belong to
+  // its own output matrix (weight gradients) or end at the tensor's end (one group)
+  if (a.epi == EPI_F32 && (a.ragged_k || a.num_groups == 1)) {
+    const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
+    const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
+    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs) ? 1 : 0;
+  }
   const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
 
   if (BN == 32) return launch_impl<32, false, false, EPI_F32>(kp, grid, stream);

@@ -62,6 +62,9 @@ CONFIGS = {
     "mixtral": MoEConfig("mixtral", 4096, 4096, 14336, 8, 2),
     "dsv3": MoEConfig("dsv3", 4096, 7168, 2048, 256, 8, gate="sigmoid", use_bias=True,
                       n_shared=1, d_ff_shared=2048, bias_beta=0.55, n_cold=4),
+    # profiling case: the Mixtral layer with a quarter of d_ff (about 3 GB on
+    # the device, operands still far larger than L2)
+    "mixtral_quarter": MoEConfig("mixtral_quarter", 4096, 4096, 3584, 8, 2),
     # mid-size parity cases: several tiles in every GEMM dimension, ragged tails
     "small_softmax": MoEConfig("small_softmax", 1000, 256, 384, 8, 2),
     "small_sigmoid": MoEConfig("small_sigmoid", 777, 512, 256, 16, 4, gate="sigmoid",
