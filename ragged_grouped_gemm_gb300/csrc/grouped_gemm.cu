@@ -90,16 +90,20 @@ template <bool RAGGED_K, int BN>
 __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const int* s_off, const int* s_pre) {
   Tile t;
   if (!RAGGED_K) {
-    const int total_m = s_pre[p.num_groups];
-    t.nt = tile / total_m;
-    const int rem = tile - t.nt * total_m;
+    // Expert-major raster: expert, then N tile, then M tile (innermost), so the
+    // CTAs running at once share one expert's rows of A (L2-resident) and each
+    // weight block is streamed from HBM once.  s_pre holds the prefix of
+    // per-expert tile counts mtiles_g * ntiles.
     int lo = 0, hi = p.num_groups;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_pre[mid] <= rem) lo = mid; else hi = mid;
+      if (s_pre[mid] <= tile) lo = mid; else hi = mid;
     }
     t.g = lo;
-    t.mt = rem - s_pre[lo];
+    const int mtiles = max(0, s_off[lo + 1] - s_off[lo] + BM - 1) / BM;
+    const int rem = tile - s_pre[lo];
+    t.nt = rem / mtiles;
+    t.mt = rem - t.nt * mtiles;
     t.row0 = s_off[lo] + t.mt * BM;
     t.rows_valid = min(BM, s_off[lo + 1] - t.row0);
     t.k_rows = 0;
@@ -170,15 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
-  // group offsets and (ragged M) the prefix of per-group 128-row tile counts
+  // group offsets and (ragged M) the prefix of per-group tile counts
+  // (128-row M tiles times N tiles)
   for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
   if (!RAGGED_K && warp == 0) {
+    const int ntiles = (p.n_size + p.tile_n - 1) / p.tile_n;
     const int per = (G + 31) / 32;
     const int lo = lane * per;
     const int hi = min(G, lo + per);
     int sum = 0;
-    for (int g = lo; g < hi; ++g) sum += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    for (int g = lo; g < hi; ++g) sum += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM * ntiles;
     int incl = sum;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     int run = incl - sum;
     for (int g = lo; g < hi; ++g) {
       s_pre[g] = run;
-      run += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM;
+      run += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM * ntiles;
     }
     if (lane == 31) s_pre[G] = incl;
   }
@@ -199,8 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   int total_tiles;
   if (!RAGGED_K) {
-    const int ntiles = (p.n_size + p.tile_n - 1) / p.tile_n;
-    total_tiles = s_pre[G] * ntiles;
+    total_tiles = s_pre[G];
   } else {
     total_tiles = G * ((p.m_size + BM - 1) / BM) * ((p.n_size + BN - 1) / BN);
   }
