@@ -55,6 +55,29 @@ def flops(cfg) -> dict:
             "ffn_bwd": 12 * n * k * d * f + 12 * n * d * fs, "router_bwd": 4 * n * d * e}
 
 
+def ffn_bytes(cfg, nonempty: int) -> int:
+    """Algorithmic HBM bytes of one moe_grouped_ffn call (training forward):
+    GEMM1 reads x_perm and w1, w3 of the experts that received tokens and
+    writes h, a1, a3; GEMM2 reads h and w2 and writes y_perm; the shared expert
+    does the same over all tokens."""
+    n, k, d, f = cfg.n_tok, cfg.top_k, cfg.d_model, cfg.d_ff
+    r = n * k
+    b = 2 * (r * d + 2 * nonempty * f * d + 3 * r * f)          # GEMM1
+    b += 2 * (r * f + nonempty * d * f + r * d)                 # GEMM2
+    if cfg.n_shared:
+        fs = cfg.d_ff_shared
+        b += 2 * (n * d + 2 * fs * d + 3 * n * fs) + 2 * (n * fs + d * fs + n * d)
+    return b
+
+
+def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, reduce_max) -> tuple[float, float]:
+    """Whole-job throughput of `world` replicas: every rank processes
+    `tokens_per_step` tokens per step; the job takes the slowest rank's time.
+    Returns (tokens/s over all ranks, max milliseconds)."""
+    ms = reduce_max(ms_local) if world > 1 else ms_local
+    return world * tokens_per_step * steps / (ms / 1e3), ms
+
+
 def launches_per_step(cfg) -> int:
     """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
     from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
@@ -66,7 +89,7 @@ def launches_per_step(cfg) -> int:
         bwd += 6
     splits = -(-304 // (cfg.n_exp * (-(-cfg.d_model // 8 // 256))))
     bwd += 2 if min(max(splits, 1), 64) > 1 else 1   # router weight gradient (+ split reduction)
-    return fwd + bwd
+    return fwd + bwd + (1 if cfg.use_bias else 0)      # route-bias update
 
 
 class ClockSampler:
@@ -278,14 +301,16 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {bits} at site {site}")
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
         t = torch.tensor([v], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    ms, ms_fwd, ms_e2e = max_over_ranks(ms), max_over_ranks(ms_fwd), max_over_ranks(ms_e2e)
-    return cfg, ms, ms_fwd, ms_e2e, per_call, clk.summary(), hx.numel() * 2 + hdy.numel() * 2, hout.numel() * 2
+    nonempty = int((b["counts"] > 0).sum().item())
+    res = {"cfg": cfg, "per_call": per_call, "clocks": clk.summary(), "nonempty": nonempty,
+           "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2}
+    for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
+        res[key] = aggregate(world, cfg.n_tok, args.steps, v, max_over_ranks)
+    return res
 
 
 def main():
@@ -322,39 +347,50 @@ def main():
     import torch.distributed as dist
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    cfg, ms, ms_fwd, ms_e2e, per_call, clocks, h2d, d2h = run_ours(args, rank, world, local_rank)
+    res = run_ours(args, rank, world, local_rank)
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return
+    cfg, per_call = res["cfg"], res["per_call"]
+    tok_s, ms = res["step"]
     fl = flops(cfg)
     peaks = measured_peaks()
-    step_s = ms / 1e3 / args.steps
-    tok_s = world * tokens_per_step / step_s
     ffn_s = per_call["grouped_ffn"] / 1e3
     ffn_tflops = fl["ffn_fwd"] / ffn_s / 1e12
+    ffn_b = ffn_bytes(cfg, res["nonempty"])
     bwd_s = per_call["backward"] / 1e3
     peak = peaks["bf16_tflops_sustained"]
+    wbytes = 2 * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
+    # the binding roof of the grouped FFN: tensor time vs HBM time at the measured peaks
+    if fl["ffn_fwd"] / (peak * 1e12) >= ffn_b / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": ffn_tflops / peak, "peak_source": f"{peaks['source']} bf16_tflops_sustained"}
+    else:
+        gbs = ffn_b / ffn_s / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} hbm_gbs"}
+    roof.update(kernel="moe_grouped_ffn (GEMM1 w1|w3+SwiGLU, GEMM2 w2)", algorithmic_bytes=ffn_b,
+                algorithmic_flops=fl["ffn_fwd"], traffic=recorded_traffic("grouped_ffn", cfg.name))
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} F={cfg.d_ff} E={cfg.n_exp} "
-                               f"K={cfg.top_k} {cfg.gate}, fwd+bwd",
-                   "l2": "no flush: the 2.8 GB of expert weights streamed every step exceed the 126 MB L2",
-                   "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 dY=9"},
-        "fwd_tokens_per_s": world * tokens_per_step * args.steps / (ms_fwd / 1e3),
+                               f"K={cfg.top_k} {cfg.gate}" + (" +route bias" if cfg.use_bias else "")
+                               + (f" +shared Fs={cfg.d_ff_shared}" if cfg.n_shared else "") + ", fwd+bwd",
+                   "l2": f"no flush: the {wbytes / 1e9:.1f} GB of expert weights streamed every step exceed "
+                         "the 126 MB L2",
+                   "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 shared=6/7/8 dY=9"},
+        "fwd_tokens_per_s": res["fwd"][0],
         "grouped_ffn_tflops": ffn_tflops,
         "backward_tflops": (fl["ffn_bwd"] + fl["router_bwd"]) / bwd_s / 1e12,
         "per_call_ms": per_call,
-        "roofline": {"bound": "tensor", "kernel": "moe_grouped_ffn (GEMM1 w1|w3+SwiGLU, GEMM2 w2)",
-                     "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s", "frac": ffn_tflops / peak,
-                     "peak_source": f"{peaks['source']} bf16_tflops_sustained",
-                     "traffic": recorded_traffic("grouped_ffn", cfg.name)},
-        "e2e": {"value": world * tokens_per_step * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": roof,
+        "e2e": {"value": res["e2e"][0], "unit": "tokens/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": launches_per_step(cfg) * args.steps,
-        "clocks": clocks,
+        "clocks": res["clocks"],
     }
     if not args.no_cpu_baseline:
         sample = args.sample or 64
