@@ -1,6 +1,6 @@
 // Persistent, warp-specialised tcgen05 grouped GEMM for sm_103a.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer: one lane streams A/B k-blocks into a ring of
 //               shared-memory stages (128-byte swizzle), signalled by
 //               mbarriers with transaction counts.
@@ -8,8 +8,9 @@
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into a
 //               double-buffered fp32 accumulator in tensor memory and commits
 //               stage releases and accumulator hand-offs to mbarriers.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31 = tile rows), apply the fused epilogue and store.
+//   warps 2..9  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31 = tile rows, and half (w-2)/4 of the columns),
+//               apply the fused epilogue and store.
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
 // main loop of tile i+1.  Tiles are walked in a persistent loop; for the
 // ragged-M form the tile list is derived on the device from the group
@@ -34,7 +35,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 1024;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 
@@ -43,6 +45,7 @@ struct KParams {
   CUtensorMap tmB[2];
   CUtensorMap tmC;       // fp32 output map {n, m, group}, used when c_tma != 0
   int32_t c_tma;
+  int32_t c_rows;        // rows of the output map (ragged M, one group)
   const int32_t* offsets;
   int32_t num_groups;
   int32_t m_size;
@@ -66,7 +69,7 @@ struct Cfg {
   static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  // stages | epilogue staging (4 warps x 32x32 fp32) | barriers (2S+5) |
+  // stages | epilogue staging (8 warps x 32x16 fp32) | barriers (2S+5) |
   // tmem base, abort | offsets[G+1] | prefix[G+1]
   static constexpr int kEpiOff = kStages * kStageBytes;
   static constexpr int kEpiBytes = 4 * 4096;
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], kEpiThreads);
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -333,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;           // TMEM lane quarter = tile rows 32q..32q+31
+    const int hf = (warp - 2) >> 2;   // column half of the tile
     const int r = q * 32 + lane;
     uint32_t tcount = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
@@ -354,70 +358,87 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           obase += static_cast<int64_t>(t.g) * p.group_stride_out * (EPI == EPI_F32 ? 4 : 2);
         }
         const bool zero = RAGGED_K && t.num_kb == 0;
+        const int c_begin = hf * (BN / 2);
         if (EPI == EPI_F32 && p.c_tma) {
-          // Stage this warp's 32 rows x 32 columns in shared memory (128-byte
-          // swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7)) and write
-          // them with one TMA tensor store; the map clips rows and columns
-          // outside the output.
-          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 4096;
+          // Stage this warp's 32 rows x 16 columns in a 2 KB shared-memory
+          // buffer (64-byte swizzle: 16-byte chunk j of row r at chunk
+          // j ^ ((r >> 1) & 3)) and write them with a TMA tensor store, which
+          // clips rows and columns outside the output.  The TMEM load of the
+          // next chunk is in flight while this one is staged.
+          constexpr int NCH = BN / 32;
+          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
           const uint32_t stg_addr = smem_u32(stg);
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            uint32_t v[32];
-            if (!zero) {
-              tmem_ld_32x32b_x32(tb + c, v);
-              tmem_wait_ld();
-            } else {
+          uint32_t va[16], vb[16];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = 0u;
-            }
+          for (int j = 0; j < 16; ++j) va[j] = vb[j] = 0u;
+          if (!zero) {
+            tmem_ld_32x32b_x16(tb + c_begin, va);
+            tmem_wait_ld(va);
+          }
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            if (!zero && i + 1 < NCH) tmem_ld_32x32b_x16(tb + c_begin + 16 * (i + 1), vb);
             if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
             __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(stg_addr + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                           v[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+              st_shared_v4(stg_addr + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), va[4 * j], va[4 * j + 1],
+                           va[4 * j + 2], va[4 * j + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (RAGGED_K) tma_store_3d(&p.tmC, stg, t.nt * BN + c, t.mt * BM + q * 32, t.g);
-              else tma_store_3d(&p.tmC, stg, t.nt * BN + c, t.row0 + q * 32, 0);
-              bulk_commit_group();
+              // boxes that start past the output's last column or row hold nothing to write
+              const int col = t.nt * BN + c_begin + 16 * i;
+              const int row = RAGGED_K ? t.mt * BM + q * 32 : t.row0 + q * 32;
+              const int rows = RAGGED_K ? p.m_size : p.c_rows;
+              if (col < p.n_size && row < rows) {
+                tma_store_3d(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0);
+                bulk_commit_group();
+              }
+            }
+            if (i + 1 < NCH) {
+              if (!zero) tmem_wait_ld(vb);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) va[j] = vb[j];
             }
           }
-        } else
+        } else {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          if (!zero) {
-            tmem_ld_32x32b_x16(tb + c, v);
-            tmem_wait_ld();
-          } else {
+          for (int c = c_begin; c < c_begin + BN / 2; c += 16) {
+            uint32_t v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0u;
-          }
-          const int col = t.nt * BN + c;
-          if (row_ok && col < p.n_size) {
-            const int nvalid = min(16, p.n_size - col);
-            if (EPI == EPI_F32) {
-              float* dst = reinterpret_cast<float*>(obase) + grow * p.ld_out + col;
-              if (nvalid == 16 && (p.ld_out & 3) == 0) {
+            if (!zero) {
+              tmem_ld_32x32b_x16(tb + c, v);
+              tmem_wait_ld(v);
+            }
+            const int col = t.nt * BN + c;
+            if (row_ok && col < p.n_size) {
+              const int nvalid = min(16, p.n_size - col);
+              if (EPI == EPI_F32) {
+                float* dst = reinterpret_cast<float*>(obase) + grow * p.ld_out + col;
+                if (nvalid == 16 && (p.ld_out & 3) == 0) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  reinterpret_cast<uint4*>(dst)[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-              } else {
-                for (int j = 0; j < nvalid; ++j) dst[j] = __uint_as_float(v[j]);
-              }
-            } else {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(obase) + grow * p.ld_out + col;
-              uint32_t w[8];
+                  for (int j = 0; j < 4; ++j)
+                    reinterpret_cast<uint4*>(dst)[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-              if (nvalid == 16) {
-                reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                  for (int j = 0; j < 16; ++j)
+                    if (j < nvalid) dst[j] = __uint_as_float(v[j]);
+                }
               } else {
-                for (int j = 0; j < nvalid; ++j) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(obase) + grow * p.ld_out + col;
+                uint32_t w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                if (nvalid == 16) {
+                  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    if (j < nvalid) dst[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                }
               }
             }
           }
@@ -426,11 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int64_t grow = t.row0 + r;
         const int f0 = t.nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 16) {
+        for (int c = hf * (BN / 4); c < (hf + 1) * (BN / 4); c += 16) {
           uint32_t u[16], v[16];
           tmem_ld_32x32b_x16(tb + c, u);
           tmem_ld_32x32b_x16(tb + BN / 2 + c, v);
-          tmem_wait_ld();
+          tmem_wait_ld(u);
+          reg_fence(v);
           const int col = f0 + c;
           if (row_ok && col < p.n_size) {
             uint32_t hw[8], aw[8], bw[8];
@@ -461,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       } else {  // EPI_SWIGLU_BWD
         const int64_t grow = t.row0 + r;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = hf * (BN / 2); c < (hf + 1) * (BN / 2); c += 16) {
           uint32_t u[16];
           tmem_ld_32x32b_x16(tb + c, u);
-          tmem_wait_ld();
+          tmem_wait_ld(u);
           const int col = t.nt * BN + c;
           if (row_ok && col < p.n_size) {
             const int64_t off = grow * p.ld_out + col;
@@ -478,13 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int j = 0; j < 8; ++j) {
               float o1[2], o3[2];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float dh = __uint_as_float(u[2 * j + h]);
-                const float a1 = h ? bf16hi(aw[j]) : bf16lo(aw[j]);
-                const float a3 = h ? bf16hi(bw[j]) : bf16lo(bw[j]);
+              for (int hh = 0; hh < 2; ++hh) {
+                const float dh = __uint_as_float(u[2 * j + hh]);
+                const float a1 = hh ? bf16hi(aw[j]) : bf16lo(aw[j]);
+                const float a3 = hh ? bf16hi(bw[j]) : bf16lo(bw[j]);
                 const float sg = sigmoidf_fast(a1);
-                o3[h] = dh * a1 * sg;
-                o1[h] = dh * a3 * sg * (1.0f + a1 * (1.0f - sg));
+                o3[hh] = dh * a1 * sg;
+                o1[hh] = dh * a3 * sg * (1.0f + a1 * (1.0f - sg));
               }
               d1[j] = pack_bf16x2(o1[0], o1[1]);
               d3[j] = pack_bf16x2(o3[0], o3[1]);
@@ -551,7 +573,7 @@ bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t b
   return r == CUDA_SUCCESS;
 }
 
-// fp32 output map {n, m, groups} with a 32x32 box and 128-byte swizzle, for
+// fp32 output map {n, m, groups} with a 16x32 box and 64-byte swizzle, for
 // the TMA-store epilogue.  False when the layout is not TMA-compatible.
 bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_t groups, int64_t ld,
                       int64_t group_stride) {
@@ -560,10 +582,10 @@ bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_
   if ((ld * 4) % 16 != 0 || (group_stride * 4) % 16 != 0 || group_stride < m * ld) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(groups)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(group_stride) * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {16, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -659,6 +681,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
     const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
     kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs) ? 1 : 0;
+    kp.c_rows = static_cast<int32_t>(m);
   }
   const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
 

@@ -397,26 +397,58 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
 }
 
 // ------------------------------------------------------------ router weight gradient
+// Block = (expert e, 2048-column slice, row split s); each thread owns 8
+// columns.  The rows' logit gradients are staged in shared memory 256 at a
+// time, and rows are consumed four at a time so their loads are in flight
+// together.  Fixed summation order: deterministic.
 __global__ void __launch_bounds__(256) dwgate_kernel(int E, int d8, int splits, const int32_t* __restrict__ offsets,
                                                      const int32_t* __restrict__ copy_of_row,
                                                      const float* __restrict__ dl, const uint4* __restrict__ x_perm,
                                                      float* __restrict__ out) {
+  __shared__ float s_w[256];
   const int e = blockIdx.x;
   const int s = blockIdx.z;
   const int i = blockIdx.y * blockDim.x + threadIdx.x;
-  if (i >= d8) return;
+  const bool col_ok = i < d8;
   const int lo = offsets[e], hi = offsets[e + 1];
   const int64_t len = hi - lo;
   const int r0 = lo + static_cast<int>(len * s / splits);
   const int r1 = lo + static_cast<int>(len * (s + 1) / splits);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int r = r0; r < r1; ++r) {
-    const float w = dl[copy_of_row[r]];
-    float x[8];
-    unpack8(x_perm[static_cast<int64_t>(r) * d8 + i], x);
+  for (int c0 = r0; c0 < r1; c0 += 256) {
+    const int n = min(256, r1 - c0);
+    __syncthreads();
+    if (threadIdx.x < n) s_w[threadIdx.x] = dl[copy_of_row[c0 + threadIdx.x]];
+    __syncthreads();
+    if (!col_ok) continue;
+    const uint4* src = x_perm + static_cast<int64_t>(c0) * d8 + i;
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {
+      const uint4 v0 = src[static_cast<int64_t>(j) * d8];
+      const uint4 v1 = src[static_cast<int64_t>(j + 1) * d8];
+      const uint4 v2 = src[static_cast<int64_t>(j + 2) * d8];
+      const uint4 v3 = src[static_cast<int64_t>(j + 3) * d8];
+      float x0[8], x1[8], x2[8], x3[8];
+      unpack8(v0, x0);
+      unpack8(v1, x1);
+      unpack8(v2, x2);
+      unpack8(v3, x3);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, x[j], acc[j]);
+      for (int q = 0; q < 8; ++q) {
+        acc[q] = fmaf(s_w[j], x0[q], acc[q]);
+        acc[q] = fmaf(s_w[j + 1], x1[q], acc[q]);
+        acc[q] = fmaf(s_w[j + 2], x2[q], acc[q]);
+        acc[q] = fmaf(s_w[j + 3], x3[q], acc[q]);
+      }
+    }
+    for (; j < n; ++j) {
+      float x[8];
+      unpack8(src[static_cast<int64_t>(j) * d8], x);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_w[j], x[q], acc[q]);
+    }
   }
+  if (!col_ok) return;
   float4* dst = reinterpret_cast<float4*>(out + (static_cast<int64_t>(e) * splits + s) * d8 * 8) + 2 * i;
   dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
