@@ -87,8 +87,7 @@ def launches_per_step(cfg) -> int:
     bwd = 1 + 5 + 1              # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3; unpermute-sum
     if cfg.n_shared:
         bwd += 6
-    splits = -(-304 // (cfg.n_exp * (-(-cfg.d_model // 8 // 256))))
-    bwd += 2 if min(max(splits, 1), 64) > 1 else 1   # router weight gradient (+ split reduction)
+    bwd += 3                     # router weight gradient: chunk prefix, chunk partials, reduction
     return fwd + bwd + (1 if cfg.use_bias else 0)      # route-bias update
 
 

@@ -41,7 +41,7 @@ WsLayout layout(const moe_desc_t& d) {
   L.da1s = o; o = align_up(o + N * Fs * 2);
   L.da3s = o; o = align_up(o + N * Fs * 2);
   L.dxs = o; o = align_up(o + (Fs ? N * D * 2 : 0));
-  L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_exp, d.d_model) * 4);
+  L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_tok, d.top_k, d.n_exp, d.d_model) * 4);
   L.total = o;
   return L;
 }
@@ -417,8 +417,8 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
                          at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st));
   }
-  MOE_CUDA(moe::launch_dwgate(E, D, s->offsets, s->copy_of_row, dl, s->x_perm, at<float>(ws, L.dwg), g->dw_gate,
-                              st));
+  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, at<float>(ws, L.dwg),
+                              g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
 }

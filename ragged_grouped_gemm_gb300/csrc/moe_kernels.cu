@@ -397,73 +397,106 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
 }
 
 // ------------------------------------------------------------ router weight gradient
-// Block = (expert e, 2048-column slice, row split s); each thread owns 8
-// columns.  The rows' logit gradients are staged in shared memory 256 at a
-// time, and rows are consumed four at a time so their loads are in flight
-// together.  Fixed summation order: deterministic.
-__global__ void __launch_bounds__(256) dwgate_kernel(int E, int d8, int splits, const int32_t* __restrict__ offsets,
-                                                     const int32_t* __restrict__ copy_of_row,
-                                                     const float* __restrict__ dl, const uint4* __restrict__ x_perm,
-                                                     float* __restrict__ out) {
-  __shared__ float s_w[256];
-  const int e = blockIdx.x;
-  const int s = blockIdx.z;
-  const int i = blockIdx.y * blockDim.x + threadIdx.x;
-  const bool col_ok = i < d8;
-  const int lo = offsets[e], hi = offsets[e + 1];
-  const int64_t len = hi - lo;
-  const int r0 = lo + static_cast<int>(len * s / splits);
-  const int r1 = lo + static_cast<int>(len * (s + 1) / splits);
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int c0 = r0; c0 < r1; c0 += 256) {
-    const int n = min(256, r1 - c0);
-    __syncthreads();
-    if (threadIdx.x < n) s_w[threadIdx.x] = dl[copy_of_row[c0 + threadIdx.x]];
-    __syncthreads();
-    if (!col_ok) continue;
-    const uint4* src = x_perm + static_cast<int64_t>(c0) * d8 + i;
-    int j = 0;
-    for (; j + 4 <= n; j += 4) {
-      const uint4 v0 = src[static_cast<int64_t>(j) * d8];
-      const uint4 v1 = src[static_cast<int64_t>(j + 1) * d8];
-      const uint4 v2 = src[static_cast<int64_t>(j + 2) * d8];
-      const uint4 v3 = src[static_cast<int64_t>(j + 3) * d8];
-      float x0[8], x1[8], x2[8], x3[8];
-      unpack8(v0, x0);
-      unpack8(v1, x1);
-      unpack8(v2, x2);
-      unpack8(v3, x3);
+// dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r].
+// Ragged and deterministic: every expert's rows are cut into 64-row chunks
+// (chunk list derived on the device from the offsets), each chunk's partial
+// sum is written once, and the partials of an expert are added in chunk order.
+constexpr int kDwgChunk = 64;
+
+__global__ void dwg_chunk_prefix_kernel(int E, const int32_t* __restrict__ offsets, int32_t* __restrict__ cpre) {
+  // single warp: prefix of ceil(m_e / 64) over the experts
+  const int lane = threadIdx.x;
+  const int per = (E + 31) / 32;
+  const int lo = lane * per, hi = min(E, lo + per);
+  int sum = 0;
+  for (int e = lo; e < hi; ++e) sum += max(0, offsets[e + 1] - offsets[e] + kDwgChunk - 1) / kDwgChunk;
+  int incl = sum;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        acc[q] = fmaf(s_w[j], x0[q], acc[q]);
-        acc[q] = fmaf(s_w[j + 1], x1[q], acc[q]);
-        acc[q] = fmaf(s_w[j + 2], x2[q], acc[q]);
-        acc[q] = fmaf(s_w[j + 3], x3[q], acc[q]);
-      }
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  int run = incl - sum;
+  for (int e = lo; e < hi; ++e) {
+    cpre[e] = run;
+    run += max(0, offsets[e + 1] - offsets[e] + kDwgChunk - 1) / kDwgChunk;
+  }
+  if (lane == 31) cpre[E] = incl;
+}
+
+__global__ void __launch_bounds__(256) dwg_partial_kernel(int E, int d8, const int32_t* __restrict__ offsets,
+                                                          const int32_t* __restrict__ cpre,
+                                                          const int32_t* __restrict__ copy_of_row,
+                                                          const float* __restrict__ dl,
+                                                          const uint4* __restrict__ x_perm,
+                                                          float* __restrict__ partial) {
+  __shared__ float s_w[kDwgChunk];
+  __shared__ int s_e;
+  const int c = blockIdx.x;
+  if (c >= cpre[E]) return;                      // uniform across the block
+  if (threadIdx.x == 0) {
+    int lo = 0, hi = E;                          // largest e with cpre[e] <= c
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cpre[mid] <= c) lo = mid; else hi = mid;
     }
-    for (; j < n; ++j) {
-      float x[8];
-      unpack8(src[static_cast<int64_t>(j) * d8], x);
+    s_e = lo;
+  }
+  __syncthreads();
+  const int e = s_e;
+  const int r0 = offsets[e] + (c - cpre[e]) * kDwgChunk;
+  const int n = min(kDwgChunk, offsets[e + 1] - r0);
+  if (threadIdx.x < n) s_w[threadIdx.x] = dl[copy_of_row[r0 + threadIdx.x]];
+  __syncthreads();
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;
+  if (i >= d8) return;
+  const uint4* src = x_perm + static_cast<int64_t>(r0) * d8 + i;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int j = 0;
+  for (; j + 4 <= n; j += 4) {
+    const uint4 v0 = src[static_cast<int64_t>(j) * d8];
+    const uint4 v1 = src[static_cast<int64_t>(j + 1) * d8];
+    const uint4 v2 = src[static_cast<int64_t>(j + 2) * d8];
+    const uint4 v3 = src[static_cast<int64_t>(j + 3) * d8];
+    float x0[8], x1[8], x2[8], x3[8];
+    unpack8(v0, x0);
+    unpack8(v1, x1);
+    unpack8(v2, x2);
+    unpack8(v3, x3);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_w[j], x[q], acc[q]);
+    for (int q = 0; q < 8; ++q) {
+      acc[q] = fmaf(s_w[j], x0[q], acc[q]);
+      acc[q] = fmaf(s_w[j + 1], x1[q], acc[q]);
+      acc[q] = fmaf(s_w[j + 2], x2[q], acc[q]);
+      acc[q] = fmaf(s_w[j + 3], x3[q], acc[q]);
     }
   }
-  if (!col_ok) return;
-  float4* dst = reinterpret_cast<float4*>(out + (static_cast<int64_t>(e) * splits + s) * d8 * 8) + 2 * i;
+  for (; j < n; ++j) {
+    float x[8];
+    unpack8(src[static_cast<int64_t>(j) * d8], x);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_w[j], x[q], acc[q]);
+  }
+  float4* dst = reinterpret_cast<float4*>(partial + static_cast<int64_t>(c) * d8 * 8) + 2 * i;
   dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-__global__ void reduce_splits_kernel(int E, int d, int splits, const float* __restrict__ partial,
-                                     float* __restrict__ out) {
-  const int64_t n = static_cast<int64_t>(E) * d;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t e = i / d, c = i - e * d;
-    float acc = 0.0f;
-    for (int s = 0; s < splits; ++s) acc += partial[(e * splits + s) * d + c];
-    out[i] = acc;
+__global__ void __launch_bounds__(256) dwg_reduce_kernel(int E, int d, const int32_t* __restrict__ cpre,
+                                                         const float* __restrict__ partial, float* __restrict__ out) {
+  const int e = blockIdx.x;
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;
+  if (i * 4 >= d) return;
+  const int c0 = cpre[e], c1 = cpre[e + 1];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = c0; c < c1; ++c) {
+    const float4 v = reinterpret_cast<const float4*>(partial + static_cast<int64_t>(c) * d)[i];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
   }
+  reinterpret_cast<float4*>(out + static_cast<int64_t>(e) * d)[i] = acc;
 }
 
 // ------------------------------------------------------------ unpermute-sum of dx
@@ -606,30 +639,22 @@ cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void
   return cudaGetLastError();
 }
 
-// Row splits of the router weight gradient: enough blocks for about two per
-// SM of a 152-SM part.  Independent of the device so that workspace sizes are.
-static int dwgate_splits(int n_exp, int d) {
-  const int colblocks = (d / 8 + 255) / 256;
-  const int base = n_exp * colblocks;
-  int s = (304 + base - 1) / base;
-  return s < 1 ? 1 : (s > 64 ? 64 : s);
+size_t dwgate_partial_floats(int n_tok, int top_k, int n_exp, int d) {
+  const size_t chunks = (static_cast<size_t>(n_tok) * top_k + kDwgChunk - 1) / kDwgChunk + n_exp;
+  return chunks * d + (n_exp + 1 + 3) / 4 * 4;   // partials + chunk prefix (int32)
 }
 
-size_t dwgate_partial_floats(int n_exp, int d) {
-  const int s = dwgate_splits(n_exp, d);
-  return s > 1 ? static_cast<size_t>(n_exp) * s * d : 0;
-}
-
-cudaError_t launch_dwgate(int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row, const float* dl,
-                          const void* x_perm, float* partial, float* dw_gate, cudaStream_t st) {
-  const int s = dwgate_splits(n_exp, d);
+cudaError_t launch_dwgate(int n_tok, int top_k, int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row,
+                          const float* dl, const void* x_perm, float* scratch, float* dw_gate, cudaStream_t st) {
+  if (n_exp > 1024 || !scratch) return cudaErrorInvalidValue;
+  const int chunks = static_cast<int>((static_cast<int64_t>(n_tok) * top_k + kDwgChunk - 1) / kDwgChunk + n_exp);
+  float* partial = scratch;
+  int32_t* cpre = reinterpret_cast<int32_t*>(scratch + static_cast<size_t>(chunks) * d);
   const int d8 = d / 8;
-  dim3 grid(n_exp, (d8 + 255) / 256, s);
-  float* dst = s > 1 ? partial : dw_gate;
-  if (s > 1 && !partial) return cudaErrorInvalidValue;
-  dwgate_kernel<<<grid, 256, 0, st>>>(n_exp, d8, s, offsets, copy_of_row, dl, static_cast<const uint4*>(x_perm),
-                                      dst);
-  if (s > 1) reduce_splits_kernel<<<256, 256, 0, st>>>(n_exp, d, s, partial, dw_gate);
+  dwg_chunk_prefix_kernel<<<1, 32, 0, st>>>(n_exp, offsets, cpre);
+  dwg_partial_kernel<<<dim3(chunks, (d8 + 255) / 256), 256, 0, st>>>(n_exp, d8, offsets, cpre, copy_of_row, dl,
+                                                                     static_cast<const uint4*>(x_perm), partial);
+  dwg_reduce_kernel<<<dim3(n_exp, (d / 4 + 255) / 256), 256, 0, st>>>(n_exp, d, cpre, partial, dw_gate);
   return cudaGetLastError();
 }
 
