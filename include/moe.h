@@ -86,7 +86,7 @@ typedef struct {
   int32_t use_bias;    /* 1: select on logits + route_bias (§6.3) */
   int32_t n_shared;    /* 0 or 1 shared expert (§5) */
   int32_t d_ff_shared; /* Fs */
-  int32_t precision;   /* 0: bf16 operands, fp32 accumulation (only value implemented) */
+  int32_t precision;   /* 0: bf16 operands; 1: MXFP8 expert GEMM operands (forward); fp32 accumulation */
 } moe_desc_t;
 
 /* Expert weights (all bf16, nn.Linear layout, see above).  ws1/ws3/ws2 are
@@ -240,6 +240,72 @@ MOE_API moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const
  * the bias unchanged. */
 MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
                              void* stream);
+
+/* ---------------------------------------------------------------- MXFP8 --
+ * The MXFP8 forward path: the expert GEMMs read their operands as MXFP8 (OCP
+ * Microscaling v1.0: E4M3 elements, one E8M0 power-of-two scale per 32
+ * consecutive elements along the contraction dimension), halving the bytes of
+ * weights and activations ("Accelerating Dropless MoE Training in JAX with
+ * NVIDIA Transformer Engine" ¶6: group-aware MXFP8 grouped GEMM; "LLM
+ * Infrastructure Engineering 08: MoE Training Engineering" §13.6: fine-
+ * grained scaling, fp32 accumulation).  Block scale 2^(floor(log2 amax) - 8);
+ * elements rounded to nearest even and saturated at +-448; an all-zero block
+ * has scale byte 0.  Scales are stored k-block-major: for a matrix [rows,
+ * cols] (cols = contraction dimension) the byte of row r, block b is at
+ * scales[b * scale_ld + r] with scale_ld >= rows and a multiple of 16.
+ * The tensor cores run bf16 MMAs on the exactly dequantised operands (every
+ * E4M3 value times a power of two is a bf16 value), with fp32 accumulation.
+ * The backward (moe_backward) runs in bf16. */
+
+/* Round up to the scale leading dimension the library expects (multiple of 16). */
+#define MOE_MX_SCALE_LD(rows) ((((rows) + 15) / 16) * 16)
+
+/* MXFP8 expert weights: codes (uint8) in the weights' layouts, scales
+ * [groups][K/32][N] per matrix [N,K] (K = contraction dimension):
+ *   w1, w3 codes [E,F,D], scales [E, D/32, F];  w2 codes [E,D,F], scales [E, F/32, D];
+ *   ws1, ws3 codes [Fs,D], scales [D/32, Fs];   ws2 codes [D,Fs], scales [Fs/32, D]. */
+typedef struct {
+  const void* w1;
+  const void* w1_scale;
+  const void* w3;
+  const void* w3_scale;
+  const void* w2;
+  const void* w2_scale;
+  const void* ws1;
+  const void* ws1_scale;
+  const void* ws3;
+  const void* ws3_scale;
+  const void* ws2;
+  const void* ws2_scale;
+} moe_expert_weights_mx_t;
+
+/* Quantise bf16 src [groups, rows, cols] rowwise to MXFP8 along cols: codes
+ * [groups, rows, cols] and scales [groups, cols/32, scale_ld].  cols must be
+ * a multiple of 32; scale_ld >= rows and a multiple of 16.  Used for weights
+ * (once per optimiser step, outside the layer). */
+MOE_API moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
+                                        void* scales, int64_t scale_ld, void* stream);
+
+/* moe_permute with MXFP8 quantisation fused in: the same row_of_copy /
+ * copy_of_row maps, and the permuted rows as codes xq_perm [R,D] with scales
+ * xs_perm [D/32, MOE_MX_SCALE_LD(R)]; optionally (xq_tok non-NULL) the
+ * token-order rows xq_tok [N,D], xs_tok [D/32, MOE_MX_SCALE_LD(N)] for the
+ * shared expert.  d->precision must be 1.  Needs the forward workspace. */
+MOE_API moe_status_t moe_permute_mxfp8(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
+                                       const int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row,
+                                       void* xq_perm, void* xs_perm, void* xq_tok, void* xs_tok, void* ws,
+                                       size_t ws_bytes, void* stream);
+
+/* moe_grouped_ffn with MXFP8 operands: GEMM1 reads xq_perm/xs_perm and the
+ * MXFP8 w1, w3; its epilogue computes h = silu(a1) * a3 and quantises it to
+ * MXFP8 along F (kept in the workspace); GEMM2 reads it with w2 and writes
+ * y_perm [R,D] bf16.  The shared expert does the same from xq_tok/xs_tok into
+ * y_shared.  `saved` may hold bf16 a1, a3, h (and a1s, a3s, hs) for a bf16
+ * backward, or NULL pointers.  d->precision must be 1. */
+MOE_API moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_perm, const void* xs_perm,
+                                           const int32_t* offsets, const void* xq_tok, const void* xs_tok,
+                                           const moe_expert_weights_mx_t* w, const moe_ffn_saved_t* saved,
+                                           void* y_perm, void* y_shared, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_permute without a workspace (no counterpart in the pages; an addition
  * of this library for callers that cannot allocate).  Same inputs, outputs

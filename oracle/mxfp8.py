@@ -22,7 +22,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["e4m3_decode", "e4m3_encode", "e8m0_scale_exponent", "mx_quantize",
-           "mx_dequantize", "E4M3_MAX", "MX_BLOCK"]
+           "mx_dequantize", "mx_fake_quant", "swiglu_expert_mxfp8", "moe_forward_mxfp8",
+           "E4M3_MAX", "MX_BLOCK"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
@@ -124,3 +125,43 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray, starts, axis: int = -1)
     for b, (lo, hi) in enumerate(zip(starts, ends)):
         out[..., lo:hi] = vals[..., lo:hi] * np.exp2(s[..., b].astype(np.float64) - 127)[..., None]
     return np.moveaxis(out, -1, axis)
+
+
+def mx_fake_quant(x: np.ndarray, axis: int = -1) -> np.ndarray:
+    """Quantise to MXFP8 along ``axis`` and dequantise again (float64)."""
+    codes, scales, starts = mx_quantize(x, axis=axis)
+    return mx_dequantize(codes, scales, starts, axis=axis)
+
+
+def swiglu_expert_mxfp8(x, w1, w3, w2):
+    """One SwiGLU expert with MXFP8 operands (quantisation-aware reference).
+
+    Every GEMM operand is quantised along its contraction dimension: x, w1,
+    w3 along D; h and w2 along F.  The arithmetic on the dequantised values
+    is fp32, as on the tensor cores.  Returns (y, a1, a3, h) with h before its
+    quantisation."""
+    f32 = np.float32
+    xq = mx_fake_quant(x, axis=1).astype(f32)
+    a1 = np.matmul(xq, mx_fake_quant(w1, axis=1).astype(f32).T)
+    a3 = np.matmul(xq, mx_fake_quant(w3, axis=1).astype(f32).T)
+    h = (a1 / (f32(1.0) + np.exp(-a1)) * a3).astype(f32)
+    y = np.matmul(mx_fake_quant(h, axis=1).astype(f32), mx_fake_quant(w2, axis=1).astype(f32).T)
+    return y, a1, a3, h
+
+
+def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None):
+    """Layer forward of the dropless MoE layer with MXFP8 expert GEMMs: the
+    loop over experts of the simplified MoE layer ("LLM Infrastructure
+    Engineering 08: MoE Training Engineering" §9) with every expert replaced
+    by :func:`swiglu_expert_mxfp8`; gate weights and the combine stay fp32."""
+    n, d = x.shape
+    out = np.zeros((n, d), dtype=np.float32)
+    for e in range(w1.shape[0]):
+        tok, kk = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        y = swiglu_expert_mxfp8(x[tok], w1[e], w3[e], w2[e])[0]
+        np.add.at(out, tok, y * g[tok, kk].astype(np.float32)[:, None])
+    if shared is not None:
+        out = out + swiglu_expert_mxfp8(x, shared[0], shared[1], shared[2])[0]
+    return out

@@ -41,6 +41,11 @@ class MoeGrads(ctypes.Structure):
                 ("dws3", c_vp), ("dws2", c_vp), ("dg", c_vp), ("dlogits", c_vp)]
 
 
+class MoeExpertWeightsMx(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("w1", "w1_scale", "w3", "w3_scale", "w2", "w2_scale",
+                                    "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")]
+
+
 # name -> (restype, argtypes); every entry point of include/moe.h
 SIGNATURES = {
     "moe_abi_version": (c_i32, []),
@@ -63,6 +68,13 @@ SIGNATURES = {
                              c_vp]),
     "moe_update_bias": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, ctypes.c_float, c_i32, c_vp]),
     "moe_permute_noalloc": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_quantize_mxfp8": (c_i32, [c_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_vp, c_vp,
+                                   ctypes.c_int64, c_vp]),
+    "moe_permute_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                  c_vp, ctypes.c_size_t, c_vp]),
+    "moe_grouped_ffn_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp,
+                                      ctypes.POINTER(MoeExpertWeightsMx), ctypes.POINTER(MoeFfnSaved), c_vp, c_vp,
+                                      c_vp, ctypes.c_size_t, c_vp]),
 }
 
 _LIB = None

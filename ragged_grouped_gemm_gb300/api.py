@@ -182,6 +182,72 @@ def moe_update_bias(desc, counts, bias, gamma: float, mode: int = 0, stream=None
         ctypes.c_float(gamma), mode, _s(stream)))
 
 
+# --------------------------------------------------------------- MXFP8 forward
+U8 = torch.uint8
+
+
+def mx_scale_ld(rows: int) -> int:
+    """Leading dimension of an MXFP8 scale array (rows rounded up to 16)."""
+    return (rows + 15) // 16 * 16
+
+
+def moe_quantize_mxfp8(src, codes, scales, stream=None):
+    """src bf16 [G, rows, cols] (or [rows, cols]) -> codes uint8 (same shape),
+    scales uint8 [G, cols/32, ld] (or [cols/32, ld]), ld = mx_scale_ld(rows)."""
+    g, rows, cols = (1,) + tuple(src.shape) if src.dim() == 2 else tuple(src.shape)
+    ld = scales.shape[-1]
+    _check("moe_quantize_mxfp8", _lib.load().moe_quantize_mxfp8(
+        _p(src, BF16, name="src"), g, rows, cols, _p(codes, U8, tuple(src.shape), "codes"),
+        _p(scales, U8, (scales.shape if src.dim() == 3 else (cols // 32, ld)), "scales"), ld, _s(stream)))
+
+
+def quantize_weights_mxfp8(p: dict, stream=None) -> dict:
+    """MXFP8 copies (codes, scales) of the expert weights in ``p``."""
+    out = {}
+    for key in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+        w = p.get(key)
+        if w is None:
+            continue
+        codes = torch.empty(w.shape, dtype=U8, device=w.device)
+        rows, cols = w.shape[-2], w.shape[-1]
+        sshape = (w.shape[0], cols // 32, mx_scale_ld(rows)) if w.dim() == 3 else (cols // 32, mx_scale_ld(rows))
+        scales = torch.zeros(sshape, dtype=U8, device=w.device)
+        moe_quantize_mxfp8(w, codes, scales, stream)
+        out[key], out[key + "_scale"] = codes, scales
+    return out
+
+
+def moe_permute_mxfp8(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, xq_perm, xs_perm, xq_tok, xs_tok, ws,
+                      stream=None):
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_permute_mxfp8", _lib.load().moe_permute_mxfp8(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(offsets, I32, (e + 1,), "offsets"), _p(row_of_copy, I32, (r,), "row_of_copy"),
+        _p(copy_of_row, I32, (r,), "copy_of_row"), _p(xq_perm, U8, (r, d), "xq_perm"),
+        _p(xs_perm, U8, (d // 32, mx_scale_ld(r)), "xs_perm"), _p(xq_tok, U8, (n, d), "xq_tok"),
+        _p(xs_tok, U8, (d // 32, mx_scale_ld(n)), "xs_tok"), _p(ws, name="ws"), ws.numel() * ws.element_size(),
+        _s(stream)))
+
+
+def moe_grouped_ffn_mxfp8(desc, xq_perm, xs_perm, offsets, xq_tok, xs_tok, wq: dict, saved: dict, y_perm, y_shared,
+                          ws, stream=None):
+    """``wq``: output of :func:`quantize_weights_mxfp8`; ``saved``: optional bf16
+    a1, a3, h, a1s, a3s, hs for a bf16 backward (missing keys = not saved)."""
+    n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
+    r, fs, sh = n * k, desc.d_ff_shared, desc.n_shared
+    w = _lib.MoeExpertWeightsMx(*[_p(wq.get(key)) if (sh or not key.startswith("ws")) else None
+                                  for key in ("w1", "w1_scale", "w3", "w3_scale", "w2", "w2_scale",
+                                              "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")])
+    sv = _lib.MoeFfnSaved(*[_p(saved.get(key)) for key in ("a1", "a3", "h", "a1s", "a3s", "hs")])
+    _check("moe_grouped_ffn_mxfp8", _lib.load().moe_grouped_ffn_mxfp8(
+        ctypes.byref(desc), _p(xq_perm, U8, (r, d), "xq_perm"), _p(xs_perm, U8, (d // 32, mx_scale_ld(r)), "xs_perm"),
+        _p(offsets, I32, (e + 1,), "offsets"), _p(xq_tok, U8, (n, d), "xq_tok") if sh else None,
+        _p(xs_tok, U8, (d // 32, mx_scale_ld(n)), "xs_tok") if sh else None, ctypes.byref(w), ctypes.byref(sv),
+        _p(y_perm, BF16, (r, d), "y_perm"), _p(y_shared, BF16, (n, d), "y_shared") if sh else None,
+        _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
 # --------------------------------------------------------------- layer runner
 class MoELayer:
     """Buffers of one layer plus the forward / backward call sequences.
@@ -209,6 +275,13 @@ class MoELayer:
                             a3s=z(n, fs) if train else None)
         else:
             self.buf.update(hs=None, y_shared=None, a1s=None, a3s=None)
+        self.mx = cfg.precision == "mxfp8"
+        if self.mx:
+            self.wq = quantize_weights_mxfp8(params)
+            self.buf.update(xq_perm=z(r, d, dt=U8), xs_perm=torch.zeros(d // 32, mx_scale_ld(r), dtype=U8, device=device),
+                            xq_tok=z(n, d, dt=U8) if cfg.n_shared else None,
+                            xs_tok=(torch.zeros(d // 32, mx_scale_ld(n), dtype=U8, device=device)
+                                    if cfg.n_shared else None))
         fwd_b, bwd_b = moe_workspace_size(self.desc)
         self.ws = torch.empty((bwd_b if train else fwd_b) + 256, dtype=torch.uint8, device=device)
         moe_workspace_init(self.ws)
@@ -226,6 +299,8 @@ class MoELayer:
         self.x = x
         moe_route(self.desc, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
                   b["offsets"], self.ws, stream)
+        if self.mx:
+            return self._forward_mx(x, stream)
         moe_permute(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"],
                     self.ws, stream)
         moe_grouped_ffn(self.desc, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
@@ -234,7 +309,19 @@ class MoELayer:
         moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
         return b["out"]
 
+    def _forward_mx(self, x, stream=None):
+        b = self.buf
+        moe_permute_mxfp8(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
+                          b["xq_perm"], b["xs_perm"], b["xq_tok"], b["xs_tok"], self.ws, stream)
+        saved = {key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
+        moe_grouped_ffn_mxfp8(self.desc, b["xq_perm"], b["xs_perm"], b["offsets"], b["xq_tok"], b["xs_tok"], self.wq,
+                              saved, b["y_perm"], b["y_shared"], self.ws, stream)
+        moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
+        return b["out"]
+
     def backward(self, dy: torch.Tensor, stream=None) -> dict:
+        if self.mx:
+            raise NotImplementedError("the MXFP8 layer runner is forward-only")
         b = self.buf
         state = {key: b[key] for key in ("x_perm", "logits", "topk_idx", "topk_w", "offsets", "row_of_copy",
                                          "copy_of_row", "a1", "a3", "h", "y_perm", "a1s", "a3s", "hs")}

@@ -27,6 +27,7 @@
 #include "sm100_ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 
@@ -35,14 +36,18 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;        // producer, MMA, 8 epilogue warps
+constexpr int kThreadsQ = 576;       // + 8 converter warps (MXFP8 operands)
 constexpr int kEpiThreads = 256;
+constexpr int kConvThreads = 256;
+
 constexpr int kMaxGroups = 1024;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 
 struct KParams {
-  CUtensorMap tmA[2];
-  CUtensorMap tmB[2];
+  CUtensorMap tmA[2];    // MXFP8: [0] A codes, [1] A scales
+  CUtensorMap tmB[2];    // MXFP8: B codes (W1 | W3 halves, or one map)
+  CUtensorMap tmBs[2];   // MXFP8: B scales
   CUtensorMap tmC;       // fp32 output map {n, m, group}, used when c_tma != 0
   int32_t c_tma;
   int32_t c_rows;        // rows of the output map (ragged M, one group)
@@ -56,6 +61,9 @@ struct KParams {
   void* out0;
   void* out1;
   void* out2;
+  void* out3;
+  void* out4;
+  int64_t s_ld;
   const void* in0;
   const void* in1;
   int64_t ld_out;
@@ -63,18 +71,25 @@ struct KParams {
   int32_t* status;
 };
 
-template <int BN>
+template <int BN, bool QUANT = false>
 struct Cfg {
   static constexpr int kStageBytes = (BM + BN) * BK * 2;
   static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  static constexpr int kStages = QUANT ? 3 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  // stages | epilogue staging (8 warps x 32x16 fp32) | barriers (2S+5) |
-  // tmem base, abort | offsets[G+1] | prefix[G+1]
-  static constexpr int kEpiOff = kStages * kStageBytes;
+  // MXFP8 staging stage: A codes [128][64] | B codes [256][64] | A scales
+  // [2][144] (rows from a 16-aligned start) | B scales 2 x [2][128]
+  static constexpr int kQStages = QUANT ? 2 : 0;
+  static constexpr int kQStageBytes = 25600;
+  static constexpr int kQACodes = 0, kQBCodes = 8192, kQAScales = 24576, kQBScales = 24960;
+  static constexpr uint32_t kQTxBytes = 8192 + 16384 + 2 * 144 + 2 * 2 * 128;
+  // stages | MXFP8 staging | epilogue staging (8 warps x 32x16 fp32) |
+  // barriers (2S + 2QS + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kEpiOff = kQOff + kQStages * kQStageBytes;
   static constexpr int kEpiBytes = 4 * 4096;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
-  static constexpr int kMiscOff = kBarOff + (2 * kStages + 5) * 8;
+  static constexpr int kMiscOff = kBarOff + (2 * kStages + 2 * kQStages + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr size_t smem_bytes(int groups) {
     return 1024 + kOffOff + 2 * 4 * (groups + 1);
@@ -135,16 +150,43 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float sigmoidf_fast(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<BN>;
+// E4M3 codes (16, little-endian in a uint4) times a power-of-two scale -> 8 bf16x2 words (exact).
+__device__ __forceinline__ void dequant16(const uint4 c, float sc, uint32_t (&w)[8]) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[i] >> (16 * hh)), __NV_E4M3);
+      __half2 h2;
+      *reinterpret_cast<__half2_raw*>(&h2) = hr;
+      const float2 f = __half22float2(h2);
+      w[2 * i + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+  }
+}
+
+__device__ __forceinline__ int mx_exponent_of(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  const uint32_t b = __float_as_uint(amax);
+  const int ex = static_cast<int>(b >> 23);
+  const int fl = ex ? ex - 127 : -149 + (31 - __clz(static_cast<int>(b)));
+  return max(-127, min(127, fl - 8));
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT>
+__global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<BN, QUANT>;
   constexpr bool RAGGED_K = A_MN;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + S;
-  uint64_t* tfull = empty + S;
+  uint64_t* qfull = empty + S;            // MXFP8 staging ring (QUANT only)
+  uint64_t* qempty = qfull + C::kQStages;
+  uint64_t* tfull = qempty + C::kQStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -158,8 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], QUANT ? kConvThreads : 1);   // TMA (tx bytes) or the converter threads
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], kConvThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -172,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA[0]);
     tma_prefetch_desc(&p.tmB[0]);
+    if (QUANT) {
+      tma_prefetch_desc(&p.tmA[1]);
+      tma_prefetch_desc(&p.tmBs[0]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(s_tmem, C::kTmemCols);
@@ -179,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   }
   // group offsets and (ragged M) the prefix of per-group tile counts
   // (128-row M tiles times N tiles)
-  for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
   __syncthreads();
   if (!RAGGED_K && warp == 0) {
     const int ntiles = (p.n_size + p.tile_n - 1) / p.tile_n;
@@ -215,7 +265,43 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (QUANT && lane == 0) {
+      // MXFP8 operands: codes and scales of each k-block into the staging ring
+      constexpr int QS = C::kQStages > 0 ? C::kQStages : 1;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int qs = it % QS;
+          const uint32_t qph = (it / QS) & 1u;
+          if (!mbar_wait_bounded(&qempty[qs], qph ^ 1u, s_abort, p.status, 110 + qs)) { ok = false; break; }
+          uint8_t* q = smem + C::kQOff + qs * C::kQStageBytes;
+          mbar_arrive_expect_tx(&qfull[qs], C::kQTxBytes);
+          const int k0 = kb * BK;
+          const int a_x = t.row0 & ~15;   // scale rows start at a 16-byte boundary
+          tma_load_2d(q + C::kQACodes, &p.tmA[0], &qfull[qs], k0, t.row0);
+          tma_load_2d(q + C::kQAScales, &p.tmA[1], &qfull[qs], a_x, kb * 2);
+          if (p.b_dual_n) {
+            const int f0 = t.nt * (BN / 2);
+            tma_load_3d(q + C::kQBCodes, &p.tmB[0], &qfull[qs], k0, f0, t.g);
+            tma_load_3d(q + C::kQBCodes + (BN / 2) * 64, &p.tmB[1], &qfull[qs], k0, f0, t.g);
+            tma_load_3d(q + C::kQBScales, &p.tmBs[0], &qfull[qs], f0, kb * 2, t.g);
+            tma_load_3d(q + C::kQBScales + 256, &p.tmBs[1], &qfull[qs], f0, kb * 2, t.g);
+          } else {
+            tma_load_3d(q + C::kQBCodes, &p.tmB[0], &qfull[qs], k0, t.nt * BN, t.g);
+            tma_load_3d(q + C::kQBScales, &p.tmBs[0], &qfull[qs], t.nt * BN, kb * 2, t.g);
+            tma_load_3d(q + C::kQBScales + 256, &p.tmBs[0], &qfull[qs], t.nt * BN + 128, kb * 2, t.g);
+          }
+        }
+      }
+      for (int s = 0; s < QS; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t last = s + QS * ((it - 1 - s) / QS);
+          mbar_wait_drain(&qfull[s], (last / QS) & 1u);
+        }
+      }
+    } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -334,6 +420,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_wait_drain(mma_done, 0);
     }
     __syncwarp();
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ converters (MXFP8)
+    if (QUANT) {
+      constexpr int QS = C::kQStages > 0 ? C::kQStages : 1;
+      const int ct = threadIdx.x - 10 * 32;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+        const int a_rem = t.row0 & 15;
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int qs = it % QS;
+          const uint32_t qph = (it / QS) & 1u;
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait_bounded(&qfull[qs], qph, s_abort, p.status, 500 + qs)) { ok = false; break; }
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 520 + s)) { ok = false; break; }
+          const uint8_t* q = smem + C::kQOff + qs * C::kQStageBytes;
+          uint8_t* dst = smem + s * C::kStageBytes;
+          // 384 operand rows (128 of A, 256 of B) x 4 chunks of 16 codes
+          for (int task = ct; task < (BM + BN) * 4; task += kConvThreads) {
+            const int row = task >> 2;
+            const int j = task & 3;
+            const bool is_a = row < BM;
+            const int rb = is_a ? row : row - BM;
+            const uint4 codes = *reinterpret_cast<const uint4*>(q + (is_a ? C::kQACodes : C::kQBCodes) + rb * 64 + j * 16);
+            const int kbl = j >> 1;
+            const uint32_t sb = is_a ? q[C::kQAScales + kbl * 144 + a_rem + rb]
+                                     : q[C::kQBScales + (rb >> 7) * 256 + kbl * 128 + (rb & 127)];
+            const float sc = __uint_as_float(sb ? (sb << 23) : 0x00400000u);
+            uint32_t w[8];
+            dequant16(codes, sc, w);
+            uint8_t* rowp = dst + (is_a ? rb * 128 : kABytes + rb * 128);
+            const int sw = rb & 7;
+            *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&full[s]);
+          mbar_arrive(&qempty[qs]);
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;           // TMEM lane quarter = tile rows 32q..32q+31
@@ -480,6 +609,80 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             }
           }
         }
+      } else if (EPI == EPI_SWIGLU_FWD_Q) {
+        // h = silu(a1) * a3 per row, quantised to MXFP8 in 32-column blocks
+        // (each thread owns a row, so a block's amax is thread-local)
+        const int64_t grow = t.row0 + r;
+        const int f0 = t.nt * (BN / 2);
+#pragma unroll 1
+        for (int c = hf * (BN / 4); c < (hf + 1) * (BN / 4); c += 32) {
+          const int col = f0 + c;
+          const bool ok = row_ok && col < p.n_size;
+          const int64_t off = grow * p.ld_out + col;
+          float h[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t u[16], v[16];
+            tmem_ld_32x32b_x16(tb + c + 16 * half, u);
+            tmem_ld_32x32b_x16(tb + BN / 2 + c + 16 * half, v);
+            tmem_wait_ld(u);
+            reg_fence(v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float a = __uint_as_float(u[j]), b = __uint_as_float(v[j]);
+              h[16 * half + j] = a * sigmoidf_fast(a) * b;
+            }
+            if (ok && p.out3) {
+              uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out3) + off + 16 * half);
+              d[0] = make_uint4(pack_bf16x2(__uint_as_float(u[0]), __uint_as_float(u[1])),
+                                pack_bf16x2(__uint_as_float(u[2]), __uint_as_float(u[3])),
+                                pack_bf16x2(__uint_as_float(u[4]), __uint_as_float(u[5])),
+                                pack_bf16x2(__uint_as_float(u[6]), __uint_as_float(u[7])));
+              d[1] = make_uint4(pack_bf16x2(__uint_as_float(u[8]), __uint_as_float(u[9])),
+                                pack_bf16x2(__uint_as_float(u[10]), __uint_as_float(u[11])),
+                                pack_bf16x2(__uint_as_float(u[12]), __uint_as_float(u[13])),
+                                pack_bf16x2(__uint_as_float(u[14]), __uint_as_float(u[15])));
+            }
+            if (ok && p.out4) {
+              uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out4) + off + 16 * half);
+              d[0] = make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                                pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                                pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                                pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+              d[1] = make_uint4(pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9])),
+                                pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11])),
+                                pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13])),
+                                pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15])));
+            }
+          }
+          if (ok) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int e = mx_exponent_of(amax);
+            const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+            uint32_t cw[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_fp8x2_storage_t lo =
+                  __nv_cvt_float2_to_fp8x2(make_float2(h[4 * i] * inv, h[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+              const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                  make_float2(h[4 * i + 2] * inv, h[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+              cw[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            uint4* cd = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out0) + off);
+            cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            static_cast<uint8_t*>(p.out1)[static_cast<int64_t>(col / 32) * p.s_ld + grow] = static_cast<uint8_t>(e + 127);
+            if (p.out2) {
+              uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out2) + off);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                d[j] = make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                  pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+            }
+          }
+        }
       } else {  // EPI_SWIGLU_BWD
         const int64_t grow = t.row0 + r;
 #pragma unroll 1
@@ -589,11 +792,33 @@ bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+// uint8 tensor map (MXFP8 codes or scales), no swizzle, zero fill.
+bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                 const uint32_t* box) {
+  EncodeFn enc = get_encode_fn();
+  if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  cuuint64_t d[3];
+  cuuint64_t st[2];
+  cuuint32_t b[3];
+  cuuint32_t e[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    if (i + 1 < rank) {
+      if (strides[i] % 16 != 0) return false;
+      st[i] = strides[i];
+    }
+  }
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, b, e,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false>
 cudaError_t launch_impl(const KParams& kp, int grid, cudaStream_t stream) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, QUANT>;
   const size_t smem = C::smem_bytes(kp.num_groups);
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -601,7 +826,7 @@ cudaError_t launch_impl(const KParams& kp, int grid, cudaStream_t stream) {
                                     static_cast<int>(C::smem_bytes(kMaxGroups)));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, kThreads, smem, stream>>>(kp);
+  kern<<<grid, QUANT ? kThreadsQ : kThreads, smem, stream>>>(kp);
   return cudaGetLastError();
 }
 
@@ -636,6 +861,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   kp.out0 = a.out0;
   kp.out1 = a.out1;
   kp.out2 = a.out2;
+  kp.out3 = a.out3;
+  kp.out4 = a.out4;
+  kp.s_ld = a.s_ld;
   kp.in0 = a.in0;
   kp.in1 = a.in1;
   kp.ld_out = a.ld_out;
@@ -643,6 +871,47 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   kp.status = a.status;
 
   int64_t tiles_ub = 0;
+  if (a.quant) {
+    // MXFP8 operands: K-major A and B only, one contraction source, BN = 256
+    if (a.ragged_k || a.a_mn || a.b_mn || BN != 256 || a.k1 != 0 || a.max_rows <= 0) return cudaErrorInvalidValue;
+    if (a.epi != EPI_SWIGLU_FWD_Q && a.epi != EPI_BF16) return cudaErrorInvalidValue;
+    const int64_t K = a.k0;
+    if (K <= 0 || K % 64 || a.qa.cols != K) return cudaErrorInvalidValue;
+    kp.kb0 = static_cast<int>(K / BK);
+    kp.kb1 = 0;
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(a.qa.rows)};
+      const uint64_t str[1] = {static_cast<uint64_t>(K)};
+      const uint32_t box[2] = {64, BM};
+      if (!make_map_u8(&kp.tmA[0], a.qa.codes, 2, dims, str, box)) return cudaErrorInvalidValue;
+      const uint64_t sd[2] = {static_cast<uint64_t>(a.qa.rows), static_cast<uint64_t>(K / 32)};
+      const uint64_t ss[1] = {static_cast<uint64_t>(a.qa.scale_ld)};
+      const uint32_t sbox[2] = {144, 2};
+      if (!make_map_u8(&kp.tmA[1], a.qa.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
+    }
+    const int nb = a.b_dual_n ? 2 : 1;
+    for (int i = 0; i < nb; ++i) {
+      const MxOperand& b = a.qb[i];
+      if (b.cols != K) return cudaErrorInvalidValue;
+      const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows), static_cast<uint64_t>(b.groups)};
+      const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows * K)};
+      const uint32_t box[3] = {64, static_cast<uint32_t>(a.b_dual_n ? BN / 2 : BN), 1};
+      if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box)) return cudaErrorInvalidValue;
+      const uint64_t sd[3] = {static_cast<uint64_t>(b.rows), static_cast<uint64_t>(K / 32), static_cast<uint64_t>(b.groups)};
+      const uint64_t ss[2] = {static_cast<uint64_t>(b.scale_ld), static_cast<uint64_t>(b.scale_ld * (K / 32))};
+      const uint32_t sbox[3] = {128, 2, 1};
+      if (!make_map_u8(&kp.tmBs[i], b.scales, 3, sd, ss, sbox)) return cudaErrorInvalidValue;
+    }
+    if (nb == 1) {
+      kp.tmB[1] = kp.tmB[0];
+      kp.tmBs[1] = kp.tmBs[0];
+    }
+    const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
+    tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+    const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
+    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<256, false, false, EPI_SWIGLU_FWD_Q, true>(kp, grid, stream);
+    return launch_impl<256, false, false, EPI_BF16, true>(kp, grid, stream);
+  }
   if (!a.ragged_k) {
     if (a.max_rows <= 0) return cudaSuccess;
     kp.kb0 = (a.k0 + BK - 1) / BK;

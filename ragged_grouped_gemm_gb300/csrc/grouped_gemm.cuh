@@ -22,6 +22,19 @@ enum EpiKind : int {
   EPI_F32 = 1,         // out0[row, col] = acc
   EPI_SWIGLU_FWD = 2,  // acc = [a1 | a3] -> out0 = h = silu(a1) * a3, out1 = a1, out2 = a3 (bf16)
   EPI_SWIGLU_BWD = 3,  // acc = dh; in0 = a1, in1 = a3 -> out0 = da1, out1 = da3 (bf16)
+  EPI_SWIGLU_FWD_Q = 4,  // acc = [a1 | a3] -> h quantised to MXFP8 along F: out0 = codes [rows, n],
+                         // out1 = scales [n/32, s_ld]; optional bf16 out2 = h, out3 = a1, out4 = a3
+};
+
+// MXFP8 operand: E4M3 codes [groups][rows, cols] and E8M0 scales
+// [groups][cols/32, scale_ld] (see mxfp8.cuh), cols = contraction dimension.
+struct MxOperand {
+  const void* codes = nullptr;
+  const void* scales = nullptr;
+  int64_t rows = 0;
+  int64_t cols = 0;
+  int64_t groups = 1;
+  int64_t scale_ld = 0;
 };
 
 // One operand source: a bf16 matrix in global memory.
@@ -52,9 +65,15 @@ struct GemmArgs {
   int64_t max_rows = 0;       // upper bound of offsets[num_groups] (grid sizing)
   int m_size = 0;             // ragged K: rows of each C_g
   int n_size = 0;             // columns of C (f extent for EPI_SWIGLU_FWD)
+  bool quant = false;         // operands are MXFP8 (qa, qb), dequantised to bf16 on the way in
+  MxOperand qa;               // A: [rows, K] with scales [K/32, scale_ld]
+  MxOperand qb[2];            // B: [groups][N, K]; qb[1] is the W3 half of a dual-N tile
   void* out0 = nullptr;
   void* out1 = nullptr;
   void* out2 = nullptr;
+  void* out3 = nullptr;
+  void* out4 = nullptr;
+  int64_t s_ld = 0;           // EPI_SWIGLU_FWD_Q: leading dimension of the h scales
   const void* in0 = nullptr;
   const void* in1 = nullptr;
   int64_t ld_out = 0;

@@ -8,6 +8,7 @@
 
 #include "grouped_gemm.cuh"
 #include "moe_kernels.cuh"
+#include "mxfp8.cuh"
 
 namespace {
 
@@ -19,6 +20,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
   size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, fwd_end = 0;
+  size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
 };
 
@@ -32,6 +34,12 @@ WsLayout layout(const moe_desc_t& d) {
   L.dense_off = o; o += kAlign;
   L.blk_counts = o; o = align_up(o + nch * E * 4);
   L.blk_base = o; o = align_up(o + nch * E * 4);
+  if (d.precision == 1) {
+    L.hq = o; o = align_up(o + R * F);
+    L.hs = o; o = align_up(o + F / 32 * moe::mx_scale_ld(R));
+    L.hq_sh = o; o = align_up(o + N * Fs);
+    L.hs_sh = o; o = align_up(o + Fs / 32 * moe::mx_scale_ld(N));
+  }
   L.fwd_end = o;
   L.dl = o; o = align_up(o + R * 4);
   L.dg = o; o = align_up(o + R * 4);
@@ -62,7 +70,7 @@ moe_status_t check_desc(const moe_desc_t* d) {
   if (d->use_bias != 0 && d->use_bias != 1) return MOE_ERR_INVALID_ARG;
   if (d->n_shared != 0 && d->n_shared != 1) return d->n_shared > 1 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
   if (d->n_shared && (d->d_ff_shared <= 0 || d->d_ff_shared % 64)) return MOE_ERR_INVALID_ARG;
-  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;
+  if (d->precision != 0 && d->precision != 1) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->n_tok) * d->top_k >= (int64_t{1} << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -334,6 +342,7 @@ moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int3
                              void* y_shared, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // MXFP8 operands: moe_grouped_ffn_mxfp8
   if (!w || !saved || !offsets) return MOE_ERR_INVALID_ARG;
   if (!all16({x_perm, w->w1, w->w3, w->w2, saved->h, y_perm})) return MOE_ERR_INVALID_ARG;
   if ((saved->a1 && !aligned16(saved->a1)) || (saved->a3 && !aligned16(saved->a3))) return MOE_ERR_INVALID_ARG;
@@ -372,6 +381,7 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
                           size_t ws_bytes, void* stream) {
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, true));
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // the backward runs in bf16
   if (!w || !s || !g) return MOE_ERR_INVALID_ARG;
   if (!all16({w_gate, w->w1, w->w3, w->w2, s->x, s->x_perm, s->a1, s->a3, s->h, s->y_perm, dy, g->dx, g->dw_gate,
               g->dw1, g->dw3, g->dw2}))
@@ -420,6 +430,118 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
   MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, at<float>(ws, L.dwg),
                               g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
+                                void* scales, int64_t scale_ld, void* stream) {
+  if (groups <= 0 || rows <= 0 || cols <= 0 || cols % 32 || scale_ld < rows || scale_ld % 16) return MOE_ERR_INVALID_ARG;
+  if (!all16({src, codes, scales})) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_mx_quant_rows(src, nullptr, 1, groups * rows, static_cast<int>(cols), rows, scale_ld,
+                                               static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute_mxfp8(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
+                               int32_t* row_of_copy, int32_t* copy_of_row, void* xq_perm, void* xs_perm,
+                               void* xq_tok, void* xs_tok, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 1) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!all16({x, xq_perm, xs_perm}) || !topk_idx || !offsets || !row_of_copy || !copy_of_row)
+    return MOE_ERR_INVALID_ARG;
+  if (xq_tok && !all16({xq_tok, xs_tok})) return MOE_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  MOE_CUDA(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, at<int32_t>(ws, L.blk_counts),
+                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row,
+                                    at<int32_t>(ws, L.status), st));
+  MOE_CUDA(moe::launch_mx_quant_rows(x, copy_of_row, d->top_k, R, d->d_model, R, moe::mx_scale_ld(R),
+                                     static_cast<uint8_t*>(xq_perm), static_cast<uint8_t*>(xs_perm), st));
+  if (xq_tok)
+    MOE_CUDA(moe::launch_mx_quant_rows(x, nullptr, 1, d->n_tok, d->d_model, d->n_tok, moe::mx_scale_ld(d->n_tok),
+                                       static_cast<uint8_t*>(xq_tok), static_cast<uint8_t*>(xs_tok), st));
+  return MOE_OK;
+}
+
+namespace {
+// MXFP8 SwiGLU FFN of one expert set: GEMM1 (w1|w3, SwiGLU, h quantised) then GEMM2.
+moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, int F, int groups,
+                         const int32_t* offsets, const void* w1, const void* w1s, const void* w3, const void* w3s,
+                         const void* w2, const void* w2s, void* hq, void* hs, void* h, void* a1, void* a3, void* y,
+                         int32_t* status, cudaStream_t st) {
+  GemmArgs g1;
+  g1.quant = true;
+  g1.epi = moe::EPI_SWIGLU_FWD_Q;
+  g1.qa = moe::MxOperand{aq, as, rows, D, 1, moe::mx_scale_ld(rows)};
+  g1.qb[0] = moe::MxOperand{w1, w1s, F, D, groups, F};
+  g1.qb[1] = moe::MxOperand{w3, w3s, F, D, groups, F};
+  g1.b_dual_n = true;
+  g1.k0 = D;
+  g1.offsets = offsets;
+  g1.num_groups = groups;
+  g1.max_rows = rows;
+  g1.n_size = F;
+  g1.out0 = hq;
+  g1.out1 = hs;
+  g1.out2 = h;
+  g1.out3 = a1;
+  g1.out4 = a3;
+  g1.s_ld = moe::mx_scale_ld(rows);
+  g1.ld_out = F;
+  g1.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g1, st));
+  GemmArgs g2;
+  g2.quant = true;
+  g2.epi = moe::EPI_BF16;
+  g2.qa = moe::MxOperand{hq, hs, rows, F, 1, moe::mx_scale_ld(rows)};
+  g2.qb[0] = moe::MxOperand{w2, w2s, D, F, groups, D};
+  g2.k0 = F;
+  g2.offsets = offsets;
+  g2.num_groups = groups;
+  g2.max_rows = rows;
+  g2.n_size = D;
+  g2.out0 = y;
+  g2.ld_out = D;
+  g2.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g2, st));
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_perm, const void* xs_perm,
+                                   const int32_t* offsets, const void* xq_tok, const void* xs_tok,
+                                   const moe_expert_weights_mx_t* w, const moe_ffn_saved_t* saved, void* y_perm,
+                                   void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 1) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!w || !offsets || !all16({xq_perm, xs_perm, w->w1, w->w1_scale, w->w3, w->w3_scale, w->w2, w->w2_scale, y_perm}))
+    return MOE_ERR_INVALID_ARG;
+  moe_ffn_saved_t sv{};
+  if (saved) sv = *saved;
+  for (const void* q : {sv.a1, sv.a3, sv.h, sv.a1s, sv.a3s, sv.hs})
+    if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && !all16({xq_tok, xs_tok, w->ws1, w->ws1_scale, w->ws3, w->ws3_scale, w->ws2, w->ws2_scale,
+                             y_shared}))
+    return MOE_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  MOE_TRY(ffn_pair_mx(xq_perm, xs_perm, R, d->d_model, d->d_ff, d->n_exp, offsets, w->w1, w->w1_scale, w->w3,
+                      w->w3_scale, w->w2, w->w2_scale, at<void>(ws, L.hq), at<void>(ws, L.hs), sv.h, sv.a1, sv.a3,
+                      y_perm, status, st));
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
+    MOE_TRY(ffn_pair_mx(xq_tok, xs_tok, d->n_tok, d->d_model, d->d_ff_shared, 1, dense, w->ws1, w->ws1_scale, w->ws3,
+                        w->ws3_scale, w->ws2, w->ws2_scale, at<void>(ws, L.hq_sh), at<void>(ws, L.hs_sh), sv.hs,
+                        sv.a1s, sv.a3s, y_shared, status, st));
+  }
   return MOE_OK;
 }
 

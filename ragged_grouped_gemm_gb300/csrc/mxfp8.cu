@@ -1,0 +1,88 @@
+// MXFP8 quantisation kernel: one thread per (row, 32-element block), a warp
+// covering 32 consecutive rows of one block, so every thread reads 64
+// contiguous bytes, writes 32 contiguous code bytes, and the warp writes 32
+// consecutive scale bytes.
+//
+// Scale rule (OCP MX v1.0 with E4M3 elements, emax = 8): the block's shared
+// scale is 2^(floor(log2(amax)) - 8), clamped to [2^-127, 2^127]; an all-zero
+// block gets 2^-127 and zero codes.  floor(log2(amax)) is read from amax's
+// exponent bits (leading-bit position for a subnormal amax).  Elements are
+// divided by the scale (an exact power-of-two multiply) and converted to E4M3
+// with round-to-nearest-even and saturation at +-448 (cvt.rn.satfinite).
+#include "mxfp8.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  const uint32_t b = __float_as_uint(amax);
+  const int ex = static_cast<int>(b >> 23);
+  const int fl = ex ? ex - 127 : -149 + (31 - __clz(static_cast<int>(b)));
+  return max(-127, min(127, fl - 8));
+}
+
+__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16* __restrict__ src,
+                                                            const int32_t* __restrict__ src_row_of, int src_div,
+                                                            int64_t rows, int cols, int64_t rows_per_group,
+                                                            int64_t ld_s, uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ scales) {
+  const int nkb = cols / 32;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t rgroup = w / nkb;
+  const int kb = static_cast<int>(w - rgroup * nkb);
+  const int64_t row = rgroup * 32 + (threadIdx.x & 31);
+  if (rgroup * 32 >= rows || row >= rows) return;
+  const int64_t sr = src_row_of ? src_row_of[row] / src_div : row;
+  const uint4* p = reinterpret_cast<const uint4*>(src + sr * cols + kb * 32);
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = p[i];
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
+      f[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int e = mx_scale_exponent(amax);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e in [-127, 119]
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(codes + row * cols + kb * 32);
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  const int64_t g = row / rows_per_group;
+  const int64_t n = row - g * rows_per_group;
+  scales[(g * nkb + kb) * ld_s + n] = static_cast<uint8_t>(e + 127);
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quant_rows(const void* src, const int32_t* src_row_of, int src_div, int64_t rows, int cols,
+                                 int64_t rows_per_group, int64_t ld_s, uint8_t* codes, uint8_t* scales,
+                                 cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (cols % 32 || rows_per_group <= 0 || rows % rows_per_group || ld_s < rows_per_group) return cudaErrorInvalidValue;
+  const int64_t warps = (rows + 31) / 32 * (cols / 32);
+  const int64_t blocks = (warps + 7) / 8;
+  mx_quant_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(src), src_row_of, src_div, rows, cols, rows_per_group, ld_s, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

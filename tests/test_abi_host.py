@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_ctypes_structs_match_c_layout():
     structs = {"moe_desc_t": _lib.MoeDesc, "moe_expert_weights_t": _lib.MoeExpertWeights,
                "moe_ffn_saved_t": _lib.MoeFfnSaved, "moe_fwd_state_t": _lib.MoeFwdState,
-               "moe_grads_t": _lib.MoeGrads}
+               "moe_grads_t": _lib.MoeGrads, "moe_expert_weights_mx_t": _lib.MoeExpertWeightsMx}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
@@ -94,7 +94,7 @@ def test_workspace_sizes(lib):
 
 @pytest.mark.parametrize("field,value,code", [
     ("top_k", 0, 1), ("top_k", 9, 1), ("d_model", 96, 1), ("d_ff", 100, 1), ("gate", 2, 1),
-    ("n_exp", 2000, 1), ("precision", 1, 2), ("n_shared", 2, 2), ("n_tok", -1, 1), ("top_k", 33, 1),
+    ("n_exp", 2000, 1), ("precision", 2, 2), ("n_shared", 2, 2), ("n_tok", -1, 1), ("top_k", 33, 1),
 ])
 def test_invalid_descriptions_rejected(lib, field, value, code):
     d = _desc(**{field: value})

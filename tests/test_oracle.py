@@ -376,3 +376,35 @@ def test_mx_quantize_group_aware_blocks():
     assert starts == [0, 32, 40, 45]
     deq = O.mx_dequantize(codes, scales, starts, axis=0)
     assert np.abs(deq - x).max() <= np.abs(x).max() * 2 ** -3
+
+
+def test_mx_fake_quant_properties():
+    r = _rng(20)
+    # rows spanning 2^-20 .. 2^20 in magnitude: blocks along the right axis keep
+    # every row's error within its own scale: half an E4M3 step (2^-4) of each
+    # element, except a block maximum in [448, 512) * 2^e, which saturates to
+    # 448 * 2^e (at most 1/8 of the row maximum)
+    x = r.standard_normal((16, 96)) * np.exp2(np.linspace(-20, 20, 16))[:, None]
+    fq = O.mx_fake_quant(x, axis=1)
+    rel_rows = np.abs(fq - x).max(axis=1) / np.abs(x).max(axis=1)
+    assert (rel_rows <= 0.125).all()
+    wrong = O.mx_fake_quant(x, axis=0)           # blocks across rows lose the small rows
+    assert (np.abs(wrong - x).max(axis=1) / np.abs(x).max(axis=1)).max() > 0.5
+    assert np.array_equal(O.mx_fake_quant(fq, axis=1), fq)              # idempotent
+    assert np.array_equal(O.mx_fake_quant(x * 2.0 ** 7, axis=1), fq * 2.0 ** 7)   # power-of-two scale invariance
+
+
+def test_mxfp8_forward_reduces_to_exact_on_representable_operands():
+    """With x and weights already MXFP8-representable and h quantisation the
+    only rounding left, the quantisation-aware layer differs from the fp64
+    dense brute force by at most h's quantisation (relative 2^-4 per element)."""
+    p = _layer(24, 64, 64, 4, 2, seed=21)
+    for key in ("x", "w1", "w3", "w2"):
+        axis = 1 if p[key].ndim == 2 else 2
+        p[key] = O.mx_fake_quant(p[key], axis=axis).astype(np.float32)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, None, 2, "softmax")
+    out = O.moe_forward_mxfp8(p["x"], idx, g, p["w1"], p["w3"], p["w2"])
+    ref = O.moe_forward_dense_bruteforce(p["x"], idx, g, p["w1"], p["w3"], p["w2"])
+    e = np.linalg.norm(out - ref) / np.linalg.norm(ref)
+    assert 1e-4 < e < 6e-2          # h quantisation is visible, and bounded
