@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--sample", type=int, default=0, help="oracle token sample (0: automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="forward-only load-skew sweep, bf16 and MXFP8 (prints one JSON line of results)")
     return ap.parse_args()
 
 
@@ -312,8 +314,72 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def run_sweep(args):
+    """Forward-only timing of the layer under prescribed load skews, bf16 and
+    MXFP8 operands.  Routing comes from the workload's own gate and bias
+    ("bias") or from synthetic fp32 logits through moe_route_from_logits
+    (uniform, Zipf s=1, half of the tokens on expert 0)."""
+    import torch
+
+    from ragged_grouped_gemm_gb300 import api
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_layer, skewed_logits
+    base = CONFIGS[args.workload]
+    peaks = measured_peaks()
+    dev = torch.device("cuda", 0)
+    p = make_layer(base, dev)
+    results = []
+    for prec in ("bf16", "mxfp8"):
+        cfg = base.replace(precision=prec)
+        layer = api.MoELayer(cfg, p, train=False, device=dev)
+        b, d, ws = layer.buf, layer.desc, layer.ws
+        for skew in ("bias", "uniform", "zipf", "half0"):
+            lg = None if skew == "bias" else skewed_logits(cfg.n_tok, cfg.n_exp, skew).to(dev)
+            zero_bias = torch.zeros(cfg.n_exp, dtype=torch.float32, device=dev) if cfg.use_bias else None
+
+            def fwd():
+                if lg is None:
+                    return layer.forward(p["x"])
+                api.moe_route_from_logits(d, lg, zero_bias, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], ws)
+                if layer.mx:
+                    return layer._forward_mx(p["x"])
+                api.moe_permute(d, p["x"], b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
+                                b["x_perm"], ws)
+                api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], p["x"], p["w1"], p["w3"], p["w2"], p.get("ws1"),
+                                    p.get("ws3"), p.get("ws2"), None, None, b["h"], None, None, b["hs"], b["y_perm"],
+                                    b["y_shared"], ws)
+                api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
+                return b["out"]
+            for _ in range(args.warmup):
+                fwd()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                fwd()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            counts = b["counts"].cpu()
+            ne = int((counts > 0).sum())
+            wb = 3 * ne * cfg.d_ff * cfg.d_model + (3 * cfg.d_ff_shared * cfg.d_model if cfg.n_shared else 0)
+            wbytes = wb * (1 + 1 / 32) if prec == "mxfp8" else 2 * wb
+            results.append({"precision": prec, "skew": skew, "ms_fwd": ms, "tokens_per_s": cfg.n_tok / ms * 1e3,
+                            "experts_nonempty": ne, "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
+                            "weight_bytes": wbytes, "weight_stream_gbs": wbytes / ms / 1e6,
+                            "weight_stream_frac_of_hbm": wbytes / ms / 1e6 / peaks["hbm_gbs"],
+                            "tflops": flops(cfg)["ffn_fwd"] / ms / 1e9})
+            assert layer.device_status()[0] == 0
+        del layer
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": f"{base.name} forward, steps={args.steps}", "peaks": peaks, "results": results}),
+          flush=True)
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

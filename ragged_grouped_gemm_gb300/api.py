@@ -313,7 +313,8 @@ class MoELayer:
         b = self.buf
         moe_permute_mxfp8(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
                           b["xq_perm"], b["xs_perm"], b["xq_tok"], b["xs_tok"], self.ws, stream)
-        saved = {key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
+        saved = ({key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
+                 if self.train else {})
         moe_grouped_ffn_mxfp8(self.desc, b["xq_perm"], b["xs_perm"], b["offsets"], b["xq_tok"], b["xs_tok"], self.wq,
                               saved, b["y_perm"], b["y_shared"], self.ws, stream)
         moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
