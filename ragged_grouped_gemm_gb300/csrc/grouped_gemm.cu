@@ -12,7 +12,18 @@
 //               32*(w%4)..+31 = tile rows, and half (w-2)/4 of the columns),
 //               apply the fused epilogue and store.
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
-// main loop of tile i+1.  Tiles are walked in a persistent loop; for the
+// main loop of tile i+1.
+//
+// CTA-pair form (PAIR, ragged M, bf16 operands): a cluster of two CTAs on two
+// SMs shares one 256 x BN tile through tcgen05.mma.cta_group::2 (M = 256).
+// Each CTA loads its own 128 rows of A and half of the B tile (B columns
+// 0..BN/2-1 in rank 0, the rest in rank 1), so each SM streams half of the B
+// bytes it would need alone.  Both CTAs' TMA loads complete on rank 0's stage
+// barrier; rank 0's MMA lane issues for the pair and its commits arrive on
+// both CTAs' stage-release and accumulator-ready barriers (multicast).  Each
+// CTA's epilogue reads its own 128 TMEM lanes and signals rank 0's
+// accumulator-free barrier.  TMEM is allocated and freed by both CTAs
+// together, between cluster barriers.  Tiles are walked in a persistent loop; for the
 // ragged-M form the tile list is derived on the device from the group
 // offsets (prefix of per-group 128-row tile counts), so a launch needs no
 // host-side knowledge of the group sizes.
@@ -29,6 +40,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <cstdlib>
 #include <mutex>
 
 namespace moe {
@@ -71,9 +83,10 @@ struct KParams {
   int32_t* status;
 };
 
-template <int BN, bool QUANT = false>
+template <int BN, bool QUANT = false, bool PAIR = false>
 struct Cfg {
-  static constexpr int kStageBytes = (BM + BN) * BK * 2;
+  // PAIR: this CTA holds half of the B tile (the CTA pair shares a 256-row tile)
+  static constexpr int kStageBytes = (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
   static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
   static constexpr int kStages = QUANT ? 3 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
@@ -104,9 +117,11 @@ struct Tile {
   int num_kb;
 };
 
-template <bool RAGGED_K, int BN>
-__device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const int* s_off, const int* s_pre) {
+template <bool RAGGED_K, int BN, bool PAIR = false>
+__device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const int* s_off, const int* s_pre,
+                                            int rank = 0) {
   Tile t;
+  constexpr int UR = PAIR ? 2 * BM : BM;   // rows of one M unit (a CTA pair covers 256)
   if (!RAGGED_K) {
     // Expert-major raster: expert, then N tile, then M tile (innermost), so the
     // CTAs running at once share one expert's rows of A (L2-resident) and each
@@ -118,11 +133,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
       if (s_pre[mid] <= tile) lo = mid; else hi = mid;
     }
     t.g = lo;
-    const int mtiles = max(0, s_off[lo + 1] - s_off[lo] + BM - 1) / BM;
+    const int mtiles = max(0, s_off[lo + 1] - s_off[lo] + UR - 1) / UR;
     const int rem = tile - s_pre[lo];
     t.nt = rem / mtiles;
     t.mt = rem - t.nt * mtiles;
-    t.row0 = s_off[lo] + t.mt * BM;
+    t.row0 = s_off[lo] + t.mt * UR + rank * BM;
     t.rows_valid = min(BM, s_off[lo + 1] - t.row0);
     t.k_rows = 0;
     t.num_kb = p.kb0 + p.kb1;
@@ -175,9 +190,9 @@ __device__ __forceinline__ int mx_exponent_of(float amax) {
   return max(-127, min(127, fl - 8));
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<BN, QUANT>;
+  using C = Cfg<BN, QUANT, PAIR>;
   constexpr bool RAGGED_K = A_MN;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -197,6 +212,11 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.num_groups;
+  // CTA pair (2-SM MMA): rank 0 issues the MMAs for both CTAs
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kEpiThreads);
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * (kEpiThreads / 32));   // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -224,8 +244,13 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     }
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {   // collective: one warp of each CTA of the pair
+      tmem_alloc_pair(s_tmem, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(s_tmem, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   // group offsets and (ragged M) the prefix of per-group tile counts
   // (128-row M tiles times N tiles)
@@ -237,7 +262,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     const int lo = lane * per;
     const int hi = min(G, lo + per);
     int sum = 0;
-    for (int g = lo; g < hi; ++g) sum += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM * ntiles;
+    constexpr int UR = PAIR ? 2 * BM : BM;
+    for (int g = lo; g < hi; ++g) sum += max(0, s_off[g + 1] - s_off[g] + UR - 1) / UR * ntiles;
     int incl = sum;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -247,12 +273,13 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     int run = incl - sum;
     for (int g = lo; g < hi; ++g) {
       s_pre[g] = run;
-      run += max(0, s_off[g + 1] - s_off[g] + BM - 1) / BM * ntiles;
+      run += max(0, s_off[g + 1] - s_off[g] + UR - 1) / UR * ntiles;
     }
     if (lane == 31) s_pre[G] = incl;
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();   // the peer's barriers are initialised and its TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
@@ -270,8 +297,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       constexpr int QS = C::kQStages > 0 ? C::kQStages : 1;
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int qs = it % QS;
           const uint32_t qph = (it / QS) & 1u;
@@ -304,14 +331,31 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* sA = smem + s * C::kStageBytes;
           uint8_t* sB = sA + kABytes;
+          if (PAIR) {
+            // both CTAs' loads complete on the leader's barrier, armed by the leader
+            if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+            const int src = (kb < p.kb0) ? 0 : 1;
+            const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
+            tma_load_2d_pair(sA, &p.tmA[src], bar, k0, t.row0);
+            if (!B_MN) {
+              if (p.b_dual_n) tma_load_3d_pair(sB, &p.tmB[rank], bar, k0, t.nt * (BN / 2), t.g);  // W1 | W3 half
+              else tma_load_3d_pair(sB, &p.tmB[src], bar, k0, t.nt * BN + rank * (BN / 2), t.g);
+            } else {
+#pragma unroll
+              for (int a = 0; a < BN / 128; ++a)
+                tma_load_3d_pair(sB + a * 8192, &p.tmB[src], bar, t.nt * BN + rank * (BN / 2) + 64 * a, k0, t.g);
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           if (!RAGGED_K) {
             const int src = (kb < p.kb0) ? 0 : 1;
@@ -343,21 +387,24 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         }
       }
       // Wait (bounded) for every stage's last armed load so that no copy is
-      // still landing in shared memory when the CTA exits.
-      for (int s = 0; s < S; ++s) {
+      // still landing in shared memory when the CTA exits (for a pair the
+      // leader's barriers count both CTAs' copies).
+      for (int s = 0; s < S && (!PAIR || leader); ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = s + S * ((it - 1 - s) / S);
           mbar_wait_drain(&full[s], (last / S) & 1u);
         }
       }
     }
+  } else if (PAIR && warp == 1 && !leader) {
+    // the leader CTA issues the pair's MMAs
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
     uint32_t it = 0, tcount = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+    for (int tile = unit0; ok && tile < total_tiles; tile += ustride, ++tcount) {
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
@@ -401,22 +448,26 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
                                      : smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
                                      : smem_desc_sw128(b_base + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            if (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            else tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&empty[s]);
+          if (PAIR) tc_commit_pair_mc(&empty[s], 3);
+          else tc_commit(&empty[s]);
         }
         __syncwarp();
       }
       if (!ok) break;
       if (lane == 0) {
-        if (t.num_kb > 0) tc_commit(&tfull[buf]);
+        if (PAIR) tc_commit_pair_mc(&tfull[buf], 3);
+        else if (t.num_kb > 0) tc_commit(&tfull[buf]);
         else mbar_arrive(&tfull[buf]);
       }
       __syncwarp();
     }
     // every MMA issued by this CTA has completed before TMEM is released
     if (lane == 0) {
-      tc_commit(mma_done);
+      if (PAIR) tc_commit_pair_mc(mma_done, 1);
+      else tc_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
     __syncwarp();
@@ -427,8 +478,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       const int ct = threadIdx.x - 10 * 32;
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         const int a_rem = t.row0 & 15;
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int qs = it % QS;
@@ -469,8 +520,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     const int hf = (warp - 2) >> 2;   // column half of the tile
     const int r = q * 32 + lane;
     uint32_t tcount = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN>(tile, p, s_off, s_pre);
+    for (int tile = unit0; tile < total_tiles; tile += ustride, ++tcount) {
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tfull[buf], aph, s_abort, p.status, 400)) break;
@@ -724,7 +775,11 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+        else mbar_arrive(&tempty[buf]);
+      }
     }
     if (EPI == EPI_F32 && lane == 0) bulk_wait_group0();   // every TMA store of this warp has landed
     __syncwarp();
@@ -732,8 +787,12 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();   // the leader's MMAs into the peer's TMEM and all cross-CTA arrivals are done
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) {
+    if (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -814,20 +873,64 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false>
-cudaError_t launch_impl(const KParams& kp, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, QUANT>;
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false>
+cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
+  using C = Cfg<BN, QUANT, PAIR>;
   const size_t smem = C::smem_bytes(kp.num_groups);
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_units = 0;   // co-resident CTAs (or CTA pairs)
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::smem_bytes(kMaxGroups)));
+    max_units = PAIR ? num_sms() / 2 : num_sms();
+    if (attr_err == cudaSuccess && PAIR) {
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * max_units);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::smem_bytes(kMaxGroups);
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) max_units = n;
+      cudaGetLastError();
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
-  kern<<<grid, QUANT ? kThreadsQ : kThreads, smem, stream>>>(kp);
-  return cudaGetLastError();
+  const int units = static_cast<int>(units_ub < max_units ? units_ub : max_units);
+  if (!PAIR) {
+    kern<<<units, QUANT ? kThreadsQ : kThreads, smem, stream>>>(kp);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kp);
+}
+
+// 2-SM MMA (CTA pairs) for the ragged-M forms; MOE_GEMM_CTA_PAIR=0 selects
+// the one-SM path.
+bool use_cta_pair() {
+  static const bool on = [] {
+    const char* e = std::getenv("MOE_GEMM_CTA_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 }  // namespace
@@ -908,10 +1011,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
     const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
     tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
-    const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
-    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<256, false, false, EPI_SWIGLU_FWD_Q, true>(kp, grid, stream);
-    return launch_impl<256, false, false, EPI_BF16, true>(kp, grid, stream);
+    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<256, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
+    return launch_impl<256, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
   }
+  // CTA pairs: each CTA loads its 128 rows of A and half of the B tile
+  const bool pair = !a.ragged_k && BN == 256 && use_cta_pair() &&
+                    (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD);
   if (!a.ragged_k) {
     if (a.max_rows <= 0) return cudaSuccess;
     kp.kb0 = (a.k0 + BK - 1) / BK;
@@ -921,7 +1026,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     for (int s = 0; s < nsrc; ++s) {
       if (!make_map(&kp.tmA[s], a.a[s], 64, BM, false)) return cudaErrorInvalidValue;
       if (!a.b_mn) {
-        if (!make_map(&kp.tmB[s], a.b[s], 64, a.b_dual_n ? BN / 2 : BN, true)) return cudaErrorInvalidValue;
+        const int box_rows = (a.b_dual_n || pair) ? BN / 2 : BN;
+        if (!make_map(&kp.tmB[s], a.b[s], 64, box_rows, true)) return cudaErrorInvalidValue;
       } else {
         if (!make_map(&kp.tmB[s], a.b[s], 64, 64, true)) return cudaErrorInvalidValue;
       }
@@ -934,7 +1040,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       if (!a.b_dual_n) kp.tmB[1] = kp.tmB[0];
     }
     const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
-    tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+    const int64_t ur = pair ? 2 * BM : BM;
+    tiles_ub = ntiles * ((a.max_rows + ur - 1) / ur + a.num_groups);
   } else {
     if (a.m_size <= 0) return cudaSuccess;
     if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
@@ -952,25 +1059,33 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs) ? 1 : 0;
     kp.c_rows = static_cast<int32_t>(m);
   }
-  const int grid = static_cast<int>(tiles_ub < num_sms() ? tiles_ub : num_sms());
+  const int64_t u = tiles_ub;
 
-  if (BN == 32) return launch_impl<32, false, false, EPI_F32>(kp, grid, stream);
+  if (BN == 32) return launch_impl<32, false, false, EPI_F32>(kp, u, stream);
   if (!a.a_mn && !a.b_mn) {
     switch (a.epi) {
-      case EPI_BF16: return launch_impl<256, false, false, EPI_BF16>(kp, grid, stream);
-      case EPI_F32: return launch_impl<256, false, false, EPI_F32>(kp, grid, stream);
-      case EPI_SWIGLU_FWD: return launch_impl<256, false, false, EPI_SWIGLU_FWD>(kp, grid, stream);
+      case EPI_BF16:
+        return pair ? launch_impl<256, false, false, EPI_BF16, false, true>(kp, u, stream)
+                    : launch_impl<256, false, false, EPI_BF16>(kp, u, stream);
+      case EPI_F32: return launch_impl<256, false, false, EPI_F32>(kp, u, stream);
+      case EPI_SWIGLU_FWD:
+        return pair ? launch_impl<256, false, false, EPI_SWIGLU_FWD, false, true>(kp, u, stream)
+                    : launch_impl<256, false, false, EPI_SWIGLU_FWD>(kp, u, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   if (!a.a_mn && a.b_mn) {
     switch (a.epi) {
-      case EPI_BF16: return launch_impl<256, false, true, EPI_BF16>(kp, grid, stream);
-      case EPI_SWIGLU_BWD: return launch_impl<256, false, true, EPI_SWIGLU_BWD>(kp, grid, stream);
+      case EPI_BF16:
+        return pair ? launch_impl<256, false, true, EPI_BF16, false, true>(kp, u, stream)
+                    : launch_impl<256, false, true, EPI_BF16>(kp, u, stream);
+      case EPI_SWIGLU_BWD:
+        return pair ? launch_impl<256, false, true, EPI_SWIGLU_BWD, false, true>(kp, u, stream)
+                    : launch_impl<256, false, true, EPI_SWIGLU_BWD>(kp, u, stream);
       default: return cudaErrorInvalidValue;
     }
   }
-  if (a.a_mn && a.b_mn && a.epi == EPI_F32) return launch_impl<256, true, true, EPI_F32>(kp, grid, stream);
+  if (a.a_mn && a.b_mn && a.epi == EPI_F32) return launch_impl<256, true, true, EPI_F32>(kp, u, stream);
   return cudaErrorInvalidValue;
 }
 
