@@ -112,7 +112,8 @@ struct Cfg {
 struct Tile {
   int g, mt, nt;
   int row0;        // ragged M: first permuted row of the tile; ragged K: first row of the group
-  int rows_valid;  // ragged M: valid rows of the tile
+  int m0;          // ragged K: first output row of this CTA's 128 rows
+  int rows_valid;  // valid output rows of this CTA's 128 (may be <= 0 in a CTA pair)
   int k_rows;      // ragged K: rows of the group (contraction length)
   int num_kb;
 };
@@ -139,10 +140,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
     t.mt = rem - t.nt * mtiles;
     t.row0 = s_off[lo] + t.mt * UR + rank * BM;
     t.rows_valid = min(BM, s_off[lo + 1] - t.row0);
+    t.m0 = 0;
     t.k_rows = 0;
     t.num_kb = p.kb0 + p.kb1;
   } else {
-    const int mtiles = (p.m_size + BM - 1) / BM;
+    const int mtiles = (p.m_size + UR - 1) / UR;
     const int ntiles = (p.n_size + BN - 1) / BN;
     const int per_g = mtiles * ntiles;
     t.g = tile / per_g;
@@ -150,8 +152,9 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
     t.mt = rem / ntiles;
     t.nt = rem - t.mt * ntiles;
     t.row0 = s_off[t.g];
+    t.m0 = t.mt * UR + rank * BM;
     t.k_rows = s_off[t.g + 1] - s_off[t.g];
-    t.rows_valid = min(BM, p.m_size - t.mt * BM);
+    t.rows_valid = min(BM, p.m_size - t.m0);
     t.num_kb = (t.k_rows + BK - 1) / BK;
   }
   return t;
@@ -190,6 +193,30 @@ __device__ __forceinline__ int mx_exponent_of(float amax) {
   return max(-127, min(127, fl - 8));
 }
 
+// Ragged K: rows rv..nkk*16-1 of a k-block's operands belong to the next
+// group; zero them in this CTA's stage (A: 2 MN atoms, B: nb_atoms MN atoms,
+// each 64 K-rows x 128 B) and make the writes visible to the tensor cores.
+// Returns the number of K=16 steps that hold rows of the group.
+__device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int nb_atoms, int lane) {
+  if (rv >= BK) return BK / 16;
+  const int nkk = (rv + 15) / 16;
+  const int zrows = nkk * 16 - rv;
+  if (zrows > 0) {
+    const int nreg = 2 + nb_atoms;
+    const int per_reg = zrows * 8;  // 16-byte chunks
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = lane; i < nreg * per_reg; i += 32) {
+      const int reg = i / per_reg;
+      const int j = i - reg * per_reg;
+      uint8_t* base = (reg < 2) ? (sA + reg * 8192) : (sB + (reg - 2) * 8192);
+      *reinterpret_cast<uint4*>(base + rv * 128 + j * 16) = z;
+    }
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  return nkk;
+}
+
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
   using C = Cfg<BN, QUANT, PAIR>;
@@ -220,7 +247,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], QUANT ? kConvThreads : 1);   // TMA (tx bytes) or the converter threads
+      // TMA (tx bytes), the converter threads, or (ragged-K pair, rank 0) this
+      // CTA's TMA plus the peer's forwarded arrival
+      mbar_init(&full[s], QUANT ? kConvThreads : ((PAIR && RAGGED_K && leader) ? 2 : 1));
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < C::kQStages; ++s) {
@@ -287,7 +316,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
   if (!RAGGED_K) {
     total_tiles = s_pre[G];
   } else {
-    total_tiles = G * ((p.m_size + BM - 1) / BM) * ((p.n_size + BN - 1) / BN);
+    constexpr int UR = PAIR ? 2 * BM : BM;
+    total_tiles = G * ((p.m_size + UR - 1) / UR) * ((p.n_size + BN - 1) / BN);
   }
 
   if (warp == 0) {
@@ -339,7 +369,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* sA = smem + s * C::kStageBytes;
           uint8_t* sB = sA + kABytes;
-          if (PAIR) {
+          if (PAIR && !RAGGED_K) {
             // both CTAs' loads complete on the leader's barrier, armed by the leader
             if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
@@ -376,20 +406,23 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
                 tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
             }
           } else {
+            // (a CTA pair: this CTA's 128 output rows and half of the N tile,
+            // completing on its own barrier)
             const int r = t.row0 + kb * BK;
-            const int m0 = t.mt * BM;
-            tma_load_2d(sA, &p.tmA[0], &full[s], m0, r);
-            tma_load_2d(sA + 8192, &p.tmA[0], &full[s], m0 + 64, r);
+            tma_load_2d(sA, &p.tmA[0], &full[s], t.m0, r);
+            tma_load_2d(sA + 8192, &p.tmA[0], &full[s], t.m0 + 64, r);
+            constexpr int NB = PAIR ? BN / 128 : BN / 64;
+            const int n0 = t.nt * BN + (PAIR ? rank * (BN / 2) : 0);
 #pragma unroll
-            for (int a = 0; a < BN / 64; ++a)
-              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], t.nt * BN + 64 * a, r);
+            for (int a = 0; a < NB; ++a)
+              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], n0 + 64 * a, r);
           }
         }
       }
       // Wait (bounded) for every stage's last armed load so that no copy is
-      // still landing in shared memory when the CTA exits (for a pair the
-      // leader's barriers count both CTAs' copies).
-      for (int s = 0; s < S && (!PAIR || leader); ++s) {
+      // still landing in shared memory when the CTA exits (for a ragged-M
+      // pair the leader's barriers count both CTAs' copies).
+      for (int s = 0; s < S && (!PAIR || RAGGED_K || leader); ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = s + S * ((it - 1 - s) / S);
           mbar_wait_drain(&full[s], (last / S) & 1u);
@@ -397,7 +430,31 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       }
     }
   } else if (PAIR && warp == 1 && !leader) {
-    // the leader CTA issues the pair's MMAs
+    // The leader CTA issues the pair's MMAs.  Ragged K: this warp waits for
+    // each of this CTA's stages, zeroes its rows past the group's end and
+    // forwards the stage to the leader's barrier.
+    if (RAGGED_K) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 600 + s)) { ok = false; break; }
+          uint8_t* sA = smem + s * C::kStageBytes;
+          const bool tail = t.k_rows - kb * BK < BK;
+          zero_k_tail(sA, sA + kABytes, t.k_rows - kb * BK, BN / 128, lane);
+          if (lane == 0) {
+            // after zeroing, release the writes to the leader's MMA
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+            if (tail) mbar_arrive_cluster(bar);
+            else mbar_arrive_remote(bar);
+          }
+          __syncwarp();
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
@@ -417,29 +474,10 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         tc_fence_after();
         uint8_t* sA = smem + s * C::kStageBytes;
         uint8_t* sB = sA + kABytes;
-        int nkk = BK / 16;
-        if (RAGGED_K) {
-          const int rv = min(BK, t.k_rows - kb * BK);
-          if (rv < BK) {
-            // Rows past the group's end belong to the next expert: zero them
-            // up to the next multiple of 16 and skip the empty K=16 steps.
-            nkk = (rv + 15) / 16;
-            const int zrows = nkk * 16 - rv;
-            if (zrows > 0) {
-              const int nreg = 2 + BN / 64;
-              const int per_reg = zrows * 8;  // 16-byte chunks
-              const uint4 z = make_uint4(0, 0, 0, 0);
-              for (int i = lane; i < nreg * per_reg; i += 32) {
-                const int reg = i / per_reg;
-                const int j = i - reg * per_reg;
-                uint8_t* base = (reg < 2) ? (sA + reg * 8192) : (sB + (reg - 2) * 8192);
-                *reinterpret_cast<uint4*>(base + rv * 128 + j * 16) = z;
-              }
-              fence_proxy_async_smem();
-            }
-            __syncwarp();
-          }
-        }
+        // Ragged K: rows past the group's end belong to the next expert;
+        // they are zeroed up to the next multiple of 16 and the empty K=16
+        // steps are skipped (a pair's peer zeroes its own stage).
+        const int nkk = RAGGED_K ? zero_k_tail(sA, sB, t.k_rows - kb * BK, PAIR ? BN / 128 : BN / 64, lane) : BK / 16;
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA);
           const uint32_t b_base = smem_u32(sB);
@@ -534,7 +572,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         if (!RAGGED_K) {
           grow = t.row0 + r;
         } else {
-          grow = static_cast<int64_t>(t.mt) * BM + r;
+          grow = static_cast<int64_t>(t.m0) + r;
           obase += static_cast<int64_t>(t.g) * p.group_stride_out * (EPI == EPI_F32 ? 4 : 2);
         }
         const bool zero = RAGGED_K && t.num_kb == 0;
@@ -569,7 +607,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
             if (lane == 0) {
               // boxes that start past the output's last column or row hold nothing to write
               const int col = t.nt * BN + c_begin + 16 * i;
-              const int row = RAGGED_K ? t.mt * BM + q * 32 : t.row0 + q * 32;
+              const int row = RAGGED_K ? t.m0 + q * 32 : t.row0 + q * 32;
               const int rows = RAGGED_K ? p.m_size : p.c_rows;
               if (col < p.n_size && row < rows) {
                 tma_store_3d(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0);
@@ -777,7 +815,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+        if (PAIR) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[buf]), 0));
         else mbar_arrive(&tempty[buf]);
       }
     }
@@ -1015,8 +1053,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     return launch_impl<256, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
   }
   // CTA pairs: each CTA loads its 128 rows of A and half of the B tile
-  const bool pair = !a.ragged_k && BN == 256 && use_cta_pair() &&
-                    (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD);
+  const bool pair = BN == 256 && use_cta_pair() &&
+                    (a.ragged_k ? a.epi == EPI_F32
+                                : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));
   if (!a.ragged_k) {
     if (a.max_rows <= 0) return cudaSuccess;
     kp.kb0 = (a.k0 + BK - 1) / BK;
@@ -1048,7 +1087,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     kp.tmA[1] = kp.tmA[0];
     kp.tmB[1] = kp.tmB[0];
-    tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + BN - 1) / BN);
+    const int64_t ur = pair ? 2 * BM : BM;
+    tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + ur - 1) / ur) * ((a.n_size + BN - 1) / BN);
   }
   if (tiles_ub <= 0) return cudaSuccess;
   // fp32 outputs go through TMA stores when every tile's rows either belong to
@@ -1085,7 +1125,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       default: return cudaErrorInvalidValue;
     }
   }
-  if (a.a_mn && a.b_mn && a.epi == EPI_F32) return launch_impl<256, true, true, EPI_F32>(kp, u, stream);
+  if (a.a_mn && a.b_mn && a.epi == EPI_F32)
+    return pair ? launch_impl<256, true, true, EPI_F32, false, true>(kp, u, stream)
+                : launch_impl<256, true, true, EPI_F32>(kp, u, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -252,9 +252,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier given by its shared::cluster address (may be the peer's).
+// Arrive on an mbarrier given by its shared::cluster address (may be the
+// peer's), releasing this thread's prior writes at cluster scope (a memory
+// barrier: use only after writes the waiter must see).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// The same arrival with default (CTA-scope) semantics: a signal that orders
+// no generic-proxy writes of this thread for the waiter (completed TMEM loads,
+// TMA data observed complete).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA tile loads into this CTA's shared memory that complete on an mbarrier
 // of either CTA of the pair (bar = shared::cluster address).
