@@ -12,21 +12,23 @@
 //               32*(w%4)..+31 = tile rows, and half (w-2)/4 of the columns),
 //               apply the fused epilogue and store.
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
-// main loop of tile i+1.
-//
-// CTA-pair form (PAIR, ragged M, bf16 operands): a cluster of two CTAs on two
-// SMs shares one 256 x BN tile through tcgen05.mma.cta_group::2 (M = 256).
-// Each CTA loads its own 128 rows of A and half of the B tile (B columns
-// 0..BN/2-1 in rank 0, the rest in rank 1), so each SM streams half of the B
-// bytes it would need alone.  Both CTAs' TMA loads complete on rank 0's stage
-// barrier; rank 0's MMA lane issues for the pair and its commits arrive on
-// both CTAs' stage-release and accumulator-ready barriers (multicast).  Each
-// CTA's epilogue reads its own 128 TMEM lanes and signals rank 0's
-// accumulator-free barrier.  TMEM is allocated and freed by both CTAs
-// together, between cluster barriers.  Tiles are walked in a persistent loop; for the
+// main loop of tile i+1.  Tiles are walked in a persistent loop; for the
 // ragged-M form the tile list is derived on the device from the group
-// offsets (prefix of per-group 128-row tile counts), so a launch needs no
-// host-side knowledge of the group sizes.
+// offsets (prefix of per-group tile counts), so a launch needs no host-side
+// knowledge of the group sizes.
+//
+// CTA-pair form (PAIR, bf16 operands): a cluster of two CTAs on two SMs
+// shares one 256 x BN tile through tcgen05.mma.cta_group::2 (M = 256).  Each
+// CTA loads its own 128 rows of the output's A operand and half of the B tile
+// (B columns 0..BN/2-1 in rank 0, the rest in rank 1), so each SM streams
+// half of the B bytes it would need alone.  Rank 0's MMA lane issues for the
+// pair and its commits arrive on both CTAs' stage-release and
+// accumulator-ready barriers (multicast).  Ragged M: both CTAs' TMA loads
+// complete on rank 0's stage barrier.  Ragged K: each CTA's loads complete on
+// its own barrier; the peer's idle MMA warp zeroes its rows past the group's
+// end and forwards the stage to rank 0.  Each CTA's epilogue reads its own
+// 128 TMEM lanes and signals rank 0's accumulator-free barrier.  TMEM is
+// allocated and freed by both CTAs together, between cluster barriers.
 //
 // Shared-memory operand layouts (both 1024-byte aligned per stage):
 //   K-major : rows of 64 bf16 (128 B), 8-row swizzle atoms of 1024 B;
@@ -360,6 +362,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       }
     } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
+      uint32_t lph = 0, lused = 0;   // ragged-K pair peer: phases of its own stage barriers
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
@@ -369,6 +372,37 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* sA = smem + s * C::kStageBytes;
           uint8_t* sB = sA + kABytes;
+          if (PAIR && RAGGED_K) {
+            // A k-block whose group rows end off a 16-row boundary is loaded
+            // into each CTA's own barrier and zeroed past the group's end
+            // before the MMA (the peer forwards it); any other k-block loads
+            // straight onto the leader's barrier, which also counts one
+            // arrival from the peer's producer.
+            const int rv = t.k_rows - kb * BK;
+            const bool zfix = rv < BK && (rv & 15) != 0;
+            const int r = t.row0 + kb * BK;
+            const int n0 = t.nt * BN + rank * (BN / 2);
+            if (!zfix) {
+              if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+              const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+              tma_load_2d_pair(sA, &p.tmA[0], bar, t.m0, r);
+              tma_load_2d_pair(sA + 8192, &p.tmA[0], bar, t.m0 + 64, r);
+#pragma unroll
+              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, &p.tmB[0], bar, n0 + 64 * a, r);
+              if (!leader) mbar_arrive_remote(bar);
+            } else {
+              mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+              tma_load_2d(sA, &p.tmA[0], &full[s], t.m0, r);
+              tma_load_2d(sA + 8192, &p.tmA[0], &full[s], t.m0 + 64, r);
+#pragma unroll
+              for (int a = 0; a < BN / 128; ++a) tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], n0 + 64 * a, r);
+              if (!leader) {
+                lph ^= 1u << s;
+                lused |= 1u << s;
+              }
+            }
+            continue;
+          }
           if (PAIR && !RAGGED_K) {
             // both CTAs' loads complete on the leader's barrier, armed by the leader
             if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
@@ -406,51 +440,47 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
                 tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
             }
           } else {
-            // (a CTA pair: this CTA's 128 output rows and half of the N tile,
-            // completing on its own barrier)
             const int r = t.row0 + kb * BK;
             tma_load_2d(sA, &p.tmA[0], &full[s], t.m0, r);
             tma_load_2d(sA + 8192, &p.tmA[0], &full[s], t.m0 + 64, r);
-            constexpr int NB = PAIR ? BN / 128 : BN / 64;
-            const int n0 = t.nt * BN + (PAIR ? rank * (BN / 2) : 0);
 #pragma unroll
-            for (int a = 0; a < NB; ++a)
-              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], n0 + 64 * a, r);
+            for (int a = 0; a < BN / 64; ++a)
+              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], t.nt * BN + 64 * a, r);
           }
         }
       }
       // Wait (bounded) for every stage's last armed load so that no copy is
-      // still landing in shared memory when the CTA exits (for a ragged-M
-      // pair the leader's barriers count both CTAs' copies).
-      for (int s = 0; s < S && (!PAIR || RAGGED_K || leader); ++s) {
+      // still landing in shared memory when the CTA exits (for a pair the
+      // leader's barriers count both CTAs' copies, except the peer's
+      // zero-fixed ragged-K blocks, which land on its own barriers).
+      for (int s = 0; s < S && (!PAIR || leader); ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = s + S * ((it - 1 - s) / S);
           mbar_wait_drain(&full[s], (last / S) & 1u);
         }
       }
+      for (int s = 0; s < S && PAIR && RAGGED_K && !leader; ++s)
+        if ((lused >> s) & 1u) mbar_wait_drain(&full[s], ((lph >> s) & 1u) ^ 1u);
     }
   } else if (PAIR && warp == 1 && !leader) {
-    // The leader CTA issues the pair's MMAs.  Ragged K: this warp waits for
-    // each of this CTA's stages, zeroes its rows past the group's end and
-    // forwards the stage to the leader's barrier.
+    // The leader CTA issues the pair's MMAs.  Ragged K: for each k-block
+    // whose group rows end off a 16-row boundary this warp waits for the
+    // CTA's own copy, zeroes the rows past the group's end and releases the
+    // stage to the leader's barrier.
     if (RAGGED_K) {
-      uint32_t it = 0;
+      uint32_t it = 0, lph = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int rv = t.k_rows - kb * BK;
+          if (rv >= BK || (rv & 15) == 0) continue;
           const int s = it % S;
-          const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 600 + s)) { ok = false; break; }
+          if (!mbar_wait_bounded(&full[s], (lph >> s) & 1u, s_abort, p.status, 600 + s)) { ok = false; break; }
+          lph ^= 1u << s;
           uint8_t* sA = smem + s * C::kStageBytes;
-          const bool tail = t.k_rows - kb * BK < BK;
-          zero_k_tail(sA, sA + kABytes, t.k_rows - kb * BK, BN / 128, lane);
-          if (lane == 0) {
-            // after zeroing, release the writes to the leader's MMA
-            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-            if (tail) mbar_arrive_cluster(bar);
-            else mbar_arrive_remote(bar);
-          }
+          zero_k_tail(sA, sA + kABytes, rv, BN / 128, lane);
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&full[s]), 0));
           __syncwarp();
         }
       }
