@@ -991,14 +991,16 @@ cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, kern, kp);
 }
 
-// 2-SM MMA (CTA pairs) for the ragged-M forms; MOE_GEMM_CTA_PAIR=0 selects
-// the one-SM path.
-bool use_cta_pair() {
-  static const bool on = [] {
-    const char* e = std::getenv("MOE_GEMM_CTA_PAIR");
-    return !(e && e[0] == '0');
-  }();
-  return on;
+// 2-SM MMA (CTA pairs) is chosen when the groups average at least 512 rows:
+// a pair tile spans 256 rows (ragged M), so smaller groups leave tiles half
+// empty, and short contractions (ragged K) are bound by the fp32 output
+// writes, where the pair gains nothing.  MOE_GEMM_CTA_PAIR=0 or =1 forces the
+// one-SM or the pair form (read at every launch).
+bool use_cta_pair(int64_t rows, int groups) {
+  const char* e = std::getenv("MOE_GEMM_CTA_PAIR");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  return rows >= 512LL * groups;
 }
 
 }  // namespace
@@ -1083,7 +1085,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     return launch_impl<256, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
   }
   // CTA pairs: each CTA loads its 128 rows of A and half of the B tile
-  const bool pair = BN == 256 && use_cta_pair() &&
+  const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&
                     (a.ragged_k ? a.epi == EPI_F32
                                 : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));
   if (!a.ragged_k) {

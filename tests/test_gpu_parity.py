@@ -41,6 +41,14 @@ def _status_ok(ws):
     assert bits == 0, f"device status {bits} (site {site})"
 
 
+@pytest.fixture(params=["1", "0"], ids=["cta_pair", "one_sm"])
+def gemm_form(request, monkeypatch):
+    """Runs a test with the grouped GEMMs forced to the 2-SM (CTA pair) or the
+    one-SM form; by default the library picks the form from the group sizes."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", request.param)
+    return request.param
+
+
 def _layer(name):
     cfg = CONFIGS[name] if isinstance(name, str) else name
     p_cpu = make_layer(cfg, "cpu")
@@ -131,7 +139,7 @@ def _oracle_route(cfg, h):
 
 
 @pytest.mark.parametrize("name", SMALL)
-def test_grouped_ffn(name):
+def test_grouped_ffn(name, gemm_form):
     cfg, p, h = _layer(name)
     n, dm, f, e, k = cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k
     r, fs = cfg.rows, cfg.d_ff_shared
@@ -214,7 +222,7 @@ def _expert_mask(idx_gpu, idx_ref, same, e):
 
 
 @pytest.mark.parametrize("name", SMALL)
-def test_backward_end_to_end(name):
+def test_backward_end_to_end(name, gemm_form):
     cfg, p, h = _layer(name)
     dy = make_dy(cfg, "cpu")
     layer, out, gr = _run_layer(cfg, p, dy.cuda())
@@ -266,7 +274,7 @@ EDGE = [
 
 
 @pytest.mark.parametrize("cfg", EDGE, ids=lambda c: c.name)
-def test_edge_cases(cfg):
+def test_edge_cases(cfg, gemm_form):
     p_cpu = make_layer(cfg, "cpu")
     p, h = to_dev(p_cpu), host_params(p_cpu)
     dy = make_dy(cfg, "cpu")
