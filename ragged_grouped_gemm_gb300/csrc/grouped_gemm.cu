@@ -51,9 +51,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 320;        // producer, MMA, 8 epilogue warps
-constexpr int kThreadsQ = 576;       // + 8 converter warps (MXFP8 operands)
+constexpr int kThreadsQ = 448;       // + 4 scale-factor warps (MXFP8 operands)
 constexpr int kEpiThreads = 256;
-constexpr int kConvThreads = 256;
+constexpr int kSfWarps = 4;
 
 constexpr int kMaxGroups = 1024;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
@@ -87,24 +87,29 @@ struct KParams {
 
 template <int BN, bool QUANT = false, bool PAIR = false>
 struct Cfg {
-  // PAIR: this CTA holds half of the B tile (the CTA pair shares a 256-row tile)
-  static constexpr int kStageBytes = (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-  static constexpr int kStages = QUANT ? 3 : (kStagesRaw > 6 ? 6 : kStagesRaw);
-  static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  // MXFP8 staging stage: A codes [128][64] | B codes [256][64] | A scales
-  // [2][144] (rows from a 16-aligned start) | B scales 2 x [2][128]
-  static constexpr int kQStages = QUANT ? 2 : 0;
-  static constexpr int kQStageBytes = 25600;
-  static constexpr int kQACodes = 0, kQBCodes = 8192, kQAScales = 24576, kQBScales = 24960;
-  static constexpr uint32_t kQTxBytes = 8192 + 16384 + 2 * 144 + 2 * 2 * 128;
-  // stages | MXFP8 staging | epilogue staging (8 warps x 32x16 fp32) |
-  // barriers (2S + 2QS + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
-  static constexpr int kQOff = kStages * kStageBytes;
-  static constexpr int kEpiOff = kQOff + kQStages * kQStageBytes;
+  // MXFP8 (QUANT) stage, one k-block of 128 E4M3 elements = 4 scale blocks:
+  //   A codes [128][128] | B codes [BN][128] (both 128-byte swizzled) |
+  //   A scale rows [4][144] (from a 16-aligned row) | B scale rows [4][BN] |
+  //   scale atoms for tcgen05.cp: A 512 B, B 2 x 512 B
+  static constexpr int kQBCodes = BM * 128;
+  static constexpr int kQARaw = kQBCodes + BN * 128;
+  static constexpr int kQBRaw = kQARaw + 640;
+  static constexpr int kQAtoms = kQBRaw + 4 * BN;
+  static constexpr uint32_t kQTxBytes = BM * 128 + BN * 128 + 4 * 144 + 4 * BN;
+  // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
+  static constexpr int kStageBytes =
+      QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
+  static constexpr int kStagesRaw = (QUANT ? 206 * 1024 : 200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
+  static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
+  static constexpr uint32_t kSfCol = 2 * BN;
+  // stages | epilogue staging (8 warps x 32x16 fp32) |
+  // barriers (2S, + S scale-ready for MXFP8, + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
+  static constexpr int kEpiOff = kStages * kStageBytes;
   static constexpr int kEpiBytes = 4 * 4096;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
-  static constexpr int kMiscOff = kBarOff + (2 * kStages + 2 * kQStages + 5) * 8;
+  static constexpr int kMiscOff = kBarOff + ((QUANT ? 3 : 2) * kStages + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr size_t smem_bytes(int groups) {
     return 1024 + kOffOff + 2 * 4 * (groups + 1);
@@ -170,23 +175,6 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float sigmoidf_fast(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
-// E4M3 codes (16, little-endian in a uint4) times a power-of-two scale -> 8 bf16x2 words (exact).
-__device__ __forceinline__ void dequant16(const uint4 c, float sc, uint32_t (&w)[8]) {
-  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const __half2_raw hr =
-          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[i] >> (16 * hh)), __NV_E4M3);
-      __half2 h2;
-      *reinterpret_cast<__half2_raw*>(&h2) = hr;
-      const float2 f = __half22float2(h2);
-      w[2 * i + hh] = pack_bf16x2(f.x * sc, f.y * sc);
-    }
-  }
-}
-
 __device__ __forceinline__ int mx_exponent_of(float amax) {
   if (!(amax > 0.0f)) return -127;
   const uint32_t b = __float_as_uint(amax);
@@ -228,9 +216,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + S;
-  uint64_t* qfull = empty + S;            // MXFP8 staging ring (QUANT only)
-  uint64_t* qempty = qfull + C::kQStages;
-  uint64_t* tfull = qempty + C::kQStages;
+  uint64_t* sready = empty + S;           // MXFP8: scale atoms of the stage built
+  uint64_t* tfull = sready + (QUANT ? S : 0);
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -251,13 +238,10 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     for (int s = 0; s < S; ++s) {
       // TMA (tx bytes), the converter threads, or (ragged-K pair, rank 0) this
       // CTA's TMA plus the peer's forwarded arrival
-      mbar_init(&full[s], QUANT ? kConvThreads : ((PAIR && RAGGED_K && leader) ? 2 : 1));
+      mbar_init(&full[s], (PAIR && RAGGED_K && leader) ? 2 : 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < C::kQStages; ++s) {
-      mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kConvThreads);
-    }
+    for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], kSfWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], (PAIR ? 2 : 1) * (kEpiThreads / 32));   // one arrival per epilogue warp
@@ -272,6 +256,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     if (QUANT) {
       tma_prefetch_desc(&p.tmA[1]);
       tma_prefetch_desc(&p.tmBs[0]);
+      tma_prefetch_desc(&p.tmB[1]);
+      tma_prefetch_desc(&p.tmBs[1]);
     }
   }
   if (warp == 1) {
@@ -325,39 +311,37 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (QUANT && lane == 0) {
-      // MXFP8 operands: codes and scales of each k-block into the staging ring
-      constexpr int QS = C::kQStages > 0 ? C::kQStages : 1;
+      // MXFP8 operands: E4M3 codes (128-byte swizzled, straight to the MMA) and
+      // the raw scale rows of each 128-element k-block
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
-          const int qs = it % QS;
-          const uint32_t qph = (it / QS) & 1u;
-          if (!mbar_wait_bounded(&qempty[qs], qph ^ 1u, s_abort, p.status, 110 + qs)) { ok = false; break; }
-          uint8_t* q = smem + C::kQOff + qs * C::kQStageBytes;
-          mbar_arrive_expect_tx(&qfull[qs], C::kQTxBytes);
-          const int k0 = kb * BK;
-          const int a_x = t.row0 & ~15;   // scale rows start at a 16-byte boundary
-          tma_load_2d(q + C::kQACodes, &p.tmA[0], &qfull[qs], k0, t.row0);
-          tma_load_2d(q + C::kQAScales, &p.tmA[1], &qfull[qs], a_x, kb * 2);
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
+          uint8_t* st = smem + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], C::kQTxBytes);
+          const int k0 = kb * 128;
+          tma_load_2d(st, &p.tmA[0], &full[s], k0, t.row0);
+          tma_load_2d(st + C::kQARaw, &p.tmA[1], &full[s], t.row0 & ~15, kb * 4);   // 16-byte aligned x
           if (p.b_dual_n) {
             const int f0 = t.nt * (BN / 2);
-            tma_load_3d(q + C::kQBCodes, &p.tmB[0], &qfull[qs], k0, f0, t.g);
-            tma_load_3d(q + C::kQBCodes + (BN / 2) * 64, &p.tmB[1], &qfull[qs], k0, f0, t.g);
-            tma_load_3d(q + C::kQBScales, &p.tmBs[0], &qfull[qs], f0, kb * 2, t.g);
-            tma_load_3d(q + C::kQBScales + 256, &p.tmBs[1], &qfull[qs], f0, kb * 2, t.g);
+            tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, f0, t.g);
+            tma_load_3d(st + C::kQBCodes + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
+            tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], f0, kb * 4, t.g);
+            tma_load_3d(st + C::kQBRaw + 2 * BN, &p.tmBs[1], &full[s], f0, kb * 4, t.g);
           } else {
-            tma_load_3d(q + C::kQBCodes, &p.tmB[0], &qfull[qs], k0, t.nt * BN, t.g);
-            tma_load_3d(q + C::kQBScales, &p.tmBs[0], &qfull[qs], t.nt * BN, kb * 2, t.g);
-            tma_load_3d(q + C::kQBScales + 256, &p.tmBs[0], &qfull[qs], t.nt * BN + 128, kb * 2, t.g);
+            tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, t.nt * BN, t.g);
+            tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], t.nt * BN, kb * 4, t.g);
           }
         }
       }
-      for (int s = 0; s < QS; ++s) {
+      for (int s = 0; s < S; ++s) {
         if (it > static_cast<uint32_t>(s)) {
-          const uint32_t last = s + QS * ((it - 1 - s) / QS);
-          mbar_wait_drain(&qfull[s], (last / QS) & 1u);
+          const uint32_t last = s + S * ((it - 1 - s) / S);
+          mbar_wait_drain(&full[s], (last / S) & 1u);
         }
       }
     } else if (!QUANT && lane == 0) {
@@ -485,6 +469,58 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         }
       }
     }
+  } else if (warp == 1 && QUANT) {
+    // ------------------------------------------------------------ MMA issuer (MXFP8)
+    // Per k-block: the scale atoms go to tensor memory by tcgen05.cp, then four
+    // block-scaled MMAs (K = 32 each) select scale byte 0..3.  Both are issued
+    // by the same thread, so the copies are ordered before the MMAs.
+    uint32_t it = 0, tcount = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < total_tiles; tile += ustride, ++tcount) {
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
+      const uint32_t buf = tcount & 1u;
+      const uint32_t aph = (tcount >> 1) & 1u;
+      if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        if (!mbar_wait_bounded(&sready[s], ph, s_abort, p.status, 320 + s)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint8_t* st = smem + s * C::kStageBytes;
+          // one 16-column scale buffer per stage (A: +0..3, B: +4..11): a buffer is
+          // rewritten only after the MMAs that read it have completed (stage release)
+          const uint32_t sf = tmem_base + C::kSfCol + s * 16;
+          const uint32_t atoms = smem_u32(st + C::kQAtoms);
+          tc_cp_32x128b_warpx4(sf, atoms);
+          tc_cp_32x128b_warpx4(sf + 4, atoms + 512);
+          if (BN > 128) tc_cp_32x128b_warpx4(sf + 8, atoms + 1024);
+          const uint32_t a_base = smem_u32(st);
+          const uint32_t b_base = smem_u32(st + C::kQBCodes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sf, sf + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (t.num_kb > 0) tc_commit(&tfull[buf]);
+        else mbar_arrive(&tfull[buf]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      tc_commit(mma_done);
+      mbar_wait_drain(mma_done, 0);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
@@ -540,45 +576,44 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     }
     __syncwarp();
   } else if (warp >= 10) {
-    // ------------------------------------------------------------ converters (MXFP8)
+    // ------------------------------------------------------------ scale atoms (MXFP8)
+    // Rearrange the stage's raw scale rows ([block][row]) into the 512-byte
+    // atoms tcgen05.cp expects: for row r, byte j (scale block) of 32-bit word
+    // (r/32)%4 of 16-byte row r%32; one atom per 128 rows of A or of B.
     if (QUANT) {
-      constexpr int QS = C::kQStages > 0 ? C::kQStages : 1;
-      const int ct = threadIdx.x - 10 * 32;
+      const int ct = threadIdx.x - 10 * 32;   // 0..127
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         const int a_rem = t.row0 & 15;
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
-          const int qs = it % QS;
-          const uint32_t qph = (it / QS) & 1u;
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait_bounded(&qfull[qs], qph, s_abort, p.status, 500 + qs)) { ok = false; break; }
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 520 + s)) { ok = false; break; }
-          const uint8_t* q = smem + C::kQOff + qs * C::kQStageBytes;
-          uint8_t* dst = smem + s * C::kStageBytes;
-          // 384 operand rows (128 of A, 256 of B) x 4 chunks of 16 codes
-          for (int task = ct; task < (BM + BN) * 4; task += kConvThreads) {
-            const int row = task >> 2;
-            const int j = task & 3;
-            const bool is_a = row < BM;
-            const int rb = is_a ? row : row - BM;
-            const uint4 codes = *reinterpret_cast<const uint4*>(q + (is_a ? C::kQACodes : C::kQBCodes) + rb * 64 + j * 16);
-            const int kbl = j >> 1;
-            const uint32_t sb = is_a ? q[C::kQAScales + kbl * 144 + a_rem + rb]
-                                     : q[C::kQBScales + (rb >> 7) * 256 + kbl * 128 + (rb & 127)];
-            const float sc = __uint_as_float(sb ? (sb << 23) : 0x00400000u);
-            uint32_t w[8];
-            dequant16(codes, sc, w);
-            uint8_t* rowp = dst + (is_a ? rb * 128 : kABytes + rb * 128);
-            const int sw = rb & 7;
-            *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 500 + s)) { ok = false; break; }
+          uint8_t* st = smem + s * C::kStageBytes;
+          const uint8_t* ra = st + C::kQARaw;
+          const uint8_t* rb = st + C::kQBRaw;
+          uint32_t* atoms = reinterpret_cast<uint32_t*>(st + C::kQAtoms);
+          {
+            const int r = ct;
+            const uint32_t w = static_cast<uint32_t>(ra[a_rem + r]) | (static_cast<uint32_t>(ra[144 + a_rem + r]) << 8) |
+                               (static_cast<uint32_t>(ra[288 + a_rem + r]) << 16) |
+                               (static_cast<uint32_t>(ra[432 + a_rem + r]) << 24);
+            atoms[(r & 31) * 4 + (r >> 5)] = w;
+          }
+          for (int r = ct; r < BN; r += 128) {
+            // dual N: rows [0, BN/2) from the W1 scale rows, the rest from W3's
+            const int half = p.b_dual_n ? (r >= BN / 2 ? 1 : 0) : 0;
+            const int w_ = p.b_dual_n ? BN / 2 : BN;
+            const uint8_t* src = rb + half * 2 * BN + (r - half * (BN / 2));
+            const uint32_t w = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[w_]) << 8) |
+                               (static_cast<uint32_t>(src[2 * w_]) << 16) | (static_cast<uint32_t>(src[3 * w_]) << 24);
+            atoms[128 + (r >> 7) * 128 + (r & 31) * 4 + ((r >> 5) & 3)] = w;
           }
           fence_proxy_async_smem();
-          mbar_arrive(&full[s]);
-          mbar_arrive(&qempty[qs]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sready[s]);
         }
       }
     }
@@ -733,8 +768,10 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
         // (each thread owns a row, so a block's amax is thread-local)
         const int64_t grow = t.row0 + r;
         const int f0 = t.nt * (BN / 2);
+        // 32-column quantisation blocks of the BN/2 f columns, alternating between
+        // the two warps of this lane quarter
 #pragma unroll 1
-        for (int c = hf * (BN / 4); c < (hf + 1) * (BN / 4); c += 32) {
+        for (int c = 32 * hf; c < BN / 2; c += 64) {
           const int col = f0 + c;
           const bool ok = row_ok && col < p.n_size;
           const int64_t off = grow * p.ld_out + col;
@@ -919,9 +956,10 @@ bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// uint8 tensor map (MXFP8 codes or scales), no swizzle, zero fill.
+// uint8 tensor map (MXFP8 codes, 128-byte swizzled for the MMA, or scales,
+// unswizzled), zero fill.
 bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                 const uint32_t* box) {
+                 const uint32_t* box, bool swizzle128 = false) {
   EncodeFn enc = get_encode_fn();
   if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
   cuuint64_t d[3];
@@ -937,8 +975,8 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
     }
   }
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, b, e,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false>
@@ -1045,34 +1083,39 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
 
   int64_t tiles_ub = 0;
   if (a.quant) {
-    // MXFP8 operands: K-major A and B only, one contraction source, BN = 256
-    if (a.ragged_k || a.a_mn || a.b_mn || BN != 256 || a.k1 != 0 || a.max_rows <= 0) return cudaErrorInvalidValue;
+    // MXFP8 operands (block-scaled MMA): K-major A and B only, one contraction
+    // source, 128 x 192 tiles, k-blocks of 128 elements (4 scale blocks); a
+    // partial last k-block reads zero codes past K
+    constexpr int QBN = 192;
+    if (a.ragged_k || a.a_mn || a.b_mn || a.k1 != 0 || a.max_rows <= 0) return cudaErrorInvalidValue;
     if (a.epi != EPI_SWIGLU_FWD_Q && a.epi != EPI_BF16) return cudaErrorInvalidValue;
     const int64_t K = a.k0;
-    if (K <= 0 || K % 64 || a.qa.cols != K) return cudaErrorInvalidValue;
-    kp.kb0 = static_cast<int>(K / BK);
+    if (K <= 0 || K % 32 || a.qa.cols != K) return cudaErrorInvalidValue;
+    kp.kb0 = static_cast<int>((K + 127) / 128);
     kp.kb1 = 0;
+    kp.tile_n = a.b_dual_n ? QBN / 2 : QBN;
     {
       const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(a.qa.rows)};
       const uint64_t str[1] = {static_cast<uint64_t>(K)};
-      const uint32_t box[2] = {64, BM};
-      if (!make_map_u8(&kp.tmA[0], a.qa.codes, 2, dims, str, box)) return cudaErrorInvalidValue;
+      const uint32_t box[2] = {128, BM};
+      if (!make_map_u8(&kp.tmA[0], a.qa.codes, 2, dims, str, box, true)) return cudaErrorInvalidValue;
       const uint64_t sd[2] = {static_cast<uint64_t>(a.qa.rows), static_cast<uint64_t>(K / 32)};
       const uint64_t ss[1] = {static_cast<uint64_t>(a.qa.scale_ld)};
-      const uint32_t sbox[2] = {144, 2};
+      const uint32_t sbox[2] = {144, 4};
       if (!make_map_u8(&kp.tmA[1], a.qa.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
     }
     const int nb = a.b_dual_n ? 2 : 1;
+    const uint32_t brows = a.b_dual_n ? QBN / 2 : QBN;
     for (int i = 0; i < nb; ++i) {
       const MxOperand& b = a.qb[i];
       if (b.cols != K) return cudaErrorInvalidValue;
       const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows), static_cast<uint64_t>(b.groups)};
       const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows * K)};
-      const uint32_t box[3] = {64, static_cast<uint32_t>(a.b_dual_n ? BN / 2 : BN), 1};
-      if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box)) return cudaErrorInvalidValue;
+      const uint32_t box[3] = {128, brows, 1};
+      if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box, true)) return cudaErrorInvalidValue;
       const uint64_t sd[3] = {static_cast<uint64_t>(b.rows), static_cast<uint64_t>(K / 32), static_cast<uint64_t>(b.groups)};
       const uint64_t ss[2] = {static_cast<uint64_t>(b.scale_ld), static_cast<uint64_t>(b.scale_ld * (K / 32))};
-      const uint32_t sbox[3] = {128, 2, 1};
+      const uint32_t sbox[3] = {brows, 4, 1};
       if (!make_map_u8(&kp.tmBs[i], b.scales, 3, sd, ss, sbox)) return cudaErrorInvalidValue;
     }
     if (nb == 1) {
@@ -1081,10 +1124,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
     const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
     tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
-    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<256, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
-    return launch_impl<256, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
+    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
+    return launch_impl<QBN, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
   }
-  // CTA pairs: each CTA loads its 128 rows of A and half of the B tile
+  // CTA pairs: each CTA loads its own 128 rows of A and half of the B tile
   const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&
                     (a.ragged_k ? a.epi == EPI_F32
                                 : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));

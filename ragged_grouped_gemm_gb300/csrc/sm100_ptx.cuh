@@ -311,6 +311,42 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) 
       : "memory");
 }
 
+// ---------------------------------------------------------------- MXFP8 MMA
+// Block-scaled MMA: E4M3 A and B (K = 32 per instruction), one E8M0 scale per
+// 32 elements of K for every row of A and of B, read from tensor memory.
+// Scale-factor layout in tensor memory (measured on sm_103a):
+//   A row m          : lane m,                      column sfa + m/32, byte a_sf_id
+//   B row (column) n : lane n%32 (of every lane quarter), column sfb + n/32, byte b_sf_id
+// which is what tcgen05.cp.32x128b.warpx4 produces from a 512-byte shared-memory
+// atom holding, for 128 rows r and 4 scale blocks j, byte j of 32-bit word
+// (r/32)%4 of 16-byte row r%32.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory (no swizzle, rows 16 bytes apart)
+// into 4 columns of tensor memory, row r to lane r of every lane quarter.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;   // 8-row groups 128 bytes apart
+  d |= 1ull << 46;                               // descriptor version; layout 0 = no swizzle
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, E8M0 scales, fp32 D,
+// K-major A and B: bits 4-5 B scale id, 7-9 / 10-12 A / B format (0 = E4M3),
+// 17-22 N>>3, 23 scale format (1 = E8M0), 24-28 M>>4, 29-30 A scale id.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, uint32_t sf_id) {
+  return (sf_id << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) |
+         (sf_id << 29);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D:
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 // (1 = bf16), 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N>>3,
