@@ -23,7 +23,7 @@ import numpy as np
 
 __all__ = ["e4m3_decode", "e4m3_encode", "e8m0_scale_exponent", "mx_quantize",
            "mx_dequantize", "mx_fake_quant", "swiglu_expert_mxfp8", "moe_forward_mxfp8",
-           "E4M3_MAX", "MX_BLOCK"]
+           "moe_backward_mxfp8", "E4M3_MAX", "MX_BLOCK"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
@@ -149,19 +149,105 @@ def swiglu_expert_mxfp8(x, w1, w3, w2):
     return y, a1, a3, h
 
 
-def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None):
+def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None, return_saved=False):
     """Layer forward of the dropless MoE layer with MXFP8 expert GEMMs: the
     loop over experts of the simplified MoE layer ("LLM Infrastructure
     Engineering 08: MoE Training Engineering" §9) with every expert replaced
-    by :func:`swiglu_expert_mxfp8`; gate weights and the combine stay fp32."""
+    by :func:`swiglu_expert_mxfp8`; gate weights and the combine stay fp32.
+
+    With ``return_saved`` also returns what the backward needs, in the layout
+    of the bf16 oracle's ``moe_forward``: ``experts[e] = (tok, kk, y, a1, a3,
+    h)`` (rows in ascending token order) and ``shared = (y, a1, a3, h)``."""
     n, d = x.shape
     out = np.zeros((n, d), dtype=np.float32)
+    saved = {"experts": {}}
     for e in range(w1.shape[0]):
         tok, kk = np.nonzero(idx == e)
         if tok.size == 0:
             continue
-        y = swiglu_expert_mxfp8(x[tok], w1[e], w3[e], w2[e])[0]
+        y, a1, a3, h = swiglu_expert_mxfp8(x[tok], w1[e], w3[e], w2[e])
+        saved["experts"][e] = (tok, kk, y, a1, a3, h)
         np.add.at(out, tok, y * g[tok, kk].astype(np.float32)[:, None])
     if shared is not None:
-        out = out + swiglu_expert_mxfp8(x, shared[0], shared[1], shared[2])[0]
-    return out
+        ys, a1s, a3s, hs = swiglu_expert_mxfp8(x, shared[0], shared[1], shared[2])
+        saved["shared"] = (ys, a1s, a3s, hs)
+        out = out + ys
+    return (out, saved) if return_saved else out
+
+
+def _mx_matmul(a, a_axis, b, b_axis, quant=mx_fake_quant):
+    """``a @ b`` in fp32 with both operands MXFP8-quantised along the
+    contraction: ``a`` along ``a_axis`` (its columns, 1, or its rows, 0, in
+    which case the product is ``a^T @ b``) and ``b`` along ``b_axis``."""
+    f32 = np.float32
+    aq = quant(a, axis=a_axis).astype(f32)
+    bq = quant(b, axis=b_axis).astype(f32)
+    return np.matmul(aq.T if a_axis == 0 else aq, bq.T if b_axis == 1 else bq)
+
+
+def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, shared=None,
+                       quant=mx_fake_quant):
+    """Backward of the MXFP8 layer.
+
+    The chain rule is that of the bf16 oracle's ``moe_backward`` (sparse
+    per-expert backward, "LLM Infrastructure Engineering 08: MoE Training
+    Engineering" §11.3); what changes is that every expert GEMM takes both
+    operands MXFP8-quantised along its own contraction dimension (reading of
+    the group-aware MXFP8 grouped GEMM of "Accelerating Dropless MoE Training
+    in JAX with NVIDIA Transformer Engine" ¶6 for the backward):
+
+    * ``dh = dYw w2``: dYw along D (its columns), w2 [D, F] along D (rows);
+    * ``dx_e = da1 w1 + da3 w3``: da1, da3 along F, w1, w3 [F, D] along F;
+    * ``dW2 = dYw^T h``, ``dW1 = da1^T x_e``, ``dW3 = da3^T x_e``: every
+      operand along the expert's rows (tokens); the blocks start at the
+      expert's first row, so no block spans two experts (group-aware).
+
+    The SwiGLU derivative, the router gradient and the combine backward are
+    fp32 as in the bf16 oracle.  ``saved`` comes from
+    ``moe_forward_mxfp8(..., return_saved=True)``.  ``quant`` is the fake
+    quantiser (replaced by the identity, this is the bf16 oracle's backward).
+    """
+    f32 = np.float32
+    n, d = x.shape
+    n_exp, f, _ = w1.shape
+    k = idx.shape[1]
+    xx = x.astype(f32)
+    dyy = dy.astype(f32)
+    dx = np.zeros((n, d), dtype=f32)
+    dw1 = np.zeros((n_exp, f, d), dtype=f32)
+    dw3 = np.zeros((n_exp, f, d), dtype=f32)
+    dw2 = np.zeros((n_exp, d, f), dtype=f32)
+    dg = np.zeros((n, k), dtype=f32)
+
+    def expert_bwd(dyw, xe, a1, a3, h, we1, we3, we2):
+        dh = _mx_matmul(dyw, 1, we2, 0, quant)
+        s = 1.0 / (1.0 + np.exp(-a1))
+        da3 = dh * (a1 * s)
+        da1 = dh * a3 * s * (1.0 + a1 * (1.0 - s))
+        gw2 = _mx_matmul(dyw, 0, h, 0, quant)
+        gw1 = _mx_matmul(da1, 0, xe, 0, quant)
+        gw3 = _mx_matmul(da3, 0, xe, 0, quant)
+        gx = _mx_matmul(da1, 1, we1, 0, quant) + _mx_matmul(da3, 1, we3, 0, quant)
+        return gw1, gw3, gw2, gx
+
+    for e, (tok, kk, y, a1, a3, h) in saved["experts"].items():
+        dg[tok, kk] = (dyy[tok] * y).sum(axis=1)
+        dyw = dyy[tok] * g[tok, kk].astype(f32)[:, None]
+        gw1, gw3, gw2, gx = expert_bwd(dyw, xx[tok], a1, a3, h, w1[e], w3[e], w2[e])
+        dw1[e], dw3[e], dw2[e] = gw1, gw3, gw2
+        np.add.at(dx, tok, gx)
+
+    res = {}
+    if shared is not None:
+        ys, a1s, a3s, hs = saved["shared"]
+        gw1, gw3, gw2, gx = expert_bwd(dyy, xx, a1s, a3s, hs, shared[0], shared[1], shared[2])
+        res.update(dws1=gw1, dws3=gw3, dws2=gw2)
+        dx = dx + gx
+
+    # router: as the bf16 oracle (fp32 logits, no quantised GEMM)
+    from .moe_oracle import router_logit_grad
+    dl = router_logit_grad(dg, g, logits, idx, gate, f32)
+    dw_gate = np.matmul(dl.T, xx)
+    dx = dx + np.matmul(dl, w_gate.astype(f32))
+    res.update(dx=dx, dw1=dw1, dw3=dw3, dw2=dw2, dw_gate=dw_gate, dg=dg, dlogits=dl)
+    return res

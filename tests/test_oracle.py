@@ -408,3 +408,83 @@ def test_mxfp8_forward_reduces_to_exact_on_representable_operands():
     ref = O.moe_forward_dense_bruteforce(p["x"], idx, g, p["w1"], p["w3"], p["w2"])
     e = np.linalg.norm(out - ref) / np.linalg.norm(ref)
     assert 1e-4 < e < 6e-2          # h quantisation is visible, and bounded
+
+
+# ------------------------------------------------------- MXFP8 backward ---
+def _mx_case(seed, gate="sigmoid", shared=64):
+    p = _layer(40, 64, 96, 4, 2, gate=gate, bias=gate == "sigmoid", shared=shared, seed=seed)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, p["bias"], 2, gate)
+    dy = _bf16(_rng(seed + 100).standard_normal(p["x"].shape))
+    return p, lg, idx, g, dy
+
+
+def test_mxfp8_backward_with_identity_quantiser_is_the_bf16_backward():
+    """Wiring pin: with the quantiser replaced by the identity every GEMM of
+    the MXFP8 backward is the plain fp32 product, so the result must be the
+    (finite-difference-pinned) bf16 oracle's backward on the same saved
+    activations."""
+    p, lg, idx, g, dy = _mx_case(31)
+    _, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"])
+    ref = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid",
+                         p["shared"])
+    got = O.moe_backward_mxfp8(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid",
+                               p["shared"], quant=lambda a, axis: np.asarray(a, np.float64))
+    for key in ("dx", "dw1", "dw3", "dw2", "dw_gate", "dg", "dlogits", "dws1", "dws3", "dws2"):
+        assert np.allclose(got[key], ref[key], rtol=1e-5, atol=1e-5 * np.abs(ref[key]).max()), key
+
+
+def _block_scaled_product(a, b, starts):
+    """sum_r a[r, i] b[r, j] with both operands quantised along r: per block,
+    the products of the decoded E4M3 codes times 2^(scale_a + scale_b)."""
+    ca, sa, st = O.mx_quantize(a, axis=0, group_starts=starts)
+    cb, sb, _ = O.mx_quantize(b, axis=0, group_starts=starts)
+    va, vb = O.e4m3_decode(ca), O.e4m3_decode(cb)
+    ends = list(st[1:]) + [a.shape[0]]
+    out = np.zeros((a.shape[1], b.shape[1]))
+    for blk, (lo, hi) in enumerate(zip(st, ends)):
+        part = va[lo:hi].T @ vb[lo:hi]
+        out += part * np.exp2(sa[blk].astype(np.float64) - 127)[:, None] * np.exp2(sb[blk].astype(np.float64) - 127)[None, :]
+    return out
+
+
+def test_mxfp8_backward_weight_gradients_are_group_aware_block_products():
+    """Axis pin: dW2 of every expert equals the block-scaled product of dYw and
+    h quantised along the tokens of the whole expert-major permuted buffer
+    with blocks restarting at each expert's first row (``group_starts``), and
+    dh-side gradients differ from the ones with blocks across experts."""
+    p, lg, idx, g, dy = _mx_case(32, shared=0)
+    out, saved = O.moe_forward_mxfp8(p["x"], idx, g, p["w1"], p["w3"], p["w2"], None, return_saved=True)
+    res = O.moe_backward_mxfp8(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid")
+    exps = sorted(saved["experts"])
+    dyw = np.concatenate([dy[saved["experts"][e][0]] * g[saved["experts"][e][0], saved["experts"][e][1]][:, None]
+                          for e in exps])
+    hh = np.concatenate([saved["experts"][e][5] for e in exps])
+    sizes = [len(saved["experts"][e][0]) for e in exps]
+    starts = list(np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(int))
+    assert any(s % 32 for s in starts)      # some expert starts off a 32-row boundary
+    lo = 0
+    for e, m in zip(exps, sizes):
+        want = _block_scaled_product(dyw[lo:lo + m], hh[lo:lo + m], [0])
+        assert np.allclose(res["dw2"][e], want, rtol=1e-5, atol=1e-6 * np.abs(want).max()), e
+        lo += m
+    # blocks taken across the whole buffer (ignoring expert boundaries) give other values
+    whole = _block_scaled_product(dyw, hh, list(range(0, len(dyw), 32)))
+    per_expert = sum(res["dw2"][e] for e in exps)
+    assert not np.allclose(whole, per_expert, rtol=1e-4)
+
+
+def test_mxfp8_backward_error_is_bounded_and_visible():
+    """Against the fp32 backward of the fp32 forward, the MXFP8 backward
+    differs by the quantisation of its GEMM operands: visible (> 1e-3) and
+    bounded (< 0.1 normwise) for every gradient."""
+    p, lg, idx, g, dy = _mx_case(33)
+    _, saved_q = O.moe_forward_mxfp8(p["x"], idx, g, p["w1"], p["w3"], p["w2"], p["shared"], return_saved=True)
+    got = O.moe_backward_mxfp8(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved_q, "sigmoid",
+                               p["shared"])
+    _, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"])
+    ref = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid",
+                         p["shared"])
+    for key in ("dx", "dw1", "dw3", "dw2", "dws1", "dws2"):
+        e = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert 1e-3 < e < 0.1, (key, e)
