@@ -23,7 +23,7 @@ import numpy as np
 
 __all__ = ["e4m3_decode", "e4m3_encode", "e8m0_scale_exponent", "mx_quantize",
            "mx_dequantize", "mx_fake_quant", "swiglu_expert_mxfp8", "moe_forward_mxfp8",
-           "moe_backward_mxfp8", "E4M3_MAX", "MX_BLOCK"]
+           "moe_backward_mxfp8", "bf16_round", "E4M3_MAX", "MX_BLOCK"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
@@ -127,6 +127,14 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray, starts, axis: int = -1)
     return np.moveaxis(out, -1, axis)
 
 
+def bf16_round(a) -> np.ndarray:
+    """Round fp32 values to the nearest bfloat16 value (ties to even), kept as
+    fp32: the storage precision of the layer's intermediate activations."""
+    u = np.ascontiguousarray(np.asarray(a, dtype=np.float32)).view(np.uint32)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
 def mx_fake_quant(x: np.ndarray, axis: int = -1) -> np.ndarray:
     """Quantise to MXFP8 along ``axis`` and dequantise again (float64)."""
     codes, scales, starts = mx_quantize(x, axis=axis)
@@ -149,7 +157,7 @@ def swiglu_expert_mxfp8(x, w1, w3, w2):
     return y, a1, a3, h
 
 
-def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None, return_saved=False):
+def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None, return_saved=False, store=bf16_round):
     """Layer forward of the dropless MoE layer with MXFP8 expert GEMMs: the
     loop over experts of the simplified MoE layer ("LLM Infrastructure
     Engineering 08: MoE Training Engineering" §9) with every expert replaced
@@ -157,7 +165,9 @@ def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None, return_saved=False):
 
     With ``return_saved`` also returns what the backward needs, in the layout
     of the bf16 oracle's ``moe_forward``: ``experts[e] = (tok, kk, y, a1, a3,
-    h)`` (rows in ascending token order) and ``shared = (y, a1, a3, h)``."""
+    h)`` (rows in ascending token order) and ``shared = (y, a1, a3, h)``, as
+    the layer stores them (``store``: bf16 by default, the intermediate
+    precision the layer keeps; the identity keeps fp32)."""
     n, d = x.shape
     out = np.zeros((n, d), dtype=np.float32)
     saved = {"experts": {}}
@@ -166,11 +176,11 @@ def moe_forward_mxfp8(x, idx, g, w1, w3, w2, shared=None, return_saved=False):
         if tok.size == 0:
             continue
         y, a1, a3, h = swiglu_expert_mxfp8(x[tok], w1[e], w3[e], w2[e])
-        saved["experts"][e] = (tok, kk, y, a1, a3, h)
+        saved["experts"][e] = (tok, kk, store(y), store(a1), store(a3), store(h))
         np.add.at(out, tok, y * g[tok, kk].astype(np.float32)[:, None])
     if shared is not None:
         ys, a1s, a3s, hs = swiglu_expert_mxfp8(x, shared[0], shared[1], shared[2])
-        saved["shared"] = (ys, a1s, a3s, hs)
+        saved["shared"] = (store(ys), store(a1s), store(a3s), store(hs))
         out = out + ys
     return (out, saved) if return_saved else out
 
@@ -186,7 +196,7 @@ def _mx_matmul(a, a_axis, b, b_axis, quant=mx_fake_quant):
 
 
 def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, shared=None,
-                       quant=mx_fake_quant):
+                       quant=mx_fake_quant, store=bf16_round):
     """Backward of the MXFP8 layer.
 
     The chain rule is that of the bf16 oracle's ``moe_backward`` (sparse
@@ -203,9 +213,12 @@ def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, s
       expert's first row, so no block spans two experts (group-aware).
 
     The SwiGLU derivative, the router gradient and the combine backward are
-    fp32 as in the bf16 oracle.  ``saved`` comes from
-    ``moe_forward_mxfp8(..., return_saved=True)``.  ``quant`` is the fake
-    quantiser (replaced by the identity, this is the bf16 oracle's backward).
+    fp32 as in the bf16 oracle.  The tensors the layer stores between steps
+    (dYw, da1, da3) pass through ``store`` (bf16 by default) before they are
+    quantised or reused, as the activations in ``saved`` did.  ``saved``
+    comes from ``moe_forward_mxfp8(..., return_saved=True)``.  ``quant`` is
+    the fake quantiser; with the identity for both ``quant`` and ``store``
+    this is the bf16 oracle's backward.
     """
     f32 = np.float32
     n, d = x.shape
@@ -222,8 +235,8 @@ def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, s
     def expert_bwd(dyw, xe, a1, a3, h, we1, we3, we2):
         dh = _mx_matmul(dyw, 1, we2, 0, quant)
         s = 1.0 / (1.0 + np.exp(-a1))
-        da3 = dh * (a1 * s)
-        da1 = dh * a3 * s * (1.0 + a1 * (1.0 - s))
+        da3 = store(dh * (a1 * s))
+        da1 = store(dh * a3 * s * (1.0 + a1 * (1.0 - s)))
         gw2 = _mx_matmul(dyw, 0, h, 0, quant)
         gw1 = _mx_matmul(da1, 0, xe, 0, quant)
         gw3 = _mx_matmul(da3, 0, xe, 0, quant)
@@ -232,7 +245,7 @@ def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, s
 
     for e, (tok, kk, y, a1, a3, h) in saved["experts"].items():
         dg[tok, kk] = (dyy[tok] * y).sum(axis=1)
-        dyw = dyy[tok] * g[tok, kk].astype(f32)[:, None]
+        dyw = store(dyy[tok] * g[tok, kk].astype(f32)[:, None])
         gw1, gw3, gw2, gx = expert_bwd(dyw, xx[tok], a1, a3, h, w1[e], w3[e], w2[e])
         dw1[e], dw3[e], dw2[e] = gw1, gw3, gw2
         np.add.at(dx, tok, gx)

@@ -428,8 +428,9 @@ def test_mxfp8_backward_with_identity_quantiser_is_the_bf16_backward():
     _, saved = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], p["shared"])
     ref = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid",
                          p["shared"])
+    ident = lambda a, axis=None: np.asarray(a, np.float64)   # noqa: E731
     got = O.moe_backward_mxfp8(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid",
-                               p["shared"], quant=lambda a, axis: np.asarray(a, np.float64))
+                               p["shared"], quant=ident, store=ident)
     for key in ("dx", "dw1", "dw3", "dw2", "dw_gate", "dg", "dlogits", "dws1", "dws3", "dws2"):
         assert np.allclose(got[key], ref[key], rtol=1e-5, atol=1e-5 * np.abs(ref[key]).max()), key
 
@@ -457,7 +458,8 @@ def test_mxfp8_backward_weight_gradients_are_group_aware_block_products():
     out, saved = O.moe_forward_mxfp8(p["x"], idx, g, p["w1"], p["w3"], p["w2"], None, return_saved=True)
     res = O.moe_backward_mxfp8(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "sigmoid")
     exps = sorted(saved["experts"])
-    dyw = np.concatenate([dy[saved["experts"][e][0]] * g[saved["experts"][e][0], saved["experts"][e][1]][:, None]
+    # dYw as the layer stores it (bf16), h as saved
+    dyw = np.concatenate([O.bf16_round(dy[saved["experts"][e][0]] * g[saved["experts"][e][0], saved["experts"][e][1]][:, None])
                           for e in exps])
     hh = np.concatenate([saved["experts"][e][5] for e in exps])
     sizes = [len(saved["experts"][e][0]) for e in exps]
@@ -488,3 +490,14 @@ def test_mxfp8_backward_error_is_bounded_and_visible():
     for key in ("dx", "dw1", "dw3", "dw2", "dws1", "dws2"):
         e = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
         assert 1e-3 < e < 0.1, (key, e)
+
+
+def test_bf16_round_is_round_to_nearest_even():
+    """The oracle's bf16 storage rounding against torch's fp32 -> bf16
+    conversion (round to nearest even), including exact ties."""
+    r = _rng(34)
+    v = np.concatenate([r.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** r.integers(-30, 30, 20000),
+                        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 0.0, -0.0], np.float32)])
+    want = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    got = O.bf16_round(v)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
