@@ -253,9 +253,10 @@ MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts,
  * has scale byte 0.  Scales are stored k-block-major: for a matrix [rows,
  * cols] (cols = contraction dimension) the byte of row r, block b is at
  * scales[b * scale_ld + r] with scale_ld >= rows and a multiple of 16.
- * The tensor cores run bf16 MMAs on the exactly dequantised operands (every
- * E4M3 value times a power of two is a bf16 value), with fp32 accumulation.
- * The backward (moe_backward) runs in bf16. */
+ * The tensor cores run block-scaled MMAs (tcgen05 kind::mxf8f6f4 with the
+ * E8M0 scales in tensor memory) with fp32 accumulation.  The backward is
+ * moe_backward_mxfp8 (every expert GEMM with MXFP8 operands) or moe_backward
+ * (bf16) on the bf16 activations the MXFP8 forward saved. */
 
 /* Round up to the scale leading dimension the library expects (multiple of 16). */
 #define MOE_MX_SCALE_LD(rows) ((((rows) + 15) / 16) * 16)
@@ -286,6 +287,16 @@ typedef struct {
 MOE_API moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
                                         void* scales, int64_t scale_ld, void* stream);
 
+/* Quantise bf16 src [groups, rows, cols] to MXFP8 along ROWS and store it
+ * transposed: codes [groups, cols, rows] and scales [groups, rows/32,
+ * scale_ld] (scale_ld >= cols, a multiple of 16; rows a multiple of 32).  The
+ * weights' copies for the backward's data-gradient GEMMs, whose contraction
+ * runs over the other weight dimension: w2 [E,D,F] -> codes [E,F,D] with
+ * scales [E,D/32,F]; w1, w3 [E,F,D] -> codes [E,D,F] with scales [E,F/32,D]
+ * (once per optimiser step, outside the layer). */
+MOE_API moe_status_t moe_quantize_mxfp8_t(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
+                                          void* scales, int64_t scale_ld, void* stream);
+
 /* moe_permute with MXFP8 quantisation fused in: the same row_of_copy /
  * copy_of_row maps, and the permuted rows as codes xq_perm [R,D] with scales
  * xs_perm [D/32, MOE_MX_SCALE_LD(R)]; optionally (xq_tok non-NULL) the
@@ -306,6 +317,28 @@ MOE_API moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_p
                                            const int32_t* offsets, const void* xq_tok, const void* xs_tok,
                                            const moe_expert_weights_mx_t* w, const moe_ffn_saved_t* saved,
                                            void* y_perm, void* y_shared, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the MXFP8 layer: the steps of moe_backward with every expert
+ * GEMM on MXFP8 operands, each quantised along that GEMM's contraction
+ * ("Accelerating Dropless MoE Training in JAX with NVIDIA Transformer Engine"
+ * ¶6, group-aware MXFP8 grouped GEMM, read for the backward):
+ *   dh = dYw w2      : dYw quantised along D, w2 along D (wt->w2: codes
+ *                      [E,F,D], scales [E,D/32,F] from moe_quantize_mxfp8_t),
+ *                      SwiGLU derivative in the epilogue -> da1, da3 (bf16);
+ *   dx = da1 w1 + da3 w3 : da1, da3 quantised along F, w1, w3 along F
+ *                      (wt->w1, wt->w3: codes [E,D,F], scales [E,F/32,D]);
+ *   dW2 = dYw^T h, dW1 = da1^T x, dW3 = da3^T x : operands quantised along
+ *                      each expert's tokens, blocks restarting at the
+ *                      expert's first row (fp32 out, zero for empty experts).
+ * The shared expert is the same with one group (wt->ws1/ws3: codes [D,Fs],
+ * scales [Fs/32,D]; wt->ws2: codes [Fs,D], scales [D/32,Fs]).  The combine
+ * and router backward are those of moe_backward.  s->x_perm is not read (the
+ * permuted input is gathered from s->x); s->a1, a3, h (a1s, a3s, hs) are the
+ * bf16 activations saved by moe_grouped_ffn_mxfp8.  d->precision must be 1;
+ * needs the backward workspace of that description. */
+MOE_API moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wt,
+                                        const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                                        size_t ws_bytes, void* stream);
 
 /* moe_permute without a workspace (no counterpart in the pages; an addition
  * of this library for callers that cannot allocate).  Same inputs, outputs

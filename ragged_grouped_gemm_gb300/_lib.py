@@ -75,6 +75,11 @@ SIGNATURES = {
     "moe_grouped_ffn_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(MoeExpertWeightsMx), ctypes.POINTER(MoeFfnSaved), c_vp, c_vp,
                                       c_vp, ctypes.c_size_t, c_vp]),
+    "moe_quantize_mxfp8_t": (c_i32, [c_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_vp, c_vp,
+                                     ctypes.c_int64, c_vp]),
+    "moe_backward_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, ctypes.POINTER(MoeExpertWeightsMx),
+                                   ctypes.POINTER(MoeFwdState), c_vp, ctypes.POINTER(MoeGrads), c_vp,
+                                   ctypes.c_size_t, c_vp]),
 }
 
 _LIB = None

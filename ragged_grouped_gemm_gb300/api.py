@@ -145,19 +145,14 @@ def moe_combine(desc, y_perm, row_of_copy, topk_w, y_shared, out, stream=None):
         _s(stream)))
 
 
-def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, stream=None):
-    """``weights``: w1, w3, w2 (+ ws1, ws3, ws2); ``state``: the fields of
-    moe_fwd_state_t; ``grads``: the fields of moe_grads_t (dg, dlogits optional)."""
+def _bwd_structs(desc, state: dict, grads: dict, need_x_perm: bool = True):
     n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
     r, fs, sh = n * k, desc.d_ff_shared, desc.n_shared
-    w = _lib.MoeExpertWeights(_p(weights["w1"], BF16, (e, f, d), "w1"), _p(weights["w3"], BF16, (e, f, d), "w3"),
-                              _p(weights["w2"], BF16, (e, d, f), "w2"),
-                              _p(weights.get("ws1"), BF16, (fs, d), "ws1") if sh else None,
-                              _p(weights.get("ws3"), BF16, (fs, d), "ws3") if sh else None,
-                              _p(weights.get("ws2"), BF16, (d, fs), "ws2") if sh else None)
     S = state
     st = _lib.MoeFwdState(
-        _p(S["x"], BF16, (n, d), "x"), _p(S["x_perm"], BF16, (r, d), "x_perm"), _p(S["logits"], F32, (n, e), "logits"),
+        _p(S["x"], BF16, (n, d), "x"),
+        _p(S.get("x_perm"), BF16, (r, d), "x_perm") if (need_x_perm or S.get("x_perm") is not None) else None,
+        _p(S["logits"], F32, (n, e), "logits"),
         _p(S["topk_idx"], I32, (n, k), "topk_idx"), _p(S["topk_w"], F32, (n, k), "topk_w"),
         _p(S["offsets"], I32, (e + 1,), "offsets"), _p(S["row_of_copy"], I32, (r,), "row_of_copy"),
         _p(S["copy_of_row"], I32, (r,), "copy_of_row"), _p(S["a1"], BF16, (r, f), "a1"), _p(S["a3"], BF16, (r, f), "a3"),
@@ -171,6 +166,20 @@ def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, 
         _p(G.get("dws1"), F32, (fs, d), "dws1") if sh else None, _p(G.get("dws3"), F32, (fs, d), "dws3") if sh else None,
         _p(G.get("dws2"), F32, (d, fs), "dws2") if sh else None,
         _p(G.get("dg"), F32, (n, k), "dg"), _p(G.get("dlogits"), F32, (n, k), "dlogits"))
+    return st, gr
+
+
+def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, stream=None):
+    """``weights``: w1, w3, w2 (+ ws1, ws3, ws2); ``state``: the fields of
+    moe_fwd_state_t; ``grads``: the fields of moe_grads_t (dg, dlogits optional)."""
+    n, d, f, e = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp
+    fs, sh = desc.d_ff_shared, desc.n_shared
+    w = _lib.MoeExpertWeights(_p(weights["w1"], BF16, (e, f, d), "w1"), _p(weights["w3"], BF16, (e, f, d), "w3"),
+                              _p(weights["w2"], BF16, (e, d, f), "w2"),
+                              _p(weights.get("ws1"), BF16, (fs, d), "ws1") if sh else None,
+                              _p(weights.get("ws3"), BF16, (fs, d), "ws3") if sh else None,
+                              _p(weights.get("ws2"), BF16, (d, fs), "ws2") if sh else None)
+    st, gr = _bwd_structs(desc, state, grads)
     _check("moe_backward", _lib.load().moe_backward(
         ctypes.byref(desc), _p(w_gate, BF16, (e, d), "w_gate"), ctypes.byref(w), ctypes.byref(st),
         _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
@@ -215,6 +224,50 @@ def quantize_weights_mxfp8(p: dict, stream=None) -> dict:
         moe_quantize_mxfp8(w, codes, scales, stream)
         out[key], out[key + "_scale"] = codes, scales
     return out
+
+
+def moe_quantize_mxfp8_t(src, codes, scales, stream=None):
+    """src bf16 [G, rows, cols] (or [rows, cols]) quantised along rows and
+    transposed: codes uint8 [G, cols, rows], scales uint8 [G, rows/32, ld]
+    (ld = scales.shape[-1] >= cols, a multiple of 16)."""
+    g, rows, cols = (1,) + tuple(src.shape) if src.dim() == 2 else tuple(src.shape)
+    ld = scales.shape[-1]
+    cshape = (cols, rows) if src.dim() == 2 else (g, cols, rows)
+    sshape = (rows // 32, ld) if src.dim() == 2 else (g, rows // 32, ld)
+    _check("moe_quantize_mxfp8_t", _lib.load().moe_quantize_mxfp8_t(
+        _p(src, BF16, name="src"), g, rows, cols, _p(codes, U8, cshape, "codes"), _p(scales, U8, sshape, "scales"),
+        ld, _s(stream)))
+
+
+def quantize_weights_mxfp8_t(p: dict, stream=None) -> dict:
+    """Transposed MXFP8 copies of the expert weights for the backward's data
+    gradients (quantised along the other weight dimension)."""
+    out = {}
+    for key in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+        w = p.get(key)
+        if w is None:
+            continue
+        rows, cols = w.shape[-2], w.shape[-1]
+        lead = (w.shape[0],) if w.dim() == 3 else ()
+        codes = torch.empty(lead + (cols, rows), dtype=U8, device=w.device)
+        scales = torch.zeros(lead + (rows // 32, mx_scale_ld(cols)), dtype=U8, device=w.device)
+        moe_quantize_mxfp8_t(w, codes, scales, stream)
+        out[key], out[key + "_scale"] = codes, scales
+    return out
+
+
+def moe_backward_mxfp8(desc, w_gate, wt: dict, state: dict, dy, grads: dict, ws, stream=None):
+    """Backward of the MXFP8 layer.  ``wt``: output of
+    :func:`quantize_weights_mxfp8_t`; ``state`` as for :func:`moe_backward`
+    (x_perm not needed)."""
+    n, d, e, sh = desc.n_tok, desc.d_model, desc.n_exp, desc.n_shared
+    w = _lib.MoeExpertWeightsMx(*[_p(wt.get(key)) if (sh or not key.startswith("ws")) else None
+                                  for key in ("w1", "w1_scale", "w3", "w3_scale", "w2", "w2_scale",
+                                              "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")])
+    st, gr = _bwd_structs(desc, state, grads, need_x_perm=False)
+    _check("moe_backward_mxfp8", _lib.load().moe_backward_mxfp8(
+        ctypes.byref(desc), _p(w_gate, BF16, (e, d), "w_gate"), ctypes.byref(w), ctypes.byref(st),
+        _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
 def moe_permute_mxfp8(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, xq_perm, xs_perm, xq_tok, xs_tok, ws,
@@ -278,6 +331,7 @@ class MoELayer:
         self.mx = cfg.precision == "mxfp8"
         if self.mx:
             self.wq = quantize_weights_mxfp8(params)
+            self.wqt = quantize_weights_mxfp8_t(params) if train else None
             self.buf.update(xq_perm=z(r, d, dt=U8), xs_perm=torch.zeros(d // 32, mx_scale_ld(r), dtype=U8, device=device),
                             xq_tok=z(n, d, dt=U8) if cfg.n_shared else None,
                             xs_tok=(torch.zeros(d // 32, mx_scale_ld(n), dtype=U8, device=device)
@@ -321,9 +375,13 @@ class MoELayer:
         return b["out"]
 
     def backward(self, dy: torch.Tensor, stream=None) -> dict:
-        if self.mx:
-            raise NotImplementedError("the MXFP8 layer runner is forward-only")
         b = self.buf
+        if self.mx:
+            state = {key: b[key] for key in ("logits", "topk_idx", "topk_w", "offsets", "row_of_copy",
+                                             "copy_of_row", "a1", "a3", "h", "y_perm", "a1s", "a3s", "hs")}
+            state["x"] = self.x
+            moe_backward_mxfp8(self.desc, self.p["w_gate"], self.wqt, state, dy, self.grads, self.ws, stream)
+            return self.grads
         state = {key: b[key] for key in ("x_perm", "logits", "topk_idx", "topk_w", "offsets", "row_of_copy",
                                          "copy_of_row", "a1", "a3", "h", "y_perm", "a1s", "a3s", "hs")}
         state["x"] = self.x

@@ -59,9 +59,10 @@ constexpr int kMaxGroups = 1024;
 constexpr int kABytes = BM * BK * 2;   // 16 KB
 
 struct KParams {
-  CUtensorMap tmA[2];    // MXFP8: [0] A codes, [1] A scales
-  CUtensorMap tmB[2];    // MXFP8: B codes (W1 | W3 halves, or one map)
-  CUtensorMap tmBs[2];   // MXFP8: B scales
+  CUtensorMap tmA[2];    // A per contraction source (MXFP8: codes)
+  CUtensorMap tmB[2];    // B per source, or the W1 | W3 halves of a dual-N tile (MXFP8: codes)
+  CUtensorMap tmAs[2];   // MXFP8: A scales per source
+  CUtensorMap tmBs[2];   // MXFP8: B scales (per source or per half)
   CUtensorMap tmC;       // fp32 output map {n, m, group}, used when c_tma != 0
   int32_t c_tma;
   int32_t c_rows;        // rows of the output map (ragged M, one group)
@@ -70,6 +71,7 @@ struct KParams {
   int32_t m_size;
   int32_t n_size;
   int32_t kb0, kb1;
+  int32_t kblk;          // contraction elements per k-block (64 bf16, 128 MXFP8)
   int32_t b_dual_n;
   int32_t tile_n;
   void* out0;
@@ -95,7 +97,8 @@ struct Cfg {
   static constexpr int kQARaw = kQBCodes + BN * 128;
   static constexpr int kQBRaw = kQARaw + 640;
   static constexpr int kQAtoms = kQBRaw + 4 * BN;
-  static constexpr uint32_t kQTxBytes = BM * 128 + BN * 128 + 4 * 144 + 4 * BN;
+  static constexpr uint32_t kQTxBytes = BM * 128 + BN * 128 + 4 * 144 + 4 * BN;    // ragged M
+  static constexpr uint32_t kQTxBytesK = BM * 128 + BN * 128 + 4 * 128 + 4 * BN;   // ragged K
   // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
   static constexpr int kStageBytes =
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
@@ -162,7 +165,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
     t.m0 = t.mt * UR + rank * BM;
     t.k_rows = s_off[t.g + 1] - s_off[t.g];
     t.rows_valid = min(BM, p.m_size - t.m0);
-    t.num_kb = (t.k_rows + BK - 1) / BK;
+    t.num_kb = (t.k_rows + p.kblk - 1) / p.kblk;
   }
   return t;
 }
@@ -210,6 +213,8 @@ __device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
   using C = Cfg<BN, QUANT, PAIR>;
+  // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
+  // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -254,10 +259,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     tma_prefetch_desc(&p.tmA[0]);
     tma_prefetch_desc(&p.tmB[0]);
     if (QUANT) {
-      tma_prefetch_desc(&p.tmA[1]);
+      tma_prefetch_desc(&p.tmAs[0]);
       tma_prefetch_desc(&p.tmBs[0]);
-      tma_prefetch_desc(&p.tmB[1]);
-      tma_prefetch_desc(&p.tmBs[1]);
     }
   }
   if (warp == 1) {
@@ -322,19 +325,31 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* st = smem + s * C::kStageBytes;
+          if (RAGGED_K) {
+            // weight gradient: A [M][tokens] and B [N][tokens] codes (tokens of
+            // each group padded to 128 with zero codes), scales [tokens/32][M or N]
+            mbar_arrive_expect_tx(&full[s], C::kQTxBytesK);
+            const int k0 = t.row0 + kb * 128;
+            tma_load_2d(st, &p.tmA[0], &full[s], k0, t.m0);
+            tma_load_2d(st + C::kQARaw, &p.tmAs[0], &full[s], t.m0, k0 / 32);
+            tma_load_2d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, t.nt * BN);
+            tma_load_2d(st + C::kQBRaw, &p.tmBs[0], &full[s], t.nt * BN, k0 / 32);
+            continue;
+          }
           mbar_arrive_expect_tx(&full[s], C::kQTxBytes);
-          const int k0 = kb * 128;
-          tma_load_2d(st, &p.tmA[0], &full[s], k0, t.row0);
-          tma_load_2d(st + C::kQARaw, &p.tmA[1], &full[s], t.row0 & ~15, kb * 4);   // 16-byte aligned x
+          const int src = (kb < p.kb0) ? 0 : 1;
+          const int k0 = (src == 0 ? kb : kb - p.kb0) * 128;
+          tma_load_2d(st, &p.tmA[src], &full[s], k0, t.row0);
+          tma_load_2d(st + C::kQARaw, &p.tmAs[src], &full[s], t.row0 & ~15, k0 / 32);   // 16-byte aligned x
           if (p.b_dual_n) {
             const int f0 = t.nt * (BN / 2);
             tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, f0, t.g);
             tma_load_3d(st + C::kQBCodes + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
-            tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], f0, kb * 4, t.g);
-            tma_load_3d(st + C::kQBRaw + 2 * BN, &p.tmBs[1], &full[s], f0, kb * 4, t.g);
+            tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], f0, k0 / 32, t.g);
+            tma_load_3d(st + C::kQBRaw + 2 * BN, &p.tmBs[1], &full[s], f0, k0 / 32, t.g);
           } else {
-            tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, t.nt * BN, t.g);
-            tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], t.nt * BN, kb * 4, t.g);
+            tma_load_3d(st + C::kQBCodes, &p.tmB[src], &full[s], k0, t.nt * BN, t.g);
+            tma_load_3d(st + C::kQBRaw, &p.tmBs[src], &full[s], t.nt * BN, k0 / 32, t.g);
           }
         }
       }
@@ -586,7 +601,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
-        const int a_rem = t.row0 & 15;
+        // A scale rows: ragged M [4][144] from a 16-aligned row; ragged K [4][128]
+        const int a_rem = RAGGED_K ? 0 : (t.row0 & 15);
+        constexpr int AS = RAGGED_K ? 128 : 144;
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
@@ -597,9 +614,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           uint32_t* atoms = reinterpret_cast<uint32_t*>(st + C::kQAtoms);
           {
             const int r = ct;
-            const uint32_t w = static_cast<uint32_t>(ra[a_rem + r]) | (static_cast<uint32_t>(ra[144 + a_rem + r]) << 8) |
-                               (static_cast<uint32_t>(ra[288 + a_rem + r]) << 16) |
-                               (static_cast<uint32_t>(ra[432 + a_rem + r]) << 24);
+            const uint32_t w = static_cast<uint32_t>(ra[a_rem + r]) | (static_cast<uint32_t>(ra[AS + a_rem + r]) << 8) |
+                               (static_cast<uint32_t>(ra[2 * AS + a_rem + r]) << 16) |
+                               (static_cast<uint32_t>(ra[3 * AS + a_rem + r]) << 24);
             atoms[(r & 31) * 4 + (r >> 5)] = w;
           }
           for (int r = ct; r < BN; r += 128) {
@@ -1060,7 +1077,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   if (a.block_n != 256 && !(a.block_n == 32 && !a.b_mn && !a.a_mn && a.epi == EPI_F32))
     return cudaErrorInvalidValue;
-  if (a.ragged_k != a.a_mn) return cudaErrorInvalidValue;  // the two forms this kernel implements
+  // bf16: ragged K comes with MN-major A (the two forms this kernel implements)
+  if (!a.quant && a.ragged_k != a.a_mn) return cudaErrorInvalidValue;
   const int BN = a.block_n;
   KParams kp{};
   kp.offsets = a.offsets;
@@ -1083,54 +1101,94 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
 
   int64_t tiles_ub = 0;
   if (a.quant) {
-    // MXFP8 operands (block-scaled MMA): K-major A and B only, one contraction
-    // source, 128 x 192 tiles, k-blocks of 128 elements (4 scale blocks); a
-    // partial last k-block reads zero codes past K
+    // MXFP8 operands (block-scaled MMA), K-major A and B, 128 x 192 tiles,
+    // k-blocks of 128 elements (4 scale blocks); a partial last k-block of a
+    // source reads zero codes past its K.
     constexpr int QBN = 192;
-    if (a.ragged_k || a.a_mn || a.b_mn || a.k1 != 0 || a.max_rows <= 0) return cudaErrorInvalidValue;
-    if (a.epi != EPI_SWIGLU_FWD_Q && a.epi != EPI_BF16) return cudaErrorInvalidValue;
-    const int64_t K = a.k0;
-    if (K <= 0 || K % 32 || a.qa.cols != K) return cudaErrorInvalidValue;
-    kp.kb0 = static_cast<int>((K + 127) / 128);
-    kp.kb1 = 0;
-    kp.tile_n = a.b_dual_n ? QBN / 2 : QBN;
+    kp.kblk = 128;
+    if (a.a_mn || a.b_mn) return cudaErrorInvalidValue;
+    if (!a.ragged_k) {
+      if (a.epi != EPI_SWIGLU_FWD_Q && a.epi != EPI_BF16 && a.epi != EPI_SWIGLU_BWD) return cudaErrorInvalidValue;
+      if (a.max_rows <= 0) return cudaSuccess;
+      const int nsrc = a.k1 > 0 ? 2 : 1;
+      if (a.b_dual_n && nsrc != 1) return cudaErrorInvalidValue;
+      kp.kb0 = static_cast<int>((a.k0 + 127) / 128);
+      kp.kb1 = static_cast<int>((a.k1 + 127) / 128);
+      if (kp.kb0 <= 0) return cudaErrorInvalidValue;
+      kp.tile_n = a.b_dual_n ? QBN / 2 : QBN;
+      const uint32_t brows = a.b_dual_n ? QBN / 2 : QBN;
+      for (int src = 0; src < nsrc; ++src) {
+        const int64_t K = src == 0 ? a.k0 : a.k1;
+        const MxOperand& q = a.qa[src];
+        if (K <= 0 || K % 32 || q.cols != K) return cudaErrorInvalidValue;
+        const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(q.rows)};
+        const uint64_t str[1] = {static_cast<uint64_t>(K)};
+        const uint32_t box[2] = {128, BM};
+        if (!make_map_u8(&kp.tmA[src], q.codes, 2, dims, str, box, true)) return cudaErrorInvalidValue;
+        const uint64_t sd[2] = {static_cast<uint64_t>(q.rows), static_cast<uint64_t>(K / 32)};
+        const uint64_t ss[1] = {static_cast<uint64_t>(q.scale_ld)};
+        const uint32_t sbox[2] = {144, 4};
+        if (!make_map_u8(&kp.tmAs[src], q.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
+      }
+      const int nb = a.b_dual_n ? 2 : nsrc;
+      for (int i = 0; i < nb; ++i) {
+        const int64_t K = (a.b_dual_n || i == 0) ? a.k0 : a.k1;
+        const MxOperand& b = a.qb[i];
+        if (b.cols != K) return cudaErrorInvalidValue;
+        const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows), static_cast<uint64_t>(b.groups)};
+        const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows * K)};
+        const uint32_t box[3] = {128, brows, 1};
+        if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+        const uint64_t sd[3] = {static_cast<uint64_t>(b.rows), static_cast<uint64_t>(K / 32), static_cast<uint64_t>(b.groups)};
+        const uint64_t ss[2] = {static_cast<uint64_t>(b.scale_ld), static_cast<uint64_t>(b.scale_ld * (K / 32))};
+        const uint32_t sbox[3] = {brows, 4, 1};
+        if (!make_map_u8(&kp.tmBs[i], b.scales, 3, sd, ss, sbox)) return cudaErrorInvalidValue;
+      }
+      const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
+      tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+      switch (a.epi) {
+        case EPI_SWIGLU_FWD_Q: return launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
+        case EPI_SWIGLU_BWD: return launch_impl<QBN, false, false, EPI_SWIGLU_BWD, true>(kp, tiles_ub, stream);
+        default: return launch_impl<QBN, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
+      }
+    }
+    // ragged K (weight gradients): offsets are the padded group starts, every
+    // group a multiple of 128 tokens; A [m_size][K_padded], B [n_size][K_padded]
+    if (a.epi != EPI_F32 || a.m_size <= 0) return a.m_size <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    const MxOperand& qa = a.qa[0];
+    const MxOperand& qb = a.qb[0];
+    const int64_t Kp = qa.cols;
+    if (Kp <= 0 || Kp % 128 || qb.cols != Kp || qa.rows < a.m_size || qb.rows < a.n_size) return cudaErrorInvalidValue;
     {
-      const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(a.qa.rows)};
-      const uint64_t str[1] = {static_cast<uint64_t>(K)};
+      const uint64_t dims[2] = {static_cast<uint64_t>(Kp), static_cast<uint64_t>(qa.rows)};
+      const uint64_t str[1] = {static_cast<uint64_t>(Kp)};
       const uint32_t box[2] = {128, BM};
-      if (!make_map_u8(&kp.tmA[0], a.qa.codes, 2, dims, str, box, true)) return cudaErrorInvalidValue;
-      const uint64_t sd[2] = {static_cast<uint64_t>(a.qa.rows), static_cast<uint64_t>(K / 32)};
-      const uint64_t ss[1] = {static_cast<uint64_t>(a.qa.scale_ld)};
-      const uint32_t sbox[2] = {144, 4};
-      if (!make_map_u8(&kp.tmA[1], a.qa.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
+      if (!make_map_u8(&kp.tmA[0], qa.codes, 2, dims, str, box, true)) return cudaErrorInvalidValue;
+      const uint64_t sd[2] = {static_cast<uint64_t>(qa.rows), static_cast<uint64_t>(Kp / 32)};
+      const uint64_t ss[1] = {static_cast<uint64_t>(qa.scale_ld)};
+      const uint32_t sbox[2] = {BM, 4};
+      if (!make_map_u8(&kp.tmAs[0], qa.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
     }
-    const int nb = a.b_dual_n ? 2 : 1;
-    const uint32_t brows = a.b_dual_n ? QBN / 2 : QBN;
-    for (int i = 0; i < nb; ++i) {
-      const MxOperand& b = a.qb[i];
-      if (b.cols != K) return cudaErrorInvalidValue;
-      const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows), static_cast<uint64_t>(b.groups)};
-      const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows * K)};
-      const uint32_t box[3] = {128, brows, 1};
-      if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box, true)) return cudaErrorInvalidValue;
-      const uint64_t sd[3] = {static_cast<uint64_t>(b.rows), static_cast<uint64_t>(K / 32), static_cast<uint64_t>(b.groups)};
-      const uint64_t ss[2] = {static_cast<uint64_t>(b.scale_ld), static_cast<uint64_t>(b.scale_ld * (K / 32))};
-      const uint32_t sbox[3] = {brows, 4, 1};
-      if (!make_map_u8(&kp.tmBs[i], b.scales, 3, sd, ss, sbox)) return cudaErrorInvalidValue;
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(Kp), static_cast<uint64_t>(qb.rows)};
+      const uint64_t str[1] = {static_cast<uint64_t>(Kp)};
+      const uint32_t box[2] = {128, QBN};
+      if (!make_map_u8(&kp.tmB[0], qb.codes, 2, dims, str, box, true)) return cudaErrorInvalidValue;
+      const uint64_t sd[2] = {static_cast<uint64_t>(qb.rows), static_cast<uint64_t>(Kp / 32)};
+      const uint64_t ss[1] = {static_cast<uint64_t>(qb.scale_ld)};
+      const uint32_t sbox[2] = {QBN, 4};
+      if (!make_map_u8(&kp.tmBs[0], qb.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
     }
-    if (nb == 1) {
-      kp.tmB[1] = kp.tmB[0];
-      kp.tmBs[1] = kp.tmBs[0];
-    }
-    const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
-    tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
-    if (a.epi == EPI_SWIGLU_FWD_Q) return launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
-    return launch_impl<QBN, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
+    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, a.m_size, a.num_groups, a.ld_out, a.group_stride_out) ? 1 : 0;
+    kp.c_rows = a.m_size;
+    tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + QBN - 1) / QBN);
+    return launch_impl<QBN, true, true, EPI_F32, true>(kp, tiles_ub, stream);
   }
   // CTA pairs: each CTA loads its own 128 rows of A and half of the B tile
   const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&
                     (a.ragged_k ? a.epi == EPI_F32
                                 : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));
+  kp.kblk = BK;
   if (!a.ragged_k) {
     if (a.max_rows <= 0) return cudaSuccess;
     kp.kb0 = (a.k0 + BK - 1) / BK;

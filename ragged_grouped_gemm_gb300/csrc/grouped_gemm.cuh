@@ -66,7 +66,8 @@ struct GemmArgs {
   int m_size = 0;             // ragged K: rows of each C_g
   int n_size = 0;             // columns of C (f extent for EPI_SWIGLU_FWD)
   bool quant = false;         // operands are MXFP8 (qa, qb), dequantised to bf16 on the way in
-  MxOperand qa;               // A: [rows, K] with scales [K/32, scale_ld]
+  MxOperand qa[2];            // A per contraction source: [rows, K] with scales [K/32, scale_ld]
+                              // (ragged K: [M, K_padded] with scales [K_padded/32, scale_ld])
   MxOperand qb[2];            // B: [groups][N, K]; qb[1] is the W3 half of a dual-N tile
   void* out0 = nullptr;
   void* out1 = nullptr;

@@ -22,7 +22,15 @@ struct WsLayout {
   size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
+  // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
+  // padded group starts, and four transposed token-blocked code matrices
+  // (weight-gradient operands: two [D, Rp], two [max(F,Fs), Rp]) with scales
+  size_t q_dy = 0, q_dys = 0, q_da1 = 0, q_da1s = 0, q_da3 = 0, q_da3s = 0, pad = 0, pad_sh = 0;
+  size_t t_d0 = 0, t_d0s = 0, t_d1 = 0, t_d1s = 0, t_f0 = 0, t_f0s = 0, t_f1 = 0, t_f1s = 0;
+  int64_t rp = 0;   // leading dimension of the transposed code matrices
 };
+
+int64_t ld16(int64_t v) { return (v + 15) / 16 * 16; }
 
 WsLayout layout(const moe_desc_t& d) {
   WsLayout L;
@@ -50,6 +58,28 @@ WsLayout layout(const moe_desc_t& d) {
   L.da3s = o; o = align_up(o + N * Fs * 2);
   L.dxs = o; o = align_up(o + (Fs ? N * D * 2 : 0));
   L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_tok, d.top_k, d.n_exp, d.d_model) * 4);
+  if (d.precision == 1) {
+    const size_t Fm = F > Fs ? F : Fs;
+    const size_t ldr = moe::mx_scale_ld(R);
+    L.q_dy = o; o = align_up(o + R * D);
+    L.q_dys = o; o = align_up(o + D / 32 * ldr);
+    L.q_da1 = o; o = align_up(o + R * Fm);
+    L.q_da1s = o; o = align_up(o + Fm / 32 * ldr);
+    L.q_da3 = o; o = align_up(o + R * Fm);
+    L.q_da3s = o; o = align_up(o + Fm / 32 * ldr);
+    L.pad = o; o = align_up(o + (E + 1) * 4);
+    L.pad_sh = o; o = align_up(o + 2 * 4);
+    L.rp = (moe::mx_padded_rows(static_cast<int64_t>(R), static_cast<int>(E)) + 127) / 128 * 128;
+    const size_t rp = static_cast<size_t>(L.rp);
+    L.t_d0 = o; o = align_up(o + D * rp);
+    L.t_d0s = o; o = align_up(o + rp / 32 * ld16(D));
+    L.t_d1 = o; o = align_up(o + D * rp);
+    L.t_d1s = o; o = align_up(o + rp / 32 * ld16(D));
+    L.t_f0 = o; o = align_up(o + Fm * rp);
+    L.t_f0s = o; o = align_up(o + rp / 32 * ld16(Fm));
+    L.t_f1 = o; o = align_up(o + Fm * rp);
+    L.t_f1s = o; o = align_up(o + rp / 32 * ld16(Fm));
+  }
   L.total = o;
   return L;
 }
@@ -427,7 +457,7 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
                          at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st));
   }
-  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, at<float>(ws, L.dwg),
+  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, 0, at<float>(ws, L.dwg),
                               g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
@@ -475,7 +505,7 @@ moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, in
   GemmArgs g1;
   g1.quant = true;
   g1.epi = moe::EPI_SWIGLU_FWD_Q;
-  g1.qa = moe::MxOperand{aq, as, rows, D, 1, moe::mx_scale_ld(rows)};
+  g1.qa[0] = moe::MxOperand{aq, as, rows, D, 1, moe::mx_scale_ld(rows)};
   g1.qb[0] = moe::MxOperand{w1, w1s, F, D, groups, F};
   g1.qb[1] = moe::MxOperand{w3, w3s, F, D, groups, F};
   g1.b_dual_n = true;
@@ -496,7 +526,7 @@ moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, in
   GemmArgs g2;
   g2.quant = true;
   g2.epi = moe::EPI_BF16;
-  g2.qa = moe::MxOperand{hq, hs, rows, F, 1, moe::mx_scale_ld(rows)};
+  g2.qa[0] = moe::MxOperand{hq, hs, rows, F, 1, moe::mx_scale_ld(rows)};
   g2.qb[0] = moe::MxOperand{w2, w2s, D, F, groups, D};
   g2.k0 = F;
   g2.offsets = offsets;
@@ -507,6 +537,109 @@ moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, in
   g2.ld_out = D;
   g2.status = status;
   MOE_CUDA(moe::launch_grouped_gemm(g2, st));
+  return MOE_OK;
+}
+// Workspace scratch of one MXFP8 backward expert set.
+struct MxBwdScratch {
+  uint8_t *q_dy, *q_dys, *q_da1, *q_da1s, *q_da3, *q_da3s;
+  int32_t* pad;
+  int64_t rp;
+  uint8_t *t_d0, *t_d0s, *t_d1, *t_d1s, *t_f0, *t_f0s, *t_f1, *t_f1s;
+};
+
+// MXFP8 backward of one expert set (moe_backward_mxfp8): dgrad through w2
+// with the SwiGLU derivative, dW2, dgrad through w1|w3, dW1, dW3.  x_rows is
+// the expert set's input, row r read as x_rows[gather[r] / gather_k] when
+// `gather` is given.  dx_rows may alias dyw.
+moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t* gather, int gather_k,
+                             const void* a1, const void* a3, const void* h, int64_t rows, int D, int F, int groups,
+                             const int32_t* offsets, const void* w1t, const void* w1ts, const void* w3t,
+                             const void* w3ts, const void* w2t, const void* w2ts, void* da1, void* da3,
+                             void* dx_rows, float* dw1, float* dw3, float* dw2, const MxBwdScratch& q,
+                             int32_t* status, cudaStream_t st) {
+  const int64_t ldr = moe::mx_scale_ld(rows);
+  // dYw row-wise along D; dh = dYw w2 with the SwiGLU derivative -> da1, da3 (bf16)
+  MOE_CUDA(moe::launch_mx_quant_rows(dyw, nullptr, 1, rows, D, rows, ldr, q.q_dy, q.q_dys, st));
+  GemmArgs g;
+  g.quant = true;
+  g.epi = moe::EPI_SWIGLU_BWD;
+  g.qa[0] = moe::MxOperand{q.q_dy, q.q_dys, rows, D, 1, ldr};
+  g.qb[0] = moe::MxOperand{w2t, w2ts, F, D, groups, F};
+  g.k0 = D;
+  g.offsets = offsets;
+  g.num_groups = groups;
+  g.max_rows = rows;
+  g.n_size = F;
+  g.in0 = a1;
+  g.in1 = a3;
+  g.out0 = da1;
+  g.out1 = da3;
+  g.ld_out = F;
+  g.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+
+  // weight-gradient operands: blocks of 32 tokens per expert, transposed
+  MOE_CUDA(moe::launch_pad_offsets(offsets, groups, q.pad, st));
+  auto tquant = [&](const void* src, const int32_t* gat, int gk, int cols, uint8_t* codes, uint8_t* scales) {
+    return moe::launch_mx_quant_cols_t(src, 1, rows, cols, gat, gk, offsets, q.pad, groups, q.rp, codes, ld16(cols),
+                                       scales, st);
+  };
+  MOE_CUDA(tquant(dyw, nullptr, 1, D, q.t_d0, q.t_d0s));
+  MOE_CUDA(tquant(h, nullptr, 1, F, q.t_f0, q.t_f0s));
+  GemmArgs w;
+  w.quant = true;
+  w.epi = moe::EPI_F32;
+  w.ragged_k = true;
+  w.offsets = q.pad;
+  w.num_groups = groups;
+  w.max_rows = rows;
+  w.status = status;
+  // dW2_e [D,F] = dYw_e^T h_e
+  w.qa[0] = moe::MxOperand{q.t_d0, q.t_d0s, D, q.rp, 1, ld16(D)};
+  w.qb[0] = moe::MxOperand{q.t_f0, q.t_f0s, F, q.rp, 1, ld16(F)};
+  w.m_size = D;
+  w.n_size = F;
+  w.out0 = dw2;
+  w.ld_out = F;
+  w.group_stride_out = static_cast<int64_t>(D) * F;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+
+  // da1, da3 row-wise along F; dx_rows = da1 w1 + da3 w3 (dYw is no longer read)
+  MOE_CUDA(moe::launch_mx_quant_rows(da1, nullptr, 1, rows, F, rows, ldr, q.q_da1, q.q_da1s, st));
+  MOE_CUDA(moe::launch_mx_quant_rows(da3, nullptr, 1, rows, F, rows, ldr, q.q_da3, q.q_da3s, st));
+  GemmArgs d;
+  d.quant = true;
+  d.epi = moe::EPI_BF16;
+  d.qa[0] = moe::MxOperand{q.q_da1, q.q_da1s, rows, F, 1, ldr};
+  d.qa[1] = moe::MxOperand{q.q_da3, q.q_da3s, rows, F, 1, ldr};
+  d.qb[0] = moe::MxOperand{w1t, w1ts, D, F, groups, D};
+  d.qb[1] = moe::MxOperand{w3t, w3ts, D, F, groups, D};
+  d.k0 = F;
+  d.k1 = F;
+  d.offsets = offsets;
+  d.num_groups = groups;
+  d.max_rows = rows;
+  d.n_size = D;
+  d.out0 = dx_rows;
+  d.ld_out = D;
+  d.status = status;
+  MOE_CUDA(moe::launch_grouped_gemm(d, st));
+
+  // dW1_e [F,D] = da1_e^T x_e, dW3_e = da3_e^T x_e
+  MOE_CUDA(tquant(da1, nullptr, 1, F, q.t_f0, q.t_f0s));
+  MOE_CUDA(tquant(da3, nullptr, 1, F, q.t_f1, q.t_f1s));
+  MOE_CUDA(tquant(x_rows, gather, gather_k, D, q.t_d1, q.t_d1s));
+  w.qa[0] = moe::MxOperand{q.t_f0, q.t_f0s, F, q.rp, 1, ld16(F)};
+  w.qb[0] = moe::MxOperand{q.t_d1, q.t_d1s, D, q.rp, 1, ld16(D)};
+  w.m_size = F;
+  w.n_size = D;
+  w.out0 = dw1;
+  w.ld_out = D;
+  w.group_stride_out = static_cast<int64_t>(F) * D;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  w.qa[0] = moe::MxOperand{q.t_f1, q.t_f1s, F, q.rp, 1, ld16(F)};
+  w.out0 = dw3;
+  MOE_CUDA(moe::launch_grouped_gemm(w, st));
   return MOE_OK;
 }
 }  // namespace
@@ -542,6 +675,81 @@ moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_perm, con
                         w->ws3_scale, w->ws2, w->ws2_scale, at<void>(ws, L.hq_sh), at<void>(ws, L.hs_sh), sv.hs,
                         sv.a1s, sv.a3s, y_shared, status, st));
   }
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_mxfp8_t(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
+                                  void* scales, int64_t scale_ld, void* stream) {
+  if (!all16({src, codes}) || !scales || groups < 1 || rows <= 0 || cols <= 0 || rows % 32 || cols % 8 ||
+      scale_ld < cols || scale_ld % 16 || cols > (int64_t{1} << 30))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_mx_quant_cols_t(src, groups, rows, static_cast<int>(cols), nullptr, 1, nullptr,
+                                                 nullptr, 1, rows, static_cast<uint8_t*>(codes), scale_ld,
+                                                 static_cast<uint8_t*>(scales), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wt,
+                                const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                                size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 1) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(*d, ws, ws_bytes, true));
+  if (!wt || !s || !g) return MOE_ERR_INVALID_ARG;
+  if (!all16({w_gate, wt->w1, wt->w1_scale, wt->w3, wt->w3_scale, wt->w2, wt->w2_scale, s->x, s->a1, s->a3, s->h,
+              s->y_perm, dy, g->dx, g->dw_gate, g->dw1, g->dw3, g->dw2}))
+    return MOE_ERR_INVALID_ARG;
+  if (!s->logits || !s->topk_idx || !s->topk_w || !s->offsets || !s->row_of_copy || !s->copy_of_row)
+    return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && !all16({wt->ws1, wt->ws1_scale, wt->ws3, wt->ws3_scale, wt->ws2, wt->ws2_scale, s->a1s,
+                             s->a3s, s->hs, g->dws1, g->dws3, g->dws2}))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  const int N = d->n_tok, D = d->d_model, F = d->d_ff, E = d->n_exp, K = d->top_k;
+  const int64_t R = static_cast<int64_t>(N) * K;
+  if (N == 0) {
+    MOE_CUDA(cudaMemsetAsync(g->dw_gate, 0, sizeof(float) * E * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw1, 0, sizeof(float) * E * F * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw3, 0, sizeof(float) * E * F * D, st));
+    MOE_CUDA(cudaMemsetAsync(g->dw2, 0, sizeof(float) * E * F * D, st));
+    if (d->n_shared) {
+      const size_t fs = d->d_ff_shared;
+      MOE_CUDA(cudaMemsetAsync(g->dws1, 0, sizeof(float) * fs * D, st));
+      MOE_CUDA(cudaMemsetAsync(g->dws3, 0, sizeof(float) * fs * D, st));
+      MOE_CUDA(cudaMemsetAsync(g->dws2, 0, sizeof(float) * fs * D, st));
+    }
+    return MOE_OK;
+  }
+  int32_t* status = at<int32_t>(ws, L.status);
+  float* dl = g->dlogits ? g->dlogits : at<float>(ws, L.dl);
+  float* dg = g->dg ? g->dg : at<float>(ws, L.dg);
+  void* dyw = at<void>(ws, L.dyw);
+  MxBwdScratch q{at<uint8_t>(ws, L.q_dy), at<uint8_t>(ws, L.q_dys), at<uint8_t>(ws, L.q_da1),
+                 at<uint8_t>(ws, L.q_da1s), at<uint8_t>(ws, L.q_da3), at<uint8_t>(ws, L.q_da3s),
+                 at<int32_t>(ws, L.pad), L.rp, at<uint8_t>(ws, L.t_d0), at<uint8_t>(ws, L.t_d0s),
+                 at<uint8_t>(ws, L.t_d1), at<uint8_t>(ws, L.t_d1s), at<uint8_t>(ws, L.t_f0),
+                 at<uint8_t>(ws, L.t_f0s), at<uint8_t>(ws, L.t_f1), at<uint8_t>(ws, L.t_f1s)};
+
+  MOE_CUDA(moe::launch_combine_bwd(N, D, K, d->gate, dy, s->y_perm, s->row_of_copy, s->topk_w, s->logits, E,
+                                   s->topk_idx, dyw, dg, dl, st));
+  // routed experts (x read in permuted order through copy_of_row); dx_perm overwrites dYw
+  MOE_TRY(ffn_pair_bwd_mx(dyw, s->x, s->copy_of_row, K, s->a1, s->a3, s->h, R, D, F, E, s->offsets, wt->w1,
+                          wt->w1_scale, wt->w3, wt->w3_scale, wt->w2, wt->w2_scale, at<void>(ws, L.da1),
+                          at<void>(ws, L.da3), dyw, g->dw1, g->dw3, g->dw2, q, status, st));
+  void* dxs = nullptr;
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, N, st));
+    dxs = at<void>(ws, L.dxs);
+    MxBwdScratch qs = q;
+    qs.pad = at<int32_t>(ws, L.pad_sh);
+    MOE_TRY(ffn_pair_bwd_mx(dy, s->x, nullptr, 1, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, wt->ws1,
+                            wt->ws1_scale, wt->ws3, wt->ws3_scale, wt->ws2, wt->ws2_scale, at<void>(ws, L.da1s),
+                            at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, qs, status, st));
+  }
+  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x, K, at<float>(ws, L.dwg), g->dw_gate,
+                              st));
+  MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
 }
 

@@ -428,9 +428,10 @@ __global__ void __launch_bounds__(256) dwg_partial_kernel(int E, int d8, const i
                                                           const int32_t* __restrict__ cpre,
                                                           const int32_t* __restrict__ copy_of_row,
                                                           const float* __restrict__ dl,
-                                                          const uint4* __restrict__ x_perm,
+                                                          const uint4* __restrict__ x_rows, int gather_k,
                                                           float* __restrict__ partial) {
   __shared__ float s_w[kDwgChunk];
+  __shared__ int s_row[kDwgChunk];
   __shared__ int s_e;
   const int c = blockIdx.x;
   if (c >= cpre[E]) return;                      // uniform across the block
@@ -446,18 +447,23 @@ __global__ void __launch_bounds__(256) dwg_partial_kernel(int E, int d8, const i
   const int e = s_e;
   const int r0 = offsets[e] + (c - cpre[e]) * kDwgChunk;
   const int n = min(kDwgChunk, offsets[e + 1] - r0);
-  if (threadIdx.x < n) s_w[threadIdx.x] = dl[copy_of_row[r0 + threadIdx.x]];
+  if (threadIdx.x < n) {
+    // permuted row r0 + t: a row of x_perm, or (gather_k > 0) token row copy / K of x
+    const int cp = copy_of_row[r0 + threadIdx.x];
+    s_w[threadIdx.x] = dl[cp];
+    s_row[threadIdx.x] = gather_k > 0 ? cp / gather_k : r0 + threadIdx.x;
+  }
   __syncthreads();
   const int i = blockIdx.y * blockDim.x + threadIdx.x;
   if (i >= d8) return;
-  const uint4* src = x_perm + static_cast<int64_t>(r0) * d8 + i;
+  const uint4* src = x_rows + i;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   int j = 0;
   for (; j + 4 <= n; j += 4) {
-    const uint4 v0 = src[static_cast<int64_t>(j) * d8];
-    const uint4 v1 = src[static_cast<int64_t>(j + 1) * d8];
-    const uint4 v2 = src[static_cast<int64_t>(j + 2) * d8];
-    const uint4 v3 = src[static_cast<int64_t>(j + 3) * d8];
+    const uint4 v0 = src[static_cast<int64_t>(s_row[j]) * d8];
+    const uint4 v1 = src[static_cast<int64_t>(s_row[j + 1]) * d8];
+    const uint4 v2 = src[static_cast<int64_t>(s_row[j + 2]) * d8];
+    const uint4 v3 = src[static_cast<int64_t>(s_row[j + 3]) * d8];
     float x0[8], x1[8], x2[8], x3[8];
     unpack8(v0, x0);
     unpack8(v1, x1);
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(256) dwg_partial_kernel(int E, int d8, const i
   }
   for (; j < n; ++j) {
     float x[8];
-    unpack8(src[static_cast<int64_t>(j) * d8], x);
+    unpack8(src[static_cast<int64_t>(s_row[j]) * d8], x);
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_w[j], x[q], acc[q]);
   }
@@ -645,15 +651,16 @@ size_t dwgate_partial_floats(int n_tok, int top_k, int n_exp, int d) {
 }
 
 cudaError_t launch_dwgate(int n_tok, int top_k, int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row,
-                          const float* dl, const void* x_perm, float* scratch, float* dw_gate, cudaStream_t st) {
+                          const float* dl, const void* x_rows, int gather_k, float* scratch, float* dw_gate,
+                          cudaStream_t st) {
   if (n_exp > 1024 || !scratch) return cudaErrorInvalidValue;
   const int chunks = static_cast<int>((static_cast<int64_t>(n_tok) * top_k + kDwgChunk - 1) / kDwgChunk + n_exp);
   float* partial = scratch;
   int32_t* cpre = reinterpret_cast<int32_t*>(scratch + static_cast<size_t>(chunks) * d);
   const int d8 = d / 8;
   dwg_chunk_prefix_kernel<<<1, 32, 0, st>>>(n_exp, offsets, cpre);
-  dwg_partial_kernel<<<dim3(chunks, (d8 + 255) / 256), 256, 0, st>>>(n_exp, d8, offsets, cpre, copy_of_row, dl,
-                                                                     static_cast<const uint4*>(x_perm), partial);
+  dwg_partial_kernel<<<dim3(chunks, (d8 + 255) / 256), 256, 0, st>>>(
+      n_exp, d8, offsets, cpre, copy_of_row, dl, static_cast<const uint4*>(x_rows), gather_k, partial);
   dwg_reduce_kernel<<<dim3(n_exp, (d / 4 + 255) / 256), 256, 0, st>>>(n_exp, d, cpre, partial, dw_gate);
   return cudaGetLastError();
 }

@@ -42,10 +42,13 @@ cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void
                                const int32_t* row_of_copy, const float* topk_w, const float* logits, int n_exp,
                                const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st);
 // dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r] (fp32).
+// x_rows is x_perm [R,D] (gather_k = 0) or x [N,D] read in permuted order,
+// row r = x[copy_of_row[r] / gather_k] (gather_k = top_k).
 // Scratch (in floats) of launch_dwgate: 64-row chunk partials and the chunk prefix.
 size_t dwgate_partial_floats(int n_tok, int top_k, int n_exp, int d);
 cudaError_t launch_dwgate(int n_tok, int top_k, int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row,
-                          const float* dl, const void* x_perm, float* scratch, float* dw_gate, cudaStream_t st);
+                          const float* dl, const void* x_rows, int gather_k, float* scratch, float* dw_gate,
+                          cudaStream_t st);
 // dx[t] = sum_k dx_perm[row(t,k)] + sum_k dl[t,k] * W_g[idx[t,k]] (+ dx_shared[t]); bf16 out.
 cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm, const int32_t* row_of_copy,
                                 const float* dl, const int32_t* topk_idx, const void* w_gate,

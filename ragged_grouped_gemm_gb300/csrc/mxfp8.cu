@@ -71,7 +71,105 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16*
   scales[(g * nkb + kb) * ld_s + n] = static_cast<uint8_t>(e + 127);
 }
 
+// One CTA: one output block of 32 quantised rows x 128 columns; thread t
+// owns column t, reads its 32 values (a warp reads 64 contiguous bytes per
+// row), and writes its 32 codes as two 16-byte stores.
+__global__ void __launch_bounds__(128) mx_quant_cols_t_kernel(
+    const __nv_bfloat16* __restrict__ src, int64_t rows, int cols, const int32_t* __restrict__ src_row_of,
+    int src_div, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets, int n_groups,
+    int64_t ld_codes, uint8_t* __restrict__ codes, int64_t ld_s, uint8_t* __restrict__ scales) {
+  const int64_t jb = blockIdx.x;
+  const int b = blockIdx.z;
+  const int c = blockIdx.y * 128 + threadIdx.x;
+  int64_t r0, nvalid;
+  if (offsets) {
+    const int64_t p0 = jb * 32;
+    if (p0 >= pad_offsets[n_groups]) return;
+    int lo = 0, hi = n_groups;   // largest g with pad_offsets[g] <= p0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pad_offsets[mid] <= p0) lo = mid; else hi = mid;
+    }
+    r0 = offsets[lo] + (p0 - pad_offsets[lo]);
+    nvalid = max(int64_t{0}, min(int64_t{32}, static_cast<int64_t>(offsets[lo + 1]) - r0));
+  } else {
+    r0 = jb * 32;
+    nvalid = max(int64_t{0}, min(int64_t{32}, rows - r0));
+  }
+  if (c >= cols) return;
+  const __nv_bfloat16* m = src + static_cast<int64_t>(b) * rows * cols;
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float v = 0.0f;
+    if (i < nvalid) {
+      const int64_t r = r0 + i;
+      const int64_t sr = src_row_of ? src_row_of[r] / src_div : r;
+      v = __bfloat162float(m[sr * cols + c]);
+    }
+    f[i] = v;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int e = mx_scale_exponent(amax);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(codes + (static_cast<int64_t>(b) * cols + c) * ld_codes + jb * 32);
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  scales[(static_cast<int64_t>(b) * (ld_codes / 32) + jb) * ld_s + c] = static_cast<uint8_t>(e + 127);
+}
+
+// Single block: counts rounded up to 128, exclusive scan over n_groups <= 1024.
+__global__ void __launch_bounds__(1024) pad_offsets_kernel(const int32_t* __restrict__ offsets, int n_groups,
+                                                           int32_t* __restrict__ pad_offsets) {
+  __shared__ int32_t s[1024];
+  const int g = threadIdx.x;
+  const int32_t v = g < n_groups ? (offsets[g + 1] - offsets[g] + 127) / 128 * 128 : 0;
+  s[g] = v;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    const int32_t add = g >= d ? s[g - d] : 0;
+    __syncthreads();
+    s[g] += add;
+    __syncthreads();
+  }
+  if (g < n_groups) pad_offsets[g + 1] = s[g];
+  if (g == 0) pad_offsets[0] = 0;
+}
+
 }  // namespace
+
+cudaError_t launch_mx_quant_cols_t(const void* src, int64_t batch, int64_t rows, int cols,
+                                   const int32_t* src_row_of, int src_div, const int32_t* offsets,
+                                   const int32_t* pad_offsets, int n_groups, int64_t ld_codes, uint8_t* codes,
+                                   int64_t ld_s, uint8_t* scales, cudaStream_t st) {
+  if (rows <= 0 || batch <= 0) return cudaSuccess;
+  if (cols <= 0 || ld_codes % 32 || ld_s < cols || (offsets && (!pad_offsets || batch != 1 || n_groups < 1)))
+    return cudaErrorInvalidValue;
+  if (!offsets && ld_codes < (rows + 31) / 32 * 32) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ld_codes / 32), static_cast<unsigned>((cols + 127) / 128),
+                  static_cast<unsigned>(batch));
+  mx_quant_cols_t_kernel<<<grid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, src_row_of,
+                                                src_div, offsets, pad_offsets, n_groups, ld_codes, codes, ld_s,
+                                                scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_offsets(const int32_t* offsets, int n_groups, int32_t* pad_offsets, cudaStream_t st) {
+  if (n_groups < 1 || n_groups > 1024) return cudaErrorInvalidValue;
+  pad_offsets_kernel<<<1, 1024, 0, st>>>(offsets, n_groups, pad_offsets);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mx_quant_rows(const void* src, const int32_t* src_row_of, int src_div, int64_t rows, int cols,
                                  int64_t rows_per_group, int64_t ld_s, uint8_t* codes, uint8_t* scales,
