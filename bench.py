@@ -315,22 +315,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_sweep(args):
-    """Forward-only timing of the layer under prescribed load skews, bf16 and
-    MXFP8 operands.  Routing comes from the workload's own gate and bias
-    ("bias") or from synthetic fp32 logits through moe_route_from_logits
-    (uniform, Zipf s=1, half of the tokens on expert 0)."""
+    """Forward and forward+backward timing of the layer under prescribed load
+    skews, bf16 and MXFP8 operands (the MXFP8 backward quantises every expert
+    GEMM's operands as its forward does).  Routing comes from the workload's
+    own gate and bias ("bias") or from synthetic fp32 logits through
+    moe_route_from_logits (uniform, Zipf s=1, half of the tokens on expert 0)."""
     import torch
 
     from ragged_grouped_gemm_gb300 import api
-    from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_layer, skewed_logits
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_dy, make_layer, skewed_logits
     base = CONFIGS[args.workload]
     peaks = measured_peaks()
     dev = torch.device("cuda", 0)
     p = make_layer(base, dev)
+    dy = make_dy(base, dev)
     results = []
     for prec in ("bf16", "mxfp8"):
         cfg = base.replace(precision=prec)
-        layer = api.MoELayer(cfg, p, train=False, device=dev)
+        layer = api.MoELayer(cfg, p, train=True, device=dev)
         b, d, ws = layer.buf, layer.desc, layer.ws
         for skew in ("bias", "uniform", "zipf", "half0"):
             lg = None if skew == "bias" else skewed_logits(cfg.n_tok, cfg.n_exp, skew).to(dev)
@@ -340,25 +342,35 @@ def run_sweep(args):
                 if lg is None:
                     return layer.forward(p["x"])
                 api.moe_route_from_logits(d, lg, zero_bias, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], ws)
+                b["logits"].copy_(lg)        # the router gradient reads the logits the routing used
+                layer.x = p["x"]
                 if layer.mx:
                     return layer._forward_mx(p["x"])
                 api.moe_permute(d, p["x"], b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
                                 b["x_perm"], ws)
                 api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], p["x"], p["w1"], p["w3"], p["w2"], p.get("ws1"),
-                                    p.get("ws3"), p.get("ws2"), None, None, b["h"], None, None, b["hs"], b["y_perm"],
-                                    b["y_shared"], ws)
+                                    p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
+                                    b["y_perm"], b["y_shared"], ws)
                 api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
                 return b["out"]
-            for _ in range(args.warmup):
+
+            def fwd_bwd():
                 fwd()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(args.steps):
-                fwd()
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / args.steps
+                layer.backward(dy)
+
+            def timed(fn):
+                for _ in range(args.warmup):
+                    fn()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / args.steps
+            ms = timed(fwd)
+            ms_fb = timed(fwd_bwd)
             counts = b["counts"].cpu()
             ne = int((counts > 0).sum())
             wb = 3 * ne * cfg.d_ff * cfg.d_model + (3 * cfg.d_ff_shared * cfg.d_model if cfg.n_shared else 0)
@@ -367,11 +379,14 @@ def run_sweep(args):
                             "experts_nonempty": ne, "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
                             "weight_bytes": wbytes, "weight_stream_gbs": wbytes / ms / 1e6,
                             "weight_stream_frac_of_hbm": wbytes / ms / 1e6 / peaks["hbm_gbs"],
-                            "tflops": flops(cfg)["ffn_fwd"] / ms / 1e9})
+                            "tflops": flops(cfg)["ffn_fwd"] / ms / 1e9, "ms_fwd_bwd": ms_fb,
+                            "tokens_per_s_fwd_bwd": cfg.n_tok / ms_fb * 1e3,
+                            "tflops_fwd_bwd": (flops(cfg)["ffn_fwd"] + flops(cfg)["ffn_bwd"]) / ms_fb / 1e9})
             assert layer.device_status()[0] == 0
         del layer
         torch.cuda.empty_cache()
-    print(json.dumps({"sweep": f"{base.name} forward, steps={args.steps}", "peaks": peaks, "results": results}),
+    print(json.dumps({"sweep": f"{base.name} forward and forward+backward, steps={args.steps}", "peaks": peaks,
+                      "results": results}),
           flush=True)
 
 
