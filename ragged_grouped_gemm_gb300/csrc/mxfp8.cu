@@ -1,7 +1,6 @@
-// MXFP8 quantisation kernel: one thread per (row, 32-element block), a warp
-// covering 32 consecutive rows of one block, so every thread reads 64
-// contiguous bytes, writes 32 contiguous code bytes, and the warp writes 32
-// consecutive scale bytes.
+// MXFP8 quantisation kernels.  Row-wise: one thread per (row, 32-element
+// block), a warp covering 32 consecutive blocks of one row, so the warp
+// reads 2 KB and writes 1 KB of codes contiguously.
 //
 // Scale rule (OCP MX v1.0 with E4M3 elements, emax = 8): the block's shared
 // scale is 2^(floor(log2(amax)) - 8), clamped to [2^-127, 2^127]; an all-zero
@@ -31,11 +30,11 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16*
                                                             int64_t ld_s, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ scales) {
   const int nkb = cols / 32;
+  const int chunks = (nkb + 31) / 32;
   const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t rgroup = w / nkb;
-  const int kb = static_cast<int>(w - rgroup * nkb);
-  const int64_t row = rgroup * 32 + (threadIdx.x & 31);
-  if (rgroup * 32 >= rows || row >= rows) return;
+  const int64_t row = w / chunks;
+  const int kb = static_cast<int>(w - row * chunks) * 32 + (threadIdx.x & 31);
+  if (row >= rows || kb >= nkb) return;
   const int64_t sr = src_row_of ? src_row_of[row] / src_div : row;
   const uint4* p = reinterpret_cast<const uint4*>(src + sr * cols + kb * 32);
   float f[32];
@@ -71,20 +70,22 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16*
   scales[(g * nkb + kb) * ld_s + n] = static_cast<uint8_t>(e + 127);
 }
 
-// One CTA: one output block of 32 quantised rows x 128 columns; thread t
-// owns column t, reads its 32 values (a warp reads 64 contiguous bytes per
-// row), and writes its 32 codes as two 16-byte stores.
+// Transposing quantiser.  One CTA: one output block of 32 quantised rows x
+// 128 columns.  The 32 x 128 bf16 tile is staged in shared memory with
+// coalesced 16-byte loads (16 threads per 256-byte row segment); thread t
+// then quantises column t and writes its 32 codes with one 32-byte store.
 __global__ void __launch_bounds__(128) mx_quant_cols_t_kernel(
     const __nv_bfloat16* __restrict__ src, int64_t rows, int cols, const int32_t* __restrict__ src_row_of,
     int src_div, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets, int n_groups,
     int64_t ld_codes, uint8_t* __restrict__ codes, int64_t ld_s, uint8_t* __restrict__ scales) {
+  __shared__ __align__(16) __nv_bfloat16 tile[32][128 + 8];   // +8: rows 16 B apart in the bank pattern
   const int64_t jb = blockIdx.x;
   const int b = blockIdx.z;
-  const int c = blockIdx.y * 128 + threadIdx.x;
+  const int c0 = blockIdx.y * 128;
   int64_t r0, nvalid;
   if (offsets) {
     const int64_t p0 = jb * 32;
-    if (p0 >= pad_offsets[n_groups]) return;
+    if (p0 >= pad_offsets[n_groups]) return;   // uniform across the block
     int lo = 0, hi = n_groups;   // largest g with pad_offsets[g] <= p0
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -96,19 +97,25 @@ __global__ void __launch_bounds__(128) mx_quant_cols_t_kernel(
     r0 = jb * 32;
     nvalid = max(int64_t{0}, min(int64_t{32}, rows - r0));
   }
-  if (c >= cols) return;
   const __nv_bfloat16* m = src + static_cast<int64_t>(b) * rows * cols;
+  // stage: 32 rows x 16 chunks of 8 bf16; cols is a multiple of 8
+  for (int i = threadIdx.x; i < 32 * 16; i += 128) {
+    const int rr = i >> 4, ch = i & 15;
+    const int c = c0 + ch * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (rr < nvalid && c < cols) {
+      const int64_t r = r0 + rr;
+      const int64_t sr = src_row_of ? src_row_of[r] / src_div : r;
+      v = *reinterpret_cast<const uint4*>(m + sr * cols + c);
+    }
+    *reinterpret_cast<uint4*>(&tile[rr][ch * 8]) = v;
+  }
+  __syncthreads();
+  const int c = c0 + threadIdx.x;
+  if (c >= cols) return;
   float f[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float v = 0.0f;
-    if (i < nvalid) {
-      const int64_t r = r0 + i;
-      const int64_t sr = src_row_of ? src_row_of[r] / src_div : r;
-      v = __bfloat162float(m[sr * cols + c]);
-    }
-    f[i] = v;
-  }
+  for (int i = 0; i < 32; ++i) f[i] = __bfloat162float(tile[i][threadIdx.x]);
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -123,9 +130,10 @@ __global__ void __launch_bounds__(128) mx_quant_cols_t_kernel(
         __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
     out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + (static_cast<int64_t>(b) * cols + c) * ld_codes + jb * 32);
-  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  uint8_t* dst = codes + (static_cast<int64_t>(b) * cols + c) * ld_codes + jb * 32;   // 32-byte aligned
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(out[0]), "r"(out[1]),
+               "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]), "r"(out[6]), "r"(out[7])
+               : "memory");
   scales[(static_cast<int64_t>(b) * (ld_codes / 32) + jb) * ld_s + c] = static_cast<uint8_t>(e + 127);
 }
 
@@ -154,8 +162,11 @@ cudaError_t launch_mx_quant_cols_t(const void* src, int64_t batch, int64_t rows,
                                    const int32_t* pad_offsets, int n_groups, int64_t ld_codes, uint8_t* codes,
                                    int64_t ld_s, uint8_t* scales, cudaStream_t st) {
   if (rows <= 0 || batch <= 0) return cudaSuccess;
-  if (cols <= 0 || ld_codes % 32 || ld_s < cols || (offsets && (!pad_offsets || batch != 1 || n_groups < 1)))
+  if (cols <= 0 || cols % 8 || ld_codes % 32 || ld_s < cols ||
+      (offsets && (!pad_offsets || batch != 1 || n_groups < 1)))
     return cudaErrorInvalidValue;
+  // 16-byte source rows and 32-byte code runs
+  if ((reinterpret_cast<uintptr_t>(src) & 15) || (reinterpret_cast<uintptr_t>(codes) & 31)) return cudaErrorInvalidValue;
   if (!offsets && ld_codes < (rows + 31) / 32 * 32) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ld_codes / 32), static_cast<unsigned>((cols + 127) / 128),
                   static_cast<unsigned>(batch));
@@ -176,7 +187,7 @@ cudaError_t launch_mx_quant_rows(const void* src, const int32_t* src_row_of, int
                                  cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (cols % 32 || rows_per_group <= 0 || rows % rows_per_group || ld_s < rows_per_group) return cudaErrorInvalidValue;
-  const int64_t warps = (rows + 31) / 32 * (cols / 32);
+  const int64_t warps = rows * ((cols / 32 + 31) / 32);
   const int64_t blocks = (warps + 7) / 8;
   mx_quant_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(src), src_row_of, src_div, rows, cols, rows_per_group, ld_s, codes, scales);
