@@ -663,8 +663,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           // Stage this warp's 32 rows x 16 columns in a 2 KB shared-memory
           // buffer (64-byte swizzle: 16-byte chunk j of row r at chunk
           // j ^ ((r >> 1) & 3)) and write them with a TMA tensor store, which
-          // clips rows and columns outside the output.  The TMEM load of the
-          // next chunk is in flight while this one is staged.
+          // clips rows and columns outside the output (evict-first in L2:
+          // the fp32 output is written once and not read back).  The TMEM
+          // load of the next chunk is in flight while this one is staged.
           constexpr int NCH = BN / 32;
           uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
           const uint32_t stg_addr = smem_u32(stg);
@@ -692,7 +693,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
               const int row = RAGGED_K ? t.m0 + q * 32 : t.row0 + q * 32;
               const int rows = RAGGED_K ? p.m_size : p.c_rows;
               if (col < p.n_size && row < rows) {
-                tma_store_3d(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0);
+                tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0, policy_evict_first());
                 bulk_commit_group();
               }
             }
