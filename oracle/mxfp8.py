@@ -31,9 +31,7 @@ _E4M3_BIAS = 7
 _E4M3_EMAX = 8
 
 
-def e4m3_decode(codes: np.ndarray) -> np.ndarray:
-    """E4M3 byte -> float64 value (NaN for S.1111.111)."""
-    c = np.asarray(codes).astype(np.int64)
+def _e4m3_decode_formula(c: np.ndarray) -> np.ndarray:
     sign = np.where(c & 0x80, -1.0, 1.0)
     exp = (c >> 3) & 0xF
     man = c & 0x7
@@ -44,30 +42,41 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
     return sign * val
 
 
+_E4M3_TABLE = _e4m3_decode_formula(np.arange(256, dtype=np.int64))
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """E4M3 byte -> float64 value (NaN for S.1111.111): sign, 4 exponent bits
+    (bias 7), 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6).  Looked up
+    in the 256-entry table of that formula."""
+    return _E4M3_TABLE[np.asarray(codes).astype(np.uint8)]
+
+
 def e4m3_encode(v: np.ndarray) -> np.ndarray:
-    """float -> E4M3 byte, round to nearest even, saturate to +-448, NaN -> 0x7F."""
+    """float -> E4M3 byte, round to nearest even, saturate to +-448, NaN -> 0x7F.
+
+    The binade exponent e = floor(log2|v|) comes from frexp (subnormals share
+    the minimum normal exponent -6); |v| / 2^(e-3) rounded half to even gives
+    the significand m in 8..16 (16 carries into the next binade) or, for
+    subnormals, 0..8; the code is then (e + 7) * 8 + (m - 8), or m for a
+    subnormal.  Values past 448 (and infinities) saturate to 448."""
     v = np.asarray(v, dtype=np.float64)
     a = np.abs(v)
-    finite = np.isfinite(a)
-    a_f = np.where(finite, a, 0.0)
-    # exponent of the binade (subnormals share the minimum normal exponent -6)
-    with np.errstate(divide="ignore"):
-        e = np.floor(np.log2(np.where(a_f > 0, a_f, 1.0)))
-    e = np.maximum(e, 1 - _E4M3_BIAS)
-    q = np.exp2(e - 3)                      # spacing of values in that binade
-    r = np.rint(a_f / q) * q                # np.rint rounds half to even
-    r = np.minimum(r, E4M3_MAX)             # saturate (also +-inf)
-    r = np.where(np.isinf(a), E4M3_MAX, r)
-    # value -> code
-    e2 = np.floor(np.log2(np.where(r > 0, r, 1.0)))
-    is_sub = r < 2.0 ** (1 - _E4M3_BIAS)
-    man_sub = np.rint(r / 2.0 ** (1 - _E4M3_BIAS - 3))
-    man_nrm = np.rint((r / np.exp2(e2) - 1.0) * 8.0)
-    exp_nrm = e2 + _E4M3_BIAS
-    code = np.where(is_sub, man_sub, exp_nrm * 8 + man_nrm).astype(np.int64)
-    code = np.where(r == 0, 0, code)
+    nan = np.isnan(v)
+    inf = np.isinf(v)
+    a_f = np.where(nan | inf, 0.0, a)
+    _, ex = np.frexp(a_f)                    # a = f * 2^ex with f in [0.5, 1)
+    e = np.maximum(ex - 1, 1 - _E4M3_BIAS)
+    m = np.rint(np.ldexp(a_f, -(e - 3)))     # exact power-of-two scaling, then RNE
+    carry = m >= 16
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, 8, m)
+    over = inf | (e > _E4M3_EMAX) | ((e == _E4M3_EMAX) & (m > 14))   # 14 -> 1.75 * 2^8 = 448
+    e = np.where(over, _E4M3_EMAX, e)
+    m = np.where(over, 14, m)
+    code = np.where(m < 8, m, (e + _E4M3_BIAS) * 8 + (m - 8)).astype(np.int64)
     code = code | np.where(np.signbit(v), 0x80, 0)
-    code = np.where(np.isnan(v), 0x7F, code)
+    code = np.where(nan, 0x7F, code)
     return code.astype(np.uint8)
 
 
@@ -95,6 +104,13 @@ def mx_quantize(x: np.ndarray, axis: int = -1, group_starts=None):
     """
     x = np.moveaxis(np.asarray(x, dtype=np.float64), axis, -1)
     length = x.shape[-1]
+    if group_starts is None and length % MX_BLOCK == 0:
+        # every block is a full 32 elements: the same steps on all blocks at once
+        xb = x.reshape(x.shape[:-1] + (length // MX_BLOCK, MX_BLOCK))
+        ex = e8m0_scale_exponent(np.abs(xb).max(axis=-1))
+        codes = e4m3_encode(xb / np.exp2(ex)[..., None]).reshape(x.shape)
+        scales = (ex + 127).astype(np.uint8)
+        return np.moveaxis(codes, -1, axis), np.moveaxis(scales, -1, axis), list(range(0, length, MX_BLOCK))
     if group_starts is None:
         starts = list(range(0, length, MX_BLOCK))
     else:
@@ -119,6 +135,10 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray, starts, axis: int = -1)
     c = np.moveaxis(np.asarray(codes), axis, -1)
     s = np.moveaxis(np.asarray(scales), axis, -1)
     length = c.shape[-1]
+    if list(starts) == list(range(0, length, MX_BLOCK)) and length % MX_BLOCK == 0:
+        vals = e4m3_decode(c).reshape(c.shape[:-1] + (length // MX_BLOCK, MX_BLOCK))
+        out = vals * np.exp2(s.astype(np.float64) - 127)[..., None]
+        return np.moveaxis(out.reshape(c.shape), -1, axis)
     ends = list(starts[1:]) + [length]
     out = np.empty(c.shape, dtype=np.float64)
     vals = e4m3_decode(c)

@@ -25,6 +25,7 @@ from ragged_grouped_gemm_gb300 import api
 from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_dy, make_layer, sample_tokens
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+MX_TOL = 3e-2       # MXFP8 against the quantisation-aware oracle
 
 
 def _experts(t, used):
@@ -115,6 +116,79 @@ def test_full_size_sampled(name):
         for key in ("dw1", "dw3", "dw2"):
             assert rel(gr[key][e_hot].cpu().numpy(), rg[key][0]) < BF16_TOL, key
     for e in np.nonzero(gcounts == 0)[0][:2]:
+        assert not gr["dw1"][int(e)].any() and not gr["dw2"][int(e)].any()
+    del layer, p
+    torch.cuda.empty_cache()
+
+
+def test_full_size_sampled_mxfp8_dsv3():
+    """The DeepSeek-V3-shaped layer with MXFP8 expert GEMMs, forward and
+    backward at full size, against the quantisation-aware oracle.  Row-wise
+    quantisation (x, h along D/F; dYw, da1, da3 along D/F) keeps token rows
+    independent, so outputs and input-side gradients are checked on a token
+    sample; the weight gradients of the most loaded expert depend on its
+    tokens in 32-row blocks, so the oracle runs that expert's whole row set."""
+    cfg = CONFIGS["dsv3"].replace(precision="mxfp8")
+    torch.cuda.empty_cache()
+    p = make_layer(cfg, "cuda")
+    dy = make_dy(cfg, "cuda")
+    layer = api.MoELayer(cfg, p, train=True)
+    out = layer.forward(p["x"])
+    gr = layer.backward(dy)
+    torch.cuda.synchronize()
+    assert layer.device_status()[0] == 0
+
+    x = np32(p["x"])
+    wg = np32(p["w_gate"])
+    bias = np32(p["bias"])
+    lg = O.gate_logits(x, wg)
+    glg = np32(layer.buf["logits"])
+    keys = O.selection_keys(lg, bias)
+    idx, g = O.route(lg, bias, cfg.top_k, cfg.gate)
+    gidx = layer.buf["topk_idx"].cpu().numpy()
+    tol = 2 * float(np.abs(glg - lg).max()) + 1e-6
+    same = routing_agreement(keys, gidx, idx, tol)
+    shared = (np32(p["ws1"]), np32(p["ws3"]), np32(p["ws2"]))
+    dyh = np32(dy)
+
+    # a token sample whose experts stay within 16 (every expert's weights are
+    # quantised once per contraction axis by the oracle, which bounds its time)
+    cand = sample_tokens(cfg.n_tok, 512).numpy()
+    grp, used_e = [], set()
+    for t in cand:
+        es = set(idx[t].tolist())
+        if same[t] and len(used_e | es) <= 16:
+            grp.append(t)
+            used_e |= es
+        if len(grp) == 8:
+            break
+    grp = np.array(grp)
+    assert len(grp) >= 2
+    used = np.unique(idx[grp])
+    ic = np.searchsorted(used, idx[grp]).astype(np.int32)
+    lgc = lg[grp][:, used]
+    w1, w3, w2 = _experts(p["w1"], used), _experts(p["w3"], used), _experts(p["w2"], used)
+    o, saved = O.moe_forward_mxfp8(x[grp], ic, g[grp], w1, w3, w2, shared, return_saved=True)
+    rg = O.moe_backward_mxfp8(dyh[grp], x[grp], lgc, ic, g[grp], wg[used], w1, w3, w2, saved, cfg.gate, shared)
+    assert rel(np32(out)[grp], o) < MX_TOL, "out"
+    assert rel(np32(gr["dx"])[grp], rg["dx"]) < MX_TOL, "dx"
+    assert rel(np32(gr["dg"])[grp], rg["dg"]) < MX_TOL, "dg"
+    assert rel(np32(gr["dlogits"])[grp], np.take_along_axis(rg["dlogits"], ic.astype(np.int64), axis=1)) < MX_TOL
+
+    counts = O.histogram(idx, cfg.n_exp)
+    e_hot = int(np.argmax(counts))
+    tok, kk = np.nonzero(idx == e_hot)
+    if same[tok].all():
+        used = np.array([e_hot])
+        w1, w3, w2 = _experts(p["w1"], used), _experts(p["w3"], used), _experts(p["w2"], used)
+        i1 = np.zeros((len(tok), 1), np.int32)
+        g1 = g[tok, kk][:, None]
+        lg1 = lg[tok][:, [e_hot]]
+        _, saved = O.moe_forward_mxfp8(x[tok], i1, g1, w1, w3, w2, None, return_saved=True)
+        rg = O.moe_backward_mxfp8(dyh[tok], x[tok], lg1, i1, g1, wg[used], w1, w3, w2, saved, cfg.gate, None)
+        for key in ("dw1", "dw3", "dw2"):
+            assert rel(gr[key][e_hot].cpu().numpy(), rg[key][0]) < MX_TOL, key
+    for e in np.nonzero(O.histogram(gidx, cfg.n_exp) == 0)[0][:2]:
         assert not gr["dw1"][int(e)].any() and not gr["dw2"][int(e)].any()
     del layer, p
     torch.cuda.empty_cache()

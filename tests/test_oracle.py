@@ -501,3 +501,17 @@ def test_bf16_round_is_round_to_nearest_even():
     want = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
     got = O.bf16_round(v)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_mx_quantize_block_vectorised_path_equals_block_loop():
+    """The all-blocks-at-once path (no group boundaries, whole blocks) against
+    the block-by-block path (forced through group_starts=[0])."""
+    r = _rng(35)
+    x = r.standard_normal((5, 7, 96)) * np.exp2(r.integers(-40, 40, (5, 7, 1)))
+    for axis in (2, 0):
+        xa = np.moveaxis(x, 2, axis) if axis == 0 else x
+        c1, s1, st1 = O.mx_quantize(xa, axis=axis if axis == 2 else 0)
+        c2, s2, st2 = O.mx_quantize(xa, axis=axis if axis == 2 else 0, group_starts=[0])
+        assert st1 == st2 and np.array_equal(c1, c2) and np.array_equal(s1, s2)
+        assert np.array_equal(O.mx_dequantize(c1, s1, st1, axis=axis if axis == 2 else 0),
+                              O.mx_dequantize(c2, s2, [0] + st2[1:], axis=axis if axis == 2 else 0))
