@@ -38,7 +38,7 @@ __all__ = [
     "gate_logits", "selection_keys", "topk_select", "topk_select_bruteforce",
     "gate_weights", "route", "histogram", "exclusive_offsets", "permutation",
     "swiglu_expert", "moe_forward", "moe_forward_dense_bruteforce",
-    "moe_backward", "router_logit_grad", "update_bias", "aux_loss",
+    "moe_backward", "router_logit_grad", "update_bias", "aux_loss", "aux_loss_grad",
     "monitor_stats", "load_stat",
 ]
 
@@ -401,6 +401,34 @@ def aux_loss(logits: np.ndarray, idx: np.ndarray, n_exp: int, gate: str = "softm
     f = mask.mean(axis=0)
     p = probs.mean(axis=0)
     return float(n_exp * (f * p).sum())
+
+
+def aux_loss_grad(logits: np.ndarray, idx: np.ndarray, n_exp: int, gate: str = "softmax") -> np.ndarray:
+    """Gradient of :func:`aux_loss` with respect to the logits [N, E] (fp64),
+    the top-K fractions ``f`` held fixed (they come from the discrete
+    selection).  With ``P_i = mean_t q_{t,i}``:
+
+    * softmax: ``q = softmax(l)``, ``dq_i/dl_j = q_i (delta_ij - q_j)``, so
+      ``d aux / d l_{t,j} = E/N * q_{t,j} (f_j - sum_i f_i q_{t,i})``;
+    * sigmoid: ``q_i = s_i / S`` with ``s = sigmoid(l)``, ``S = sum s``, so
+      ``d aux / d l_{t,j} = E/N * s_j (1 - s_j) / S * (f_j - sum_i f_i q_{t,i})``.
+    """
+    lg = logits.astype(np.float64)
+    n = lg.shape[0]
+    mask = np.zeros_like(lg)
+    np.put_along_axis(mask, idx.astype(np.int64), 1.0, axis=1)
+    f = mask.mean(axis=0)
+    if gate == "softmax":
+        ex = np.exp(lg - lg.max(axis=1, keepdims=True))
+        q = ex / ex.sum(axis=1, keepdims=True)
+        dq = q
+    else:
+        sg = 1.0 / (1.0 + np.exp(-lg))
+        ssum = sg.sum(axis=1, keepdims=True)
+        q = sg / ssum
+        dq = sg * (1.0 - sg) / ssum
+    inner = (q * f[None, :]).sum(axis=1, keepdims=True)
+    return n_exp / n * dq * (f[None, :] - inner)
 
 
 def monitor_stats(history: list[np.ndarray], last: int = 100) -> dict:

@@ -515,3 +515,24 @@ def test_mx_quantize_block_vectorised_path_equals_block_loop():
         assert st1 == st2 and np.array_equal(c1, c2) and np.array_equal(s1, s2)
         assert np.array_equal(O.mx_dequantize(c1, s1, st1, axis=axis if axis == 2 else 0),
                               O.mx_dequantize(c2, s2, [0] + st2[1:], axis=axis if axis == 2 else 0))
+
+
+@pytest.mark.parametrize("gate", ["softmax", "sigmoid"])
+def test_aux_loss_grad_matches_finite_differences(gate):
+    """The aux-loss logit gradient against fp64 central differences of the
+    aux-loss value with the top-K selection held fixed."""
+    r = _rng(36)
+    n, e, k = 12, 6, 2
+    lg = r.standard_normal((n, e))
+    idx = O.topk_select(O.selection_keys(lg.astype(np.float32), None), k)
+    grad = O.aux_loss_grad(lg, idx, e, gate)
+    h = 1e-6
+    fd = np.zeros_like(lg)
+    for t in range(n):
+        for j in range(e):
+            lp, lm = lg.copy(), lg.copy()
+            lp[t, j] += h
+            lm[t, j] -= h
+            fd[t, j] = (O.aux_loss(lp, idx, e, gate) - O.aux_loss(lm, idx, e, gate)) / (2 * h)
+    assert np.allclose(grad, fd, rtol=1e-6, atol=1e-9)
+    assert abs(grad.sum()) < 1e-9 if gate == "softmax" else True   # softmax: invariant to a per-token shift
