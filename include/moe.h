@@ -241,6 +241,29 @@ MOE_API moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const
 MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
                              void* stream);
 
+/* Auxiliary load-balancing loss (§6.2, GShard form) of the routing that
+ * produced `logits` [N,E] (fp32, from moe_route) and `counts` [E]:
+ *   loss[0] = coef * E * sum_i f_i P_i,  f_i = counts_i / N (mean of the
+ *   top-K mask), P_i = mean over tokens of the softmax over all E logits
+ *   (softmax gate) or of the sigmoid scores normalised over all E (sigmoid
+ *   gate; the pages give no P for it).
+ * dlogits_aux [N,E] (fp32, NULL: not computed) receives d loss / d logits with
+ * f held fixed (the selection is discrete); the caller adds it to the
+ * router's logit gradient.  Deterministic (fixed-order sums).  loss is a
+ * device pointer.  Needs the forward workspace. */
+MOE_API moe_status_t moe_aux_loss(const moe_desc_t* d, const float* logits, const int32_t* counts, float coef,
+                                  float* loss, float* dlogits_aux, void* ws, size_t ws_bytes, void* stream);
+
+/* Load monitor statistics (§13.9) over a window of routing histograms:
+ * counts_hist [n_hist, n_exp] int32 on the device, one row per step (e.g. the
+ * counts of the last 100 steps; rows must not sum to 0).  Each row becomes
+ * the load fraction counts / sum (fp32); the window mean r (fp64) gives
+ *   stats[0] = min_e r_e, stats[1] = -sum_e r_e log(r_e + 1e-9),
+ *   stats[2] = number of experts with r_e < 0.3 / n_exp (as a float).
+ * stats is a device pointer to 3 floats.  n_exp <= 1024. */
+MOE_API moe_status_t moe_monitor_stats(int32_t n_exp, const int32_t* counts_hist, int32_t n_hist, float* stats,
+                                       void* stream);
+
 /* ---------------------------------------------------------------- MXFP8 --
  * The MXFP8 forward path: the expert GEMMs read their operands as MXFP8 (OCP
  * Microscaling v1.0: E4M3 elements, one E8M0 power-of-two scale per 32

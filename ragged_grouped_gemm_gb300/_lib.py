@@ -75,6 +75,9 @@ SIGNATURES = {
     "moe_grouped_ffn_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(MoeExpertWeightsMx), ctypes.POINTER(MoeFfnSaved), c_vp, c_vp,
                                       c_vp, ctypes.c_size_t, c_vp]),
+    "moe_aux_loss": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp,
+                             ctypes.c_size_t, c_vp]),
+    "moe_monitor_stats": (c_i32, [c_i32, c_vp, c_i32, c_vp, c_vp]),
     "moe_quantize_mxfp8_t": (c_i32, [c_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_vp, c_vp,
                                      ctypes.c_int64, c_vp]),
     "moe_backward_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, ctypes.POINTER(MoeExpertWeightsMx),

@@ -185,6 +185,24 @@ def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, 
         _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
+def moe_aux_loss(desc, logits, counts, loss, dlogits_aux=None, ws=None, coef: float = 1.0, stream=None):
+    """``loss``: fp32 device tensor of one element; ``dlogits_aux``: optional
+    fp32 [N, E] receiving the loss's logit gradient."""
+    n, e = desc.n_tok, desc.n_exp
+    _check("moe_aux_loss", _lib.load().moe_aux_loss(
+        ctypes.byref(desc), _p(logits, F32, (n, e), "logits"), _p(counts, I32, (e,), "counts"), ctypes.c_float(coef),
+        _p(loss, F32, (1,), "loss"), _p(dlogits_aux, F32, (n, e), "dlogits_aux"), _p(ws, name="ws"),
+        ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_monitor_stats(counts_hist, stats, stream=None):
+    """``counts_hist``: int32 [H, E] device tensor (one routing histogram per
+    step); ``stats``: fp32 device tensor [3] <- min load, entropy, cold experts."""
+    h, e = counts_hist.shape
+    _check("moe_monitor_stats", _lib.load().moe_monitor_stats(
+        e, _p(counts_hist, I32, (h, e), "counts_hist"), h, _p(stats, F32, (3,), "stats"), _s(stream)))
+
+
 def moe_update_bias(desc, counts, bias, gamma: float, mode: int = 0, stream=None):
     _check("moe_update_bias", _lib.load().moe_update_bias(
         ctypes.byref(desc), _p(counts, I32, (desc.n_exp,), "counts"), _p(bias, F32, (desc.n_exp,), "bias"),

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 
+#include "balance.cuh"
 #include "grouped_gemm.cuh"
 #include "moe_kernels.cuh"
 #include "mxfp8.cuh"
@@ -19,7 +20,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, fwd_end = 0;
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, aux = 0, fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
   // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
@@ -42,6 +43,7 @@ WsLayout layout(const moe_desc_t& d) {
   L.dense_off = o; o += kAlign;
   L.blk_counts = o; o = align_up(o + nch * E * 4);
   L.blk_base = o; o = align_up(o + nch * E * 4);
+  L.aux = o; o = align_up(o + moe::aux_partial_floats(d.n_tok > 0 ? d.n_tok : 1, d.n_exp) * 4);
   if (d.precision == 1) {
     L.hq = o; o = align_up(o + R * F);
     L.hs = o; o = align_up(o + F / 32 * moe::mx_scale_ld(R));
@@ -751,6 +753,24 @@ moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const m
                               st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
+}
+
+moe_status_t moe_aux_loss(const moe_desc_t* d, const float* logits, const int32_t* counts, float coef, float* loss,
+                          float* dlogits_aux, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!logits || !counts || !loss) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  const WsLayout L = layout(*d);
+  return cuda_status(moe::launch_aux_loss(logits, d->n_tok, d->n_exp, d->gate, counts, coef, at<float>(ws, L.aux),
+                                          loss, dlogits_aux, st));
+}
+
+moe_status_t moe_monitor_stats(int32_t n_exp, const int32_t* counts_hist, int32_t n_hist, float* stats,
+                               void* stream) {
+  if (n_exp < 1 || n_exp > 1024 || n_hist < 1 || !counts_hist || !stats) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_monitor(counts_hist, n_hist, n_exp, stats, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
