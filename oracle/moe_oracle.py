@@ -39,6 +39,7 @@ __all__ = [
     "gate_weights", "route", "histogram", "exclusive_offsets", "permutation",
     "swiglu_expert", "moe_forward", "moe_forward_dense_bruteforce",
     "moe_backward", "router_logit_grad", "update_bias", "aux_loss", "aux_loss_grad",
+    "capacity", "permutation_capacity", "moe_forward_capacity",
     "monitor_stats", "load_stat",
 ]
 
@@ -237,6 +238,66 @@ def moe_forward(x, logits, idx, g, w1, w3, w2, shared=None, dtype=F32):
         ys, a1s, a3s, hs = swiglu_expert(x, shared[0], shared[1], shared[2], dtype)
         out = out + ys
         saved["shared"] = (ys, a1s, a3s, hs)
+    return out, saved
+
+
+# ----------------------------------------------------------------------------
+# Capacity factor and token drop ([MoE-Eng] §6.4; §2.2 GShard): the
+# comparison case of the dropless layer
+# ----------------------------------------------------------------------------
+def capacity(n_tok: int, n_exp: int, top_k: int, capacity_factor: float) -> int:
+    """``capacity_factor * (tokens_per_batch / n_experts * top_k)`` ([MoE-Eng]
+    §6.4), rounded up to whole token copies (reading)."""
+    return int(np.ceil(capacity_factor * (n_tok / n_exp * top_k) - 1e-9))
+
+
+def permutation_capacity(idx: np.ndarray, n_exp: int, cap: int):
+    """Expert-major permutation with at most ``cap`` copies per expert: each
+    expert keeps its first ``cap`` copies in token order (the order of the
+    dropless permutation) and drops the rest (reading: overflow is dropped,
+    [MoE-Eng] §6.4 "drop ... through the residual").
+
+    Returns (row_of_copy with -1 for dropped copies, copy_of_row of the kept
+    rows, kept counts, kept offsets [E+1], number of dropped copies)."""
+    n, k = idx.shape
+    roc_full, _ = permutation(idx, n_exp)
+    off_full = exclusive_offsets(histogram(idx, n_exp))
+    flat = idx.reshape(-1).astype(np.int64)
+    rank = roc_full - off_full[flat]
+    kept = np.minimum(histogram(idx, n_exp), cap).astype(np.int64)
+    off = exclusive_offsets(kept)
+    roc = np.where(rank < cap, off[flat] + rank, -1).astype(np.int64)
+    cor = np.empty(int(kept.sum()), dtype=np.int64)
+    keep = roc >= 0
+    cor[roc[keep]] = np.nonzero(keep)[0]
+    return roc, cor, kept, off, int((~keep).sum())
+
+
+def moe_forward_capacity(x, logits, idx, g, w1, w3, w2, cap, shared=None, dtype=F32):
+    """The layer forward with a per-expert capacity: as :func:`moe_forward`,
+    but expert e processes only its first ``cap`` tokens (ascending token
+    order) and a dropped copy contributes nothing to the combine (the token
+    keeps only its residual path, outside the layer).  The gate weights of the
+    kept copies are not renormalised.  Returns (out, saved) in the layout of
+    :func:`moe_forward`, so :func:`moe_backward` gives the gradients: dropped
+    copies get dg = 0 and still receive a router-logit gradient through the
+    renormalisation of the kept ones."""
+    n, d = x.shape
+    xx = x.astype(dtype)
+    out = np.zeros((n, d), dtype=dtype)
+    saved = {"experts": {}}
+    for e in range(w1.shape[0]):
+        tok, kk = np.nonzero(idx == e)
+        tok, kk = tok[:cap], kk[:cap]
+        if tok.size == 0:
+            continue
+        y, a1, a3, h = swiglu_expert(xx[tok], w1[e], w3[e], w2[e], dtype)
+        saved["experts"][e] = (tok, kk, y, a1, a3, h)
+        np.add.at(out, tok, y * g[tok, kk].astype(dtype)[:, None])
+    if shared is not None:
+        ys, a1s, a3s, hs = swiglu_expert(xx, shared[0], shared[1], shared[2], dtype)
+        saved["shared"] = (ys, a1s, a3s, hs)
+        out = out + ys
     return out, saved
 
 

@@ -536,3 +536,93 @@ def test_aux_loss_grad_matches_finite_differences(gate):
             fd[t, j] = (O.aux_loss(lp, idx, e, gate) - O.aux_loss(lm, idx, e, gate)) / (2 * h)
     assert np.allclose(grad, fd, rtol=1e-6, atol=1e-9)
     assert abs(grad.sum()) < 1e-9 if gate == "softmax" else True   # softmax: invariant to a per-token shift
+
+
+# ------------------------------------------------- capacity factor / drop ---
+def test_capacity_formula():
+    """capacity = cf * (tokens / experts * top_k), rounded up to whole copies."""
+    assert O.capacity(4096, 8, 2, 1.0) == 1024
+    assert O.capacity(4096, 256, 8, 1.25) == 160
+    assert O.capacity(100, 8, 2, 1.0) == 25
+    assert O.capacity(10, 3, 1, 1.0) == 4          # 3.33 -> 4
+
+
+def test_capacity_hand_example():
+    """Ten tokens, K = 1, E = 2: tokens 0-7 pick expert 0, tokens 8-9 expert 1.
+    cf = 1 -> capacity 5: expert 0 keeps tokens 0-4, drops 5-7."""
+    idx = np.array([[0]] * 8 + [[1]] * 2, dtype=np.int32)
+    cap = O.capacity(10, 2, 1, 1.0)
+    roc, cor, kept, off, dropped = O.permutation_capacity(idx, 2, cap)
+    assert cap == 5 and dropped == 3
+    assert roc.tolist() == [0, 1, 2, 3, 4, -1, -1, -1, 5, 6]
+    assert cor.tolist() == [0, 1, 2, 3, 4, 8, 9]
+    assert kept.tolist() == [5, 2] and off.tolist() == [0, 5, 7]
+
+
+def test_capacity_large_factor_is_dropless():
+    p = _layer(40, 16, 24, 4, 2, seed=41)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, None, 2, "softmax")
+    cap = int(O.histogram(idx, 4).max())
+    roc, cor, kept, off, dropped = O.permutation_capacity(idx, 4, cap)
+    roc0, cor0 = O.permutation(idx, 4)
+    assert dropped == 0 and np.array_equal(roc, roc0) and np.array_equal(cor, cor0)
+    assert np.array_equal(off, O.exclusive_offsets(O.histogram(idx, 4)))
+    out, _ = O.moe_forward_capacity(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], cap)
+    out0, _ = O.moe_forward(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"])
+    assert np.array_equal(out, out0)
+
+
+def test_capacity_forward_is_dropless_brute_force_without_dropped_copies():
+    """Dropping a copy = giving it gate weight 0 in the dense per-token brute
+    force (fp64)."""
+    p = _layer(30, 16, 24, 4, 2, seed=42)
+    lg = O.gate_logits(p["x"], p["w_gate"])
+    idx, g = O.route(lg, None, 2, "softmax")
+    cap = O.capacity(30, 4, 2, 0.8)
+    roc, _, _, _, dropped = O.permutation_capacity(idx, 4, cap)
+    assert dropped > 0
+    g0 = np.where(roc.reshape(idx.shape) < 0, 0.0, g)
+    ref = O.moe_forward_dense_bruteforce(p["x"], idx, g0, p["w1"], p["w3"], p["w2"])
+    out, _ = O.moe_forward_capacity(p["x"], lg, idx, g, p["w1"], p["w3"], p["w2"], cap, dtype=np.float64)
+    assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_capacity_backward_finite_differences():
+    """Gradients of the layer with drops (routing and the drop pattern held
+    fixed) against fp64 central differences: dropped copies have dg = 0 but
+    still move the kept copies' renormalised gate weights."""
+    n, d, f, e, k = 16, 8, 16, 4, 2
+    p = _layer(n, d, f, e, k, "softmax", seed=43, wscale=0.5)
+    for key in ("x", "w_gate", "w1", "w3", "w2"):
+        p[key] = p[key].astype(np.float64)
+    dy = _rng(44).standard_normal((n, d))
+    lg = O.gate_logits(p["x"], p["w_gate"], np.float64)
+    idx = O.topk_select(O.selection_keys(lg.astype(np.float32), None), k)
+    keys = np.sort(O.selection_keys(lg.astype(np.float32), None), axis=1)
+    assert (keys[:, -k] - keys[:, -k - 1]).min() > 1e-3
+    cap = O.capacity(n, e, k, 0.75)
+
+    def loss_of(pp):
+        l2 = O.gate_logits(pp["x"], pp["w_gate"], np.float64)
+        g2 = O.gate_weights(l2, idx, "softmax", np.float64)
+        o, sv = O.moe_forward_capacity(pp["x"], l2, idx, g2, pp["w1"], pp["w3"], pp["w2"], cap, dtype=np.float64)
+        return float((o * dy).sum()), l2, g2, sv
+
+    _, lg, g, saved = loss_of(p)
+    assert O.permutation_capacity(idx, e, cap)[4] > 0
+    gr = O.moe_backward(dy, p["x"], lg, idx, g, p["w_gate"], p["w1"], p["w3"], p["w2"], saved, "softmax",
+                        None, dtype=np.float64)
+    r = _rng(45)
+    for src, gname in (("x", "dx"), ("w_gate", "dw_gate"), ("w1", "dw1"), ("w2", "dw2")):
+        arr = p[src]
+        for _ in range(6):
+            pos = tuple(int(r.integers(s)) for s in arr.shape)
+            old = arr[pos]
+            arr[pos] = old + 1e-6
+            lp = loss_of(p)[0]
+            arr[pos] = old - 1e-6
+            lm = loss_of(p)[0]
+            arr[pos] = old
+            fd = (lp - lm) / 2e-6
+            assert abs(fd - gr[gname][pos]) <= 1e-6 * max(1.0, abs(fd)), (gname, pos)
