@@ -131,6 +131,11 @@ typedef struct {
   const void* a1s;             /* [N,Fs] */
   const void* a3s;             /* [N,Fs] */
   const void* hs;              /* [N,Fs] */
+  /* Capacity (drop) mode only, NULL otherwise: the dropless offsets [E+1]
+   * from moe_route and copy_of_row [R] from moe_permute_capacity.  The
+   * router weight gradient sums over every copy, dropped or kept. */
+  const int32_t* offsets_full;
+  const int32_t* copy_of_row_full;
 } moe_fwd_state_t;
 
 /* Gradients written by moe_backward (fp32 unless stated).  dg and dlogits
@@ -240,6 +245,28 @@ MOE_API moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const
  * the bias unchanged. */
 MOE_API moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
                              void* stream);
+
+/* Capacity-factor mode (§6.4 "Capacity Factor and Token Drop", §2.2 GShard):
+ * the comparison case of the dropless layer.  capacity = ceil(capacity_factor
+ * * (N / E * K)) copies per expert; each expert keeps its first copies in
+ * token order and drops the rest, which contribute nothing to the combine
+ * (the token keeps only its residual path, outside the layer); the kept gate
+ * weights are not renormalised.
+ * Inputs: x [N,D], topk_idx [N,K], offsets [E+1] (dropless, from moe_route).
+ * Outputs: row_of_copy_full [R], copy_of_row_full [R] (the dropless maps of
+ * moe_permute), kept_offsets [E+1], row_of_copy [R] (-1 for a dropped copy),
+ * copy_of_row (first kept_offsets[E] entries), x_perm [R,D] (first
+ * kept_offsets[E] rows), n_dropped [1] (device int32, nullable).  The expert
+ * GEMMs, combine and backward then run on kept_offsets / row_of_copy /
+ * copy_of_row / x_perm unchanged (moe_fwd_state_t.offsets_full and
+ * copy_of_row_full take the dropless maps).  bf16 only (d->precision 0).
+ * Needs the forward workspace. */
+MOE_API moe_status_t moe_permute_capacity(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
+                                          const int32_t* offsets, double capacity_factor,
+                                          int32_t* row_of_copy_full, int32_t* copy_of_row_full,
+                                          int32_t* kept_offsets, int32_t* row_of_copy, int32_t* copy_of_row,
+                                          void* x_perm, int32_t* n_dropped, void* ws, size_t ws_bytes,
+                                          void* stream);
 
 /* Auxiliary load-balancing loss (§6.2, GShard form) of the routing that
  * produced `logits` [N,E] (fp32, from moe_route) and `counts` [E]:

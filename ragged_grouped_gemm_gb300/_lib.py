@@ -33,7 +33,8 @@ class MoeFfnSaved(ctypes.Structure):
 class MoeFwdState(ctypes.Structure):
     _fields_ = [("x", c_vp), ("x_perm", c_vp), ("logits", c_vp), ("topk_idx", c_vp), ("topk_w", c_vp),
                 ("offsets", c_vp), ("row_of_copy", c_vp), ("copy_of_row", c_vp), ("a1", c_vp), ("a3", c_vp),
-                ("h", c_vp), ("y_perm", c_vp), ("a1s", c_vp), ("a3s", c_vp), ("hs", c_vp)]
+                ("h", c_vp), ("y_perm", c_vp), ("a1s", c_vp), ("a3s", c_vp), ("hs", c_vp),
+                ("offsets_full", c_vp), ("copy_of_row_full", c_vp)]
 
 
 class MoeGrads(ctypes.Structure):
@@ -75,6 +76,8 @@ SIGNATURES = {
     "moe_grouped_ffn_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(MoeExpertWeightsMx), ctypes.POINTER(MoeFfnSaved), c_vp, c_vp,
                                       c_vp, ctypes.c_size_t, c_vp]),
+    "moe_permute_capacity": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, ctypes.c_double, c_vp, c_vp, c_vp,
+                                     c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
     "moe_aux_loss": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp,
                              ctypes.c_size_t, c_vp]),
     "moe_monitor_stats": (c_i32, [c_i32, c_vp, c_i32, c_vp, c_vp]),

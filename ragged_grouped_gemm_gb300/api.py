@@ -158,7 +158,9 @@ def _bwd_structs(desc, state: dict, grads: dict, need_x_perm: bool = True):
         _p(S["copy_of_row"], I32, (r,), "copy_of_row"), _p(S["a1"], BF16, (r, f), "a1"), _p(S["a3"], BF16, (r, f), "a3"),
         _p(S["h"], BF16, (r, f), "h"), _p(S["y_perm"], BF16, (r, d), "y_perm"),
         _p(S.get("a1s"), BF16, (n, fs), "a1s") if sh else None, _p(S.get("a3s"), BF16, (n, fs), "a3s") if sh else None,
-        _p(S.get("hs"), BF16, (n, fs), "hs") if sh else None)
+        _p(S.get("hs"), BF16, (n, fs), "hs") if sh else None,
+        _p(S.get("offsets_full"), I32, (e + 1,), "offsets_full"),
+        _p(S.get("copy_of_row_full"), I32, (r,), "copy_of_row_full"))
     G = grads
     gr = _lib.MoeGrads(
         _p(G["dx"], BF16, (n, d), "dx"), _p(G["dw_gate"], F32, (e, d), "dw_gate"), _p(G["dw1"], F32, (e, f, d), "dw1"),
@@ -183,6 +185,19 @@ def moe_backward(desc, w_gate, weights: dict, state: dict, dy, grads: dict, ws, 
     _check("moe_backward", _lib.load().moe_backward(
         ctypes.byref(desc), _p(w_gate, BF16, (e, d), "w_gate"), ctypes.byref(w), ctypes.byref(st),
         _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_permute_capacity(desc, x, topk_idx, offsets, capacity_factor: float, row_of_copy_full, copy_of_row_full,
+                         kept_offsets, row_of_copy, copy_of_row, x_perm, n_dropped, ws, stream=None):
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_permute_capacity", _lib.load().moe_permute_capacity(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(offsets, I32, (e + 1,), "offsets"), ctypes.c_double(capacity_factor),
+        _p(row_of_copy_full, I32, (r,), "row_of_copy_full"), _p(copy_of_row_full, I32, (r,), "copy_of_row_full"),
+        _p(kept_offsets, I32, (e + 1,), "kept_offsets"), _p(row_of_copy, I32, (r,), "row_of_copy"),
+        _p(copy_of_row, I32, (r,), "copy_of_row"), _p(x_perm, BF16, (r, d), "x_perm"),
+        _p(n_dropped, I32, (1,), "n_dropped"), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
 def moe_aux_loss(desc, logits, counts, loss, dlogits_aux=None, ws=None, coef: float = 1.0, stream=None):
@@ -346,6 +361,13 @@ class MoELayer:
                             a3s=z(n, fs) if train else None)
         else:
             self.buf.update(hs=None, y_shared=None, a1s=None, a3s=None)
+        self.cap = cfg.capacity_factor > 0
+        if self.cap:
+            if cfg.precision != "bf16":
+                raise ValueError("the capacity-factor mode runs with bf16 operands")
+            # routing writes the dropless offsets here; b["offsets"] holds the kept ones
+            self.buf.update(offsets_full=z(e + 1, dt=I32), row_of_copy_full=z(r, dt=I32),
+                            copy_of_row_full=z(r, dt=I32), n_dropped=z(1, dt=I32))
         self.mx = cfg.precision == "mxfp8"
         if self.mx:
             self.wq = quantize_weights_mxfp8(params)
@@ -370,11 +392,24 @@ class MoELayer:
         b, p = self.buf, self.p
         self.x = x
         moe_route(self.desc, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
-                  b["offsets"], self.ws, stream)
+                  b["offsets_full"] if self.cap else b["offsets"], self.ws, stream)
         if self.mx:
             return self._forward_mx(x, stream)
-        moe_permute(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"],
-                    self.ws, stream)
+        self._permute(x, stream)
+        return self._ffn_combine(x, stream)
+
+    def _permute(self, x, stream=None):
+        b = self.buf
+        if self.cap:
+            moe_permute_capacity(self.desc, x, b["topk_idx"], b["offsets_full"], self.cfg.capacity_factor,
+                                 b["row_of_copy_full"], b["copy_of_row_full"], b["offsets"], b["row_of_copy"],
+                                 b["copy_of_row"], b["x_perm"], b["n_dropped"], self.ws, stream)
+        else:
+            moe_permute(self.desc, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"],
+                        self.ws, stream)
+
+    def _ffn_combine(self, x, stream=None):
+        b, p = self.buf, self.p
         moe_grouped_ffn(self.desc, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
                         p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
                         b["y_perm"], b["y_shared"], self.ws, stream)
@@ -403,8 +438,16 @@ class MoELayer:
         state = {key: b[key] for key in ("x_perm", "logits", "topk_idx", "topk_w", "offsets", "row_of_copy",
                                          "copy_of_row", "a1", "a3", "h", "y_perm", "a1s", "a3s", "hs")}
         state["x"] = self.x
+        if self.cap:
+            state.update(offsets_full=b["offsets_full"], copy_of_row_full=b["copy_of_row_full"])
         moe_backward(self.desc, self.p["w_gate"], self.p, state, dy, self.grads, self.ws, stream)
         return self.grads
+
+    def drop_rate(self) -> float:
+        """Fraction of token copies dropped by the capacity in the last forward (0 when dropless)."""
+        if not self.cap:
+            return 0.0
+        return int(self.buf["n_dropped"].item()) / self.cfg.rows
 
     def update_bias(self, gamma: float = 1e-3, mode: int = 0, stream=None):
         moe_update_bias(self.desc, self.buf["counts"], self.p["bias"], gamma, mode, stream)

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "balance.cuh"
@@ -459,8 +460,12 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
                          at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st));
   }
-  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, 0, at<float>(ws, L.dwg),
-                              g->dw_gate, st));
+  if (s->offsets_full && s->copy_of_row_full)   // capacity mode: every copy, x gathered in dropless order
+    MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets_full, s->copy_of_row_full, dl, s->x, K,
+                                at<float>(ws, L.dwg), g->dw_gate, st));
+  else
+    MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x_perm, 0, at<float>(ws, L.dwg),
+                                g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
 }
@@ -749,9 +754,40 @@ moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const m
                             wt->ws1_scale, wt->ws3, wt->ws3_scale, wt->ws2, wt->ws2_scale, at<void>(ws, L.da1s),
                             at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, qs, status, st));
   }
-  MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets, s->copy_of_row, dl, s->x, K, at<float>(ws, L.dwg), g->dw_gate,
-                              st));
+  const bool full = s->offsets_full && s->copy_of_row_full;
+  MOE_CUDA(moe::launch_dwgate(N, K, E, D, full ? s->offsets_full : s->offsets,
+                              full ? s->copy_of_row_full : s->copy_of_row, dl, s->x, K, at<float>(ws, L.dwg),
+                              g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_permute_capacity(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
+                                  const int32_t* offsets, double capacity_factor, int32_t* row_of_copy_full,
+                                  int32_t* copy_of_row_full, int32_t* kept_offsets, int32_t* row_of_copy,
+                                  int32_t* copy_of_row, void* x_perm, int32_t* n_dropped, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!all16({x, x_perm}) || !topk_idx || !offsets || !row_of_copy_full || !copy_of_row_full || !kept_offsets ||
+      !row_of_copy || !copy_of_row || !(capacity_factor >= 0.0))
+    return MOE_ERR_INVALID_ARG;
+  const double capd = std::ceil(capacity_factor * (static_cast<double>(d->n_tok) / d->n_exp * d->top_k) - 1e-9);
+  if (capd > 2147483647.0) return MOE_ERR_INVALID_ARG;
+  const int cap = capd > 0.0 ? static_cast<int>(capd) : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  if (d->n_tok == 0) {
+    MOE_CUDA(cudaMemsetAsync(kept_offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+    return n_dropped ? cuda_status(cudaMemsetAsync(n_dropped, 0, sizeof(int32_t), st)) : MOE_OK;
+  }
+  MOE_CUDA(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, at<int32_t>(ws, L.blk_counts),
+                                    at<int32_t>(ws, L.blk_base), row_of_copy_full, copy_of_row_full,
+                                    at<int32_t>(ws, L.status), st));
+  MOE_CUDA(moe::launch_capacity_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, row_of_copy_full, cap,
+                                     kept_offsets, row_of_copy, copy_of_row, n_dropped, st));
+  MOE_CUDA(moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st));
   return MOE_OK;
 }
 

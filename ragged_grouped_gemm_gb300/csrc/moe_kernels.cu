@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, in
     const uint4* src = x + static_cast<int64_t>(t) * d8;
     for (int i = threadIdx.x; i < d8; i += blockDim.x) {
       const uint4 v = src[i];
-      for (int k = 0; k < K; ++k) x_perm[static_cast<int64_t>(s_rows[k]) * d8 + i] = v;
+      for (int k = 0; k < K; ++k)
+        if (s_rows[k] >= 0) x_perm[static_cast<int64_t>(s_rows[k]) * d8 + i] = v;   // -1: dropped copy
     }
   }
 }
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, 
     for (int i = threadIdx.x; i < d8; i += blockDim.x) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int k = 0; k < K; ++k) {
+        if (s_rows[k] < 0) continue;   // dropped copy (capacity mode): no expert output
         float y[8];
         unpack8(y_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], y);
         const float w = s_w[k];
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
       unpack8(dy[static_cast<int64_t>(t) * d8 + i], g8);
 #pragma unroll
       for (int k = 0; k < kMaxK; ++k) {
-        if (k < K) {
+        if (k < K && s_rows[k] >= 0) {   // a dropped copy has no row and dg = 0
           const int64_t r = s_rows[k];
           float y[8], o[8];
           unpack8(y_perm[r * d8 + i], y);
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(256) unpermute_dx_kernel(int n_tok, int d8, in
     for (int i = threadIdx.x; i < d8; i += blockDim.x) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int k = 0; k < K; ++k) {
+        if (s_rows[k] < 0) continue;   // dropped copy: no expert gradient
         float v[8];
         unpack8(dx_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], v);
 #pragma unroll
@@ -551,6 +554,48 @@ __global__ void __launch_bounds__(256) unpermute_dx_kernel(int n_tok, int d8, in
       dx[static_cast<int64_t>(t) * d8 + i] = pack8(acc);
     }
   }
+}
+
+// ------------------------------------------------------------ capacity (drop) mode
+// Kept copies per expert min(count, cap), their exclusive scan, and the
+// number of dropped copies (single block, E <= 1024).
+__global__ void __launch_bounds__(1024) kept_offsets_kernel(const int32_t* __restrict__ offsets, int E, int cap,
+                                                            int total, int32_t* __restrict__ kept_offsets,
+                                                            int32_t* __restrict__ n_dropped) {
+  __shared__ int32_t s[1024];
+  const int e = threadIdx.x;
+  const int32_t v = e < E ? min(offsets[e + 1] - offsets[e], cap) : 0;
+  s[e] = v;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    const int32_t add = e >= d ? s[e - d] : 0;
+    __syncthreads();
+    s[e] += add;
+    __syncthreads();
+  }
+  if (e < E) kept_offsets[e + 1] = s[e];
+  if (e == 0) {
+    kept_offsets[0] = 0;
+    if (n_dropped) *n_dropped = total - s[1023];
+  }
+}
+
+// Copy c keeps its rank inside its expert (position in the dropless,
+// token-ordered permutation); ranks below the capacity get the compact row
+// kept_offsets[e] + rank, the others -1.
+__global__ void capacity_rows_kernel(int64_t R, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+                                     const int32_t* __restrict__ row_full, const int32_t* __restrict__ kept_offsets,
+                                     int cap, int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= R) return;
+  const int e = idx[c];
+  const int rank = row_full[c] - offsets[e];
+  int32_t r = -1;
+  if (rank < cap) {
+    r = kept_offsets[e] + rank;
+    copy_of_row[r] = static_cast<int32_t>(c);
+  }
+  row_of_copy[c] = r;
 }
 
 __global__ void dense_offsets_kernel(int32_t* dst, int n) {
@@ -672,6 +717,19 @@ cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm
   unpermute_dx_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
       n_tok, d / 8, top_k, static_cast<const uint4*>(dx_perm), row_of_copy, dl, topk_idx,
       static_cast<const uint4*>(w_gate), static_cast<const uint4*>(dx_shared), static_cast<uint4*>(dx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_capacity_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
+                                 const int32_t* row_full, int cap, int32_t* kept_offsets, int32_t* row_of_copy,
+                                 int32_t* copy_of_row, int32_t* n_dropped, cudaStream_t st) {
+  if (n_exp > 1024 || cap < 0) return cudaErrorInvalidValue;
+  const int64_t R = static_cast<int64_t>(n_tok) * top_k;
+  kept_offsets_kernel<<<1, 1024, 0, st>>>(offsets, n_exp, cap, static_cast<int>(R), kept_offsets, n_dropped);
+  if (R > 0)
+    capacity_rows_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(R, topk_idx, offsets, row_full,
+                                                                                   kept_offsets, cap, row_of_copy,
+                                                                                   copy_of_row);
   return cudaGetLastError();
 }
 

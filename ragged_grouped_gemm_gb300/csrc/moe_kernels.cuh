@@ -49,6 +49,13 @@ size_t dwgate_partial_floats(int n_tok, int top_k, int n_exp, int d);
 cudaError_t launch_dwgate(int n_tok, int top_k, int n_exp, int d, const int32_t* offsets, const int32_t* copy_of_row,
                           const float* dl, const void* x_rows, int gather_k, float* scratch, float* dw_gate,
                           cudaStream_t st);
+// Capacity (drop) mode: from the dropless permutation (offsets, row_full),
+// keep at most `cap` copies per expert (the first in token order) in a
+// compact expert-major layout: kept_offsets [E+1], row_of_copy [R] (-1 for a
+// dropped copy), copy_of_row for the kept rows, n_dropped (nullable).
+cudaError_t launch_capacity_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
+                                 const int32_t* row_full, int cap, int32_t* kept_offsets, int32_t* row_of_copy,
+                                 int32_t* copy_of_row, int32_t* n_dropped, cudaStream_t st);
 // dx[t] = sum_k dx_perm[row(t,k)] + sum_k dl[t,k] * W_g[idx[t,k]] (+ dx_shared[t]); bf16 out.
 cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm, const int32_t* row_of_copy,
                                 const float* dl, const int32_t* topk_idx, const void* w_gate,

@@ -47,6 +47,7 @@ class MoEConfig:
     precision: str = "bf16"        # "bf16" | "mxfp8"
     bias_beta: float = 0.0         # Zipf strength of the route bias
     n_cold: int = 0                # experts whose bias keeps them empty
+    capacity_factor: float = 0.0   # > 0: capacity-factor drop mode (comparison case); 0: dropless
 
     @property
     def rows(self) -> int:
