@@ -330,8 +330,9 @@ def run_sweep(args):
     p = make_layer(base, dev)
     dy = make_dy(base, dev)
     results = []
-    for prec in ("bf16", "mxfp8"):
-        cfg = base.replace(precision=prec)
+    # dropless bf16 and MXFP8, then the capacity-factor (drop) comparison in bf16
+    for prec, cap_f in (("bf16", 0.0), ("mxfp8", 0.0), ("bf16", 1.0), ("bf16", 1.25)):
+        cfg = base.replace(precision=prec, capacity_factor=cap_f)
         layer = api.MoELayer(cfg, p, train=True, device=dev)
         b, d, ws = layer.buf, layer.desc, layer.ws
         for skew in ("bias", "uniform", "zipf", "half0"):
@@ -341,18 +342,14 @@ def run_sweep(args):
             def fwd():
                 if lg is None:
                     return layer.forward(p["x"])
-                api.moe_route_from_logits(d, lg, zero_bias, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], ws)
+                api.moe_route_from_logits(d, lg, zero_bias, b["topk_idx"], b["topk_w"], b["counts"],
+                                          b["offsets_full"] if layer.cap else b["offsets"], ws)
                 b["logits"].copy_(lg)        # the router gradient reads the logits the routing used
                 layer.x = p["x"]
                 if layer.mx:
                     return layer._forward_mx(p["x"])
-                api.moe_permute(d, p["x"], b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
-                                b["x_perm"], ws)
-                api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], p["x"], p["w1"], p["w3"], p["w2"], p.get("ws1"),
-                                    p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
-                                    b["y_perm"], b["y_shared"], ws)
-                api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
-                return b["out"]
+                layer._permute(p["x"])
+                return layer._ffn_combine(p["x"])
 
             def fwd_bwd():
                 fwd()
@@ -375,7 +372,8 @@ def run_sweep(args):
             ne = int((counts > 0).sum())
             wb = 3 * ne * cfg.d_ff * cfg.d_model + (3 * cfg.d_ff_shared * cfg.d_model if cfg.n_shared else 0)
             wbytes = wb * (1 + 1 / 32) if prec == "mxfp8" else 2 * wb
-            results.append({"precision": prec, "skew": skew, "ms_fwd": ms, "tokens_per_s": cfg.n_tok / ms * 1e3,
+            results.append({"precision": prec, "capacity_factor": cap_f, "drop_rate": layer.drop_rate(),
+                            "skew": skew, "ms_fwd": ms, "tokens_per_s": cfg.n_tok / ms * 1e3,
                             "experts_nonempty": ne, "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
                             "weight_bytes": wbytes, "weight_stream_gbs": wbytes / ms / 1e6,
                             "weight_stream_frac_of_hbm": wbytes / ms / 1e6 / peaks["hbm_gbs"],
