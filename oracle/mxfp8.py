@@ -23,10 +23,12 @@ import numpy as np
 
 __all__ = ["e4m3_decode", "e4m3_encode", "e8m0_scale_exponent", "mx_quantize",
            "mx_dequantize", "mx_fake_quant", "swiglu_expert_mxfp8", "moe_forward_mxfp8",
-           "moe_backward_mxfp8", "bf16_round", "E4M3_MAX", "MX_BLOCK"]
+           "moe_backward_mxfp8", "bf16_round", "fp8_tile_quantize", "fp8_tile_dequantize",
+           "FP8_TILE", "E4M3_MAX", "MX_BLOCK"]
 
 E4M3_MAX = 448.0
 MX_BLOCK = 32
+FP8_TILE = 128
 _E4M3_BIAS = 7
 _E4M3_EMAX = 8
 
@@ -284,3 +286,39 @@ def moe_backward_mxfp8(dy, x, logits, idx, g, w_gate, w1, w3, w2, saved, gate, s
     dx = dx + np.matmul(dl, w_gate.astype(f32))
     res.update(dx=dx, dw1=dw1, dw3=dw3, dw2=dw2, dw_gate=dw_gate, dg=dg, dlogits=dl)
     return res
+
+
+# ----------------------------------------------------------------------------
+# FP8 weights with per-tile scales ("LLM Infrastructure Engineering 08: MoE
+# Training Engineering" §13.6: forward act(BF16) x weight(FP8) -> BF16,
+# backward grad(BF16) x weight_T(FP8), per-tile scaling, FP32 accumulation)
+# ----------------------------------------------------------------------------
+def fp8_tile_quantize(w: np.ndarray, tile: int = FP8_TILE):
+    """Quantise weight matrices [..., rows, cols] to E4M3 with one fp32 scale
+    per ``tile x tile`` block (reading of "per-tile scaling": 128 x 128 blocks
+    of the weight, a plain fp32 scale ``amax / 448`` so that the block
+    maximum maps to the largest E4M3 value; an all-zero block gets scale 1).
+    Returns (codes uint8 [..., rows, cols], scales fp32 [..., ceil(rows/t),
+    ceil(cols/t)])."""
+    w = np.asarray(w, dtype=np.float32)
+    rows, cols = w.shape[-2:]
+    nr, nc = -(-rows // tile), -(-cols // tile)
+    scales = np.ones(w.shape[:-2] + (nr, nc), dtype=np.float32)
+    codes = np.zeros(w.shape, dtype=np.uint8)
+    for i in range(nr):
+        for j in range(nc):
+            blk = w[..., i * tile:(i + 1) * tile, j * tile:(j + 1) * tile]
+            amax = np.abs(blk).max(axis=(-2, -1))
+            sc = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0))
+            scales[..., i, j] = sc
+            codes[..., i * tile:(i + 1) * tile, j * tile:(j + 1) * tile] = e4m3_encode(
+                blk.astype(np.float64) / sc.astype(np.float64)[..., None, None])
+    return codes, scales
+
+
+def fp8_tile_dequantize(codes: np.ndarray, scales: np.ndarray, tile: int = FP8_TILE) -> np.ndarray:
+    """The bf16 operand the tensor cores take: decoded E4M3 value times its
+    tile's fp32 scale (an fp32 product), rounded to bf16."""
+    rows, cols = codes.shape[-2:]
+    sc = np.repeat(np.repeat(scales, tile, axis=-2), tile, axis=-1)[..., :rows, :cols]
+    return bf16_round((e4m3_decode(codes).astype(np.float32) * sc).astype(np.float32))

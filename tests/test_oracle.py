@@ -626,3 +626,51 @@ def test_capacity_backward_finite_differences():
             arr[pos] = old
             fd = (lp - lm) / 2e-6
             assert abs(fd - gr[gname][pos]) <= 1e-6 * max(1.0, abs(fd)), (gname, pos)
+
+
+# ------------------------------------------------- FP8 weights, per tile ---
+def test_fp8_tile_quantize_scale_and_layout():
+    """Per 128 x 128 block: scale = amax / 448, the block maximum encodes to
+    +-448, every code is the nearest E4M3 value of w / scale, partial edge
+    blocks have their own scale, and a zero block has scale 1."""
+    r = _rng(50)
+    w = (r.standard_normal((2, 200, 300)) * np.exp2(r.integers(-8, 8, (2, 1, 1)))).astype(np.float32)
+    w[1, :128, :128] = 0.0
+    codes, scales = O.fp8_tile_quantize(w)
+    assert scales.shape == (2, 2, 3) and scales[1, 0, 0] == 1.0
+    for e in range(2):
+        for i in range(2):
+            for j in range(3):
+                blk = w[e, 128 * i:128 * (i + 1), 128 * j:128 * (j + 1)]
+                cb = codes[e, 128 * i:128 * (i + 1), 128 * j:128 * (j + 1)]
+                if not blk.any():
+                    assert not cb.any()
+                    continue
+                sc = np.float32(np.abs(blk).max() / np.float32(448.0))
+                assert scales[e, i, j] == sc
+                assert np.abs(O.e4m3_decode(cb)).max() == 448.0
+                # nearest representable: brute force over the 126 positive values
+                grid = np.unique(np.abs(O.e4m3_decode(np.arange(127))))
+                v = np.abs(blk.astype(np.float64) / np.float64(sc)).reshape(-1)[:300]
+                dist = np.abs(grid[None, :] - v[:, None])
+                best = dist.min(axis=1)
+                got = np.abs(O.e4m3_decode(cb.reshape(-1)[:300]))
+                assert np.allclose(np.abs(got - v), best, rtol=0, atol=1e-12)
+
+
+def test_fp8_tile_dequantize_round_trip_on_representable_weights():
+    """Weights built as E4M3 value x a power-of-two tile scale (bf16 exact)
+    come back exactly; a generic weight comes back within E4M3's relative
+    step (2^-4 of each element, up to saturation at the block maximum)."""
+    r = _rng(51)
+    codes = r.integers(0, 127, (130, 260)).astype(np.uint8)
+    codes[0, 0] = 0x7E                                   # 448 in every block? one block at least
+    vals = O.e4m3_decode(codes) * np.where(r.random((130, 260)) < 0.5, -1, 1)
+    w = (vals * 2.0 ** -6).astype(np.float32)            # tile amax -> 448 * 2^-6 only where present
+    c2, s2 = O.fp8_tile_quantize(w)
+    back = O.fp8_tile_dequantize(c2, s2)
+    assert np.allclose(back, O.bf16_round(w), rtol=2 ** -3, atol=0)
+    g = r.standard_normal((256, 384)).astype(np.float32)
+    c3, s3 = O.fp8_tile_quantize(g)
+    b3 = O.fp8_tile_dequantize(c3, s3)
+    assert (np.abs(b3 - g) <= np.abs(g) * 2.0 ** -4 + np.repeat(np.repeat(s3, 128, 0), 128, 1) * 2.0 ** -9 + 1e-12).all()
