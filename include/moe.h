@@ -86,7 +86,7 @@ typedef struct {
   int32_t use_bias;    /* 1: select on logits + route_bias (§6.3) */
   int32_t n_shared;    /* 0 or 1 shared expert (§5) */
   int32_t d_ff_shared; /* Fs */
-  int32_t precision;   /* 0: bf16 operands; 1: MXFP8 expert GEMM operands (forward); fp32 accumulation */
+  int32_t precision;   /* 0: bf16; 1: MXFP8 expert GEMM operands; 2: FP8 weights (bf16 activations); fp32 accumulation */
 } moe_desc_t;
 
 /* Expert weights (all bf16, nn.Linear layout, see above).  ws1/ws3/ws2 are
@@ -389,6 +389,41 @@ MOE_API moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_p
 MOE_API moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wt,
                                         const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
                                         size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------- FP8 weights --
+ * The FP8 training recipe of "LLM Infrastructure Engineering 08: MoE
+ * Training Engineering" §13.6: forward act(BF16) x weight(FP8) -> BF16,
+ * backward grad(BF16) x weight_T(FP8) -> BF16, per-tile scaling, FP32
+ * accumulation.  Weights are E4M3 codes with one fp32 scale per 128 x 128
+ * tile (scale = tile amax / 448, reading of "per-tile"); one tile grid serves
+ * both the forward and the transposed (data-gradient) use.  The GEMMs
+ * dequantise each weight tile to bf16 in shared memory (code x scale, the
+ * fp32 product rounded to bf16) and run bf16 tensor-core MMAs; activations
+ * stay bf16 and the weight gradients are bf16 GEMMs with fp32 output, as in
+ * moe_backward.  d->precision must be 2. */
+
+/* Quantise bf16 weights src [groups, rows, cols] per 128 x 128 tile: codes
+ * [groups, rows, cols] (uint8 E4M3, w / scale rounded to nearest even,
+ * saturating at 448) and scales [groups, ceil(rows/128), ceil(cols/128)]
+ * (fp32).  cols must be a multiple of 16.  Once per optimiser step. */
+MOE_API moe_status_t moe_quantize_fp8_tile(const void* src, int64_t groups, int64_t rows, int64_t cols,
+                                           void* codes, float* scales, void* stream);
+
+/* moe_grouped_ffn with FP8 weights: the moe_expert_weights_mx_t fields hold
+ * the codes (w1, w3 [E,F,D]; w2 [E,D,F]; ws1, ws3 [Fs,D]; ws2 [D,Fs]) and, in
+ * the *_scale fields, the fp32 tile scales from moe_quantize_fp8_tile.  Other
+ * arguments, outputs and saved activations as moe_grouped_ffn. */
+MOE_API moe_status_t moe_grouped_ffn_fp8w(const moe_desc_t* d, const void* x_perm, const int32_t* offsets,
+                                          const void* x, const moe_expert_weights_mx_t* wq,
+                                          const moe_ffn_saved_t* saved, void* y_perm, void* y_shared, void* ws,
+                                          size_t ws_bytes, void* stream);
+
+/* moe_backward of the FP8-weight layer: the data gradients through w2 and
+ * w1|w3 read the same codes and tile scales as moe_grouped_ffn_fp8w; the
+ * rest as moe_backward. */
+MOE_API moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wq,
+                                       const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                                       size_t ws_bytes, void* stream);
 
 /* moe_permute without a workspace (no counterpart in the pages; an addition
  * of this library for callers that cannot allocate).  Same inputs, outputs

@@ -76,6 +76,12 @@ SIGNATURES = {
     "moe_grouped_ffn_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(MoeExpertWeightsMx), ctypes.POINTER(MoeFfnSaved), c_vp, c_vp,
                                       c_vp, ctypes.c_size_t, c_vp]),
+    "moe_quantize_fp8_tile": (c_i32, [c_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, c_vp, c_vp, c_vp]),
+    "moe_grouped_ffn_fp8w": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, ctypes.POINTER(MoeExpertWeightsMx),
+                                     ctypes.POINTER(MoeFfnSaved), c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
+    "moe_backward_fp8w": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, ctypes.POINTER(MoeExpertWeightsMx),
+                                  ctypes.POINTER(MoeFwdState), c_vp, ctypes.POINTER(MoeGrads), c_vp,
+                                  ctypes.c_size_t, c_vp]),
     "moe_permute_capacity": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, ctypes.c_double, c_vp, c_vp, c_vp,
                                      c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
     "moe_aux_loss": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp,

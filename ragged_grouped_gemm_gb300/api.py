@@ -56,7 +56,7 @@ def make_desc(cfg: MoEConfig) -> _lib.MoeDesc:
     return _lib.MoeDesc(cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k,
                         1 if cfg.gate == "sigmoid" else 0, 1 if cfg.use_bias else 0,
                         cfg.n_shared, cfg.d_ff_shared if cfg.n_shared else 0,
-                        0 if cfg.precision == "bf16" else 1)
+                        {"bf16": 0, "mxfp8": 1, "fp8w": 2}[cfg.precision])
 
 
 # --------------------------------------------------------------- entry points
@@ -303,6 +303,56 @@ def moe_backward_mxfp8(desc, w_gate, wt: dict, state: dict, dy, grads: dict, ws,
         _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
+# --------------------------------------------------------------- FP8 weights
+def quantize_weights_fp8_tile(p: dict, stream=None) -> dict:
+    """E4M3 codes with one fp32 scale per 128 x 128 tile of every expert
+    weight in ``p`` (keys w1, w3, w2, ws1, ws3, ws2 and *_scale)."""
+    out = {}
+    for key in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+        w = p.get(key)
+        if w is None:
+            continue
+        g, rows, cols = (1,) + tuple(w.shape) if w.dim() == 2 else tuple(w.shape)
+        codes = torch.empty(w.shape, dtype=U8, device=w.device)
+        lead = (w.shape[0],) if w.dim() == 3 else ()
+        scales = torch.empty(lead + ((rows + 127) // 128, (cols + 127) // 128), dtype=F32, device=w.device)
+        _check("moe_quantize_fp8_tile", _lib.load().moe_quantize_fp8_tile(
+            _p(w, BF16, name=key), g, rows, cols, _p(codes, U8, name=key + " codes"),
+            _p(scales, F32, name=key + " scales"), _s(stream)))
+        out[key], out[key + "_scale"] = codes, scales
+    return out
+
+
+def _mx_struct(desc, wq):
+    sh = desc.n_shared
+    return _lib.MoeExpertWeightsMx(*[_p(wq.get(key)) if (sh or not key.startswith("ws")) else None
+                                     for key in ("w1", "w1_scale", "w3", "w3_scale", "w2", "w2_scale",
+                                                 "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")])
+
+
+def moe_grouped_ffn_fp8w(desc, x_perm, offsets, x, wq: dict, saved: dict, y_perm, y_shared, ws, stream=None):
+    """``wq``: output of :func:`quantize_weights_fp8_tile`; other arguments as
+    :func:`moe_grouped_ffn` (``saved``: a1, a3, h, a1s, a3s, hs)."""
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r, sh = n * k, desc.n_shared
+    w = _mx_struct(desc, wq)
+    sv = _lib.MoeFfnSaved(*[_p(saved.get(key)) for key in ("a1", "a3", "h", "a1s", "a3s", "hs")])
+    _check("moe_grouped_ffn_fp8w", _lib.load().moe_grouped_ffn_fp8w(
+        ctypes.byref(desc), _p(x_perm, BF16, (r, d), "x_perm"), _p(offsets, I32, (e + 1,), "offsets"),
+        _p(x, BF16, (n, d), "x"), ctypes.byref(w), ctypes.byref(sv), _p(y_perm, BF16, (r, d), "y_perm"),
+        _p(y_shared, BF16, (n, d), "y_shared") if sh else None, _p(ws, name="ws"), ws.numel() * ws.element_size(),
+        _s(stream)))
+
+
+def moe_backward_fp8w(desc, w_gate, wq: dict, state: dict, dy, grads: dict, ws, stream=None):
+    n, d, e = desc.n_tok, desc.d_model, desc.n_exp
+    w = _mx_struct(desc, wq)
+    st, gr = _bwd_structs(desc, state, grads)
+    _check("moe_backward_fp8w", _lib.load().moe_backward_fp8w(
+        ctypes.byref(desc), _p(w_gate, BF16, (e, d), "w_gate"), ctypes.byref(w), ctypes.byref(st),
+        _p(dy, BF16, (n, d), "dy"), ctypes.byref(gr), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
 def moe_permute_mxfp8(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, xq_perm, xs_perm, xq_tok, xs_tok, ws,
                       stream=None):
     n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
@@ -361,9 +411,11 @@ class MoELayer:
                             a3s=z(n, fs) if train else None)
         else:
             self.buf.update(hs=None, y_shared=None, a1s=None, a3s=None)
+        self.w8 = cfg.precision == "fp8w"
+        self.w8q = quantize_weights_fp8_tile(params) if self.w8 else None
         self.cap = cfg.capacity_factor > 0
         if self.cap:
-            if cfg.precision != "bf16":
+            if cfg.precision == "mxfp8":
                 raise ValueError("the capacity-factor mode runs with bf16 operands")
             # routing writes the dropless offsets here; b["offsets"] holds the kept ones
             self.buf.update(offsets_full=z(e + 1, dt=I32), row_of_copy_full=z(r, dt=I32),
@@ -410,9 +462,14 @@ class MoELayer:
 
     def _ffn_combine(self, x, stream=None):
         b, p = self.buf, self.p
-        moe_grouped_ffn(self.desc, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
-                        p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
-                        b["y_perm"], b["y_shared"], self.ws, stream)
+        if self.w8:
+            saved = {key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
+            moe_grouped_ffn_fp8w(self.desc, b["x_perm"], b["offsets"], x, self.w8q, saved, b["y_perm"],
+                                 b["y_shared"], self.ws, stream)
+        else:
+            moe_grouped_ffn(self.desc, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
+                            p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
+                            b["y_perm"], b["y_shared"], self.ws, stream)
         moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
         return b["out"]
 
@@ -440,7 +497,10 @@ class MoELayer:
         state["x"] = self.x
         if self.cap:
             state.update(offsets_full=b["offsets_full"], copy_of_row_full=b["copy_of_row_full"])
-        moe_backward(self.desc, self.p["w_gate"], self.p, state, dy, self.grads, self.ws, stream)
+        if self.w8:
+            moe_backward_fp8w(self.desc, self.p["w_gate"], self.w8q, state, dy, self.grads, self.ws, stream)
+        else:
+            moe_backward(self.desc, self.p["w_gate"], self.p, state, dy, self.grads, self.ws, stream)
         return self.grads
 
     def drop_rate(self) -> float:

@@ -52,6 +52,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 320;        // producer, MMA, 8 epilogue warps
 constexpr int kThreadsQ = 448;       // + 4 scale-factor warps (MXFP8 operands)
+constexpr int kThreadsW8 = 576;      // + 8 converter warps (FP8 weights)
+constexpr int kConvWarps = 8;
 constexpr int kEpiThreads = 256;
 constexpr int kSfWarps = 4;
 
@@ -85,10 +87,20 @@ struct KParams {
   int64_t ld_out;
   int64_t group_stride_out;
   int32_t* status;
+  // FP8 weights: fp32 scale per 128 x 128 tile of each weight matrix
+  // [rows][cols] (K-major B: rows = n; MN-major B: rows = k), per source or
+  // per dual-N half, [groups][ceil(rows/128)][ceil(cols/128)]
+  const float* wscale[2];
+  int32_t ws_cols;       // column tiles per matrix
+  int64_t ws_gstride;    // tiles per matrix
 };
 
-template <int BN, bool QUANT = false, bool PAIR = false>
+template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false>
 struct Cfg {
+  // FP8 weights (W8): the B codes of a k-block (BN x 64 bytes) land in a
+  // two-slot staging ring; converters write the bf16 B tile into the stage
+  static constexpr int kW8Slots = W8 ? 2 : 0;
+  static constexpr int kW8SlotBytes = BN * 64;
   // MXFP8 (QUANT) stage, one k-block of 128 E4M3 elements = 4 scale blocks:
   //   A codes [128][128] | B codes [BN][128] (both 128-byte swizzled) |
   //   A scale rows [4][144] (from a 16-aligned row) | B scale rows [4][BN] |
@@ -102,17 +114,18 @@ struct Cfg {
   // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
   static constexpr int kStageBytes =
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
-  static constexpr int kStagesRaw = (QUANT ? 206 * 1024 : 200 * 1024) / kStageBytes;
+  static constexpr int kStagesRaw = ((QUANT ? 206 * 1024 : 200 * 1024) - kW8Slots * kW8SlotBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
   static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
   static constexpr uint32_t kSfCol = 2 * BN;
   // stages | epilogue staging (8 warps x 32x16 fp32) |
   // barriers (2S, + S scale-ready for MXFP8, + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
-  static constexpr int kEpiOff = kStages * kStageBytes;
+  static constexpr int kW8Off = kStages * kStageBytes;
+  static constexpr int kEpiOff = kW8Off + kW8Slots * kW8SlotBytes;
   static constexpr int kEpiBytes = 4 * 4096;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
-  static constexpr int kMiscOff = kBarOff + ((QUANT ? 3 : 2) * kStages + 5) * 8;
+  static constexpr int kMiscOff = kBarOff + ((QUANT ? 3 : 2) * kStages + 2 * kW8Slots + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr size_t smem_bytes(int groups) {
     return 1024 + kOffOff + 2 * 4 * (groups + 1);
@@ -178,6 +191,25 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float sigmoidf_fast(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
+// 16 E4M3 codes (little-endian in a uint4) times an fp32 tile scale ->
+// 8 bf16x2 words: each decoded value (exact in fp32) times the scale, the
+// fp32 product rounded to bf16 (round to nearest even).
+__device__ __forceinline__ void dequant16_scaled(const uint4 c, float sc, uint32_t (&w)[8]) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[i] >> (16 * hh)), __NV_E4M3);
+      __half2 h2;
+      *reinterpret_cast<__half2_raw*>(&h2) = hr;
+      const float2 f = __half22float2(h2);
+      w[2 * i + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+  }
+}
+
 __device__ __forceinline__ int mx_exponent_of(float amax) {
   if (!(amax > 0.0f)) return -127;
   const uint32_t b = __float_as_uint(amax);
@@ -210,9 +242,10 @@ __device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int
   return nkk;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR>
-__global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<BN, QUANT, PAIR>;
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false>
+__global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
+    grouped_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<BN, QUANT, PAIR, W8>;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
@@ -222,7 +255,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + S;
   uint64_t* sready = empty + S;           // MXFP8: scale atoms of the stage built
-  uint64_t* tfull = sready + (QUANT ? S : 0);
+  uint64_t* wfull = sready + (QUANT ? S : 0);   // FP8 weights: code slot loaded
+  uint64_t* wempty = wfull + C::kW8Slots;       // FP8 weights: code slot consumed
+  uint64_t* tfull = wempty + C::kW8Slots;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -243,10 +278,15 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
     for (int s = 0; s < S; ++s) {
       // TMA (tx bytes), the converter threads, or (ragged-K pair, rank 0) this
       // CTA's TMA plus the peer's forwarded arrival
-      mbar_init(&full[s], (PAIR && RAGGED_K && leader) ? 2 : 1);
+      // (FP8 weights: A's TMA bytes plus one arrival per converter warp)
+      mbar_init(&full[s], W8 ? 1 + kConvWarps : ((PAIR && RAGGED_K && leader) ? 2 : 1));
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], kSfWarps);
+    for (int s = 0; s < C::kW8Slots; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], kConvWarps);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], (PAIR ? 2 : 1) * (kEpiThreads / 32));   // one arrival per epilogue warp
@@ -371,6 +411,36 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* sA = smem + s * C::kStageBytes;
           uint8_t* sB = sA + kABytes;
+          if (W8) {
+            // FP8 weights: A (bf16) straight into the stage; the B codes of the
+            // k-block into a staging slot for the converters
+            const int src = (kb < p.kb0) ? 0 : 1;
+            const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
+            mbar_arrive_expect_tx(&full[s], kABytes);
+            tma_load_2d(sA, &p.tmA[src], &full[s], k0, t.row0);
+            const uint32_t wit = it;   // one code slot use per k-block
+            const int ws_ = wit % C::kW8Slots;
+            if (!mbar_wait_bounded(&wempty[ws_], ((wit / C::kW8Slots) & 1u) ^ 1u, s_abort, p.status, 130 + ws_)) {
+              ok = false;
+              break;
+            }
+            uint8_t* q = smem + C::kW8Off + ws_ * C::kW8SlotBytes;
+            mbar_arrive_expect_tx(&wfull[ws_], C::kW8SlotBytes);
+            if (!B_MN) {
+              if (p.b_dual_n) {
+                const int f0 = t.nt * (BN / 2);
+                tma_load_3d(q, &p.tmB[0], &wfull[ws_], k0, f0, t.g);
+                tma_load_3d(q + (BN / 2) * 64, &p.tmB[1], &wfull[ws_], k0, f0, t.g);
+              } else {
+                tma_load_3d(q, &p.tmB[src], &wfull[ws_], k0, t.nt * BN, t.g);
+              }
+            } else {
+#pragma unroll
+              for (int a = 0; a < BN / 64; ++a)
+                tma_load_3d(q + a * 4096, &p.tmB[src], &wfull[ws_], t.nt * BN + 64 * a, k0, t.g);
+            }
+            continue;
+          }
           if (PAIR && RAGGED_K) {
             // A k-block whose group rows end off a 16-row boundary is loaded
             // into each CTA's own barrier and zeroed past the group's end
@@ -460,6 +530,12 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
       }
       for (int s = 0; s < S && PAIR && RAGGED_K && !leader; ++s)
         if ((lused >> s) & 1u) mbar_wait_drain(&full[s], ((lph >> s) & 1u) ^ 1u);
+      for (int s = 0; s < C::kW8Slots; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t last = s + C::kW8Slots * ((it - 1 - s) / C::kW8Slots);
+          mbar_wait_drain(&wfull[s], (last / C::kW8Slots) & 1u);
+        }
+      }
     }
   } else if (PAIR && warp == 1 && !leader) {
     // The leader CTA issues the pair's MMAs.  Ragged K: for each k-block
@@ -631,6 +707,73 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1) grouped_gemm_
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sready[s]);
+        }
+      }
+    }
+    if (W8) {
+      // ---------------------------------------------------------- converters (FP8 weights)
+      // Each k-block: wait for its code slot and for the stage to be free,
+      // write the bf16 B tile (dequantised value = E4M3 code x its 128 x 128
+      // tile scale, rounded to bf16) in the 128-byte-swizzled layout of the
+      // MMA, release the slot and arrive on the stage.
+      const int ct = threadIdx.x - 10 * 32;   // 0..255
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          const int ws_ = it % C::kW8Slots;
+          if (!mbar_wait_bounded(&wfull[ws_], (it / C::kW8Slots) & 1u, s_abort, p.status, 540 + ws_)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 560 + s)) { ok = false; break; }
+          const int src = (kb < p.kb0) ? 0 : 1;
+          const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
+          const uint8_t* q = smem + C::kW8Off + ws_ * C::kW8SlotBytes;
+          uint8_t* sB = smem + s * C::kStageBytes + kABytes;
+          const int64_t gbase = static_cast<int64_t>(t.g) * p.ws_gstride;
+          // rows / columns past the weight matrix hold zero codes (TMA fill):
+          // clamp their tile index into this matrix's tile grid
+          const int rtiles = static_cast<int>(p.ws_gstride / p.ws_cols);
+          // BN rows (K-major) or 4 MN atoms x 64 k-rows (MN-major), 4 chunks of 16 codes each
+          for (int task = ct; task < BN * 4; task += kConvWarps * 32) {
+            const int j = task & 3;
+            const int row = task >> 2;   // K-major: tile row n; MN-major: atom * 64 + k
+            uint4 codes;
+            float sc;
+            uint8_t* rowp;
+            int sw;
+            if (!B_MN) {
+              codes = *reinterpret_cast<const uint4*>(q + row * 64 + j * 16);
+              const int half = p.b_dual_n ? row / (BN / 2) : 0;
+              const int wrow = p.b_dual_n ? t.nt * (BN / 2) + (row - half * (BN / 2)) : t.nt * BN + row;
+              const float* ss = p.wscale[p.b_dual_n ? half : src];
+              sc = ss[gbase + static_cast<int64_t>(min(wrow / 128, rtiles - 1)) * p.ws_cols + min(k0 / 128, p.ws_cols - 1)];
+              rowp = sB + row * 128;
+              sw = row & 7;
+            } else {
+              const int a = row >> 6, k = row & 63;
+              codes = *reinterpret_cast<const uint4*>(q + a * 4096 + k * 64 + j * 16);
+              const int ncol = t.nt * BN + a * 64 + j * 16;
+              sc = p.wscale[src][gbase + static_cast<int64_t>(min((k0 + k) / 128, rtiles - 1)) * p.ws_cols +
+                                 min(ncol / 128, p.ws_cols - 1)];
+              rowp = sB + a * 8192 + k * 128;
+              sw = k & 7;
+            }
+            uint32_t w[8];
+            dequant16_scaled(codes, sc, w);
+            *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&wempty[ws_]);
+            mbar_arrive(&full[s]);
+          }
         }
       }
     }
@@ -997,11 +1140,11 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
-  using C = Cfg<BN, QUANT, PAIR>;
+  using C = Cfg<BN, QUANT, PAIR, W8>;
   const size_t smem = C::smem_bytes(kp.num_groups);
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_units = 0;   // co-resident CTAs (or CTA pairs)
@@ -1029,7 +1172,7 @@ cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream
   if (attr_err != cudaSuccess) return attr_err;
   const int units = static_cast<int>(units_ub < max_units ? units_ub : max_units);
   if (!PAIR) {
-    kern<<<units, QUANT ? kThreadsQ : kThreads, smem, stream>>>(kp);
+    kern<<<units, QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), smem, stream>>>(kp);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg{};
@@ -1184,6 +1327,48 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     kp.c_rows = a.m_size;
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + QBN - 1) / QBN);
     return launch_impl<QBN, true, true, EPI_F32, true>(kp, tiles_ub, stream);
+  }
+  if (a.w8) {
+    // FP8 weights: bf16 A (K-major), E4M3 B codes dequantised by converter
+    // warps; ragged M, one-SM tiles 128 x 256
+    if (a.ragged_k || a.a_mn || BN != 256 || a.max_rows <= 0) return a.max_rows <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    if (a.epi != EPI_SWIGLU_FWD && a.epi != EPI_BF16 && a.epi != EPI_SWIGLU_BWD) return cudaErrorInvalidValue;
+    kp.kblk = BK;
+    kp.kb0 = (a.k0 + BK - 1) / BK;
+    kp.kb1 = (a.k1 + BK - 1) / BK;
+    if (kp.kb0 <= 0) return cudaErrorInvalidValue;
+    const int nsrc = kp.kb1 > 0 ? 2 : 1;
+    if (a.b_dual_n && (a.b_mn || nsrc != 1)) return cudaErrorInvalidValue;
+    for (int s2 = 0; s2 < nsrc; ++s2)
+      if (!make_map(&kp.tmA[s2], a.a[s2], 64, BM, false)) return cudaErrorInvalidValue;
+    if (nsrc == 1) kp.tmA[1] = kp.tmA[0];
+    const int nb = a.b_dual_n ? 2 : nsrc;
+    for (int i = 0; i < nb; ++i) {
+      const Operand& b = a.b[i];
+      if (!a.w8_scale[i] || (b.ld % 16) || (b.group_stride % 16)) return cudaErrorInvalidValue;
+      const uint64_t dims[3] = {static_cast<uint64_t>(b.cols), static_cast<uint64_t>(b.rows),
+                                static_cast<uint64_t>(b.groups)};
+      const uint64_t str[2] = {static_cast<uint64_t>(b.ld), static_cast<uint64_t>(b.group_stride)};
+      const uint32_t box[3] = {64, a.b_mn ? 64u : static_cast<uint32_t>(a.b_dual_n ? BN / 2 : BN), 1};
+      if (!make_map_u8(&kp.tmB[i], b.ptr, 3, dims, str, box)) return cudaErrorInvalidValue;
+      kp.wscale[i] = a.w8_scale[i];
+    }
+    if (nb == 1) {
+      kp.tmB[1] = kp.tmB[0];
+      kp.wscale[1] = kp.wscale[0];
+    }
+    kp.ws_cols = static_cast<int32_t>((a.b[0].cols + 127) / 128);
+    kp.ws_gstride = static_cast<int64_t>((a.b[0].rows + 127) / 128) * kp.ws_cols;
+    const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
+    tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+    if (!a.b_mn) {
+      if (a.epi == EPI_SWIGLU_FWD) return launch_impl<256, false, false, EPI_SWIGLU_FWD, false, false, true>(kp, tiles_ub, stream);
+      if (a.epi == EPI_BF16) return launch_impl<256, false, false, EPI_BF16, false, false, true>(kp, tiles_ub, stream);
+      return cudaErrorInvalidValue;
+    }
+    if (a.epi == EPI_SWIGLU_BWD) return launch_impl<256, false, true, EPI_SWIGLU_BWD, false, false, true>(kp, tiles_ub, stream);
+    if (a.epi == EPI_BF16) return launch_impl<256, false, true, EPI_BF16, false, false, true>(kp, tiles_ub, stream);
+    return cudaErrorInvalidValue;
   }
   // CTA pairs: each CTA loads its own 128 rows of A and half of the B tile
   const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&

@@ -80,6 +80,12 @@ struct GemmArgs {
   int64_t ld_out = 0;
   int64_t group_stride_out = 0;
   int32_t* status = nullptr;  // device status words
+  // FP8 weights (bf16 A): b[] hold E4M3 codes (uint8, ld and group_stride in
+  // bytes) of weight matrices [rows][cols] (K-major B: rows = n; MN-major B:
+  // rows = k) and w8_scale[] their fp32 scales per 128 x 128 tile,
+  // [groups][ceil(rows/128)][ceil(cols/128)]; dequantised to bf16 in shared memory
+  bool w8 = false;
+  const float* w8_scale[2] = {nullptr, nullptr};
 };
 
 // Enqueue the grouped GEMM on `stream`.  Returns cudaSuccess or the first

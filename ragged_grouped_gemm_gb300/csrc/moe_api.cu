@@ -103,7 +103,7 @@ moe_status_t check_desc(const moe_desc_t* d) {
   if (d->use_bias != 0 && d->use_bias != 1) return MOE_ERR_INVALID_ARG;
   if (d->n_shared != 0 && d->n_shared != 1) return d->n_shared > 1 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
   if (d->n_shared && (d->d_ff_shared <= 0 || d->d_ff_shared % 64)) return MOE_ERR_INVALID_ARG;
-  if (d->precision != 0 && d->precision != 1) return MOE_ERR_UNSUPPORTED;
+  if (d->precision < 0 || d->precision > 2) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->n_tok) * d->top_k >= (int64_t{1} << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -151,10 +151,16 @@ Operand wstack(const void* p, int64_t groups, int64_t rows, int64_t cols) {
 
 // SwiGLU FFN of one "expert set": GEMM1 (fused w1|w3 with SwiGLU epilogue)
 // then GEMM2, over `groups` ragged row groups of `a_in` [rows, D].
+// (w8: w1, w3, w2 are E4M3 codes with fp32 tile scales s1, s3, s2)
 moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, const int32_t* offsets,
                       const void* w1, const void* w3, const void* w2, void* h, void* a1, void* a3, void* y,
-                      int32_t* status, cudaStream_t st) {
+                      int32_t* status, cudaStream_t st, const float* s1 = nullptr, const float* s3 = nullptr,
+                      const float* s2 = nullptr) {
+  const bool w8 = s1 != nullptr;
   GemmArgs g1;
+  g1.w8 = w8;
+  g1.w8_scale[0] = s1;
+  g1.w8_scale[1] = s3;
   g1.epi = moe::EPI_SWIGLU_FWD;
   g1.a[0] = act(a_in, rows, D);
   g1.b[0] = wstack(w1, groups, F, D);
@@ -172,6 +178,8 @@ moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, 
   g1.status = status;
   MOE_CUDA(moe::launch_grouped_gemm(g1, st));
   GemmArgs g2;
+  g2.w8 = w8;
+  g2.w8_scale[0] = s2;
   g2.epi = moe::EPI_BF16;
   g2.a[0] = act(h, rows, F);
   g2.b[0] = wstack(w2, groups, D, F);
@@ -192,8 +200,12 @@ moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, 
 moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, const void* a3, const void* h,
                           int64_t rows, int D, int F, int groups, const int32_t* offsets, const void* w1,
                           const void* w3, const void* w2, void* da1, void* da3, void* dx_rows, float* dw1,
-                          float* dw3, float* dw2, int32_t* status, cudaStream_t st) {
+                          float* dw3, float* dw2, int32_t* status, cudaStream_t st, const float* s1 = nullptr,
+                          const float* s3 = nullptr, const float* s2 = nullptr) {
+  const bool w8 = s1 != nullptr;   // FP8 weights in the data gradients; weight gradients stay bf16
   GemmArgs g;
+  g.w8 = w8;
+  g.w8_scale[0] = s2;
   g.epi = moe::EPI_SWIGLU_BWD;
   g.b_mn = true;
   g.a[0] = act(dyw, rows, D);
@@ -230,6 +242,9 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
 
   // dx_rows = da1 w1_e + da3 w3_e (the dYw buffer may be reused as dx_rows)
   GemmArgs d;
+  d.w8 = w8;
+  d.w8_scale[0] = s1;
+  d.w8_scale[1] = s3;
   d.epi = moe::EPI_BF16;
   d.b_mn = true;
   d.a[0] = act(da1, rows, F);
@@ -409,12 +424,15 @@ moe_status_t moe_combine(const moe_desc_t* d, const void* y_perm, const int32_t*
                                          static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
-                          const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
-                          size_t ws_bytes, void* stream) {
-  MOE_TRY(check_desc(d));
+}  // extern "C"
+
+namespace {
+// The layer backward (moe_backward); with FP8 weights (q non-NULL) the data
+// gradients read the E4M3 weight codes w1, w3, w2 with their tile scales.
+moe_status_t backward_impl(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
+                           const moe_expert_weights_mx_t* q, const moe_fwd_state_t* s, const void* dy,
+                           const moe_grads_t* g, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_ws(*d, ws, ws_bytes, true));
-  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // the backward runs in bf16
   if (!w || !s || !g) return MOE_ERR_INVALID_ARG;
   if (!all16({w_gate, w->w1, w->w3, w->w2, s->x, s->x_perm, s->a1, s->a3, s->h, s->y_perm, dy, g->dx, g->dw_gate,
               g->dw1, g->dw3, g->dw2}))
@@ -450,15 +468,19 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
   MOE_CUDA(moe::launch_combine_bwd(N, D, K, d->gate, dy, s->y_perm, s->row_of_copy, s->topk_w, s->logits, E,
                                    s->topk_idx, dyw, dg, dl, st));
   // routed experts; dx_perm overwrites dYw once its last reader is done
+  auto sc = [&](const void* p_) { return q ? static_cast<const float*>(p_) : nullptr; };
   MOE_TRY(ffn_pair_bwd(dyw, s->x_perm, s->a1, s->a3, s->h, R, D, F, E, s->offsets, w->w1, w->w3, w->w2, da1, da3,
-                       dyw, g->dw1, g->dw3, g->dw2, status, st));
+                       dyw, g->dw1, g->dw3, g->dw2, status, st, sc(q ? q->w1_scale : nullptr),
+                       sc(q ? q->w3_scale : nullptr), sc(q ? q->w2_scale : nullptr)));
   void* dxs = nullptr;
   if (d->n_shared) {
     int32_t* dense = at<int32_t>(ws, L.dense_off);
     MOE_CUDA(moe::launch_dense_offsets(dense, N, st));
     dxs = at<void>(ws, L.dxs);
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
-                         at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st));
+                         at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st,
+                         sc(q ? q->ws1_scale : nullptr), sc(q ? q->ws3_scale : nullptr),
+                         sc(q ? q->ws2_scale : nullptr)));
   }
   if (s->offsets_full && s->copy_of_row_full)   // capacity mode: every copy, x gathered in dropless order
     MOE_CUDA(moe::launch_dwgate(N, K, E, D, s->offsets_full, s->copy_of_row_full, dl, s->x, K,
@@ -468,6 +490,28 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
                                 g->dw_gate, st));
   MOE_CUDA(moe::launch_unpermute_dx(N, D, K, dyw, s->row_of_copy, dl, s->topk_idx, w_gate, dxs, g->dx, st));
   return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
+                          const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                          size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // bf16 operands; moe_backward_mxfp8 / _fp8w otherwise
+  return backward_impl(d, w_gate, w, nullptr, s, dy, g, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wq,
+                               const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
+                               size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 2 || !wq) return MOE_ERR_INVALID_ARG;
+  if (!wq->w1_scale || !wq->w3_scale || !wq->w2_scale) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (!wq->ws1_scale || !wq->ws3_scale || !wq->ws2_scale)) return MOE_ERR_INVALID_ARG;
+  const moe_expert_weights_t w{wq->w1, wq->w3, wq->w2, wq->ws1, wq->ws3, wq->ws2};
+  return backward_impl(d, w_gate, &w, wq, s, dy, g, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
@@ -788,6 +832,46 @@ moe_status_t moe_permute_capacity(const moe_desc_t* d, const void* x, const int3
   MOE_CUDA(moe::launch_capacity_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, row_of_copy_full, cap,
                                      kept_offsets, row_of_copy, copy_of_row, n_dropped, st));
   MOE_CUDA(moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_fp8_tile(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
+                                   float* scales, void* stream) {
+  if (!src || !codes || !scales || groups < 1 || rows <= 0 || cols <= 0 || cols % 16 || !aligned16(src) ||
+      !aligned16(codes))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_fp8_tile_quant(src, groups, rows, cols, static_cast<uint8_t*>(codes), scales,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn_fp8w(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
+                                  const moe_expert_weights_mx_t* wq, const moe_ffn_saved_t* saved, void* y_perm,
+                                  void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_desc(d));
+  if (d->precision != 2) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!wq || !saved || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!all16({x_perm, wq->w1, wq->w3, wq->w2, saved->h, y_perm}) || !wq->w1_scale || !wq->w3_scale || !wq->w2_scale)
+    return MOE_ERR_INVALID_ARG;
+  if ((saved->a1 && !aligned16(saved->a1)) || (saved->a3 && !aligned16(saved->a3))) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (!all16({x, wq->ws1, wq->ws3, wq->ws2, saved->hs, y_shared}) || !wq->ws1_scale ||
+                      !wq->ws3_scale || !wq->ws2_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  MOE_TRY(ffn_pair(x_perm, R, d->d_model, d->d_ff, d->n_exp, offsets, wq->w1, wq->w3, wq->w2, saved->h, saved->a1,
+                   saved->a3, y_perm, status, st, static_cast<const float*>(wq->w1_scale),
+                   static_cast<const float*>(wq->w3_scale), static_cast<const float*>(wq->w2_scale)));
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
+    MOE_TRY(ffn_pair(x, d->n_tok, d->d_model, d->d_ff_shared, 1, dense, wq->ws1, wq->ws3, wq->ws2, saved->hs,
+                     saved->a1s, saved->a3s, y_shared, status, st, static_cast<const float*>(wq->ws1_scale),
+                     static_cast<const float*>(wq->ws3_scale), static_cast<const float*>(wq->ws2_scale)));
+  }
   return MOE_OK;
 }
 

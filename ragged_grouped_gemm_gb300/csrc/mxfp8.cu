@@ -137,6 +137,43 @@ __global__ void __launch_bounds__(128) mx_quant_cols_t_kernel(
   scales[(static_cast<int64_t>(b) * (ld_codes / 32) + jb) * ld_s + c] = static_cast<uint8_t>(e + 127);
 }
 
+// One CTA per 128 x 128 tile: thread t owns row t/2, columns (t%2)*64..+63.
+__global__ void __launch_bounds__(256) fp8_tile_quant_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows,
+                                                             int64_t cols, uint8_t* __restrict__ codes,
+                                                             float* __restrict__ scales) {
+  __shared__ float s_max[8];
+  const int64_t tr = blockIdx.y, tc = blockIdx.x, b = blockIdx.z;
+  const int64_t ntr = gridDim.y, ntc = gridDim.x;
+  const int64_t r = tr * 128 + (threadIdx.x >> 1);
+  const int64_t c0 = tc * 128 + (threadIdx.x & 1) * 64;
+  const __nv_bfloat16* m = src + b * rows * cols;
+  float v[64];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const int64_t c = c0 + i;
+    v[i] = (r < rows && c < cols) ? __bfloat162float(m[r * cols + c]) : 0.0f;
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  float tmax = 0.0f;
+  for (int w = 0; w < 8; ++w) tmax = fmaxf(tmax, s_max[w]);
+  const float sc = tmax > 0.0f ? tmax / 448.0f : 1.0f;
+  if (threadIdx.x == 0) scales[(b * ntr + tr) * ntc + tc] = sc;
+  if (r >= rows) return;
+  const double dsc = static_cast<double>(sc);
+  uint8_t* dst = codes + b * rows * cols + r * cols;
+  for (int i = 0; i < 64; ++i) {
+    const int64_t c = c0 + i;
+    if (c < cols)
+      dst[c] = static_cast<uint8_t>(
+          __nv_cvt_double_to_fp8(static_cast<double>(v[i]) / dsc, __NV_SATFINITE, __NV_E4M3));
+  }
+}
+
 // Single block: counts rounded up to 128, exclusive scan over n_groups <= 1024.
 __global__ void __launch_bounds__(1024) pad_offsets_kernel(const int32_t* __restrict__ offsets, int n_groups,
                                                            int32_t* __restrict__ pad_offsets) {
@@ -173,6 +210,15 @@ cudaError_t launch_mx_quant_cols_t(const void* src, int64_t batch, int64_t rows,
   mx_quant_cols_t_kernel<<<grid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, src_row_of,
                                                 src_div, offsets, pad_offsets, n_groups, ld_codes, codes, ld_s,
                                                 scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_tile_quant(const void* src, int64_t batch, int64_t rows, int64_t cols, uint8_t* codes,
+                                  float* scales, cudaStream_t st) {
+  if (batch <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128),
+                  static_cast<unsigned>(batch));
+  fp8_tile_quant_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, scales);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,13 @@ cudaError_t launch_mx_quant_cols_t(const void* src, int64_t batch, int64_t rows,
                                    const int32_t* pad_offsets, int n_groups, int64_t ld_codes, uint8_t* codes,
                                    int64_t ld_s, uint8_t* scales, cudaStream_t st);
 
+// FP8 weights with per-tile scaling: codes [batch][rows][cols] E4M3 and
+// scales [batch][ceil(rows/128)][ceil(cols/128)] fp32, scale = amax / 448 of
+// the 128 x 128 tile (1 for an all-zero tile), code = E4M3(w / scale), the
+// quotient formed in double and rounded once (nearest even, saturating).
+cudaError_t launch_fp8_tile_quant(const void* src, int64_t batch, int64_t rows, int64_t cols, uint8_t* codes,
+                                  float* scales, cudaStream_t st);
+
 // pad_offsets[g] = sum over g' < g of ceil(count_g' / 128) * 128 (n_groups + 1 entries).
 cudaError_t launch_pad_offsets(const int32_t* offsets, int n_groups, int32_t* pad_offsets, cudaStream_t st);
 

@@ -44,7 +44,7 @@ class MoEConfig:
     use_bias: bool = False
     n_shared: int = 0
     d_ff_shared: int = 0
-    precision: str = "bf16"        # "bf16" | "mxfp8"
+    precision: str = "bf16"        # "bf16" | "mxfp8" | "fp8w" (FP8 weights, bf16 activations)
     bias_beta: float = 0.0         # Zipf strength of the route bias
     n_cold: int = 0                # experts whose bias keeps them empty
     capacity_factor: float = 0.0   # > 0: capacity-factor drop mode (comparison case); 0: dropless

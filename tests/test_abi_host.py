@@ -94,7 +94,7 @@ def test_workspace_sizes(lib):
 
 @pytest.mark.parametrize("field,value,code", [
     ("top_k", 0, 1), ("top_k", 9, 1), ("d_model", 96, 1), ("d_ff", 100, 1), ("gate", 2, 1),
-    ("n_exp", 2000, 1), ("precision", 2, 2), ("n_shared", 2, 2), ("n_tok", -1, 1), ("top_k", 33, 1),
+    ("n_exp", 2000, 1), ("precision", 3, 2), ("n_shared", 2, 2), ("n_tok", -1, 1), ("top_k", 33, 1),
 ])
 def test_invalid_descriptions_rejected(lib, field, value, code):
     d = _desc(**{field: value})
