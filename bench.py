@@ -316,8 +316,9 @@ def run_ours(args, rank, world, local_rank):
 
 def run_sweep(args):
     """Forward and forward+backward timing of the layer under prescribed load
-    skews, bf16 and MXFP8 operands (the MXFP8 backward quantises every expert
-    GEMM's operands as its forward does).  Routing comes from the workload's
+    skews: bf16, MXFP8 operands (the MXFP8 backward quantises every expert
+    GEMM's operands as its forward does), FP8 weights with per-tile scales,
+    and the capacity-factor drop mode.  Routing comes from the workload's
     own gate and bias ("bias") or from synthetic fp32 logits through
     moe_route_from_logits (uniform, Zipf s=1, half of the tokens on expert 0)."""
     import torch
@@ -331,7 +332,7 @@ def run_sweep(args):
     dy = make_dy(base, dev)
     results = []
     # dropless bf16 and MXFP8, then the capacity-factor (drop) comparison in bf16
-    for prec, cap_f in (("bf16", 0.0), ("mxfp8", 0.0), ("bf16", 1.0), ("bf16", 1.25)):
+    for prec, cap_f in (("bf16", 0.0), ("mxfp8", 0.0), ("fp8w", 0.0), ("bf16", 1.0), ("bf16", 1.25)):
         cfg = base.replace(precision=prec, capacity_factor=cap_f)
         layer = api.MoELayer(cfg, p, train=True, device=dev)
         b, d, ws = layer.buf, layer.desc, layer.ws
@@ -371,7 +372,7 @@ def run_sweep(args):
             counts = b["counts"].cpu()
             ne = int((counts > 0).sum())
             wb = 3 * ne * cfg.d_ff * cfg.d_model + (3 * cfg.d_ff_shared * cfg.d_model if cfg.n_shared else 0)
-            wbytes = wb * (1 + 1 / 32) if prec == "mxfp8" else 2 * wb
+            wbytes = wb * (1 + 1 / 32) if prec == "mxfp8" else (wb * (1 + 4 / 128 ** 2) if prec == "fp8w" else 2 * wb)
             results.append({"precision": prec, "capacity_factor": cap_f, "drop_rate": layer.drop_rate(),
                             "skew": skew, "ms_fwd": ms, "tokens_per_s": cfg.n_tok / ms * 1e3,
                             "experts_nonempty": ne, "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
