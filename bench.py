@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--sample", type=int, default=0, help="oracle token sample (0: automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8", "fp8w"],
+                    help="expert GEMM operands: bf16; MXFP8 (E4M3 codes, E8M0 scales per 32 along the contraction,"
+                         " forward and backward); fp8w (E4M3 weights with fp32 scales per 128x128 tile)")
     ap.add_argument("--sweep", action="store_true",
                     help="forward-only load-skew sweep, bf16 and MXFP8 (prints one JSON line of results)")
     return ap.parse_args()
@@ -58,18 +61,37 @@ def flops(cfg) -> dict:
 
 
 def ffn_bytes(cfg, nonempty: int) -> int:
-    """Algorithmic HBM bytes of one moe_grouped_ffn call (training forward):
+    """Algorithmic HBM bytes of one grouped-FFN call (training forward):
     GEMM1 reads x_perm and w1, w3 of the experts that received tokens and
     writes h, a1, a3; GEMM2 reads h and w2 and writes y_perm; the shared expert
-    does the same over all tokens."""
+    does the same over all tokens.  MXFP8: operands are E4M3 codes plus one
+    E8M0 scale per 32 (1 + 1/32 bytes per element), GEMM1 also writes the
+    quantised h that GEMM2 reads; fp8w: weights are E4M3 plus one fp32 scale
+    per 128 x 128 tile."""
     n, k, d, f = cfg.n_tok, cfg.top_k, cfg.d_model, cfg.d_ff
     r = n * k
-    b = 2 * (r * d + 2 * nonempty * f * d + 3 * r * f)          # GEMM1
-    b += 2 * (r * f + nonempty * d * f + r * d)                 # GEMM2
+    q = 1 + 1 / 32
+    wb = {"bf16": 2, "mxfp8": q, "fp8w": 1 + 4 / 128 ** 2}[cfg.precision]
+
+    def pair(rows, experts, ff):
+        if cfg.precision == "mxfp8":
+            g1 = q * rows * d + wb * 2 * experts * ff * d + 2 * 3 * rows * ff + q * rows * ff
+            g2 = q * rows * ff + wb * experts * d * ff + 2 * rows * d
+        else:
+            g1 = 2 * rows * d + wb * 2 * experts * ff * d + 2 * 3 * rows * ff
+            g2 = 2 * rows * ff + wb * experts * d * ff + 2 * rows * d
+        return g1 + g2
+    b = pair(r, nonempty, f)
     if cfg.n_shared:
-        fs = cfg.d_ff_shared
-        b += 2 * (n * d + 2 * fs * d + 3 * n * fs) + 2 * (n * fs + d * fs + n * d)
-    return b
+        b += pair(n, 1, cfg.d_ff_shared)
+    return int(b)
+
+
+def workload_name(cfg) -> str:
+    """The workload string of the `config` key (both arms)."""
+    return (f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} F={cfg.d_ff} E={cfg.n_exp} K={cfg.top_k} {cfg.gate}"
+            + (" +route bias" if cfg.use_bias else "") + (f" +shared Fs={cfg.d_ff_shared}" if cfg.n_shared else "")
+            + ", fwd+bwd" + ("" if cfg.precision == "bf16" else f", {cfg.precision} expert GEMMs"))
 
 
 def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, reduce_max) -> tuple[float, float]:
@@ -83,6 +105,14 @@ def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, red
 def launches_per_step(cfg) -> int:
     """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
     from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
+    if cfg.precision == "mxfp8":
+        # route 4; permute: 3 map kernels + row quantiser (+ token quantiser for the shared expert);
+        # grouped FFN: GEMM1, GEMM2 (+ dense offsets, GEMM1, GEMM2); combine
+        fwd = 4 + 4 + 2 + 1 + (4 if cfg.n_shared else 0)
+        # per expert set: 3 row-wise quantisers, pad offsets, 5 transposing quantisers, 5 GEMMs
+        per_set = 3 + 1 + 5 + 5
+        bwd = 1 + per_set + (1 + per_set if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
+        return fwd + bwd + (1 if cfg.use_bias else 0)
     fwd = 4 + 4 + 2 + 1          # route: dense offsets, gate GEMM, top-K, scan; permute: 3 map kernels + rows;
     if cfg.n_shared:             # grouped FFN: GEMM1, GEMM2; combine
         fwd += 3
@@ -169,13 +199,20 @@ def recorded_traffic(kernel: str, workload: str):
 
 # ----------------------------------------------------------------- oracle arm
 def oracle_step_sample(cfg, host, sample_idx, dy_host):
-    """Forward + backward of the CPU oracle on a token sample (its own routing)."""
+    """Forward + backward of the CPU oracle on a token sample (its own routing);
+    the MXFP8 oracle for MXFP8 operands (fp8w: `host` holds the dequantised
+    weights, prepared once outside the timed step as on the GPU side)."""
     import oracle as O
     x = host["x"][sample_idx]
     dy = dy_host[sample_idx]
     shared = (host["ws1"], host["ws3"], host["ws2"]) if cfg.n_shared else None
     lg = O.gate_logits(x, host["w_gate"])
     idx, g = O.route(lg, host.get("bias"), cfg.top_k, cfg.gate)
+    if cfg.precision == "mxfp8":
+        out, saved = O.moe_forward_mxfp8(x, idx, g, host["w1"], host["w3"], host["w2"], shared, return_saved=True)
+        O.moe_backward_mxfp8(dy, x, lg, idx, g, host["w_gate"], host["w1"], host["w3"], host["w2"], saved, cfg.gate,
+                             shared)
+        return out
     out, saved = O.moe_forward(x, lg, idx, g, host["w1"], host["w3"], host["w2"], shared)
     O.moe_backward(dy, x, lg, idx, g, host["w_gate"], host["w1"], host["w3"], host["w2"], saved, cfg.gate, shared)
     return out
@@ -190,6 +227,11 @@ def time_oracle(cfg, sample: int, steps: int = 1):
     host = {k: (v.float().numpy() if v is not None else None) for k, v in p.items()}
     dy = make_dy(cfg, "cpu").float().numpy()
     del p
+    if cfg.precision == "fp8w":
+        import oracle as O
+        for key in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+            if host.get(key) is not None:
+                host[key] = O.fp8_tile_dequantize(*O.fp8_tile_quantize(host[key]))
     idx = sample_tokens(cfg.n_tok, sample).numpy()
     times = []
     for _ in range(steps):
@@ -208,7 +250,7 @@ def run_ours(args, rank, world, local_rank):
     from ragged_grouped_gemm_gb300 import api
     from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_dy, make_layer
 
-    cfg = CONFIGS[args.workload]
+    cfg = CONFIGS[args.workload].replace(precision=args.precision)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     p = make_layer(cfg, dev)
@@ -226,11 +268,23 @@ def run_ours(args, rank, world, local_rank):
         api.moe_route(d, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
                       b["offsets"], ws)
         mark(1)
-        api.moe_permute(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], ws)
+        if layer.mx:
+            api.moe_permute_mxfp8(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
+                                  b["xq_perm"], b["xs_perm"], b["xq_tok"], b["xs_tok"], ws)
+        else:
+            api.moe_permute(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], ws)
         mark(2)
-        api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"), p.get("ws3"),
-                            p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"], b["y_perm"],
-                            b["y_shared"], ws)
+        saved = {key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
+        if layer.mx:
+            api.moe_grouped_ffn_mxfp8(d, b["xq_perm"], b["xs_perm"], b["offsets"], b["xq_tok"], b["xs_tok"],
+                                      layer.wq, saved, b["y_perm"], b["y_shared"], ws)
+        elif layer.w8:
+            api.moe_grouped_ffn_fp8w(d, b["x_perm"], b["offsets"], x, layer.w8q, saved, b["y_perm"], b["y_shared"],
+                                     ws)
+        else:
+            api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
+                                p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
+                                b["y_perm"], b["y_shared"], ws)
         mark(3)
         api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
         mark(4)
@@ -398,7 +452,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     from ragged_grouped_gemm_gb300.inputs import CONFIGS
-    cfg = CONFIGS[args.workload]
+    cfg = CONFIGS[args.workload].replace(precision=args.precision)
     tokens_per_step = cfg.n_tok
 
     if args.impl == "reference":
@@ -413,11 +467,10 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * tokens_per_step / n,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                "data": "synthetic", "config": {"workload": f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} "
-                                                f"F={cfg.d_ff} E={cfg.n_exp} K={cfg.top_k} {cfg.gate}",
-                                                "sample_tokens": n},
+                "data": "synthetic", "config": {"workload": workload_name(cfg), "sample_tokens": n},
                 "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"},
+                                 "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"
+                                           + ("" if cfg.precision == "bf16" else f", {cfg.precision} oracle")},
                 "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -440,24 +493,28 @@ def main():
     ffn_b = ffn_bytes(cfg, res["nonempty"])
     bwd_s = per_call["backward"] / 1e3
     peak = peaks["bf16_tflops_sustained"]
-    wbytes = 2 * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
+    peak_src = f"{peaks['source']} bf16_tflops_sustained"
+    if cfg.precision == "mxfp8":      # E4M3 x E4M3 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
+        peak, peak_src = 2 * peak, peak_src + " x 2 (nominal fp8/bf16 ratio)"
+    wbytes = {"bf16": 2, "mxfp8": 1 + 1 / 32, "fp8w": 1}[cfg.precision] * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
     # the binding roof of the grouped FFN: tensor time vs HBM time at the measured peaks
     if fl["ffn_fwd"] / (peak * 1e12) >= ffn_b / (peaks["hbm_gbs"] * 1e9):
         roof = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": ffn_tflops / peak, "peak_source": f"{peaks['source']} bf16_tflops_sustained"}
+                "frac": ffn_tflops / peak, "peak_source": peak_src}
     else:
         gbs = ffn_b / ffn_s / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} hbm_gbs"}
-    roof.update(kernel="moe_grouped_ffn (GEMM1 w1|w3+SwiGLU, GEMM2 w2)", algorithmic_bytes=ffn_b,
-                algorithmic_flops=fl["ffn_fwd"], traffic=recorded_traffic("grouped_ffn", cfg.name))
+    tkey = "grouped_ffn" if cfg.precision == "bf16" else f"grouped_ffn_{cfg.precision}"
+    roof.update(kernel="grouped FFN (GEMM1 w1|w3+SwiGLU, GEMM2 w2)", algorithmic_bytes=ffn_b,
+                algorithmic_flops=fl["ffn_fwd"], traffic=recorded_traffic(tkey, cfg.name))
+    dtype = {"bf16": "bf16", "mxfp8": "mxfp8 (e4m3 x e4m3, e8m0 scales per 32)",
+             "fp8w": "e4m3 weights (fp32 tile scales) x bf16"}[cfg.precision]
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: N={cfg.n_tok} D={cfg.d_model} F={cfg.d_ff} E={cfg.n_exp} "
-                               f"K={cfg.top_k} {cfg.gate}" + (" +route bias" if cfg.use_bias else "")
-                               + (f" +shared Fs={cfg.d_ff_shared}" if cfg.n_shared else "") + ", fwd+bwd",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {"workload": workload_name(cfg),
                    "l2": f"no flush: the {wbytes / 1e9:.1f} GB of expert weights streamed every step exceed "
                          "the 126 MB L2",
                    "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 shared=6/7/8 dY=9"},
@@ -476,7 +533,8 @@ def main():
         n, times = time_oracle(cfg, sample, steps=1)
         line["cpu_baseline"] = {"value": n / times[0], "unit": "tokens/s", "cores": os.cpu_count(),
                                 "kind": "oracle",
-                                "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"}
+                                "sample": f"{n} seeded tokens of the {cfg.name} batch, fwd+bwd, numpy fp32"
+                                           + ("" if cfg.precision == "bf16" else f", {cfg.precision} oracle")}
     print(json.dumps(line), flush=True)
 
 
