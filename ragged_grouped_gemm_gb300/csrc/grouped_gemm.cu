@@ -802,13 +802,76 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         }
         const bool zero = RAGGED_K && t.num_kb == 0;
         const int c_begin = hf * (BN / 2);
-        if (EPI == EPI_F32 && p.c_tma) {
-          // Stage this warp's 32 rows x 16 columns in a 2 KB shared-memory
-          // buffer (64-byte swizzle: 16-byte chunk j of row r at chunk
-          // j ^ ((r >> 1) & 3)) and write them with a TMA tensor store, which
-          // clips rows and columns outside the output (evict-first in L2:
-          // the fp32 output is written once and not read back).  The TMEM
-          // load of the next chunk is in flight while this one is staged.
+        if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
+          // Stage this warp's 32 rows x 32 columns as two 16-row halves in a
+          // 2 KB shared-memory buffer (128-byte swizzle: 16-byte chunk j of
+          // row r at chunk j ^ (r & 7)) and write each half with a TMA tensor
+          // store of 16 full 128-byte rows, which clips rows and columns
+          // outside the output (evict-first in L2: the fp32 output is written
+          // once and not read back).  The TMEM load of the next 32 columns is
+          // in flight while these are staged.
+          constexpr int NCH = BN / 64;
+          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
+          const uint32_t stg_addr = smem_u32(stg);
+          uint32_t va[16], vb[16], vc[16], vd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) va[j] = vb[j] = vc[j] = vd[j] = 0u;
+          if (!zero) {
+            tmem_ld_32x32b_x16(tb + c_begin, va);
+            tmem_ld_32x32b_x16(tb + c_begin + 16, vb);
+            tmem_wait_ld(va);
+            reg_fence(vb);
+          }
+          const int rr = lane & 15;
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            if (!zero && i + 1 < NCH) {
+              tmem_ld_32x32b_x16(tb + c_begin + 32 * (i + 1), vc);
+              tmem_ld_32x32b_x16(tb + c_begin + 32 * (i + 1) + 16, vd);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+              __syncwarp();
+              if ((lane >> 4) == h) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  st_shared_v4(stg_addr + rr * 128 + ((j ^ (rr & 7)) << 4), va[4 * j], va[4 * j + 1],
+                               va[4 * j + 2], va[4 * j + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  st_shared_v4(stg_addr + rr * 128 + (((j + 4) ^ (rr & 7)) << 4), vb[4 * j], vb[4 * j + 1],
+                               vb[4 * j + 2], vb[4 * j + 3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                // boxes that start past the output's last column or row hold nothing to write
+                const int col = t.nt * BN + c_begin + 32 * i;
+                const int row = (RAGGED_K ? t.m0 : t.row0) + q * 32 + 16 * h;
+                const int rows = RAGGED_K ? p.m_size : p.c_rows;
+                if (col < p.n_size && row < rows) {
+                  tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0, policy_evict_first());
+                  bulk_commit_group();
+                }
+              }
+            }
+            if (i + 1 < NCH) {
+              if (!zero) {
+                tmem_wait_ld(vc);
+                reg_fence(vd);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                va[j] = vc[j];
+                vb[j] = vd[j];
+              }
+            }
+          }
+        } else if (EPI == EPI_F32 && p.c_tma) {
+          // 16-column form of the above for tiles whose column halves are not
+          // a multiple of 32 wide: 32 rows x 16 columns per 2 KB buffer
+          // (64-byte swizzle: chunk j of row r at chunk j ^ ((r >> 1) & 3)).
           constexpr int NCH = BN / 32;
           uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
           const uint32_t stg_addr = smem_u32(stg);
@@ -822,7 +885,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
 #pragma unroll
           for (int i = 0; i < NCH; ++i) {
             if (!zero && i + 1 < NCH) tmem_ld_32x32b_x16(tb + c_begin + 16 * (i + 1), vb);
-            if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+            if (lane == 0) bulk_wait_group_read0();
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -831,7 +894,6 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              // boxes that start past the output's last column or row hold nothing to write
               const int col = t.nt * BN + c_begin + 16 * i;
               const int row = RAGGED_K ? t.m0 + q * 32 : t.row0 + q * 32;
               const int rows = RAGGED_K ? p.m_size : p.c_rows;
@@ -1104,16 +1166,17 @@ bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t b
 // fp32 output map {n, m, groups} with a 16x32 box and 64-byte swizzle, for
 // the TMA-store epilogue.  False when the layout is not TMA-compatible.
 bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_t groups, int64_t ld,
-                      int64_t group_stride) {
+                      int64_t group_stride, bool wide) {
   EncodeFn enc = get_encode_fn();
   if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
   if ((ld * 4) % 16 != 0 || (group_stride * 4) % 16 != 0 || group_stride < m * ld) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(groups)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(group_stride) * 4};
-  cuuint32_t box[3] = {16, 32, 1};
+  // wide: 32 columns x 16 rows, 128-byte swizzle; else 16 columns x 32 rows, 64-byte swizzle
+  cuuint32_t box[3] = {wide ? 32u : 16u, wide ? 16u : 32u, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1323,7 +1386,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       const uint32_t sbox[2] = {QBN, 4};
       if (!make_map_u8(&kp.tmBs[0], qb.scales, 2, sd, ss, sbox)) return cudaErrorInvalidValue;
     }
-    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, a.m_size, a.num_groups, a.ld_out, a.group_stride_out) ? 1 : 0;
+    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, a.m_size, a.num_groups, a.ld_out, a.group_stride_out,
+                                (QBN / 2) % 32 == 0) ? 1 : 0;
     kp.c_rows = a.m_size;
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + BM - 1) / BM) * ((a.n_size + QBN - 1) / QBN);
     return launch_impl<QBN, true, true, EPI_F32, true>(kp, tiles_ub, stream);
@@ -1415,7 +1479,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (a.epi == EPI_F32 && (a.ragged_k || a.num_groups == 1)) {
     const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
     const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
-    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs) ? 1 : 0;
+    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs,
+                                (BN / 2) % 32 == 0) ? 1 : 0;
     kp.c_rows = static_cast<int32_t>(m);
   }
   const int64_t u = tiles_ub;
