@@ -95,7 +95,8 @@ struct KParams {
   int64_t ws_gstride;    // tiles per matrix
 };
 
-template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false>
+// STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
+template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false, bool STG = false>
 struct Cfg {
   // FP8 weights (W8): the B codes of a k-block (BN x 64 bytes) land in a
   // two-slot staging ring; converters write the bf16 B tile into the stage
@@ -114,22 +115,29 @@ struct Cfg {
   // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
   static constexpr int kStageBytes =
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
-  static constexpr int kStagesRaw = ((QUANT ? 206 * 1024 : 200 * 1024) - kW8Slots * kW8SlotBytes) / kStageBytes;
+  // shared memory left for the stages: 227 KB less the alignment slack, the
+  // staging buffers, the barriers (at most 6 stages) and the group tables
+  static constexpr int kEpiBytes = STG ? 8 * 2048 : 0;
+  static constexpr int kStageBudget = 232448 - 1024 - kEpiBytes - (3 * 6 + 2 * 2 + 5) * 8 - 16 -
+                                      2 * 4 * (kMaxGroups + 1) - kW8Slots * kW8SlotBytes;
+  static constexpr int kStagesRaw = kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
   static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
   static constexpr uint32_t kSfCol = 2 * BN;
-  // stages | epilogue staging (8 warps x 32x16 fp32) |
+  // stages | W8 code slots | fp32 staging (8 warps x 2 KB, STG only) |
   // barriers (2S, + S scale-ready for MXFP8, + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
   static constexpr int kW8Off = kStages * kStageBytes;
   static constexpr int kEpiOff = kW8Off + kW8Slots * kW8SlotBytes;
-  static constexpr int kEpiBytes = 4 * 4096;
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
   static constexpr int kMiscOff = kBarOff + ((QUANT ? 3 : 2) * kStages + 2 * kW8Slots + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr size_t smem_bytes(int groups) {
     return 1024 + kOffOff + 2 * 4 * (groups + 1);
   }
+  static_assert(kStages >= 2, "shared memory holds fewer than two stages");
+  static_assert(smem_bytes(kMaxGroups) <= 232448, "shared memory above 227 KB");
+  static_assert(!QUANT || 2 * BN + 16 * kStages <= 512, "accumulators and scale buffers exceed tensor memory");
 };
 
 struct Tile {
@@ -245,7 +253,7 @@ __device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
     grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<BN, QUANT, PAIR, W8>;
+  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
@@ -1205,7 +1213,7 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
-  using C = Cfg<BN, QUANT, PAIR, W8>;
+  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
   const size_t smem = C::smem_bytes(kp.num_groups);
   auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8>;
   static std::once_flag once;
