@@ -94,6 +94,32 @@ def workload_name(cfg) -> str:
             + ", fwd+bwd" + ("" if cfg.precision == "bf16" else f", {cfg.precision} expert GEMMs"))
 
 
+def kind_work(cfg, kind: str, nonempty: int) -> tuple[float, float]:
+    """Algorithmic FLOPs and HBM bytes of one step's grouped GEMMs of one
+    timing kind.  Operand bytes are 2 (bf16), 1 + 1/32 (MXFP8 codes and
+    scales) or, for fp8w weights, 1 + 4/128^2; the weight gradients are
+    written in fp32 for every expert (zeros for the empty ones)."""
+    n, k, d, f, e = cfg.n_tok, cfg.top_k, cfg.d_model, cfg.d_ff, cfg.n_exp
+    r, fs = n * k, cfg.d_ff_shared if cfg.n_shared else 0
+    act = 1 + 1 / 32 if cfg.precision == "mxfp8" else 2
+    wt = {"bf16": 2, "mxfp8": 1 + 1 / 32, "fp8w": 1 + 4 / 128 ** 2}[cfg.precision]
+    fl = flops(cfg)
+    if kind == "gate":
+        return fl["router_fwd"], 2 * n * d + 2 * e * d + 4 * n * e
+    if kind == "ffn_fwd":
+        return fl["ffn_fwd"], ffn_bytes(cfg, nonempty)
+    sets = [(r, nonempty, e, f)] + ([(n, 1, 1, fs)] if fs else [])
+    if kind == "dgrad":
+        # through w2 (+ SwiGLU derivative: reads dYw, w2, a1, a3; writes da1, da3), then through w1|w3
+        # (reads da1, da3, w1, w3; writes dx_perm)
+        b = sum(act * rows * d + wt * ne * d * ff + 2 * 4 * rows * ff + act * 2 * rows * ff + wt * 2 * ne * ff * d
+                + 2 * rows * d for rows, ne, _, ff in sets)
+        return fl["ffn_bwd"] / 2, b
+    # wgrad: dW2 = dYw^T h, dW1 = da1^T x, dW3 = da3^T x, each reading both operands once
+    b = sum(3 * 4 * ee * d * ff + 3 * act * rows * (d + ff) for rows, _, ee, ff in sets)
+    return fl["ffn_bwd"] / 2, b
+
+
 def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, reduce_max) -> tuple[float, float]:
     """Whole-job throughput of `world` replicas: every rank processes
     `tokens_per_step` tokens per step; the job takes the slowest rank's time.
@@ -311,6 +337,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     clk = ClockSampler(local_rank).__enter__()   # sampled over all three timed loops
+    api.moe_timing_enable(64 * args.steps + 64)   # CUDA events around every grouped GEMM of the timed steps
     t0.record()
     for i in range(args.steps):
         step(evs[i])
@@ -320,6 +347,13 @@ def run_ours(args, rank, world, local_rank):
     ms = t0.elapsed_time(t1)
     per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                 for j, n in enumerate(names)}
+    kernels = {}
+    for kind in api.TIMING_KINDS:
+        k_ms, k_n, k_u = api.moe_timing_read(kind)
+        if k_u:
+            raise RuntimeError(f"{k_u} untimed {kind} launches")
+        kernels[kind] = {"ms_total": k_ms, "launches": k_n}
+    api.moe_timing_disable()
 
     # --- forward-only steps
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -361,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
         return float(t.item())
 
     nonempty = int((b["counts"] > 0).sum().item())
-    res = {"cfg": cfg, "per_call": per_call, "clocks": clk.summary(), "nonempty": nonempty,
+    res = {"cfg": cfg, "per_call": per_call, "kernels": kernels, "clocks": clk.summary(), "nonempty": nonempty,
            "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2}
     for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
         res[key] = aggregate(world, cfg.n_tok, args.steps, v, max_over_ranks)
@@ -484,7 +518,7 @@ def main():
         dist.destroy_process_group()
     if rank != 0:
         return
-    cfg, per_call = res["cfg"], res["per_call"]
+    cfg, per_call, kernels = res["cfg"], res["per_call"], res["kernels"]
     tok_s, ms = res["step"]
     fl = flops(cfg)
     peaks = measured_peaks()
@@ -497,17 +531,34 @@ def main():
     if cfg.precision == "mxfp8":      # E4M3 x E4M3 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
         peak, peak_src = 2 * peak, peak_src + " x 2 (nominal fp8/bf16 ratio)"
     wbytes = {"bf16": 2, "mxfp8": 1 + 1 / 32, "fp8w": 1}[cfg.precision] * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
-    # the binding roof of the grouped FFN: tensor time vs HBM time at the measured peaks
-    if fl["ffn_fwd"] / (peak * 1e12) >= ffn_b / (peaks["hbm_gbs"] * 1e9):
-        roof = {"bound": "tensor", "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": ffn_tflops / peak, "peak_source": peak_src}
-    else:
-        gbs = ffn_b / ffn_s / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} hbm_gbs"}
-    tkey = "grouped_ffn" if cfg.precision == "bf16" else f"grouped_ffn_{cfg.precision}"
-    roof.update(kernel="grouped FFN (GEMM1 w1|w3+SwiGLU, GEMM2 w2)", algorithmic_bytes=ffn_b,
-                algorithmic_flops=fl["ffn_fwd"], traffic=recorded_traffic(tkey, cfg.name))
+    # Roofline per kind of grouped GEMM, from the CUDA events the library
+    # recorded around every launch of the timed steps; the binding roof is
+    # the slower of tensor time and HBM time at the measured peaks.
+    kind_names = {"gate": "router logits GEMM", "ffn_fwd": "forward expert GEMMs (GEMM1 w1|w3+SwiGLU, GEMM2 w2)",
+                  "dgrad": "data-gradient GEMMs (through w2 + SwiGLU derivative, through w1|w3)",
+                  "wgrad": "weight-gradient GEMMs (dW1, dW3, dW2; fp32 out)"}
+    roofs = {}
+    for kind, kt in kernels.items():
+        if not kt["launches"]:
+            continue
+        k_fl, k_b = kind_work(cfg, kind, res["nonempty"])
+        k_fl, k_b = k_fl * args.steps / kt["launches"], k_b * args.steps / kt["launches"]   # per launch
+        k_s = kt["ms_total"] / kt["launches"] / 1e3
+        kpeak = peak if kind != "gate" else peaks["bf16_tflops_sustained"]
+        if k_fl / (kpeak * 1e12) >= k_b / (peaks["hbm_gbs"] * 1e9):
+            r = {"bound": "tensor", "achieved": k_fl / k_s / 1e12, "peak": kpeak, "unit": "TFLOP/s",
+                 "peak_source": peak_src if kind != "gate" else f"{peaks['source']} bf16_tflops_sustained"}
+        else:
+            r = {"bound": "hbm", "achieved": k_b / k_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "peak_source": f"{peaks['source']} hbm_gbs"}
+        tkey = kind if cfg.precision == "bf16" else f"{kind}_{cfg.precision}"
+        r.update(frac=r["achieved"] / r["peak"], traffic=recorded_traffic(tkey, cfg.name), kernel=kind_names[kind],
+                 launches_per_step=kt["launches"] / args.steps, ms_per_launch=k_s * 1e3,
+                 share_of_step=kt["ms_total"] / ms, algorithmic_flops=k_fl, algorithmic_bytes=k_b)
+        roofs[kind] = r
+    dominant = max(roofs, key=lambda kk: roofs[kk]["share_of_step"])
+    roof = dict(roofs[dominant])
+    roof["kind"] = dominant
     dtype = {"bf16": "bf16", "mxfp8": "mxfp8 (e4m3 x e4m3, e8m0 scales per 32)",
              "fp8w": "e4m3 weights (fp32 tile scales) x bf16"}[cfg.precision]
     line = {
@@ -523,6 +574,7 @@ def main():
         "backward_tflops": (fl["ffn_bwd"] + fl["router_bwd"]) / bwd_s / 1e12,
         "per_call_ms": per_call,
         "roofline": roof,
+        "roofline_by_kind": roofs,
         "e2e": {"value": res["e2e"][0], "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": launches_per_step(cfg) * args.steps,

@@ -448,6 +448,38 @@ MOE_API moe_status_t moe_permute_noalloc(const moe_desc_t* d, const void* x, con
                                          const int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row,
                                          void* x_perm, void* stream);
 
+/* ---------------------------------------------------------- kernel timing --
+ * Per-kernel timing of the grouped GEMMs (no counterpart in the pages; a
+ * measurement aid of this library).  While enabled, every grouped-GEMM
+ * launch of the entry points above is bracketed by two CUDA events recorded
+ * on its stream, and its kind is noted:
+ *   MOE_TIMING_GATE     router logits GEMM (moe_route);
+ *   MOE_TIMING_FFN_FWD  expert GEMMs of the forward: GEMM1 (w1|w3 + SwiGLU)
+ *                       and GEMM2 (w2), routed and shared, every precision;
+ *   MOE_TIMING_DGRAD    data-gradient GEMMs of the backward (through w2 with
+ *                       the SwiGLU derivative, through w1|w3);
+ *   MOE_TIMING_WGRAD    weight-gradient GEMMs (dW1, dW3, dW2, routed and
+ *                       shared).
+ * The events are host driver objects (no device memory) that
+ * moe_timing_enable creates, `capacity` pairs of them (1 .. 2^20), after
+ * clearing earlier records; launches past the capacity, and launches on a
+ * stream that is capturing a graph, are counted as untimed.  The recorded
+ * events add two tiny commands per launch to the stream and nothing else.
+ * moe_timing_read waits for the recorded events of `kind` (a host
+ * synchronisation, unlike every other entry point) and returns the sum of
+ * their elapsed times in milliseconds, the number of timed launches and
+ * (nullable) the number of untimed ones since moe_timing_enable.
+ * moe_timing_disable stops timing and destroys the events.  Process-wide
+ * state; enable, read and disable must not race with launches from other
+ * host threads. */
+#define MOE_TIMING_GATE 0
+#define MOE_TIMING_FFN_FWD 1
+#define MOE_TIMING_DGRAD 2
+#define MOE_TIMING_WGRAD 3
+MOE_API moe_status_t moe_timing_enable(int32_t capacity);
+MOE_API moe_status_t moe_timing_read(int32_t kind, double* total_ms, int64_t* launches, int64_t* untimed);
+MOE_API moe_status_t moe_timing_disable(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -92,6 +92,10 @@ SIGNATURES = {
     "moe_backward_mxfp8": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, ctypes.POINTER(MoeExpertWeightsMx),
                                    ctypes.POINTER(MoeFwdState), c_vp, ctypes.POINTER(MoeGrads), c_vp,
                                    ctypes.c_size_t, c_vp]),
+    "moe_timing_enable": (c_i32, [c_i32]),
+    "moe_timing_read": (c_i32, [c_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                ctypes.POINTER(ctypes.c_int64)]),
+    "moe_timing_disable": (c_i32, []),
 }
 
 _LIB = None

@@ -218,6 +218,29 @@ def moe_monitor_stats(counts_hist, stats, stream=None):
         e, _p(counts_hist, I32, (h, e), "counts_hist"), h, _p(stats, F32, (3,), "stats"), _s(stream)))
 
 
+# --------------------------------------------------------------- kernel timing
+TIMING_KINDS = {"gate": 0, "ffn_fwd": 1, "dgrad": 2, "wgrad": 3}
+
+
+def moe_timing_enable(capacity: int = 4096):
+    """Start timing the library's grouped-GEMM launches with CUDA events
+    (``capacity`` launches at most; earlier records are cleared)."""
+    _check("moe_timing_enable", _lib.load().moe_timing_enable(capacity))
+
+
+def moe_timing_read(kind: str) -> tuple[float, int, int]:
+    """(total milliseconds, timed launches, untimed launches) of one kind of
+    grouped GEMM since moe_timing_enable; waits for the recorded events."""
+    ms, n, u = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
+    _check("moe_timing_read", _lib.load().moe_timing_read(TIMING_KINDS[kind], ctypes.byref(ms), ctypes.byref(n),
+                                                          ctypes.byref(u)))
+    return ms.value, n.value, u.value
+
+
+def moe_timing_disable():
+    _check("moe_timing_disable", _lib.load().moe_timing_disable())
+
+
 def moe_update_bias(desc, counts, bias, gamma: float, mode: int = 0, stream=None):
     _check("moe_update_bias", _lib.load().moe_update_bias(
         ctypes.byref(desc), _p(counts, I32, (desc.n_exp,), "counts"), _p(bias, F32, (desc.n_exp,), "bias"),

@@ -11,6 +11,7 @@
 #include "grouped_gemm.cuh"
 #include "moe_kernels.cuh"
 #include "mxfp8.cuh"
+#include "timing.cuh"
 
 namespace {
 
@@ -124,6 +125,11 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
   } while (0)
 #define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
 
+// Grouped-GEMM launch, timed under its kind while moe_timing is enabled.
+cudaError_t gemm(int kind, const GemmArgs& a, cudaStream_t st) {
+  return moe::timed(kind, st, [&] { return moe::launch_grouped_gemm(a, st); });
+}
+
 bool all16(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
     if (!p || !aligned16(p)) return false;
@@ -176,7 +182,7 @@ moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, 
   g1.out2 = a3;
   g1.ld_out = F;
   g1.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g1, st));
+  MOE_CUDA(gemm(moe::TIMING_FFN_FWD, g1, st));
   GemmArgs g2;
   g2.w8 = w8;
   g2.w8_scale[0] = s2;
@@ -191,7 +197,7 @@ moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, 
   g2.out0 = y;
   g2.ld_out = D;
   g2.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g2, st));
+  MOE_CUDA(gemm(moe::TIMING_FFN_FWD, g2, st));
   return MOE_OK;
 }
 
@@ -221,7 +227,7 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
   g.out1 = da3;
   g.ld_out = F;
   g.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+  MOE_CUDA(gemm(moe::TIMING_DGRAD, g, st));
 
   GemmArgs w;
   w.epi = moe::EPI_F32;
@@ -238,7 +244,7 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
   w.out0 = dw2;
   w.ld_out = F;
   w.group_stride_out = static_cast<int64_t>(D) * F;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
 
   // dx_rows = da1 w1_e + da3 w3_e (the dYw buffer may be reused as dx_rows)
   GemmArgs d;
@@ -260,7 +266,7 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
   d.out0 = dx_rows;
   d.ld_out = D;
   d.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(d, st));
+  MOE_CUDA(gemm(moe::TIMING_DGRAD, d, st));
 
   // dW1_e [F,D] = da1_e^T x_e, dW3_e = da3_e^T x_e
   w.a[0] = act(da1, rows, F);
@@ -270,10 +276,10 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
   w.out0 = dw1;
   w.ld_out = D;
   w.group_stride_out = static_cast<int64_t>(F) * D;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
   w.a[0] = act(da3, rows, F);
   w.out0 = dw3;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
   return MOE_OK;
 }
 
@@ -351,7 +357,7 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
   g.out0 = logits;
   g.ld_out = d->n_exp;
   g.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+  MOE_CUDA(gemm(moe::TIMING_GATE, g, st));
   return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, status, st);
 }
 
@@ -573,7 +579,7 @@ moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, in
   g1.s_ld = moe::mx_scale_ld(rows);
   g1.ld_out = F;
   g1.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g1, st));
+  MOE_CUDA(gemm(moe::TIMING_FFN_FWD, g1, st));
   GemmArgs g2;
   g2.quant = true;
   g2.epi = moe::EPI_BF16;
@@ -587,7 +593,7 @@ moe_status_t ffn_pair_mx(const void* aq, const void* as, int64_t rows, int D, in
   g2.out0 = y;
   g2.ld_out = D;
   g2.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g2, st));
+  MOE_CUDA(gemm(moe::TIMING_FFN_FWD, g2, st));
   return MOE_OK;
 }
 // Workspace scratch of one MXFP8 backward expert set.
@@ -627,7 +633,7 @@ moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t*
   g.out1 = da3;
   g.ld_out = F;
   g.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(g, st));
+  MOE_CUDA(gemm(moe::TIMING_DGRAD, g, st));
 
   // weight-gradient operands: blocks of 32 tokens per expert, transposed
   MOE_CUDA(moe::launch_pad_offsets(offsets, groups, q.pad, st));
@@ -653,7 +659,7 @@ moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t*
   w.out0 = dw2;
   w.ld_out = F;
   w.group_stride_out = static_cast<int64_t>(D) * F;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
 
   // da1, da3 row-wise along F; dx_rows = da1 w1 + da3 w3 (dYw is no longer read)
   MOE_CUDA(moe::launch_mx_quant_rows(da1, nullptr, 1, rows, F, rows, ldr, q.q_da1, q.q_da1s, st));
@@ -674,7 +680,7 @@ moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t*
   d.out0 = dx_rows;
   d.ld_out = D;
   d.status = status;
-  MOE_CUDA(moe::launch_grouped_gemm(d, st));
+  MOE_CUDA(gemm(moe::TIMING_DGRAD, d, st));
 
   // dW1_e [F,D] = da1_e^T x_e, dW3_e = da3_e^T x_e
   MOE_CUDA(tquant(da1, nullptr, 1, F, q.t_f0, q.t_f0s));
@@ -687,10 +693,10 @@ moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t*
   w.out0 = dw1;
   w.ld_out = D;
   w.group_stride_out = static_cast<int64_t>(F) * D;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
   w.qa[0] = moe::MxOperand{q.t_f1, q.t_f1s, F, q.rp, 1, ld16(F)};
   w.out0 = dw3;
-  MOE_CUDA(moe::launch_grouped_gemm(w, st));
+  MOE_CUDA(gemm(moe::TIMING_WGRAD, w, st));
   return MOE_OK;
 }
 }  // namespace

@@ -125,3 +125,17 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.moe_status_string(code)
     assert lib.moe_abi_version() == 1
+
+
+def test_timing_entry_points_validate_on_host(lib):
+    import ctypes as ct
+    ms, n, u = ct.c_double(), ct.c_int64(), ct.c_int64()
+    assert lib.moe_timing_enable(0) == 1                  # capacity out of range
+    assert lib.moe_timing_enable((1 << 20) + 1) == 1
+    assert lib.moe_timing_read(4, ct.byref(ms), ct.byref(n), None) == 1     # unknown kind
+    assert lib.moe_timing_read(-1, ct.byref(ms), ct.byref(n), None) == 1
+    assert lib.moe_timing_read(3, None, ct.byref(n), None) == 1
+    assert lib.moe_timing_disable() == 0
+    # nothing recorded: zero time, zero launches
+    assert lib.moe_timing_read(3, ct.byref(ms), ct.byref(n), ct.byref(u)) == 0
+    assert (ms.value, n.value, u.value) == (0.0, 0, 0)
