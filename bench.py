@@ -135,9 +135,10 @@ def launches_per_step(cfg) -> int:
         # route 4; permute: 3 map kernels + row quantiser (+ token quantiser for the shared expert);
         # grouped FFN: GEMM1, GEMM2 (+ dense offsets, GEMM1, GEMM2); combine
         fwd = 4 + 4 + 2 + 1 + (4 if cfg.n_shared else 0)
-        # per expert set: 3 row-wise quantisers, pad offsets, 5 transposing quantisers, 5 GEMMs
-        per_set = 3 + 1 + 5 + 5
-        bwd = 1 + per_set + (1 + per_set if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
+        # per expert set: row-wise quantisers of dYw (fused into the combine backward for the routed
+        # experts), da1, da3; pad offsets, 5 transposing quantisers, 5 GEMMs
+        per_set = 2 + 1 + 5 + 5
+        bwd = 1 + per_set + (1 + per_set + 1 if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
         return fwd + bwd + (1 if cfg.use_bias else 0)
     fwd = 4 + 4 + 2 + 1          # route: dense offsets, gate GEMM, top-K, scan; permute: 3 map kernels + rows;
     if cfg.n_shared:             # grouped FFN: GEMM1, GEMM2; combine

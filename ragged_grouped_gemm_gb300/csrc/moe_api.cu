@@ -613,10 +613,12 @@ moe_status_t ffn_pair_bwd_mx(const void* dyw, const void* x_rows, const int32_t*
                              const int32_t* offsets, const void* w1t, const void* w1ts, const void* w3t,
                              const void* w3ts, const void* w2t, const void* w2ts, void* da1, void* da3,
                              void* dx_rows, float* dw1, float* dw3, float* dw2, const MxBwdScratch& q,
-                             int32_t* status, cudaStream_t st) {
+                             int32_t* status, cudaStream_t st, bool dyw_quantized = false) {
   const int64_t ldr = moe::mx_scale_ld(rows);
-  // dYw row-wise along D; dh = dYw w2 with the SwiGLU derivative -> da1, da3 (bf16)
-  MOE_CUDA(moe::launch_mx_quant_rows(dyw, nullptr, 1, rows, D, rows, ldr, q.q_dy, q.q_dys, st));
+  // dYw row-wise along D (unless the combine backward already wrote these
+  // codes); dh = dYw w2 with the SwiGLU derivative -> da1, da3 (bf16)
+  if (!dyw_quantized)
+    MOE_CUDA(moe::launch_mx_quant_rows(dyw, nullptr, 1, rows, D, rows, ldr, q.q_dy, q.q_dys, st));
   GemmArgs g;
   g.quant = true;
   g.epi = moe::EPI_SWIGLU_BWD;
@@ -787,12 +789,13 @@ moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const m
                  at<uint8_t>(ws, L.t_d1), at<uint8_t>(ws, L.t_d1s), at<uint8_t>(ws, L.t_f0),
                  at<uint8_t>(ws, L.t_f0s), at<uint8_t>(ws, L.t_f1), at<uint8_t>(ws, L.t_f1s)};
 
+  // dYw and, fused, its row-wise MXFP8 codes along D
   MOE_CUDA(moe::launch_combine_bwd(N, D, K, d->gate, dy, s->y_perm, s->row_of_copy, s->topk_w, s->logits, E,
-                                   s->topk_idx, dyw, dg, dl, st));
+                                   s->topk_idx, dyw, dg, dl, st, q.q_dy, q.q_dys, moe::mx_scale_ld(R)));
   // routed experts (x read in permuted order through copy_of_row); dx_perm overwrites dYw
   MOE_TRY(ffn_pair_bwd_mx(dyw, s->x, s->copy_of_row, K, s->a1, s->a3, s->h, R, D, F, E, s->offsets, wt->w1,
                           wt->w1_scale, wt->w3, wt->w3_scale, wt->w2, wt->w2_scale, at<void>(ws, L.da1),
-                          at<void>(ws, L.da3), dyw, g->dw1, g->dw3, g->dw2, q, status, st));
+                          at<void>(ws, L.da3), dyw, g->dw1, g->dw3, g->dw2, q, status, st, true));
   void* dxs = nullptr;
   if (d->n_shared) {
     int32_t* dense = at<int32_t>(ws, L.dense_off);

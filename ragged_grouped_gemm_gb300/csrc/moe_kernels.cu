@@ -12,6 +12,7 @@
 // statistics, update_balance_bias), §12.5 sort by destination / bincount /
 // unsort and K-sum.
 #include "moe_kernels.cuh"
+#include "mx_device.cuh"
 #include "sm100_ptx.cuh"
 
 #include <cuda_bf16.h>
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
                                                           const float* __restrict__ logits,
                                                           const int32_t* __restrict__ topk_idx,
                                                           uint4* __restrict__ dyw, float* __restrict__ dg_out,
-                                                          float* __restrict__ dl_out) {
+                                                          float* __restrict__ dl_out, uint8_t* __restrict__ q_codes,
+                                                          uint8_t* __restrict__ q_scales, int64_t q_ld) {
   __shared__ int s_rows[kMaxK];
   __shared__ float s_w[kMaxK];
   __shared__ float s_part[8][kMaxK];
@@ -345,15 +347,31 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
     float part[kMaxK];
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) part[k] = 0.0f;
-    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
+    // A warp covers 32 consecutive 8-column chunks per pass and stays
+    // converged (the pass count is uniform per warp), so with q_codes the
+    // four lanes of each 32-column block combine their block maxima by
+    // shuffles.
+    for (int i0 = warp * 32; i0 < d8; i0 += blockDim.x) {
+      const int i = i0 + lane;
+      const bool act = i < d8;
       float g8[8];
-      unpack8(dy[static_cast<int64_t>(t) * d8 + i], g8);
+      if (act) {
+        unpack8(dy[static_cast<int64_t>(t) * d8 + i], g8);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g8[j] = 0.0f;
+      }
 #pragma unroll
       for (int k = 0; k < kMaxK; ++k) {
         if (k < K && s_rows[k] >= 0) {   // a dropped copy has no row and dg = 0
           const int64_t r = s_rows[k];
           float y[8], o[8];
-          unpack8(y_perm[r * d8 + i], y);
+          if (act) {
+            unpack8(y_perm[r * d8 + i], y);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = 0.0f;
+          }
           const float w = s_w[k];
           float acc = 0.0f;
 #pragma unroll
@@ -362,7 +380,24 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
             o[j] = w * g8[j];
           }
           part[k] += acc;
-          dyw[r * d8 + i] = pack8(o);
+          const uint4 packed = pack8(o);
+          if (act) dyw[r * d8 + i] = packed;
+          if (q_codes) {
+            // MXFP8 copy of the stored (bf16) dYw row along D
+            float v[8];
+            unpack8(packed, v);
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int e = mx_scale_exponent(amax);
+            if (act) {
+              *reinterpret_cast<uint2*>(q_codes + r * (8 * static_cast<int64_t>(d8)) + 8 * i) =
+                  mx_encode8(v, mx_inv_scale(e));
+              if ((i & 3) == 0) q_scales[static_cast<int64_t>(i >> 2) * q_ld + r] = static_cast<uint8_t>(e + 127);
+            }
+          }
         }
       }
     }
@@ -681,12 +716,13 @@ cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, cons
 
 cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void* dy, const void* y_perm,
                                const int32_t* row_of_copy, const float* topk_w, const float* logits, int n_exp,
-                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st) {
+                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st,
+                               uint8_t* q_codes, uint8_t* q_scales, int64_t q_ld) {
   if (n_tok <= 0) return cudaSuccess;
-  if (top_k > kMaxK) return cudaErrorInvalidValue;
+  if (top_k > kMaxK || (q_codes && (d % 32 != 0 || !q_scales))) return cudaErrorInvalidValue;
   combine_bwd_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
       n_tok, d / 8, top_k, gate, n_exp, static_cast<const uint4*>(dy), static_cast<const uint4*>(y_perm),
-      row_of_copy, topk_w, logits, topk_idx, static_cast<uint4*>(dyw), dg, dl);
+      row_of_copy, topk_w, logits, topk_idx, static_cast<uint4*>(dyw), dg, dl, q_codes, q_scales, q_ld);
   return cudaGetLastError();
 }
 

@@ -38,9 +38,13 @@ cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, cons
 cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, const int32_t* row_of_copy,
                            const float* topk_w, const void* y_shared, void* out, cudaStream_t st);
 // dYw[row] = bf16(g * dY[t]); dg[t,k] = <dY[t], y_perm[row]>; dl[t,k] = router logit gradient.
+// With q_codes, also the MXFP8 codes [R, D] of the bf16 dYw rows along D and
+// their scale bytes q_scales[(col / 32) * q_ld + row] (the row-wise layout of
+// launch_mx_quant_rows with one group).
 cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void* dy, const void* y_perm,
                                const int32_t* row_of_copy, const float* topk_w, const float* logits, int n_exp,
-                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st);
+                               const int32_t* topk_idx, void* dyw, float* dg, float* dl, cudaStream_t st,
+                               uint8_t* q_codes = nullptr, uint8_t* q_scales = nullptr, int64_t q_ld = 0);
 // dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r] (fp32).
 // x_rows is x_perm [R,D] (gather_k = 0) or x [N,D] read in permuted order,
 // row r = x[copy_of_row[r] / gather_k] (gather_k = top_k).

@@ -13,16 +13,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "mx_device.cuh"
+
 namespace moe {
 namespace {
-
-__device__ __forceinline__ int mx_scale_exponent(float amax) {
-  if (!(amax > 0.0f)) return -127;
-  const uint32_t b = __float_as_uint(amax);
-  const int ex = static_cast<int>(b >> 23);
-  const int fl = ex ? ex - 127 : -149 + (31 - __clz(static_cast<int>(b)));
-  return max(-127, min(127, fl - 8));
-}
 
 __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16* __restrict__ src,
                                                             const int32_t* __restrict__ src_row_of, int src_div,
