@@ -41,11 +41,14 @@ def _status_ok(ws):
     assert bits == 0, f"device status {bits} (site {site})"
 
 
-@pytest.fixture(params=["1", "0"], ids=["cta_pair", "one_sm"])
+@pytest.fixture(params=[("1", "1"), ("1", "0"), ("0", "1")], ids=["cta_quad", "cta_pair", "one_sm"])
 def gemm_form(request, monkeypatch):
-    """Runs a test with the grouped GEMMs forced to the 2-SM (CTA pair) or the
-    one-SM form; by default the library picks the form from the group sizes."""
-    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", request.param)
+    """Runs a test with the grouped GEMMs forced to the 2-SM (CTA pair) form,
+    with the weight gradients in clusters of two pairs sharing B (quad) or in
+    single pairs, or to the one-SM form; by default the library picks the
+    form from the group sizes."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", request.param[0])
+    monkeypatch.setenv("MOE_GEMM_QUAD", request.param[1])
     return request.param
 
 
