@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, in
 }
 
 // ------------------------------------------------------------ combine
+template <int NB>   // copies whose loads are issued together
 __global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, const uint4* __restrict__ y_perm,
                                                       const int32_t* __restrict__ row_of_copy,
                                                       const float* __restrict__ topk_w,
@@ -301,13 +302,25 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, 
     __syncthreads();
     for (int i = threadIdx.x; i < d8; i += blockDim.x) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int k = 0; k < K; ++k) {
-        if (s_rows[k] < 0) continue;   // dropped copy (capacity mode): no expert output
-        float y[8];
-        unpack8(y_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], y);
-        const float w = s_w[k];
+      // NB copies' loads in flight at once; a dropped copy (capacity mode)
+      // or a slot past K adds 0 * 0, which leaves acc unchanged (acc, a sum
+      // started at +0, is never -0)
+      for (int k0 = 0; k0 < K; k0 += NB) {
+        uint4 u[NB];
+        float wk[NB];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, y[j], acc[j]);
+        for (int j = 0; j < NB; ++j) {
+          const int r = k0 + j < K ? s_rows[k0 + j] : -1;
+          u[j] = r >= 0 ? y_perm[static_cast<int64_t>(r) * d8 + i] : make_uint4(0, 0, 0, 0);
+          wk[j] = r >= 0 ? s_w[k0 + j] : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          float y[8];
+          unpack8(u[j], y);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) acc[jj] = fmaf(wk[j], y[jj], acc[jj]);
+        }
       }
       if (y_shared) {
         float y[8];
@@ -323,7 +336,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, 
 // ------------------------------------------------------------ combine backward
 constexpr int kMaxK = 32;
 
-__global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int K, int gate, int E,
+template <int NB>
+__global__ void __launch_bounds__(256, 3) combine_bwd_kernel(int n_tok, int d8, int K, int gate, int E,
                                                           const uint4* __restrict__ dy,
                                                           const uint4* __restrict__ y_perm,
                                                           const int32_t* __restrict__ row_of_copy,
@@ -361,17 +375,23 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int n_tok, int d8, int
 #pragma unroll
         for (int j = 0; j < 8; ++j) g8[j] = 0.0f;
       }
+      // copies in groups of NB: their y_perm loads are issued together
 #pragma unroll
-      for (int k = 0; k < kMaxK; ++k) {
-        if (k < K && s_rows[k] >= 0) {   // a dropped copy has no row and dg = 0
+      for (int k0 = 0; k0 < kMaxK; k0 += NB) {
+        if (k0 >= K) break;
+        uint4 u[NB];
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          const int rr = k0 + c < K ? s_rows[k0 + c] : -1;
+          u[c] = (act && rr >= 0) ? y_perm[static_cast<int64_t>(rr) * d8 + i] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          const int k = k0 + c;
+          if (k >= K || s_rows[k] < 0) continue;   // a dropped copy has no row and dg = 0
           const int64_t r = s_rows[k];
           float y[8], o[8];
-          if (act) {
-            unpack8(y_perm[r * d8 + i], y);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) y[j] = 0.0f;
-          }
+          unpack8(u[c], y);
           const float w = s_w[k];
           float acc = 0.0f;
 #pragma unroll
@@ -543,6 +563,7 @@ __global__ void __launch_bounds__(256) dwg_reduce_kernel(int E, int d, const int
 }
 
 // ------------------------------------------------------------ unpermute-sum of dx
+template <int NB>
 __global__ void __launch_bounds__(256) unpermute_dx_kernel(int n_tok, int d8, int K, const uint4* __restrict__ dx_perm,
                                                            const int32_t* __restrict__ row_of_copy,
                                                            const float* __restrict__ dl,
@@ -564,20 +585,41 @@ __global__ void __launch_bounds__(256) unpermute_dx_kernel(int n_tok, int d8, in
     __syncthreads();
     for (int i = threadIdx.x; i < d8; i += blockDim.x) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int k = 0; k < K; ++k) {
-        if (s_rows[k] < 0) continue;   // dropped copy: no expert gradient
-        float v[8];
-        unpack8(dx_perm[static_cast<int64_t>(s_rows[k]) * d8 + i], v);
+      // NB copies' loads in flight at once; a dropped copy (no expert
+      // gradient) or a slot past K adds +0, which leaves acc unchanged (acc,
+      // a sum started at +0, is never -0)
+      for (int k0 = 0; k0 < K; k0 += NB) {
+        uint4 u[NB];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += v[j];
+        for (int j = 0; j < NB; ++j) {
+          const int r = k0 + j < K ? s_rows[k0 + j] : -1;
+          u[j] = r >= 0 ? dx_perm[static_cast<int64_t>(r) * d8 + i] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          float v[8];
+          unpack8(u[j], v);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) acc[jj] += v[jj];
+        }
       }
       if (w_gate && dl) {
-        for (int k = 0; k < K; ++k) {
-          float v[8];
-          unpack8(w_gate[static_cast<int64_t>(s_e[k]) * d8 + i], v);
-          const float w = s_dl[k];
+        for (int k0 = 0; k0 < K; k0 += NB) {
+          uint4 u[NB];
+          float wk[NB];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, v[j], acc[j]);
+          for (int j = 0; j < NB; ++j) {
+            const bool in = k0 + j < K;
+            u[j] = in ? w_gate[static_cast<int64_t>(s_e[k0 + j]) * d8 + i] : make_uint4(0, 0, 0, 0);
+            wk[j] = in ? s_dl[k0 + j] : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            float v[8];
+            unpack8(u[j], v);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc[jj] = fmaf(wk[j], v[jj], acc[jj]);
+          }
         }
       }
       if (dx_shared) {
@@ -708,9 +750,9 @@ cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, cons
 cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, const int32_t* row_of_copy,
                            const float* topk_w, const void* y_shared, void* out, cudaStream_t st) {
   if (n_tok <= 0) return cudaSuccess;
-  combine_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(y_perm),
-                                                         row_of_copy, topk_w, static_cast<const uint4*>(y_shared),
-                                                         static_cast<uint4*>(out));
+  auto kern = top_k == 1 ? combine_kernel<1> : (top_k == 2 ? combine_kernel<2> : combine_kernel<4>);
+  kern<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(y_perm), row_of_copy,
+                                               topk_w, static_cast<const uint4*>(y_shared), static_cast<uint4*>(out));
   return cudaGetLastError();
 }
 
@@ -720,7 +762,8 @@ cudaError_t launch_combine_bwd(int n_tok, int d, int top_k, int gate, const void
                                uint8_t* q_codes, uint8_t* q_scales, int64_t q_ld) {
   if (n_tok <= 0) return cudaSuccess;
   if (top_k > kMaxK || (q_codes && (d % 32 != 0 || !q_scales))) return cudaErrorInvalidValue;
-  combine_bwd_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
+  auto kern = top_k == 1 ? combine_bwd_kernel<1> : (top_k == 2 ? combine_bwd_kernel<2> : combine_bwd_kernel<4>);
+  kern<<<grid_for_tokens(n_tok), 256, 0, st>>>(
       n_tok, d / 8, top_k, gate, n_exp, static_cast<const uint4*>(dy), static_cast<const uint4*>(y_perm),
       row_of_copy, topk_w, logits, topk_idx, static_cast<uint4*>(dyw), dg, dl, q_codes, q_scales, q_ld);
   return cudaGetLastError();
@@ -750,7 +793,8 @@ cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm
                                 const float* dl, const int32_t* topk_idx, const void* w_gate,
                                 const void* dx_shared, void* dx, cudaStream_t st) {
   if (n_tok <= 0) return cudaSuccess;
-  unpermute_dx_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(
+  auto kern = top_k == 1 ? unpermute_dx_kernel<1> : (top_k == 2 ? unpermute_dx_kernel<2> : unpermute_dx_kernel<4>);
+  kern<<<grid_for_tokens(n_tok), 256, 0, st>>>(
       n_tok, d / 8, top_k, static_cast<const uint4*>(dx_perm), row_of_copy, dl, topk_idx,
       static_cast<const uint4*>(w_gate), static_cast<const uint4*>(dx_shared), static_cast<uint4*>(dx));
   return cudaGetLastError();
