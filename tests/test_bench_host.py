@@ -1,0 +1,57 @@
+"""bench.py's host-side pieces on CPU: the reference arm's JSON line (the
+oracle timed on a token sample), the per-kind algorithmic work used for the
+roofline, and the launch counts."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8", "fp8w"])
+def test_reference_arm_prints_one_contract_line(precision):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny", "--precision", precision, "--steps", "1", "--warmup", "0", "--sample", "16"],
+                         capture_output=True, text=True, check=True, cwd=ROOT, timeout=300).stdout
+    lines = [x for x in out.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert ("mxfp8" in d["config"]["workload"]) == (precision == "mxfp8")
+
+
+def test_kind_work_matches_the_flop_count():
+    sys.path.insert(0, ROOT)
+    import bench
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS
+    for name in ("mixtral", "dsv3"):
+        cfg = CONFIGS[name]
+        fl = bench.flops(cfg)
+        total = sum(bench.kind_work(cfg, k, cfg.n_exp)[0] for k in ("ffn_fwd", "dgrad", "wgrad"))
+        assert total == pytest.approx(fl["ffn_fwd"] + fl["ffn_bwd"])
+        # weight gradients write fp32 dW for every expert: at least 3 E D F 4 bytes
+        _, b = bench.kind_work(cfg, "wgrad", cfg.n_exp)
+        assert b >= 3 * cfg.n_exp * cfg.d_model * cfg.d_ff * 4
+        # MXFP8 operands move fewer bytes than bf16 ones
+        mx = cfg.replace(precision="mxfp8")
+        assert bench.kind_work(mx, "ffn_fwd", cfg.n_exp)[1] < bench.kind_work(cfg, "ffn_fwd", cfg.n_exp)[1]
+
+
+def test_launch_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS
+    mix, ds = CONFIGS["mixtral"], CONFIGS["dsv3"]
+    # forward 11 (route 4, permute 4, GEMM1, GEMM2, combine) + backward 10 (combine bwd, 5 GEMMs, unpermute,
+    # router gradient 3)
+    assert bench.launches_per_step(mix) == 21
+    # + shared expert (3 forward, 6 backward) + route-bias update
+    assert bench.launches_per_step(ds) == 21 + 3 + 6 + 1
