@@ -66,6 +66,9 @@ CONFIGS = {
     # profiling case: the Mixtral layer with a quarter of d_ff (about 3 GB on
     # the device, operands still far larger than L2)
     "mixtral_quarter": MoEConfig("mixtral_quarter", 4096, 4096, 3584, 8, 2),
+    # profiling case: DeepSeek-V3 expert shapes (~128 rows per expert) on 16
+    # experts (0.7 GB of weights, 0.94 GB of fp32 output per weight gradient)
+    "dsv3_e16": MoEConfig("dsv3_e16", 256, 7168, 2048, 16, 8, gate="sigmoid", use_bias=True),
     # mid-size parity cases: several tiles in every GEMM dimension, ragged tails
     "small_softmax": MoEConfig("small_softmax", 1000, 256, 384, 8, 2),
     "small_sigmoid": MoEConfig("small_sigmoid", 777, 512, 256, 16, 4, gate="sigmoid",
