@@ -23,12 +23,18 @@
 // (B columns 0..BN/2-1 in rank 0, the rest in rank 1), so each SM streams
 // half of the B bytes it would need alone.  Rank 0's MMA lane issues for the
 // pair and its commits arrive on both CTAs' stage-release and
-// accumulator-ready barriers (multicast).  Ragged M: both CTAs' TMA loads
-// complete on rank 0's stage barrier.  Ragged K: each CTA's loads complete on
-// its own barrier; the peer's idle MMA warp zeroes its rows past the group's
-// end and forwards the stage to rank 0.  Each CTA's epilogue reads its own
-// 128 TMEM lanes and signals rank 0's accumulator-free barrier.  TMEM is
-// allocated and freed by both CTAs together, between cluster barriers.
+// accumulator-ready barriers (multicast).  Both CTAs' TMA loads complete on
+// rank 0's stage barrier, except (ragged K) a k-block whose group ends off a
+// 16-row boundary: that one lands on each CTA's own barrier, and the peer's
+// idle MMA warp zeroes its rows past the group's end and forwards the stage
+// to rank 0.  Each CTA's epilogue reads its own 128 TMEM lanes and signals
+// rank 0's accumulator-free barrier.  TMEM is allocated and freed by both
+// CTAs together, between cluster barriers.  QUAD (ragged K, optional): two
+// pairs in a 4-CTA cluster share the B operand by TMA multicast.
+//
+// fp32 outputs leave through TMA tensor stores: each epilogue warp stages
+// 16 rows x 32 columns (whole 128-byte rows) at a time in 2 KB of shared
+// memory, or 32 x 16 when a tile's column halves are 16 wide.
 //
 // Shared-memory operand layouts (both 1024-byte aligned per stage):
 //   K-major : rows of 64 bf16 (128 B), 8-row swizzle atoms of 1024 B;
@@ -1191,8 +1197,8 @@ bool make_map(CUtensorMap* map, const Operand& op, uint32_t box_cols, uint32_t b
   return r == CUDA_SUCCESS;
 }
 
-// fp32 output map {n, m, groups} with a 16x32 box and 64-byte swizzle, for
-// the TMA-store epilogue.  False when the layout is not TMA-compatible.
+// fp32 output map {n, m, groups} for the TMA-store epilogue (box shape and
+// swizzle below).  False when the layout is not TMA-compatible.
 bool make_out_map_f32(CUtensorMap* map, void* base, int64_t n, int64_t m, int64_t groups, int64_t ld,
                       int64_t group_stride, bool wide) {
   EncodeFn enc = get_encode_fn();
