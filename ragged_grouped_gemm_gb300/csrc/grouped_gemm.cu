@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <mutex>
 
@@ -80,6 +81,7 @@ struct KParams {
   int32_t n_size;
   int32_t kb0, kb1;
   int32_t kblk;          // contraction elements per k-block (64 bf16, 128 MXFP8)
+  int32_t ksplit;        // ragged M, one group: contraction slices (tile-minor); 0 or 1 = none
   int32_t b_dual_n;
   int32_t tile_n;
   void* out0;
@@ -153,6 +155,8 @@ struct Tile {
   int rows_valid;  // valid output rows of this CTA's 128 (may be <= 0 in a CTA pair)
   int k_rows;      // ragged K: rows of the group (contraction length)
   int num_kb;
+  int kbeg;        // ragged M: first k-block of this tile's contraction slice
+  int split;       // ragged M: contraction slice (partial-output index)
 };
 
 // rank: the CTA's rank in its cluster; bit 0 picks its 128 rows of a pair
@@ -163,7 +167,13 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
   Tile t;
   constexpr int UR = PAIR ? 2 * BM : BM;   // rows of one M unit (a CTA pair covers 256)
   const int prank = rank & 1;
+  t.kbeg = 0;
+  t.split = 0;
   if (!RAGGED_K) {
+    if (p.ksplit > 1) {   // the slices of one output tile are adjacent in the tile order
+      t.split = tile % p.ksplit;
+      tile /= p.ksplit;
+    }
     // Expert-major raster: expert, then N tile, then M tile (innermost), so the
     // CTAs running at once share one expert's rows of A (L2-resident) and each
     // weight block is streamed from HBM once.  s_pre holds the prefix of
@@ -183,6 +193,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
     t.m0 = 0;
     t.k_rows = 0;
     t.num_kb = p.kb0 + p.kb1;
+    if (p.ksplit > 1) {   // slices of ceil(kb / ksplit) k-blocks; the host makes none empty
+      const int kbs = (t.num_kb + p.ksplit - 1) / p.ksplit;
+      t.kbeg = t.split * kbs;
+      t.num_kb = max(0, min(kbs, t.num_kb - t.kbeg));
+    }
   } else {
     const int mtiles = (p.m_size + UR - 1) / UR;
     const int munits = QUAD ? (mtiles + 1) / 2 : mtiles;   // a 4-CTA cluster takes two adjacent M tiles
@@ -370,7 +385,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
 
   int total_tiles;
   if (!RAGGED_K) {
-    total_tiles = s_pre[G];
+    total_tiles = s_pre[G] * (p.ksplit > 1 ? p.ksplit : 1);
   } else {
     constexpr int UR = PAIR ? 2 * BM : BM;
     const int mtiles = (p.m_size + UR - 1) / UR;
@@ -525,8 +540,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           }
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           if (!RAGGED_K) {
-            const int src = (kb < p.kb0) ? 0 : 1;
-            const int k0 = (src == 0 ? kb : kb - p.kb0) * BK;
+            const int kbg = t.kbeg + kb;   // k-block within the whole contraction
+            const int src = (kbg < p.kb0) ? 0 : 1;
+            const int k0 = (src == 0 ? kbg : kbg - p.kb0) * BK;
             tma_load_2d(sA, &p.tmA[src], &full[s], k0, t.row0);
             // B maps of the ragged-M form are always 3-D: {cols, rows, group}
             if (!B_MN) {
@@ -834,7 +850,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           grow = static_cast<int64_t>(t.m0) + r;
           obase += static_cast<int64_t>(t.g) * p.group_stride_out * (EPI == EPI_F32 ? 4 : 2);
         }
-        const bool zero = RAGGED_K && t.num_kb == 0;
+        const bool zero = t.num_kb == 0;
         const int c_begin = hf * (BN / 2);
         if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
           // Stage this warp's 32 rows x 32 columns as two 16-row halves in a
@@ -885,7 +901,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
                 const int row = (RAGGED_K ? t.m0 : t.row0) + q * 32 + 16 * h;
                 const int rows = RAGGED_K ? p.m_size : p.c_rows;
                 if (col < p.n_size && row < rows) {
-                  tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0, policy_evict_first());
+                  tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : t.split, policy_evict_first());
                   bulk_commit_group();
                 }
               }
@@ -932,7 +948,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
               const int row = RAGGED_K ? t.m0 + q * 32 : t.row0 + q * 32;
               const int rows = RAGGED_K ? p.m_size : p.c_rows;
               if (col < p.n_size && row < rows) {
-                tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : 0, policy_evict_first());
+                tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : t.split, policy_evict_first());
                 bulk_commit_group();
               }
             }
@@ -1313,6 +1329,13 @@ bool use_quad() {
 
 }  // namespace
 
+int gemm_ksplit(int64_t k, int requested) {
+  const int64_t kb = (k + BK - 1) / BK;
+  if (requested <= 1 || kb <= 1) return 1;
+  const int64_t per = (kb + requested - 1) / requested;   // k-blocks per slice
+  return static_cast<int>((kb + per - 1) / per);           // slices, none empty
+}
+
 int num_sms() {
   static int n = 0;
   static std::once_flag once;
@@ -1510,6 +1533,11 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
     const int64_t ur = pair ? 2 * BM : BM;
     tiles_ub = ntiles * ((a.max_rows + ur - 1) / ur + a.num_groups);
+    kp.ksplit = gemm_ksplit(a.k0, a.ksplit);
+    if (kp.ksplit > 1) {
+      if (a.epi != EPI_F32 || a.num_groups != 1 || pair || a.b_dual_n || kp.kb1 > 0) return cudaErrorInvalidValue;
+      tiles_ub *= kp.ksplit;
+    }
   } else {
     if (a.m_size <= 0) return cudaSuccess;
     if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
@@ -1525,10 +1553,11 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (a.epi == EPI_F32 && (a.ragged_k || a.num_groups == 1)) {
     const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
     const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
-    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : 1, a.ld_out, gs,
-                                (BN / 2) % 32 == 0) ? 1 : 0;
+    kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : std::max(1, kp.ksplit),
+                                a.ld_out, gs, (BN / 2) % 32 == 0) ? 1 : 0;
     kp.c_rows = static_cast<int32_t>(m);
   }
+  if (kp.ksplit > 1 && !kp.c_tma) return cudaErrorInvalidValue;   // partials leave through the TMA stores
   const int64_t u = tiles_ub;
 
   if (BN == 32) return launch_impl<32, false, false, EPI_F32>(kp, u, stream);

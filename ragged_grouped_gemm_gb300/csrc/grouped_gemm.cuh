@@ -55,6 +55,8 @@ struct GemmArgs {
   bool b_mn = false;          // B stored MN-major (data gradients)
   bool ragged_k = false;      // contraction over the group's rows
   int block_n = 256;          // 256, or 32 for narrow N (router logits)
+  int ksplit = 1;             // one group, fp32 out: the contraction in ksplit slices, out0 =
+                              // [ksplit][rows][ld_out] partial products (summed by the caller)
   EpiKind epi = EPI_BF16;
   Operand a[2];               // a[1]: second half of a split contraction
   Operand b[2];               // b[1]: second contraction half, or W3 half of the N tile
@@ -93,5 +95,8 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(const GemmArgs& args, cudaStream_t stream);
 
 int num_sms();
+// Contraction slices a launch with GemmArgs::ksplit = requested over k
+// elements actually uses (slices of whole 64-element k-blocks, none empty).
+int gemm_ksplit(int64_t k, int requested);
 
 }  // namespace moe

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -19,10 +20,13 @@ using moe::GemmArgs;
 using moe::Operand;
 
 constexpr size_t kAlign = 256;
+// The router logits GEMM has one 128-token tile per CTA; with few tiles its
+// contraction is cut into up to this many slices (summed in order after).
+constexpr int kGateSlices = 4;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, aux = 0, fwd_end = 0;
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, aux = 0, gpart = 0, fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
   // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
@@ -46,6 +50,7 @@ WsLayout layout(const moe_desc_t& d) {
   L.blk_counts = o; o = align_up(o + nch * E * 4);
   L.blk_base = o; o = align_up(o + nch * E * 4);
   L.aux = o; o = align_up(o + moe::aux_partial_floats(d.n_tok > 0 ? d.n_tok : 1, d.n_exp) * 4);
+  L.gpart = o; o = align_up(o + static_cast<size_t>(kGateSlices) * N * E * 4);   // router logit slices
   if (d.precision == 1) {
     L.hq = o; o = align_up(o + R * F);
     L.hs = o; o = align_up(o + F / 32 * moe::mx_scale_ld(R));
@@ -354,10 +359,17 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
   g.num_groups = 1;
   g.max_rows = d->n_tok;
   g.n_size = d->n_exp;
-  g.out0 = logits;
   g.ld_out = d->n_exp;
   g.status = status;
+  // more CTAs than 128-token tiles: contraction slices into the workspace, then their ordered sum
+  const int64_t tiles = (static_cast<int64_t>(d->n_tok) + 127) / 128 * ((d->n_exp + g.block_n - 1) / g.block_n);
+  const int64_t ne = static_cast<int64_t>(d->n_tok) * d->n_exp;
+  const int want = static_cast<int>(std::min<int64_t>(kGateSlices, moe::num_sms() / std::max<int64_t>(tiles, 1)));
+  g.ksplit = ne % 4 == 0 ? moe::gemm_ksplit(d->d_model, want) : 1;
+  float* part = at<float>(ws, L.gpart);
+  g.out0 = g.ksplit > 1 ? static_cast<void*>(part) : static_cast<void*>(logits);
   MOE_CUDA(gemm(moe::TIMING_GATE, g, st));
+  if (g.ksplit > 1) MOE_CUDA(moe::launch_sum_slices(part, g.ksplit, ne, logits, st));
   return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, status, st);
 }
 

@@ -17,6 +17,8 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 namespace moe {
 namespace {
 
@@ -453,6 +455,23 @@ __global__ void __launch_bounds__(256, 3) combine_bwd_kernel(int n_tok, int d8, 
   }
 }
 
+// out[i] = sum over s of part[s][i], slices added in order (fp32).
+__global__ void __launch_bounds__(256) sum_slices_kernel(const float4* __restrict__ part, int ks, int64_t n4,
+                                                         float4* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < ks; ++s) {
+      const float4 b = part[s * n4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    out[i] = a;
+  }
+}
+
 // ------------------------------------------------------------ router weight gradient
 // dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r].
 // Ragged and deterministic: every expert's rows are cut into 64-row chunks
@@ -744,6 +763,16 @@ cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, cons
   if (n_tok <= 0) return cudaSuccess;
   permute_rows_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(x),
                                                               row_of_copy, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_slices(const float* part, int ks, int64_t n, float* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (ks < 1 || n % 4) return cudaErrorInvalidValue;
+  const int64_t n4 = n / 4;
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, 4096));
+  sum_slices_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), ks, n4,
+                                            reinterpret_cast<float4*>(out));
   return cudaGetLastError();
 }
 

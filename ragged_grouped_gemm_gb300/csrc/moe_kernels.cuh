@@ -66,5 +66,7 @@ cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm
                                 const void* dx_shared, void* dx, cudaStream_t st);
 // dst[0] = 0, dst[1] = n (device offsets of a single dense group).
 cudaError_t launch_dense_offsets(int32_t* dst, int n, cudaStream_t st);
+// out[i] = sum_s part[s * n + i] for s = 0..ks-1 in order (fp32; n % 4 == 0, 16-byte aligned).
+cudaError_t launch_sum_slices(const float* part, int ks, int64_t n, float* out, cudaStream_t st);
 
 }  // namespace moe
