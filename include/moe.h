@@ -172,7 +172,10 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, int32_t* status_host,
 /* Router (§4.1, §4.3, §6.3, §9 step 1) and expert histogram (§9 step 4,
  * §12.5 bincount):
  *   logits[N,E] (fp32 out) = x[N,D] (bf16) * w_gate[E,D]^T  (tensor cores,
- *                            fp32 accumulation);
+ *                            fp32 accumulation; with few 128-token tiles the
+ *                            contraction runs in up to 4 slices whose fp32
+ *                            partial products, kept in the workspace, are
+ *                            added in slice order: deterministic);
  *   topk_idx[N,K] (out)    = the K experts with the largest
  *                            logits + bias (bias [E] fp32, NULL when the layer
  *                            has none), sorted by rank; equal keys: lower
