@@ -265,6 +265,8 @@ __global__ void __launch_bounds__(32) scatter_maps_kernel(int n_tok, int E, int 
       const int pos = base + rank;
       row_of_copy[c] = pos;
       copy_of_row[pos] = static_cast<int32_t>(c);
+    } else if (active) {
+      row_of_copy[c] = -1;   // expert index outside [0, E): no row (reported by block_hist_kernel)
     }
     __syncwarp();
   }
