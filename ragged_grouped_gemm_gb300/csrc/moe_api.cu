@@ -14,6 +14,8 @@
 #include "mxfp8.cuh"
 #include "timing.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace {
 
 using moe::GemmArgs;
@@ -134,6 +136,16 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 cudaError_t gemm(int kind, const GemmArgs& a, cudaStream_t st) {
   return moe::timed(kind, st, [&] { return moe::launch_grouped_gemm(a, st); });
 }
+
+// NVTX range around an entry point's enqueue work (a no-op unless a
+// profiler or tracer is attached to the process).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define MOE_RANGE(name) const NvtxRange moe_nvtx_range_(name)
 
 bool all16(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
@@ -338,6 +350,7 @@ static moe_status_t route_tail(const moe_desc_t* d, const float* logits, const f
 moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias, float* logits,
                        int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, void* ws,
                        size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_route");
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
   if (!all16({x, w_gate, logits}) || !topk_idx || !topk_w || !counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -376,6 +389,7 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
 moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, const float* bias,
                                    int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                    void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_route_from_logits");
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
   if (!logits || !topk_idx || !topk_w || !counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -390,6 +404,7 @@ moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, con
 moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
                          int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
                          void* stream) {
+  MOE_RANGE("moe_permute");
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
   if (!all16({x, x_perm}) || !topk_idx || !offsets || !row_of_copy || !copy_of_row) return MOE_ERR_INVALID_ARG;
@@ -406,6 +421,7 @@ moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk
 moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
                              const moe_expert_weights_t* w, const moe_ffn_saved_t* saved, void* y_perm,
                              void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_grouped_ffn");
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
   if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // MXFP8 operands: moe_grouped_ffn_mxfp8
@@ -435,6 +451,7 @@ moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int3
 
 moe_status_t moe_combine(const moe_desc_t* d, const void* y_perm, const int32_t* row_of_copy, const float* topk_w,
                          const void* y_shared, void* out, void* stream) {
+  MOE_RANGE("moe_combine");
   MOE_TRY(check_desc(d));
   if (!all16({y_perm, out}) || !row_of_copy || !topk_w) return MOE_ERR_INVALID_ARG;
   if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
@@ -516,6 +533,7 @@ extern "C" {
 moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_t* w,
                           const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
                           size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_backward");
   MOE_TRY(check_desc(d));
   if (d->precision != 0) return MOE_ERR_UNSUPPORTED;   // bf16 operands; moe_backward_mxfp8 / _fp8w otherwise
   return backward_impl(d, w_gate, w, nullptr, s, dy, g, ws, ws_bytes, stream);
@@ -524,6 +542,7 @@ moe_status_t moe_backward(const moe_desc_t* d, const void* w_gate, const moe_exp
 moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wq,
                                const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
                                size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_backward_fp8w");
   MOE_TRY(check_desc(d));
   if (d->precision != 2 || !wq) return MOE_ERR_INVALID_ARG;
   if (!wq->w1_scale || !wq->w3_scale || !wq->w2_scale) return MOE_ERR_INVALID_ARG;
@@ -534,6 +553,7 @@ moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, const mo
 
 moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
                                 void* scales, int64_t scale_ld, void* stream) {
+  MOE_RANGE("moe_quantize_mxfp8");
   if (groups <= 0 || rows <= 0 || cols <= 0 || cols % 32 || scale_ld < rows || scale_ld % 16) return MOE_ERR_INVALID_ARG;
   if (!all16({src, codes, scales})) return MOE_ERR_INVALID_ARG;
   return cuda_status(moe::launch_mx_quant_rows(src, nullptr, 1, groups * rows, static_cast<int>(cols), rows, scale_ld,
@@ -544,6 +564,7 @@ moe_status_t moe_quantize_mxfp8(const void* src, int64_t groups, int64_t rows, i
 moe_status_t moe_permute_mxfp8(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
                                int32_t* row_of_copy, int32_t* copy_of_row, void* xq_perm, void* xs_perm,
                                void* xq_tok, void* xs_tok, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_permute_mxfp8");
   MOE_TRY(check_desc(d));
   if (d->precision != 1) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
@@ -719,6 +740,7 @@ moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_perm, con
                                    const int32_t* offsets, const void* xq_tok, const void* xs_tok,
                                    const moe_expert_weights_mx_t* w, const moe_ffn_saved_t* saved, void* y_perm,
                                    void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_grouped_ffn_mxfp8");
   MOE_TRY(check_desc(d));
   if (d->precision != 1) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
@@ -751,6 +773,7 @@ moe_status_t moe_grouped_ffn_mxfp8(const moe_desc_t* d, const void* xq_perm, con
 
 moe_status_t moe_quantize_mxfp8_t(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
                                   void* scales, int64_t scale_ld, void* stream) {
+  MOE_RANGE("moe_quantize_mxfp8_t");
   if (!all16({src, codes}) || !scales || groups < 1 || rows <= 0 || cols <= 0 || rows % 32 || cols % 8 ||
       scale_ld < cols || scale_ld % 16 || cols > (int64_t{1} << 30))
     return MOE_ERR_INVALID_ARG;
@@ -762,6 +785,7 @@ moe_status_t moe_quantize_mxfp8_t(const void* src, int64_t groups, int64_t rows,
 moe_status_t moe_backward_mxfp8(const moe_desc_t* d, const void* w_gate, const moe_expert_weights_mx_t* wt,
                                 const moe_fwd_state_t* s, const void* dy, const moe_grads_t* g, void* ws,
                                 size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_backward_mxfp8");
   MOE_TRY(check_desc(d));
   if (d->precision != 1) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(*d, ws, ws_bytes, true));
@@ -832,6 +856,7 @@ moe_status_t moe_permute_capacity(const moe_desc_t* d, const void* x, const int3
                                   int32_t* copy_of_row_full, int32_t* kept_offsets, int32_t* row_of_copy,
                                   int32_t* copy_of_row, void* x_perm, int32_t* n_dropped, void* ws,
                                   size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_permute_capacity");
   MOE_TRY(check_desc(d));
   if (d->precision != 0) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
@@ -858,6 +883,7 @@ moe_status_t moe_permute_capacity(const moe_desc_t* d, const void* x, const int3
 
 moe_status_t moe_quantize_fp8_tile(const void* src, int64_t groups, int64_t rows, int64_t cols, void* codes,
                                    float* scales, void* stream) {
+  MOE_RANGE("moe_quantize_fp8_tile");
   if (!src || !codes || !scales || groups < 1 || rows <= 0 || cols <= 0 || cols % 16 || !aligned16(src) ||
       !aligned16(codes))
     return MOE_ERR_INVALID_ARG;
@@ -868,6 +894,7 @@ moe_status_t moe_quantize_fp8_tile(const void* src, int64_t groups, int64_t rows
 moe_status_t moe_grouped_ffn_fp8w(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
                                   const moe_expert_weights_mx_t* wq, const moe_ffn_saved_t* saved, void* y_perm,
                                   void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_grouped_ffn_fp8w");
   MOE_TRY(check_desc(d));
   if (d->precision != 2) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
@@ -898,6 +925,7 @@ moe_status_t moe_grouped_ffn_fp8w(const moe_desc_t* d, const void* x_perm, const
 
 moe_status_t moe_aux_loss(const moe_desc_t* d, const float* logits, const int32_t* counts, float coef, float* loss,
                           float* dlogits_aux, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_aux_loss");
   MOE_TRY(check_desc(d));
   MOE_TRY(check_ws(*d, ws, ws_bytes, false));
   if (!logits || !counts || !loss) return MOE_ERR_INVALID_ARG;
@@ -910,12 +938,14 @@ moe_status_t moe_aux_loss(const moe_desc_t* d, const float* logits, const int32_
 
 moe_status_t moe_monitor_stats(int32_t n_exp, const int32_t* counts_hist, int32_t n_hist, float* stats,
                                void* stream) {
+  MOE_RANGE("moe_monitor_stats");
   if (n_exp < 1 || n_exp > 1024 || n_hist < 1 || !counts_hist || !stats) return MOE_ERR_INVALID_ARG;
   return cuda_status(moe::launch_monitor(counts_hist, n_hist, n_exp, stats, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_update_bias(const moe_desc_t* d, const int32_t* counts, float* bias, float gamma, int32_t mode,
                              void* stream) {
+  MOE_RANGE("moe_update_bias");
   MOE_TRY(check_desc(d));
   if (!counts || !bias || (mode != 0 && mode != 1)) return MOE_ERR_INVALID_ARG;
   return cuda_status(
