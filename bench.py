@@ -46,7 +46,8 @@ def parse():
                     help="expert GEMM operands: bf16; MXFP8 (E4M3 codes, E8M0 scales per 32 along the contraction,"
                          " forward and backward); fp8w (E4M3 weights with fp32 scales per 128x128 tile)")
     ap.add_argument("--sweep", action="store_true",
-                    help="forward-only load-skew sweep, bf16 and MXFP8 (prints one JSON line of results)")
+                    help="load-skew sweep: forward and forward+backward for bf16, MXFP8, FP8 weights and the "
+                         "capacity-factor mode (prints one JSON line of results)")
     return ap.parse_args()
 
 
