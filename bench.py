@@ -579,8 +579,10 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "config": {"workload": workload_name(cfg),
-                   "l2": f"no flush: the {wbytes / 1e9:.1f} GB of expert weights streamed every step exceed "
-                         "the 126 MB L2",
+                   "l2": (f"no flush: the {wbytes / 1e9:.1f} GB of expert weights streamed every step exceed "
+                          "the 126 MB L2") if wbytes > 126e6 else
+                         (f"no flush: the whole workload ({wbytes / 1e6:.1f} MB of weights) fits in the 126 MB L2; "
+                          "a latency-bound case"),
                    "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 shared=6/7/8 dY=9"},
         "fwd_tokens_per_s": res["fwd"][0],
         "grouped_ffn_tflops": ffn_tflops,
