@@ -58,3 +58,39 @@ def test_launch_counts():
     assert bench.launches_per_step(ds) == 22 + 3 + 6 + 1
     # enough 128-token tiles to fill the GPU: no slices
     assert bench.route_launches(mix.replace(n_tok=65536)) == 4
+
+
+def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
+    """The GPU arm's JSON assembly (roofline per kind, e2e, launches, clocks),
+    fed with made-up timings instead of a GPU run: every contract key is
+    present and the roofline reports the kind with the largest share."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS
+
+    def fake_run_ours(args, rank, world, local_rank):
+        cfg = CONFIGS[args.workload].replace(precision=args.precision)
+        s = args.steps
+        kernels = {"gate": {"ms_total": 0.03 * s, "launches": s}, "ffn_fwd": {"ms_total": 1.8 * s, "launches": 2 * s},
+                   "dgrad": {"ms_total": 1.9 * s, "launches": 2 * s}, "wgrad": {"ms_total": 2.4 * s, "launches": 3 * s}}
+        per_call = {"route": 0.05, "permute": 0.03, "grouped_ffn": 1.86, "combine": 0.02, "backward": 4.4}
+        return {"cfg": cfg, "per_call": per_call, "kernels": kernels,
+                "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
+                "nonempty": cfg.n_exp, "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s), "fwd": (2e6, 2.0 * s),
+                "e2e": (600000.0, 6.8 * s)}
+
+    monkeypatch.setattr(bench, "run_ours", fake_run_ours)
+    for workload in ("mixtral", "tiny"):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", workload, "--steps", "3", "--warmup", "3",
+                                          "--no-cpu-baseline"])
+        bench.main()
+        d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                    "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+            assert key in d, key
+        r = d["roofline"]
+        assert r["kind"] == "wgrad" and r["bound"] in ("tensor", "hbm")
+        assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+        assert set(d["roofline_by_kind"]) == {"gate", "ffn_fwd", "dgrad", "wgrad"}
+        assert d["e2e"]["h2d_bytes_per_step"] == 2 and d["gpu_launches"] == bench.launches_per_step(
+            CONFIGS[workload]) * 3
