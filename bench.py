@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--sample", type=int, default=0, help="oracle token sample (0: automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-configs", action="store_true",
+                    help="time only the chosen workload (by default the Mixtral bf16 run is followed by the "
+                         "DeepSeek-V3 bf16 and MXFP8 and the Mixtral MXFP8 layers, reported as sub_results)")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8", "fp8w"],
                     help="expert GEMM operands: bf16; MXFP8 (E4M3 codes, E8M0 scales per 32 along the contraction,"
                          " forward and backward); fp8w (E4M3 weights with fp32 scales per 128x128 tile)")
@@ -282,14 +285,13 @@ def time_oracle(cfg, sample: int, steps: int = 1):
 
 
 # ----------------------------------------------------------------- GPU arm
-def run_ours(args, rank, world, local_rank):
+def run_ours(args, cfg, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
     from ragged_grouped_gemm_gb300 import api
-    from ragged_grouped_gemm_gb300.inputs import CONFIGS, make_dy, make_layer
+    from ragged_grouped_gemm_gb300.inputs import make_dy, make_layer
 
-    cfg = CONFIGS[args.workload].replace(precision=args.precision)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     p = make_layer(cfg, dev)
@@ -382,17 +384,21 @@ def run_ours(args, rank, world, local_rank):
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
     hout = torch.empty(b["out"].shape, dtype=b["out"].dtype).pin_memory()
-    dx_dev, ddy_dev = torch.empty_like(x), torch.empty_like(dy)
+    hdx = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    x_in, dy_in = torch.empty_like(x), torch.empty_like(dy)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record()
     for _ in range(args.steps):
-        dx_dev.copy_(hx, non_blocking=True)
-        ddy_dev.copy_(hdy, non_blocking=True)
-        layer.forward(dx_dev)
-        layer.backward(ddy_dev)
-        hout.copy_(b["out"], non_blocking=True)
+        x_in.copy_(hx, non_blocking=True)
+        dy_in.copy_(hdy, non_blocking=True)
+        layer.forward(x_in)
+        grads = layer.backward(dy_in)
+        if cfg.use_bias:
+            layer.update_bias(1e-3, 0)
+        hout.copy_(b["out"], non_blocking=True)      # the step's results: output and input gradient
+        hdx.copy_(grads["dx"], non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
     clk.__exit__(None, None, None)
@@ -408,10 +414,14 @@ def run_ours(args, rank, world, local_rank):
         return float(t.item())
 
     nonempty = int((b["counts"] > 0).sum().item())
+    counts = b["counts"].float()
     res = {"cfg": cfg, "per_call": per_call, "kernels": kernels, "clocks": clk.summary(), "nonempty": nonempty,
-           "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2}
+           "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
+           "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2 + hdx.numel() * 2}
     for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
         res[key] = aggregate(world, cfg.n_tok, args.steps, v, max_over_ranks)
+    del layer, p, dy, b, ws
+    torch.cuda.empty_cache()
     return res
 
 
@@ -490,6 +500,85 @@ def run_sweep(args):
           flush=True)
 
 
+def call_bytes(cfg) -> dict:
+    """Algorithmic HBM bytes of the memory-bound calls of one forward: the
+    bytes each must read and write at least, whatever kernels it uses.
+    route: x and W_g read, logits, top-K indices and weights, counts and
+    offsets written; permute: expert indices and x read, the two maps and
+    the permuted rows written (MXFP8: E4M3 codes + one scale byte per 32,
+    plus the token-order copy with a shared expert); combine: the permuted
+    outputs, maps and weights read (+ the shared output), the output
+    written."""
+    n, d, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
+    r = n * k
+    q = 1 + 1 / 32
+    route = 2 * n * d + 2 * e * d + 4 * n * e + 8 * r + 4 * (2 * e + 1)
+    if cfg.precision == "mxfp8":
+        permute = 4 * r + 2 * n * d + 8 * r + q * r * d + (q * n * d if cfg.n_shared else 0)
+    else:
+        permute = 4 * r + 2 * n * d + 8 * r + 2 * r * d
+    combine = 2 * r * d + 8 * r + (2 * n * d if cfg.n_shared else 0) + 2 * n * d
+    return {"route": route, "permute": permute, "combine": combine}
+
+
+def summarize(res, args, peaks) -> dict:
+    """Throughput, per-call times and GB/s, and the roofline of every kind of
+    grouped GEMM for one run of run_ours."""
+    cfg, per_call, kernels = res["cfg"], res["per_call"], res["kernels"]
+    tok_s, ms = res["step"]
+    fl = flops(cfg)
+    # Tensor-bound kinds are timed inside a step of a few milliseconds, so
+    # their roof is the burst bf16 peak (MXFP8: twice it, the nominal
+    # fp8/bf16 ratio); the sustained figure is reported beside it.
+    burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    mult, mult_note = (2.0, " x 2 (nominal fp8/bf16 ratio)") if cfg.precision == "mxfp8" else (1.0, "")
+    kind_names = {"gate": "router logits GEMM", "ffn_fwd": "forward expert GEMMs (GEMM1 w1|w3+SwiGLU, GEMM2 w2)",
+                  "dgrad": "data-gradient GEMMs (through w2 + SwiGLU derivative, through w1|w3)",
+                  "wgrad": "weight-gradient GEMMs (dW1, dW3, dW2; fp32 out)"}
+    roofs = {}
+    for kind, kt in kernels.items():
+        if not kt["launches"]:
+            continue
+        k_fl, k_b = kind_work(cfg, kind, res["nonempty"])
+        k_fl, k_b = k_fl * args.steps / kt["launches"], k_b * args.steps / kt["launches"]   # per launch
+        k_s = kt["ms_total"] / kt["launches"] / 1e3
+        m = 1.0 if kind == "gate" else mult
+        kpeak = burst * m
+        if k_fl / (kpeak * 1e12) >= k_b / (peaks["hbm_gbs"] * 1e9):
+            r = {"bound": "tensor", "achieved": k_fl / k_s / 1e12, "peak": kpeak, "unit": "TFLOP/s",
+                 "peak_source": f"{peaks['source']} bf16_tflops (burst)" + (mult_note if m > 1 else ""),
+                 "peak_sustained": sustained * m, "frac_of_sustained": k_fl / k_s / 1e12 / (sustained * m)}
+        else:
+            r = {"bound": "hbm", "achieved": k_b / k_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "peak_source": f"{peaks['source']} hbm_gbs"}
+        tkey = kind if cfg.precision == "bf16" else f"{kind}_{cfg.precision}"
+        r.update(frac=r["achieved"] / r["peak"], traffic=recorded_traffic(tkey, cfg.name), kernel=kind_names[kind],
+                 launches_per_step=kt["launches"] / args.steps, ms_per_launch=k_s * 1e3,
+                 share_of_step=kt["ms_total"] / ms, algorithmic_flops=k_fl, algorithmic_bytes=k_b,
+                 tflops=k_fl / k_s / 1e12)
+        roofs[kind] = r
+    cb = call_bytes(cfg)
+    per_call_gbs = {c: {"gbs": cb[c] / (per_call[c] / 1e3) / 1e9,
+                        "frac_of_hbm": cb[c] / (per_call[c] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "algorithmic_bytes": cb[c]} for c in cb}
+    return {
+        "workload": workload_name(cfg), "value": tok_s, "unit": "tokens/s", "ms_per_step": ms / args.steps,
+        "fwd_tokens_per_s": res["fwd"][0],
+        "grouped_ffn_tflops": fl["ffn_fwd"] / (per_call["grouped_ffn"] / 1e3) / 1e12,
+        "backward_tflops": (fl["ffn_bwd"] + fl["router_bwd"]) / (per_call["backward"] / 1e3) / 1e12,
+        "per_call_ms": per_call, "per_call_gbs": per_call_gbs, "roofline_by_kind": roofs,
+        "e2e": {"value": res["e2e"][0], "unit": "tokens/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "max_load_over_mean": res["max_load_over_mean"], "clocks": res["clocks"],
+    }
+
+
+# Further configurations timed after the headline one (one GPU only): the
+# DeepSeek-V3-shaped layer in bf16 and MXFP8 and the Mixtral-shaped layer in
+# MXFP8, each reported with its own roofline and clocks.
+SUB_CONFIGS = [("dsv3", "bf16"), ("dsv3", "mxfp8"), ("mixtral", "mxfp8")]
+
+
 def main():
     args = parse()
     if args.sweep:
@@ -526,75 +615,47 @@ def main():
     import torch.distributed as dist
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    res = run_ours(args, rank, world, local_rank)
+    res = run_ours(args, cfg, rank, world, local_rank)
+    subs = []
+    if world == 1 and not args.no_sub_configs and (args.workload, args.precision) == ("mixtral", "bf16"):
+        for wl, prec in SUB_CONFIGS:
+            subs.append(run_ours(args, CONFIGS[wl].replace(precision=prec), rank, world, local_rank))
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return
-    cfg, per_call, kernels = res["cfg"], res["per_call"], res["kernels"]
-    tok_s, ms = res["step"]
-    fl = flops(cfg)
     peaks = measured_peaks()
-    ffn_s = per_call["grouped_ffn"] / 1e3
-    ffn_tflops = fl["ffn_fwd"] / ffn_s / 1e12
-    ffn_b = ffn_bytes(cfg, res["nonempty"])
-    bwd_s = per_call["backward"] / 1e3
-    peak = peaks["bf16_tflops_sustained"]
-    peak_src = f"{peaks['source']} bf16_tflops_sustained"
-    if cfg.precision == "mxfp8":      # E4M3 x E4M3 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
-        peak, peak_src = 2 * peak, peak_src + " x 2 (nominal fp8/bf16 ratio)"
-    wbytes = {"bf16": 2, "mxfp8": 1 + 1 / 32, "fp8w": 1}[cfg.precision] * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
-    # Roofline per kind of grouped GEMM, from the CUDA events the library
-    # recorded around every launch of the timed steps; the binding roof is
-    # the slower of tensor time and HBM time at the measured peaks.
-    kind_names = {"gate": "router logits GEMM", "ffn_fwd": "forward expert GEMMs (GEMM1 w1|w3+SwiGLU, GEMM2 w2)",
-                  "dgrad": "data-gradient GEMMs (through w2 + SwiGLU derivative, through w1|w3)",
-                  "wgrad": "weight-gradient GEMMs (dW1, dW3, dW2; fp32 out)"}
-    roofs = {}
-    for kind, kt in kernels.items():
-        if not kt["launches"]:
-            continue
-        k_fl, k_b = kind_work(cfg, kind, res["nonempty"])
-        k_fl, k_b = k_fl * args.steps / kt["launches"], k_b * args.steps / kt["launches"]   # per launch
-        k_s = kt["ms_total"] / kt["launches"] / 1e3
-        kpeak = peak if kind != "gate" else peaks["bf16_tflops_sustained"]
-        if k_fl / (kpeak * 1e12) >= k_b / (peaks["hbm_gbs"] * 1e9):
-            r = {"bound": "tensor", "achieved": k_fl / k_s / 1e12, "peak": kpeak, "unit": "TFLOP/s",
-                 "peak_source": peak_src if kind != "gate" else f"{peaks['source']} bf16_tflops_sustained"}
-        else:
-            r = {"bound": "hbm", "achieved": k_b / k_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                 "peak_source": f"{peaks['source']} hbm_gbs"}
-        tkey = kind if cfg.precision == "bf16" else f"{kind}_{cfg.precision}"
-        r.update(frac=r["achieved"] / r["peak"], traffic=recorded_traffic(tkey, cfg.name), kernel=kind_names[kind],
-                 launches_per_step=kt["launches"] / args.steps, ms_per_launch=k_s * 1e3,
-                 share_of_step=kt["ms_total"] / ms, algorithmic_flops=k_fl, algorithmic_bytes=k_b)
-        roofs[kind] = r
+    head = summarize(res, args, peaks)
+    roofs = head["roofline_by_kind"]
     dominant = max(roofs, key=lambda kk: roofs[kk]["share_of_step"])
     roof = dict(roofs[dominant])
     roof["kind"] = dominant
     dtype = {"bf16": "bf16", "mxfp8": "mxfp8 (e4m3 x e4m3, e8m0 scales per 32)",
              "fp8w": "e4m3 weights (fp32 tile scales) x bf16"}[cfg.precision]
+    wbytes = {"bf16": 2, "mxfp8": 1 + 1 / 32, "fp8w": 1}[cfg.precision] * 3 * cfg.n_exp * cfg.d_ff * cfg.d_model
     line = {
-        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-        "config": {"workload": workload_name(cfg),
+        "config": {"workload": head["workload"],
                    "l2": (f"no flush: the {wbytes / 1e9:.1f} GB of expert weights streamed every step exceed "
                           "the 126 MB L2") if wbytes > 126e6 else
                          (f"no flush: the whole workload ({wbytes / 1e6:.1f} MB of weights) fits in the 126 MB L2; "
                           "a latency-bound case"),
                    "seeds": "x=1 W_g=2 W1=3 W3=4 W2=5 shared=6/7/8 dY=9"},
-        "fwd_tokens_per_s": res["fwd"][0],
-        "grouped_ffn_tflops": ffn_tflops,
-        "backward_tflops": (fl["ffn_bwd"] + fl["router_bwd"]) / bwd_s / 1e12,
-        "per_call_ms": per_call,
+        "fwd_tokens_per_s": head["fwd_tokens_per_s"],
+        "grouped_ffn_tflops": head["grouped_ffn_tflops"],
+        "backward_tflops": head["backward_tflops"],
+        "per_call_ms": head["per_call_ms"],
+        "per_call_gbs": head["per_call_gbs"],
         "roofline": roof,
         "roofline_by_kind": roofs,
-        "e2e": {"value": res["e2e"][0], "unit": "tokens/s",
-                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "e2e": head["e2e"],
         "gpu_launches": launches_per_step(cfg) * args.steps,
-        "clocks": res["clocks"],
+        "clocks": head["clocks"],
     }
+    if subs:
+        line["sub_results"] = [summarize(r, args, peaks) for r in subs]
     if not args.no_cpu_baseline:
         sample = args.sample or 64
         n, times = time_oracle(cfg, sample, steps=1)

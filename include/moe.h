@@ -72,7 +72,8 @@ typedef enum {
 /* Device status bits (moe_get_device_status). */
 #define MOE_DEV_TIMEOUT 1      /* a bounded wait inside a kernel ran out */
 #define MOE_DEV_BAD_INDEX 2    /* an expert index outside [0, E) */
-#define MOE_DEV_BAD_OFFSETS 4  /* the histogram did not sum to N*K */
+#define MOE_DEV_BAD_OFFSETS 4  /* the histogram did not sum to N*K, or (permute)
+                                  offsets inconsistent with the expert indices */
 
 /* Layer description; the pages' MoELayer(d_model, d_ff, n_experts, top_k,
  * n_shared, use_bias_balance) constructor (§9). */
@@ -439,9 +440,11 @@ MOE_API moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, 
  * fixed 512 KiB device array inside the library, resident on every GPU that
  * loads it until the process exits.  Limit: ceil(n_tok/128) * n_exp must not
  * exceed 65536; larger sizes return MOE_ERR_WORKSPACE before anything is
- * enqueued.  The call allocates nothing.  The first call on each device looks
- * up the array's device address (with that device current) and caches it,
- * so make that first call before any stream capture.  All calls share the
+ * enqueued.  The call allocates nothing.  Every call looks up the array's
+ * device address on the current device (a host-side query, no device work),
+ * so the address stays valid after a device reset; the first lookup on a
+ * device may load the library's device code there, so make the first call
+ * on each device before any stream capture.  All calls share the
  * one array (it keeps the last call's contents; every call rewrites the
  * parts it reads): calls whose work may overlap on the GPU race with each
  * other and must be serialised, e.g. issued on one stream.  Expert indices
@@ -450,6 +453,19 @@ MOE_API moe_status_t moe_backward_fp8w(const moe_desc_t* d, const void* w_gate, 
 MOE_API moe_status_t moe_permute_noalloc(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
                                          const int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row,
                                          void* x_perm, void* stream);
+
+/* Self-test of device failure detection (no counterpart in the pages; a
+ * check of this library's own bounded waits).  Enqueues one small kernel
+ * built from the wait routine every pipeline of the library uses, on
+ * mbarriers that nothing ever arrives on: one wait has the limit `limit_ns`
+ * (1 ns .. 1 s) and runs out, setting MOE_DEV_TIMEOUT in the status word at
+ * the start of `ws` and `site` in the second word; a second wait with the
+ * library's default limit (2 s) sees the first one's abort flag and returns
+ * at once.  The kernel then exits normally, so the context stays usable.
+ * `ws` needs at least 8 bytes (a layer workspace works); clear it with
+ * moe_workspace_init first and read the result with moe_get_device_status. */
+MOE_API moe_status_t moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, int32_t site,
+                                               void* stream);
 
 /* ---------------------------------------------------------- kernel timing --
  * Per-kernel timing of the grouped GEMMs (no counterpart in the pages; a

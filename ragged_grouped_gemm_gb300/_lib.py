@@ -96,6 +96,7 @@ SIGNATURES = {
     "moe_timing_read": (c_i32, [c_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                 ctypes.POINTER(ctypes.c_int64)]),
     "moe_timing_disable": (c_i32, []),
+    "moe_selftest_wait_timeout": (c_i32, [c_vp, ctypes.c_size_t, ctypes.c_uint64, c_i32, c_vp]),
 }
 
 _LIB = None

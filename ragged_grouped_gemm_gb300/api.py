@@ -241,6 +241,14 @@ def moe_timing_disable():
     _check("moe_timing_disable", _lib.load().moe_timing_disable())
 
 
+def moe_selftest_wait_timeout(ws, limit_ns: int, site: int, stream=None):
+    """Run the library's bounded-wait self-test (see moe.h): a wait that
+    nothing completes runs out after ``limit_ns`` and reports through the
+    status words of ``ws``."""
+    _check("moe_selftest_wait_timeout", _lib.load().moe_selftest_wait_timeout(
+        _p(ws, name="ws"), ws.numel() * ws.element_size(), int(limit_ns), int(site), _s(stream)))
+
+
 def moe_update_bias(desc, counts, bias, gamma: float, mode: int = 0, stream=None):
     _check("moe_update_bias", _lib.load().moe_update_bias(
         ctypes.byref(desc), _p(counts, I32, (desc.n_exp,), "counts"), _p(bias, F32, (desc.n_exp,), "bias"),

@@ -29,8 +29,7 @@
 // idle MMA warp zeroes its rows past the group's end and forwards the stage
 // to rank 0.  Each CTA's epilogue reads its own 128 TMEM lanes and signals
 // rank 0's accumulator-free barrier.  TMEM is allocated and freed by both
-// CTAs together, between cluster barriers.  QUAD (ragged K, optional): two
-// pairs in a 4-CTA cluster share the B operand by TMA multicast.
+// CTAs together, between cluster barriers.
 //
 // fp32 outputs leave through TMA tensor stores: each epilogue warp stages
 // 16 rows x 32 columns (whole 128-byte rows) at a time in 2 KB of shared
@@ -160,8 +159,8 @@ struct Tile {
 };
 
 // rank: the CTA's rank in its cluster; bit 0 picks its 128 rows of a pair
-// tile, bit 1 (QUAD, ragged K) the pair's M tile of the cluster's two.
-template <bool RAGGED_K, int BN, bool PAIR = false, bool QUAD = false>
+// tile.
+template <bool RAGGED_K, int BN, bool PAIR = false>
 __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const int* s_off, const int* s_pre,
                                             int rank = 0) {
   Tile t;
@@ -200,14 +199,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
     }
   } else {
     const int mtiles = (p.m_size + UR - 1) / UR;
-    const int munits = QUAD ? (mtiles + 1) / 2 : mtiles;   // a 4-CTA cluster takes two adjacent M tiles
     const int ntiles = (p.n_size + BN - 1) / BN;
-    const int per_g = munits * ntiles;
+    const int per_g = mtiles * ntiles;
     t.g = tile / per_g;
     const int rem = tile - t.g * per_g;
     t.mt = rem / ntiles;
     t.nt = rem - t.mt * ntiles;
-    if (QUAD) t.mt = 2 * t.mt + (rank >> 1);
     t.row0 = s_off[t.g];
     t.m0 = t.mt * UR + prank * BM;
     t.k_rows = s_off[t.g + 1] - s_off[t.g];
@@ -276,13 +273,9 @@ __device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int
   return nkk;
 }
 
-// QUAD (ragged-K CTA pairs only): clusters of four CTAs, two pairs on
-// adjacent M tiles of one N tile; each B half is loaded once per cluster,
-// half by each pair, and multicast to the CTAs of both pairs that hold it.
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false, bool QUAD = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
     grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  static_assert(!QUAD || (PAIR && A_MN && B_MN && !QUANT && !W8 && BN == 256), "QUAD: ragged-K bf16 pairs");
   using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
@@ -307,7 +300,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
   const int lane = threadIdx.x & 31;
   const int G = p.num_groups;
   // CTA pair (2-SM MMA): the even CTA of the pair issues the MMAs for both
-  constexpr int CN = QUAD ? 4 : (PAIR ? 2 : 1);   // CTAs per cluster
+  constexpr int CN = PAIR ? 2 : 1;   // CTAs per cluster
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const bool leader = (rank & 1) == 0;
   const uint32_t lead = static_cast<uint32_t>(rank & ~1);   // cluster rank of the pair's leader
@@ -320,7 +313,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       // CTA's TMA plus the peer's forwarded arrival
       // (FP8 weights: A's TMA bytes plus one arrival per converter warp)
       mbar_init(&full[s], W8 ? 1 + kConvWarps : ((PAIR && RAGGED_K && leader) ? 2 : 1));
-      mbar_init(&empty[s], QUAD ? 2 : 1);   // QUAD: both pairs' MMAs have read the stage
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], kSfWarps);
     for (int s = 0; s < C::kW8Slots; ++s) {
@@ -389,7 +382,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
   } else {
     constexpr int UR = PAIR ? 2 * BM : BM;
     const int mtiles = (p.m_size + UR - 1) / UR;
-    total_tiles = G * (QUAD ? (mtiles + 1) / 2 : mtiles) * ((p.n_size + BN - 1) / BN);
+    total_tiles = G * mtiles * ((p.n_size + BN - 1) / BN);
   }
 
   if (warp == 0) {
@@ -400,7 +393,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
@@ -445,7 +438,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       uint32_t lph = 0, lused = 0;   // ragged-K pair peer: phases of its own stage barriers
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
@@ -497,16 +490,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
               tma_load_2d_pair(sA, &p.tmA[0], bar, t.m0, r);
               tma_load_2d_pair(sA + 8192, &p.tmA[0], bar, t.m0 + 64, r);
-              if (QUAD) {
-                // this CTA's B half is also the B half of its counterpart in the
-                // other pair: each loads one of its two 64-row atoms for both
-                const int a = rank >> 1;
-                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2)));
-                tma_load_2d_pair_mc(sB + a * 8192, &p.tmB[0], bar, mask, n0 + 64 * a, r);
-              } else {
 #pragma unroll
-                for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, &p.tmB[0], bar, n0 + 64 * a, r);
-              }
+              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, &p.tmB[0], bar, n0 + 64 * a, r);
               if (!leader) mbar_arrive_remote(bar);
             } else {
               mbar_arrive_expect_tx(&full[s], C::kStageBytes);
@@ -596,7 +581,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       uint32_t it = 0, lph = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int rv = t.k_rows - kb * BK;
           if (rv >= BK || (rv & 15) == 0) continue;
@@ -618,7 +603,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     uint32_t it = 0, tcount = 0;
     bool ok = true;
     for (int tile = unit0; ok && tile < total_tiles; tile += ustride, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
@@ -668,7 +653,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     uint32_t it = 0, tcount = 0;
     bool ok = true;
     for (int tile = unit0; ok && tile < total_tiles; tile += ustride, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
@@ -696,7 +681,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             if (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
             else tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if (PAIR) tc_commit_pair_mc(&empty[s], QUAD ? 0xF : 3);
+          if (PAIR) tc_commit_pair_mc(&empty[s], 3);
           else tc_commit(&empty[s]);
         }
         __syncwarp();
@@ -726,7 +711,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         // A scale rows: ragged M [4][144] from a 16-aligned row; ragged K [4][128]
         const int a_rem = RAGGED_K ? 0 : (t.row0 & 15);
         constexpr int AS = RAGGED_K ? 128 : 144;
@@ -770,7 +755,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
@@ -834,7 +819,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     const int r = q * 32 + lane;
     uint32_t tcount = 0;
     for (int tile = unit0; tile < total_tiles; tile += ustride, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN, PAIR, QUAD>(tile, p, s_off, s_pre, rank);
+      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tfull[buf], aph, s_abort, p.status, 400)) break;
@@ -1253,13 +1238,12 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false,
-          bool QUAD = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
   using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
-  constexpr int CN = QUAD ? 4 : 2;   // CTAs per cluster (PAIR)
+  constexpr int CN = 2;   // CTAs per cluster (PAIR)
   const size_t smem = C::smem_bytes(kp.num_groups);
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8, QUAD>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_units = 0;   // co-resident CTAs (or CTA pairs)
@@ -1315,16 +1299,6 @@ bool use_cta_pair(int64_t rows, int groups) {
   if (e && e[0] == '0') return false;
   if (e && e[0] == '1') return true;
   return rows >= 512LL * groups;
-}
-
-// Weight gradients on CTA pairs can run in clusters of two pairs sharing the
-// B operand (QUAD), selected by MOE_GEMM_QUAD=1 (read at every launch).  Off
-// by default: on the Mixtral shape it cuts the operand reads from L2 by a
-// quarter but runs 4% slower, as clusters of four occupy 144 of the 152 SMs
-// and the per-SM rate does not rise.
-bool use_quad() {
-  const char* e = std::getenv("MOE_GEMM_QUAD");
-  return e && e[0] == '1';
 }
 
 }  // namespace
@@ -1585,11 +1559,6 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
   }
   if (a.a_mn && a.b_mn && a.epi == EPI_F32) {
-    if (pair && use_quad()) {
-      const int64_t mt = (a.m_size + 2 * BM - 1) / (2 * BM);   // pair tiles along M, two per cluster
-      const int64_t uq = static_cast<int64_t>(a.num_groups) * ((mt + 1) / 2) * ((a.n_size + BN - 1) / BN);
-      return launch_impl<256, true, true, EPI_F32, false, true, false, true>(kp, uq, stream);
-    }
     return pair ? launch_impl<256, true, true, EPI_F32, false, true>(kp, u, stream)
                 : launch_impl<256, true, true, EPI_F32>(kp, u, stream);
   }

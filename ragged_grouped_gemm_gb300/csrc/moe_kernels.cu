@@ -219,8 +219,13 @@ __global__ void __launch_bounds__(256) block_hist_kernel(int n_tok, int E, int K
     block_counts[static_cast<int64_t>(blockIdx.x) * E + i] = s_h[i];
 }
 
+// Each expert's first row per chunk.  The caller's offsets must be the
+// exclusive scan of the histogram; an expert whose rows do not end at
+// offsets[e+1] is reported as DEV_BAD_OFFSETS (the scatter then drops the
+// copies that fall outside [offsets[e], offsets[e+1]) or [0, R)).
 __global__ void block_base_kernel(int nchunks, int E, const int32_t* __restrict__ offsets,
-                                  const int32_t* __restrict__ block_counts, int32_t* __restrict__ block_base) {
+                                  const int32_t* __restrict__ block_counts, int32_t* __restrict__ block_base,
+                                  int32_t* status) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   int run = offsets[e];
@@ -228,18 +233,28 @@ __global__ void block_base_kernel(int nchunks, int E, const int32_t* __restrict_
     block_base[static_cast<int64_t>(ch) * E + e] = run;
     run += block_counts[static_cast<int64_t>(ch) * E + e];
   }
+  if (run != offsets[e + 1] && status) atomicOr(status, DEV_BAD_OFFSETS);
 }
 
 // One warp per chunk of tokens; copies are visited in copy order c = t*K+k,
 // (32/K) tokens per step, so each expert's rows come out in ascending token
 // order (ties of a repeated expert inside one token by ascending k).
+// A position outside the expert's own rows [offsets[e], offsets[e+1]) or
+// outside [0, R) (offsets inconsistent with the expert indices) is not
+// written: the copy gets row -1 and DEV_BAD_OFFSETS is raised.
 __global__ void __launch_bounds__(32) scatter_maps_kernel(int n_tok, int E, int K, const int32_t* __restrict__ idx,
+                                                          const int32_t* __restrict__ offsets,
                                                           const int32_t* __restrict__ block_base,
                                                           int32_t* __restrict__ row_of_copy,
-                                                          int32_t* __restrict__ copy_of_row) {
+                                                          int32_t* __restrict__ copy_of_row, int32_t* status) {
   extern __shared__ int s_base[];
+  int* s_end = s_base + E;
   const int lane = threadIdx.x;
-  for (int i = lane; i < E; i += 32) s_base[i] = block_base[static_cast<int64_t>(blockIdx.x) * E + i];
+  const int64_t R = static_cast<int64_t>(n_tok) * K;
+  for (int i = lane; i < E; i += 32) {
+    s_base[i] = block_base[static_cast<int64_t>(blockIdx.x) * E + i];
+    s_end[i] = offsets[i + 1];
+  }
   __syncwarp();
   const int t_begin = blockIdx.x * kChunkTok;
   const int t_end = min(n_tok, t_begin + kChunkTok);
@@ -263,8 +278,13 @@ __global__ void __launch_bounds__(32) scatter_maps_kernel(int n_tok, int E, int 
       }
       base = __shfl_sync(am, base, leader);
       const int pos = base + rank;
-      row_of_copy[c] = pos;
-      copy_of_row[pos] = static_cast<int32_t>(c);
+      if (pos >= 0 && pos < s_end[e] && pos < R) {
+        row_of_copy[c] = pos;
+        copy_of_row[pos] = static_cast<int32_t>(c);
+      } else {
+        row_of_copy[c] = -1;
+        if (status) atomicOr(status, DEV_BAD_OFFSETS);
+      }
     } else if (active) {
       row_of_copy[c] = -1;   // expert index outside [0, E): no row (reported by block_hist_kernel)
     }
@@ -681,15 +701,19 @@ __global__ void __launch_bounds__(1024) kept_offsets_kernel(const int32_t* __res
 // Copy c keeps its rank inside its expert (position in the dropless,
 // token-ordered permutation); ranks below the capacity get the compact row
 // kept_offsets[e] + rank, the others -1.
-__global__ void capacity_rows_kernel(int64_t R, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
-                                     const int32_t* __restrict__ row_full, const int32_t* __restrict__ kept_offsets,
-                                     int cap, int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row) {
+// A copy without a dropless row (expert index outside [0, E), or offsets
+// inconsistent with the indices, both reported by the map kernels) is dropped.
+__global__ void capacity_rows_kernel(int64_t R, int E, const int32_t* __restrict__ idx,
+                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_full,
+                                     const int32_t* __restrict__ kept_offsets, int cap,
+                                     int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row) {
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= R) return;
   const int e = idx[c];
-  const int rank = row_full[c] - offsets[e];
+  const int rf = row_full[c];
   int32_t r = -1;
-  if (rank < cap) {
+  const int rank = (e >= 0 && e < E && rf >= 0) ? rf - offsets[e] : cap;
+  if (rank >= 0 && rank < cap) {
     r = kept_offsets[e] + rank;
     copy_of_row[r] = static_cast<int32_t>(c);
   }
@@ -755,8 +779,9 @@ cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* 
   const int nch = permute_num_chunks(n_tok);
   const size_t smem = static_cast<size_t>(n_exp) * sizeof(int);
   block_hist_kernel<<<nch, 256, smem, st>>>(n_tok, n_exp, top_k, topk_idx, block_counts, status);
-  block_base_kernel<<<(n_exp + 255) / 256, 256, 0, st>>>(nch, n_exp, offsets, block_counts, block_base);
-  scatter_maps_kernel<<<nch, 32, smem, st>>>(n_tok, n_exp, top_k, topk_idx, block_base, row_of_copy, copy_of_row);
+  block_base_kernel<<<(n_exp + 255) / 256, 256, 0, st>>>(nch, n_exp, offsets, block_counts, block_base, status);
+  scatter_maps_kernel<<<nch, 32, 2 * smem, st>>>(n_tok, n_exp, top_k, topk_idx, offsets, block_base, row_of_copy,
+                                                 copy_of_row, status);
   return cudaGetLastError();
 }
 
@@ -838,7 +863,7 @@ cudaError_t launch_capacity_maps(int n_tok, int n_exp, int top_k, const int32_t*
   const int64_t R = static_cast<int64_t>(n_tok) * top_k;
   kept_offsets_kernel<<<1, 1024, 0, st>>>(offsets, n_exp, cap, static_cast<int>(R), kept_offsets, n_dropped);
   if (R > 0)
-    capacity_rows_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(R, topk_idx, offsets, row_full,
+    capacity_rows_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(R, n_exp, topk_idx, offsets, row_full,
                                                                                    kept_offsets, cap, row_of_copy,
                                                                                    copy_of_row);
   return cudaGetLastError();

@@ -20,36 +20,28 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "moe_kernels.cuh"
 
 namespace {
 
 constexpr int kScratchInts = 2 * 65536;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_permute_scratch[kScratchInts];
 
-std::mutex g_lookup_mu;
-int32_t* g_scratch_on_device[kMaxDevices] = {};
-
 // Device address of g_permute_scratch on the current device.  In host code
 // the symbol's name is only a stand-in, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
+// cudaGetSymbolAddress, with the caller's device current.  The lookup is
+// repeated on every call (a host-side query that enqueues no device work)
+// rather than cached, so the address stays right after a cudaDeviceReset or
+// a re-created primary context.  The first lookup on a device may load the
+// library's device code there, which is why the first call on each device
+// should come before any stream capture.
 cudaError_t scratch_address(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_lookup_mu);
-  if (g_scratch_on_device[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_on_device[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch_on_device[dev];
+  *out = static_cast<int32_t*>(p);
   return cudaSuccess;
 }
 

@@ -59,17 +59,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (without waiting further) when another role raised the abort flag or the
-// wait exceeded the timeout; in the latter case this thread raises the flag
+// wait exceeded `limit_ns`; in the latter case this thread raises the flag
 // and records DEV_TIMEOUT and the waiting site in the status words.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  int32_t* status, int site) {
+                                                  int32_t* status, int site, uint64_t limit_ns = kSpinTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((++n & 63u) == 0 && globaltimer_ns() - t0 > kSpinTimeoutNs) {
+    if ((++n & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       if (status) {
         atomicOr(status, DEV_TIMEOUT);
@@ -294,17 +294,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-// The same load multicast to the CTAs of `mask` (same shared-memory offset
-// in each); each destination's pair-leader barrier at bar's offset receives
-// the bytes that land in that destination.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map, uint32_t bar, uint16_t mask,
-                                                    int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {

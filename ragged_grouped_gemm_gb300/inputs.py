@@ -61,8 +61,10 @@ class MoEConfig:
 CONFIGS = {
     "tiny": MoEConfig("tiny", 256, 64, 128, 8, 2),
     "mixtral": MoEConfig("mixtral", 4096, 4096, 14336, 8, 2),
+    # bias_beta: found by bisection with the oracle router on the seeded x and
+    # W_g so that the most loaded expert takes 8x the mean load N*K/E (8.0x)
     "dsv3": MoEConfig("dsv3", 4096, 7168, 2048, 256, 8, gate="sigmoid", use_bias=True,
-                      n_shared=1, d_ff_shared=2048, bias_beta=0.55, n_cold=4),
+                      n_shared=1, d_ff_shared=2048, bias_beta=0.4833, n_cold=4),
     # profiling case: the Mixtral layer with a quarter of d_ff (about 3 GB on
     # the device, operands still far larger than L2)
     "mixtral_quarter": MoEConfig("mixtral_quarter", 4096, 4096, 3584, 8, 2),
@@ -123,9 +125,12 @@ def make_layer(cfg: MoEConfig, device="cpu") -> dict:
     None, and for a shared expert ws1, ws3 [Fs,D], ws2 [D,Fs].
     """
     big = cfg.n_exp * cfg.d_ff * cfg.d_model > (1 << 26)
+    # x and W_g are always drawn on the CPU generator, so the routing of a
+    # layer built on any device is the one the oracle computes from the same
+    # seeds; the large expert weights are drawn on ``device``.
     t = {
-        "x": randn_bf16((cfg.n_tok, cfg.d_model), SEEDS["x"], 1.0, device),
-        "w_gate": randn_bf16((cfg.n_exp, cfg.d_model), SEEDS["w_gate"], WEIGHT_STD, device),
+        "x": randn_bf16((cfg.n_tok, cfg.d_model), SEEDS["x"], 1.0, "cpu").to(device),
+        "w_gate": randn_bf16((cfg.n_exp, cfg.d_model), SEEDS["w_gate"], WEIGHT_STD, "cpu").to(device),
         "w1": randn_bf16((cfg.n_exp, cfg.d_ff, cfg.d_model), SEEDS["w1"], WEIGHT_STD, device, big),
         "w3": randn_bf16((cfg.n_exp, cfg.d_ff, cfg.d_model), SEEDS["w3"], WEIGHT_STD, device, big),
         "w2": randn_bf16((cfg.n_exp, cfg.d_model, cfg.d_ff), SEEDS["w2"], WEIGHT_STD, device, big),

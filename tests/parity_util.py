@@ -47,3 +47,16 @@ def routing_agreement(keys: np.ndarray, idx_gpu: np.ndarray, idx_ref: np.ndarray
 
 def to_dev(p: dict, device="cuda") -> dict:
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+
+
+def check_rows(got, want, tol: float, key: str = ""):
+    """Normwise relative error of the whole array within ``tol``, and per row
+    (token): the 99th percentile of ``||got_t - want_t||`` over the root mean
+    square row norm of ``want`` within ``2 * tol``, so that a few wrong rows
+    cannot hide in the pooled norm."""
+    from oracle_pool import per_token_error
+    got, want = np.asarray(got), np.asarray(want)
+    e = rel(got, want)
+    assert e < tol, (key, e)
+    pt = per_token_error(got, want)
+    assert np.quantile(pt, 0.99) <= 2 * tol, (key, float(pt.max()), int(np.argmax(pt)))

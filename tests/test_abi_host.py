@@ -139,3 +139,12 @@ def test_timing_entry_points_validate_on_host(lib):
     # nothing recorded: zero time, zero launches
     assert lib.moe_timing_read(3, ct.byref(ms), ct.byref(n), ct.byref(u)) == 0
     assert (ms.value, n.value, u.value) == (0.0, 0, 0)
+
+
+def test_selftest_wait_timeout_validates_on_host(lib):
+    # no or misaligned workspace, limit of zero or above one second: rejected before any launch
+    assert lib.moe_selftest_wait_timeout(None, 4096, 50000, 1, None) == 3
+    assert lib.moe_selftest_wait_timeout(4097, 4096, 50000, 1, None) == 3
+    assert lib.moe_selftest_wait_timeout(4096, 4, 50000, 1, None) == 3
+    assert lib.moe_selftest_wait_timeout(4096, 4096, 0, 1, None) == 1
+    assert lib.moe_selftest_wait_timeout(4096, 4096, 2_000_000_000, 1, None) == 1

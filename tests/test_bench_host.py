@@ -61,36 +61,73 @@ def test_launch_counts():
 
 
 def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
-    """The GPU arm's JSON assembly (roofline per kind, e2e, launches, clocks),
-    fed with made-up timings instead of a GPU run: every contract key is
-    present and the roofline reports the kind with the largest share."""
+    """The GPU arm's JSON assembly (roofline per kind, per-call GB/s, e2e,
+    launches, clocks, sub-results), fed with made-up timings instead of a GPU
+    run: every contract key is present, the roofline reports the kind with
+    the largest share, and tensor-bound kinds divide by the burst bf16 peak
+    (twice it for MXFP8 operands)."""
     sys.path.insert(0, ROOT)
     import bench
     from ragged_grouped_gemm_gb300.inputs import CONFIGS
 
-    def fake_run_ours(args, rank, world, local_rank):
-        cfg = CONFIGS[args.workload].replace(precision=args.precision)
+    seen = []
+
+    def fake_run_ours(args, cfg, rank, world, local_rank):
+        seen.append((cfg.name, cfg.precision))
         s = args.steps
         kernels = {"gate": {"ms_total": 0.03 * s, "launches": s}, "ffn_fwd": {"ms_total": 1.8 * s, "launches": 2 * s},
                    "dgrad": {"ms_total": 1.9 * s, "launches": 2 * s}, "wgrad": {"ms_total": 2.4 * s, "launches": 3 * s}}
         per_call = {"route": 0.05, "permute": 0.03, "grouped_ffn": 1.86, "combine": 0.02, "backward": 4.4}
         return {"cfg": cfg, "per_call": per_call, "kernels": kernels,
                 "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
-                "nonempty": cfg.n_exp, "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s), "fwd": (2e6, 2.0 * s),
-                "e2e": (600000.0, 6.8 * s)}
+                "nonempty": cfg.n_exp, "max_load_over_mean": 1.1, "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s),
+                "fwd": (2e6, 2.0 * s), "e2e": (600000.0, 6.8 * s)}
 
     monkeypatch.setattr(bench, "run_ours", fake_run_ours)
+    monkeypatch.setattr(bench, "measured_peaks", lambda: {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                                                          "bf16_tflops_sustained": 1700.0, "source": "measured"})
     for workload in ("mixtral", "tiny"):
+        seen.clear()
         monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", workload, "--steps", "3", "--warmup", "3",
                                           "--no-cpu-baseline"])
         bench.main()
         d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
         for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
-                    "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+                    "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks",
+                    "per_call_gbs"):
             assert key in d, key
         r = d["roofline"]
         assert r["kind"] == "wgrad" and r["bound"] in ("tensor", "hbm")
         assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
         assert set(d["roofline_by_kind"]) == {"gate", "ffn_fwd", "dgrad", "wgrad"}
+        for kind, rk in d["roofline_by_kind"].items():
+            if rk["bound"] == "tensor":
+                assert rk["peak"] == pytest.approx(1900.0)
+        assert set(d["per_call_gbs"]) == {"route", "permute", "combine"}
         assert d["e2e"]["h2d_bytes_per_step"] == 2 and d["gpu_launches"] == bench.launches_per_step(
             CONFIGS[workload]) * 3
+        if workload == "mixtral":
+            # the headline is followed by the other configurations, each with its own roofline
+            assert seen == [("mixtral", "bf16")] + list(bench.SUB_CONFIGS)
+            subs = d["sub_results"]
+            assert len(subs) == len(bench.SUB_CONFIGS)
+            mx = [x for x in subs if "mxfp8" in x["workload"]]
+            for x in mx:
+                for rk in x["roofline_by_kind"].values():
+                    if rk["bound"] == "tensor" and "router" not in rk["kernel"]:
+                        assert rk["peak"] == pytest.approx(3800.0)
+        else:
+            assert seen == [("tiny", "bf16")] and "sub_results" not in d
+
+
+def test_call_bytes_are_the_algorithmic_minimum():
+    sys.path.insert(0, ROOT)
+    import bench
+    from ragged_grouped_gemm_gb300.inputs import CONFIGS
+    m = CONFIGS["mixtral"]
+    b = bench.call_bytes(m)
+    n, d, r = m.n_tok, m.d_model, m.rows
+    # permute reads x once and writes every copy's row; combine reads every copy's row and writes the output
+    assert b["permute"] >= 2 * n * d + 2 * r * d
+    assert b["combine"] >= 2 * r * d + 2 * n * d
+    assert b["route"] >= 2 * n * d

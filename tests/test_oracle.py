@@ -674,3 +674,89 @@ def test_fp8_tile_dequantize_round_trip_on_representable_weights():
     c3, s3 = O.fp8_tile_quantize(g)
     b3 = O.fp8_tile_dequantize(c3, s3)
     assert (np.abs(b3 - g) <= np.abs(g) * 2.0 ** -4 + np.repeat(np.repeat(s3, 128, 0), 128, 1) * 2.0 ** -9 + 1e-12).all()
+
+
+def test_mxfp8_backward_quantises_the_stored_bf16_dyw():
+    """What the storage reading changes, worked by hand.  A 32-element row
+    of dY with dY[0] = 256 and dY[1] = v = 1.1875 - 2^-20 (fp32), the rest 0,
+    on a one-expert, top-1 layer (g = 1, so dYw = dY):
+
+    * block scale: amax 256 = 2^8, exponent floor(log2 256) - 8 = 0, X = 1
+      (E8M0 byte 127); 256 -> E4M3 0x78 (exponent field 15, mantissa 0);
+    * v lies just below 1.1875, the midpoint of the E4M3 neighbours 1.125
+      (0x39: exponent field 7, mantissa 001) and 1.25 (0x3A, mantissa 010),
+      so the fp32 operand rounds down to 0x39;
+    * bf16(v) = 1.1875 exactly (v is within half a bf16 step, 2^-8, of it),
+      a tie, which rounds to the even mantissa 010: 0x3A.
+
+    The oracle's MXFP8 backward quantises dYw as the layer stores it (bf16),
+    so the operand of its first quantised GEMM (dh = dYw w2) carries 1.1875
+    and code 0x3A; with the identity as storage it carries v and 0x39."""
+    v = np.float32(1.1875) - np.float32(2.0 ** -20)
+    row = np.zeros((1, 32), np.float32)
+    row[0, 0], row[0, 1] = 256.0, v
+    codes, scales, _ = O.mx_quantize(row, axis=1)
+    assert codes[0, 0] == 0x78 and codes[0, 1] == 0x39 and scales[0, 0] == 127
+    stored = O.bf16_round(row)
+    assert stored[0, 1] == np.float32(1.1875)
+    codes_b, scales_b, _ = O.mx_quantize(stored, axis=1)
+    assert codes_b[0, 0] == 0x78 and codes_b[0, 1] == 0x3A and scales_b[0, 0] == 127
+
+    r = _rng(35)
+    n, d, f = 1, 32, 32
+    x = r.standard_normal((n, d)).astype(np.float32)
+    w1, w3 = (r.standard_normal((1, f, d)).astype(np.float32) * np.float32(0.1) for _ in range(2))
+    w2 = r.standard_normal((1, d, f)).astype(np.float32) * np.float32(0.1)
+    w_gate = r.standard_normal((1, d)).astype(np.float32)
+    lg = O.gate_logits(x, w_gate)
+    idx, g = O.route(lg, None, 1, "softmax")
+    assert g[0, 0] == np.float32(1.0)
+    for store, want_val, want_code in ((O.bf16_round, np.float32(1.1875), 0x3A), (lambda a: a, v, 0x39)):
+        _, saved = O.moe_forward_mxfp8(x, idx, g, w1, w3, w2, None, return_saved=True, store=store)
+        seen = []
+
+        def recording_quant(a, axis):
+            seen.append(np.array(a, dtype=np.float64))
+            return O.mx_fake_quant(a, axis=axis)
+        O.moe_backward_mxfp8(row, x, lg, idx, g, w_gate, w1, w3, w2, saved, "softmax", None,
+                             quant=recording_quant, store=store)
+        dyw_operand = seen[0]                    # first quantised operand: dYw of dh = dYw w2, along D
+        assert dyw_operand.shape == (1, 32) and dyw_operand[0, 1] == want_val
+        assert O.mx_quantize(dyw_operand, axis=1)[0][0, 1] == want_code
+
+
+def test_oracle_pool_runs_the_oracle_unchanged():
+    """The parallel runner of the GPU parity tests (spawned processes, expert
+    weights shared as bf16 bits) returns what the oracle returns when called
+    directly on the same group of tokens."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from oracle_pool import SharedBf16, run_groups
+    r = _rng(40)
+    n, d, f, e, k = 6, 32, 64, 4, 2
+    bf = lambda a: O.bf16_round(a)   # noqa: E731
+    x = bf(r.standard_normal((n, d)).astype(np.float32))
+    w1, w3 = (bf(r.standard_normal((e, f, d)).astype(np.float32) * np.float32(0.1)) for _ in range(2))
+    w2 = bf(r.standard_normal((e, d, f)).astype(np.float32) * np.float32(0.1))
+    wg = bf(r.standard_normal((e, d)).astype(np.float32) * np.float32(0.1))
+    dy = bf(r.standard_normal((n, d)).astype(np.float32))
+    lg = O.gate_logits(x, wg)
+    idx, g = O.route(lg, None, k, "softmax")
+    bits = lambda a: (np.ascontiguousarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)   # noqa: E731
+    shm = {name: SharedBf16(bits(w)) for name, w in (("w1", w1), ("w3", w3), ("w2", w2))}
+    try:
+        used = np.arange(e)
+        job = {"used": used, "w1": shm["w1"].spec, "w3": shm["w3"].spec, "w2": shm["w2"].spec, "x": x,
+               "idx": idx, "g": g, "logits": lg, "dy": dy, "w_gate": wg, "shared": None, "gate": "softmax"}
+        res = run_groups([dict(job, mxfp8=True), dict(job, mxfp8=False)])
+    finally:
+        for v in shm.values():
+            v.close()
+    out_q, saved_q = O.moe_forward_mxfp8(x, idx, g, w1, w3, w2, None, return_saved=True)
+    ref_q = O.moe_backward_mxfp8(dy, x, lg, idx, g, wg, w1, w3, w2, saved_q, "softmax", None)
+    out, saved = O.moe_forward(x, lg, idx, g, w1, w3, w2, None)
+    ref = O.moe_backward(dy, x, lg, idx, g, wg, w1, w3, w2, saved, "softmax", None)
+    for got, want_out, want in ((res[0], out_q, ref_q), (res[1], out, ref)):
+        np.testing.assert_array_equal(got["out"], want_out)
+        for key in ("dx", "dg", "dlogits"):
+            np.testing.assert_array_equal(got[key], want[key])
