@@ -133,9 +133,12 @@ def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, red
 
 
 def route_launches(cfg, sms: int = 152) -> int:
-    """moe_route's kernels: dense offsets, the router logits GEMM, top-K, scan,
-    plus the ordered sum of the GEMM's contraction slices when its 128-token
-    tiles are too few to fill the GPU (at most 4 slices of 64-column blocks)."""
+    """moe_route's kernels: one fused router kernel for E <= 32; otherwise
+    dense offsets, the router logits GEMM, top-K, scan, plus the ordered sum
+    of the GEMM's contraction slices when its 128-token tiles are too few to
+    fill the GPU (at most 4 slices of 64-column blocks)."""
+    if cfg.n_exp <= 32:
+        return 1
     tiles = -(-cfg.n_tok // 128) * -(-cfg.n_exp // (32 if cfg.n_exp <= 32 else 256))
     want = min(4, sms // max(tiles, 1))
     kb = -(-cfg.d_model // 64)
@@ -146,16 +149,17 @@ def route_launches(cfg, sms: int = 152) -> int:
 def launches_per_step(cfg) -> int:
     """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
     from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
+    maps = 1 if cfg.rows <= 65536 else 3     # single-CTA permutation maps, or the token-chunked kernels
     if cfg.precision == "mxfp8":
-        # route 4; permute: 3 map kernels + row quantiser (+ token quantiser for the shared expert);
+        # route; permute: map kernels + row quantiser (+ token quantiser for the shared expert);
         # grouped FFN: GEMM1, GEMM2 (+ dense offsets, GEMM1, GEMM2); combine
-        fwd = route_launches(cfg) + 4 + 2 + 1 + (4 if cfg.n_shared else 0)
+        fwd = route_launches(cfg) + maps + 1 + 2 + 1 + (4 if cfg.n_shared else 0)
         # per expert set: row-wise quantisers of dYw (fused into the combine backward for the routed
         # experts), da1, da3; pad offsets, 5 transposing quantisers, 5 GEMMs
         per_set = 2 + 1 + 5 + 5
         bwd = 1 + per_set + (1 + per_set + 1 if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
         return fwd + bwd + (1 if cfg.use_bias else 0)
-    fwd = route_launches(cfg) + 4 + 2 + 1   # route; permute: 3 map kernels + rows; GEMM1, GEMM2; combine
+    fwd = route_launches(cfg) + maps + 1 + 2 + 1   # route; permute: maps + rows; GEMM1, GEMM2; combine
     if cfg.n_shared:
         fwd += 3
     bwd = 1 + 5 + 1              # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3; unpermute-sum

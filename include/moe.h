@@ -163,7 +163,9 @@ MOE_API const char* moe_status_string(moe_status_t s);
  * workspace of bwd_bytes serves every call.  Either output may be NULL. */
 MOE_API moe_status_t moe_workspace_size(const moe_desc_t* d, size_t* fwd_bytes, size_t* bwd_bytes);
 
-/* Clear the device status word at the start of `ws` (enqueued on stream). */
+/* Clear the 256-byte status block at the start of `ws` (enqueued on
+ * stream): the device status words and the router's completion counters,
+ * which every call leaves at zero again. */
 MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, then copy the two device status words (bits, site)
@@ -173,10 +175,15 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, int32_t* status_host,
 /* Router (§4.1, §4.3, §6.3, §9 step 1) and expert histogram (§9 step 4,
  * §12.5 bincount):
  *   logits[N,E] (fp32 out) = x[N,D] (bf16) * w_gate[E,D]^T  (tensor cores,
- *                            fp32 accumulation; with few 128-token tiles the
+ *                            fp32 accumulation, deterministic.  E <= 32: the
+ *                            whole router is one kernel (warp-level MMA over
+ *                            16-token tiles, the contraction cut into 8
+ *                            slices added in slice order, then the selection
+ *                            and histogram below).  E > 32: the grouped GEMM
+ *                            on 128-token tiles; with few tiles the
  *                            contraction runs in up to 4 slices whose fp32
  *                            partial products, kept in the workspace, are
- *                            added in slice order: deterministic);
+ *                            added in slice order);
  *   topk_idx[N,K] (out)    = the K experts with the largest
  *                            logits + bias (bias [E] fp32, NULL when the layer
  *                            has none), sorted by rank; equal keys: lower

@@ -22,6 +22,12 @@ using moe::GemmArgs;
 using moe::Operand;
 
 constexpr size_t kAlign = 256;
+// int32 words of the workspace's status block (256 bytes, cleared by
+// moe_workspace_init): 0 and 1 are the status bits and the failing site;
+// the fused router keeps its completion ticket in word 8 and its histogram
+// accumulator in words 16..47, and leaves both zero.
+constexpr int kTicketWord = 8;
+constexpr int kRouterAccWord = 16;
 // The router logits GEMM has one 128-token tile per CTA; with few tiles its
 // contraction is cut into up to this many slices (summed in order after).
 constexpr int kGateSlices = 4;
@@ -359,8 +365,19 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
   const WsLayout L = layout(*d);
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* dense = at<int32_t>(ws, L.dense_off);
+  if (d->n_tok == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+  }
+  if (d->n_exp <= 32) {
+    // one launch: logits on the warp-level MMA, top-K, histogram, scan (the
+    // ticket counter lives in the status block moe_workspace_init clears)
+    moe::RouteShape rs{d->n_tok, d->n_exp, d->top_k, d->gate};
+    return cuda_status(moe::launch_router_fused(rs, d->d_model, x, w_gate, d->use_bias ? bias : nullptr, logits,
+                                                topk_idx, topk_w, counts, offsets, status + kRouterAccWord,
+                                                status + kTicketWord, status, st));
+  }
   MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
-  if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
   MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
   GemmArgs g;
   g.epi = moe::EPI_F32;

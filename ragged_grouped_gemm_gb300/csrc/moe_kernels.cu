@@ -66,6 +66,71 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ------------------------------------------------------------------ top-K
+// Selection of one token by one warp: expert e's logit lives in lane e % 32,
+// slot e / 32 of lg.  On return lanes k < K hold the k-th selected expert
+// (largest key logit + bias first, the total order of make_key) and its
+// renormalised gate weight: softmax over all E in fp32 then p_sel / sum
+// p_sel (gate 0), or sigmoid of the unbiased logit / sum (gate 1).
+template <int PL>
+__device__ __forceinline__ void topk_token(const float (&lg)[PL], const float* __restrict__ bias, int E, int K,
+                                           int gate, int lane, int& my_e, float& my_w) {
+  unsigned long long key[PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E) {
+      const float kv = bias ? __fadd_rn(lg[j], bias[e]) : lg[j];
+      key[j] = make_key(kv, e);
+    } else {
+      key[j] = 0ull;
+    }
+  }
+  my_e = -1;
+  float my_l = 0.0f;
+  for (int k = 0; k < K; ++k) {
+    unsigned long long best = key[0];
+#pragma unroll
+    for (int j = 1; j < PL; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(kFull, best, o);
+      best = other > best ? other : best;
+    }
+    const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+    float le = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) {
+      if (lane + 32 * j == e) {
+        key[j] = 0ull;
+        le = lg[j];
+      }
+    }
+    le = __shfl_sync(kFull, le, e & 31);
+    if (lane == k) {
+      my_e = e;
+      my_l = le;
+    }
+  }
+  float sel;
+  if (gate == 0) {
+    // p = softmax over all E in fp32, then p_sel / sum(p_sel)
+    float m = lg[0];
+#pragma unroll
+    for (int j = 1; j < PL; ++j) m = fmaxf(m, lg[j]);
+    m = warp_max(m);
+    float z = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PL; ++j)
+      if (lane + 32 * j < E) z += expf(lg[j] - m);
+    z = warp_sum(z);
+    sel = (lane < K) ? expf(my_l - m) / z : 0.0f;
+  } else {
+    sel = (lane < K) ? 1.0f / (1.0f + expf(-my_l)) : 0.0f;
+  }
+  const float tot = warp_sum(sel);
+  my_w = sel / tot;
+}
+
 // One warp per token; expert e lives in lane e % 32, slot e / 32.
 template <int PL>
 __global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __restrict__ logits,
@@ -79,72 +144,171 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t < s.n_tok) {
     float lg[PL];
-    unsigned long long key[PL];
     const float* row = logits + static_cast<int64_t>(t) * E;
 #pragma unroll
     for (int j = 0; j < PL; ++j) {
       const int e = lane + 32 * j;
-      if (e < E) {
-        lg[j] = row[e];
-        const float kv = bias ? __fadd_rn(lg[j], bias[e]) : lg[j];
-        key[j] = make_key(kv, e);
-      } else {
-        lg[j] = -INFINITY;
-        key[j] = 0ull;
-      }
+      lg[j] = e < E ? row[e] : -INFINITY;
     }
-    int my_e = -1;
-    float my_l = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      unsigned long long best = key[0];
-#pragma unroll
-      for (int j = 1; j < PL; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(kFull, best, o);
-        best = other > best ? other : best;
-      }
-      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
-      float le = 0.0f;
-#pragma unroll
-      for (int j = 0; j < PL; ++j) {
-        if (lane + 32 * j == e) {
-          key[j] = 0ull;
-          le = lg[j];
-        }
-      }
-      le = __shfl_sync(kFull, le, e & 31);
-      if (lane == k) {
-        my_e = e;
-        my_l = le;
-      }
-    }
-    float sel;
-    if (s.gate == 0) {
-      // p = softmax over all E in fp32, then p_sel / sum(p_sel)
-      float m = lg[0];
-#pragma unroll
-      for (int j = 1; j < PL; ++j) m = fmaxf(m, lg[j]);
-      m = warp_max(m);
-      float z = 0.0f;
-#pragma unroll
-      for (int j = 0; j < PL; ++j)
-        if (lane + 32 * j < E) z += expf(lg[j] - m);
-      z = warp_sum(z);
-      sel = (lane < K) ? expf(my_l - m) / z : 0.0f;
-    } else {
-      sel = (lane < K) ? 1.0f / (1.0f + expf(-my_l)) : 0.0f;
-    }
-    const float tot = warp_sum(sel);
+    int my_e;
+    float my_w;
+    topk_token<PL>(lg, bias, E, K, s.gate, lane, my_e, my_w);
     if (lane < K) {
       topk_idx[static_cast<int64_t>(t) * K + lane] = my_e;
-      topk_w[static_cast<int64_t>(t) * K + lane] = sel / tot;
+      topk_w[static_cast<int64_t>(t) * K + lane] = my_w;
       atomicAdd(&s_hist[my_e], 1);
     }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     if (s_hist[i]) atomicAdd(&counts[i], s_hist[i]);
+}
+
+// ------------------------------------------------------------ fused router (E <= 32)
+// The whole router of a layer with at most 32 experts in one launch: logits,
+// top-K with renormalised weights, the expert histogram and its scan.
+//
+// The logits x W_g^T are a skinny contraction (N x D times D x E, E <= 32)
+// bound by the read of x, so they run on the warp-level tensor-core MMA
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate) straight from registers:
+// each CTA takes a tile of 16 tokens, its 8 warps each a contiguous eighth
+// of the contraction, and every lane loads 16 bytes of a token row and of
+// the matching W_g row per 32-column block.  The contraction order inside a
+// block is a fixed permutation of the columns (the same on both operands),
+// and the warps' partial products are added in warp order, so the result
+// is deterministic.  A warp per token then selects the top K; each CTA adds
+// its expert histogram to an integer accumulator in the workspace (exact in
+// any order), and the last CTA to finish (a ticket counter, no waiting)
+// takes the accumulator (resetting it to zero), writes counts and offsets,
+// checks that they sum to N*K, and resets the ticket.
+constexpr int kRtTok = 16;
+constexpr int kRtWarps = 8;
+constexpr int kRtUnroll = 4;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <int NT>   // 8-expert column tiles: E <= 8 * NT
+__global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
+    RouteShape s, int d8, const uint4* __restrict__ x, const uint4* __restrict__ wg, const float* __restrict__ bias,
+    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* acc, int32_t* ticket, int32_t* status) {
+  constexpr int EP = 8 * NT;
+  __shared__ float s_acc[kRtWarps][kRtTok][EP + 1];
+  __shared__ int s_hist[32];
+  __shared__ int s_last;
+  const int E = s.n_exp, K = s.top_k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int tok0 = blockIdx.x * kRtTok;
+  if (threadIdx.x < 32) s_hist[threadIdx.x] = 0;
+  // this warp's 32-column blocks of the contraction
+  const int nblk = d8 / 4;
+  const int b0 = nblk * warp / kRtWarps, b1 = nblk * (warp + 1) / kRtWarps;
+  const int r0 = tok0 + g, r1 = tok0 + g + 8;
+  const bool v0 = r0 < s.n_tok, v1 = r1 < s.n_tok;
+  const uint4* x0 = x + static_cast<int64_t>(v0 ? r0 : 0) * d8 + q;
+  const uint4* x1 = x + static_cast<int64_t>(v1 ? r1 : 0) * d8 + q;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  float c[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  for (int b = b0; b < b1; b += kRtUnroll) {
+    uint4 xa[kRtUnroll], xb[kRtUnroll], w[kRtUnroll][NT];
+#pragma unroll
+    for (int u = 0; u < kRtUnroll; ++u) {
+      const bool in = b + u < b1;
+      xa[u] = (in && v0) ? ld_stream(x0 + 4 * (b + u)) : zero;
+      xb[u] = (in && v1) ? ld_stream(x1 + 4 * (b + u)) : zero;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int e = 8 * j + g;
+        w[u][j] = (in && e < E) ? __ldg(wg + static_cast<int64_t>(e) * d8 + 4 * (b + u) + q) : zero;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRtUnroll; ++u) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        // lane (g, q) holds columns 8q..8q+7 of rows g, g+8 and of W_g row 8j+g:
+        // columns 8q+0..3 form the first k16 step, 8q+4..7 the second
+        mma_bf16_16816(c[j], xa[u].x, xb[u].x, xa[u].y, xb[u].y, w[u][j].x, w[u][j].y);
+        mma_bf16_16816(c[j], xa[u].z, xb[u].z, xa[u].w, xb[u].w, w[u][j].z, w[u][j].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    s_acc[warp][g][8 * j + 2 * q] = c[j][0];
+    s_acc[warp][g][8 * j + 2 * q + 1] = c[j][1];
+    s_acc[warp][g + 8][8 * j + 2 * q] = c[j][2];
+    s_acc[warp][g + 8][8 * j + 2 * q + 1] = c[j][3];
+  }
+  __syncthreads();
+  // two tokens per warp: logits (partials added in warp order), top-K, weights
+  for (int tt = warp; tt < kRtTok; tt += kRtWarps) {
+    const int t = tok0 + tt;
+    if (t >= s.n_tok) break;
+    float lg[1];
+    float v = 0.0f;
+    if (lane < E) {
+#pragma unroll
+      for (int w = 0; w < kRtWarps; ++w) v += s_acc[w][tt][lane];
+      logits[static_cast<int64_t>(t) * E + lane] = v;
+    }
+    lg[0] = lane < E ? v : -INFINITY;
+    int my_e;
+    float my_w;
+    topk_token<1>(lg, bias, E, K, s.gate, lane, my_e, my_w);
+    if (lane < K) {
+      topk_idx[static_cast<int64_t>(t) * K + lane] = my_e;
+      topk_w[static_cast<int64_t>(t) * K + lane] = my_w;
+      atomicAdd(&s_hist[my_e], 1);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < E && s_hist[threadIdx.x]) atomicAdd(acc + threadIdx.x, s_hist[threadIdx.x]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last CTA: every CTA's histogram is in the accumulator; take it, then its scan
+  if (warp == 0) {
+    const int tot = lane < E ? atomicExch(acc + lane, 0) : 0;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane < E) {
+      counts[lane] = tot;
+      offsets[lane + 1] = incl;
+    }
+    if (lane == 0) {
+      offsets[0] = 0;
+      *ticket = 0;
+    }
+    const int total = __shfl_sync(kFull, incl, E - 1);
+    if (lane == 0 && static_cast<long long>(total) != static_cast<long long>(s.n_tok) * K && status)
+      atomicOr(status, DEV_BAD_OFFSETS);
+  }
 }
 
 // ------------------------------------------------------------ offsets scan
@@ -292,6 +456,111 @@ __global__ void __launch_bounds__(32) scatter_maps_kernel(int n_tok, int E, int 
   }
 }
 
+// Single-CTA form of the three kernels above for up to kMapOnePassMax
+// copies: the copies c = 0..R-1 are cut into 32 contiguous segments, one per
+// warp; each warp counts its segment's copies per expert (warp-aggregated
+// through __match_any_sync), then one thread per expert turns the 32 counts
+// into the segment's first row of that expert (a running sum from
+// offsets[e], checked against offsets[e+1]), and each warp walks its
+// segment again in copy order assigning rows exactly as scatter_maps_kernel
+// does (same positions, same bound checks, same status bits).  Each lane
+// keeps kMapBatch copies' expert indices in registers per pass, so the
+// segment is read with kMapBatch independent loads in flight.
+constexpr int kMapBatch = 8;
+constexpr int64_t kMapOnePassMax = 65536;
+
+__global__ void __launch_bounds__(1024, 1) maps_onepass_kernel(int n_tok, int E, int K,
+                                                               const int32_t* __restrict__ idx,
+                                                               const int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ row_of_copy,
+                                                               int32_t* __restrict__ copy_of_row, int32_t* status) {
+  extern __shared__ int s_map[];
+  int* s_seg = s_map;              // [32][E]: segment counts, then segment bases
+  int* s_end = s_map + 32 * E;     // [E]: offsets[e + 1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t R = static_cast<int64_t>(n_tok) * K;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) s_seg[i] = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_end[i] = offsets[i + 1];
+  __syncthreads();
+  const int64_t per = (R + 31) / 32;
+  const int64_t c0 = min(R, warp * per), c1 = min(R, c0 + per);
+  int* hist = s_seg + warp * E;
+  bool bad_index = false, bad_offsets = false;
+  for (int64_t b = c0; b < c1; b += 32 * kMapBatch) {
+    int e[kMapBatch];
+#pragma unroll
+    for (int j = 0; j < kMapBatch; ++j) {
+      const int64_t c = b + 32 * j + lane;
+      e[j] = c < c1 ? idx[c] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kMapBatch; ++j) {
+      const int64_t c = b + 32 * j + lane;
+      const bool active = c < c1;
+      const bool ok = active && e[j] >= 0 && e[j] < E;
+      bad_index |= active && !ok;
+      const unsigned am = __ballot_sync(kFull, ok);
+      if (ok) {
+        const unsigned m = __match_any_sync(am, e[j]);
+        if (lane == __ffs(m) - 1) hist[e[j]] += __popc(m);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {
+    int run = offsets[ex];
+    for (int w = 0; w < 32; ++w) {
+      const int n = s_seg[w * E + ex];
+      s_seg[w * E + ex] = run;
+      run += n;
+    }
+    bad_offsets |= run != s_end[ex];
+  }
+  __syncthreads();
+  for (int64_t b = c0; b < c1; b += 32 * kMapBatch) {
+    int e[kMapBatch];
+#pragma unroll
+    for (int j = 0; j < kMapBatch; ++j) {
+      const int64_t c = b + 32 * j + lane;
+      e[j] = c < c1 ? idx[c] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kMapBatch; ++j) {
+      const int64_t c = b + 32 * j + lane;
+      const bool active = c < c1;
+      const bool ok = active && e[j] >= 0 && e[j] < E;
+      const unsigned am = __ballot_sync(kFull, ok);
+      if (ok) {
+        const unsigned m = __match_any_sync(am, e[j]);
+        const int leader = __ffs(m) - 1;
+        const int rank = __popc(m & ((1u << lane) - 1u));
+        int base = 0;
+        if (lane == leader) {
+          base = hist[e[j]];
+          hist[e[j]] = base + __popc(m);
+        }
+        base = __shfl_sync(am, base, leader);
+        const int pos = base + rank;
+        if (pos >= 0 && pos < s_end[e[j]] && pos < R) {
+          row_of_copy[c] = pos;
+          copy_of_row[pos] = static_cast<int32_t>(c);
+        } else {
+          row_of_copy[c] = -1;
+          bad_offsets = true;
+        }
+      } else if (active) {
+        row_of_copy[c] = -1;   // expert index outside [0, E): no row
+      }
+      __syncwarp();
+    }
+  }
+  if (status) {
+    if (bad_index) atomicOr(status, DEV_BAD_INDEX);
+    if (bad_offsets) atomicOr(status, DEV_BAD_OFFSETS);
+  }
+}
+
 __global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, int K, const uint4* __restrict__ x,
                                                            const int32_t* __restrict__ row_of_copy,
                                                            uint4* __restrict__ x_perm) {
@@ -310,49 +579,77 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, in
 }
 
 // ------------------------------------------------------------ combine
+// A warp per (token, segment of 128 16-byte chunks of its row); lane l
+// handles chunks l, l+32, l+64, l+96 of the segment, so every load and store
+// instruction of the warp covers 512 contiguous bytes.  The K copies' rows
+// are loaded NB copies at a time (4 * NB 16-byte loads in flight per lane),
+// summed in fp32 in copy order k = 0..K-1 (then the shared expert's row),
+// and stored as bf16.
 template <int NB>   // copies whose loads are issued together
 __global__ void __launch_bounds__(256) combine_kernel(int n_tok, int d8, int K, const uint4* __restrict__ y_perm,
                                                       const int32_t* __restrict__ row_of_copy,
                                                       const float* __restrict__ topk_w,
                                                       const uint4* __restrict__ y_shared, uint4* __restrict__ out) {
-  __shared__ int s_rows[32];
-  __shared__ float s_w[32];
-  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
-    __syncthreads();
-    if (threadIdx.x < K) {
-      s_rows[threadIdx.x] = row_of_copy[static_cast<int64_t>(t) * K + threadIdx.x];
-      s_w[threadIdx.x] = topk_w[static_cast<int64_t>(t) * K + threadIdx.x];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < d8; i += blockDim.x) {
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      // NB copies' loads in flight at once; a dropped copy (capacity mode)
-      // or a slot past K adds 0 * 0, which leaves acc unchanged (acc, a sum
-      // started at +0, is never -0)
-      for (int k0 = 0; k0 < K; k0 += NB) {
-        uint4 u[NB];
-        float wk[NB];
+  const int lane = threadIdx.x & 31;
+  const int segs = (d8 + 127) / 128;
+  const int64_t items = static_cast<int64_t>(n_tok) * segs;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += wstride) {
+    const int t = static_cast<int>(it / segs);
+    const int i0 = static_cast<int>(it - static_cast<int64_t>(t) * segs) * 128 + lane;
+    float acc[4][8];
 #pragma unroll
-        for (int j = 0; j < NB; ++j) {
-          const int r = k0 + j < K ? s_rows[k0 + j] : -1;
-          u[j] = r >= 0 ? y_perm[static_cast<int64_t>(r) * d8 + i] : make_uint4(0, 0, 0, 0);
-          wk[j] = r >= 0 ? s_w[k0 + j] : 0.0f;
+    for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) acc[qq][jj] = 0.0f;
+    // a dropped copy (capacity mode) or a slot past K adds 0 * 0, which
+    // leaves acc unchanged (acc, a sum started at +0, is never -0)
+    for (int k0 = 0; k0 < K; k0 += NB) {
+      uint4 v[NB][4];
+      float wk[NB];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const int k = k0 + j;
+        const int r = k < K ? __ldg(row_of_copy + static_cast<int64_t>(t) * K + k) : -1;
+        wk[j] = r >= 0 ? __ldg(topk_w + static_cast<int64_t>(t) * K + k) : 0.0f;
+        const uint4* src = y_perm + static_cast<int64_t>(r >= 0 ? r : 0) * d8;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int i = i0 + 32 * qq;
+          v[j][qq] = (r >= 0 && i < d8) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         }
+      }
 #pragma unroll
-        for (int j = 0; j < NB; ++j) {
+      for (int j = 0; j < NB; ++j) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
           float y[8];
-          unpack8(u[j], y);
+          unpack8(v[j][qq], y);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) acc[jj] = fmaf(wk[j], y[jj], acc[jj]);
+          for (int jj = 0; jj < 8; ++jj) acc[qq][jj] = fmaf(wk[j], y[jj], acc[qq][jj]);
         }
       }
-      if (y_shared) {
-        float y[8];
-        unpack8(y_shared[static_cast<int64_t>(t) * d8 + i], y);
+    }
+    if (y_shared) {
+      uint4 sv[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += y[j];
+      for (int qq = 0; qq < 4; ++qq) {
+        const int i = i0 + 32 * qq;
+        sv[qq] = i < d8 ? __ldg(y_shared + static_cast<int64_t>(t) * d8 + i) : make_uint4(0, 0, 0, 0);
       }
-      out[static_cast<int64_t>(t) * d8 + i] = pack8(acc);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        float y[8];
+        unpack8(sv[qq], y);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[qq][jj] += y[jj];
+      }
+    }
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int i = i0 + 32 * qq;
+      if (i < d8) out[static_cast<int64_t>(t) * d8 + i] = pack8(acc[qq]);
     }
   }
 }
@@ -727,11 +1024,15 @@ __global__ void dense_offsets_kernel(int32_t* dst, int n) {
   }
 }
 
-int grid_for_tokens(int n_tok) {
+int num_sms_kernels() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int g = sms > 0 ? sms * 8 : 1024;
+  return sms > 0 ? sms : 128;
+}
+
+int grid_for_tokens(int n_tok) {
+  const int g = num_sms_kernels() * 8;
   return n_tok < g ? (n_tok > 0 ? n_tok : 1) : g;
 }
 
@@ -756,6 +1057,23 @@ cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* b
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_fused(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
+                                float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                int32_t* acc, int32_t* ticket, int32_t* status, cudaStream_t st) {
+  if (s.n_tok <= 0 || s.n_exp > 32 || d % 32) return cudaErrorInvalidValue;
+  const int blocks = static_cast<int>((static_cast<int64_t>(s.n_tok) + kRtTok - 1) / kRtTok);
+  const int nt = (s.n_exp + 7) / 8;
+#define MOE_ROUTER(NT)                                                                                            \
+  router_fused_kernel<NT><<<blocks, kRtWarps * 32, 0, st>>>(s, d / 8, static_cast<const uint4*>(x),               \
+                                                            static_cast<const uint4*>(w_gate), bias, logits,       \
+                                                            topk_idx, topk_w, counts, offsets, acc, ticket, status)
+  if (nt <= 1) MOE_ROUTER(1);
+  else if (nt <= 2) MOE_ROUTER(2);
+  else MOE_ROUTER(4);
+#undef MOE_ROUTER
+  return cudaGetLastError();
+}
+
 cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
                            int32_t* status, cudaStream_t st) {
   if (n_exp > 1024) return cudaErrorInvalidValue;
@@ -774,8 +1092,19 @@ int permute_num_chunks(int n_tok) { return (n_tok + kChunkTok - 1) / kChunkTok; 
 
 cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
                                 int32_t* block_counts, int32_t* block_base, int32_t* row_of_copy,
-                                int32_t* copy_of_row, int32_t* status, cudaStream_t st) {
+                                int32_t* copy_of_row, int32_t* status, cudaStream_t st, bool chunked) {
   if (n_tok <= 0) return cudaSuccess;
+  if (!chunked && static_cast<int64_t>(n_tok) * top_k <= kMapOnePassMax) {
+    const size_t smem = static_cast<size_t>(33) * n_exp * sizeof(int);
+    if (smem > 48 * 1024) {   // above the default dynamic shared-memory limit (more than 372 experts)
+      const cudaError_t e = cudaFuncSetAttribute(maps_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    maps_onepass_kernel<<<1, 1024, smem, st>>>(n_tok, n_exp, top_k, topk_idx, offsets, row_of_copy, copy_of_row,
+                                               status);
+    return cudaGetLastError();
+  }
   const int nch = permute_num_chunks(n_tok);
   const size_t smem = static_cast<size_t>(n_exp) * sizeof(int);
   block_hist_kernel<<<nch, 256, smem, st>>>(n_tok, n_exp, top_k, topk_idx, block_counts, status);
@@ -807,8 +1136,10 @@ cudaError_t launch_combine(int n_tok, int d, int top_k, const void* y_perm, cons
                            const float* topk_w, const void* y_shared, void* out, cudaStream_t st) {
   if (n_tok <= 0) return cudaSuccess;
   auto kern = top_k == 1 ? combine_kernel<1> : (top_k == 2 ? combine_kernel<2> : combine_kernel<4>);
-  kern<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(y_perm), row_of_copy,
-                                               topk_w, static_cast<const uint4*>(y_shared), static_cast<uint4*>(out));
+  const int64_t items = static_cast<int64_t>(n_tok) * ((d / 8 + 127) / 128);   // one warp each
+  const int blocks = static_cast<int>(std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(num_sms_kernels()) * 8));
+  kern<<<blocks, 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(y_perm), row_of_copy, topk_w,
+                               static_cast<const uint4*>(y_shared), static_cast<uint4*>(out));
   return cudaGetLastError();
 }
 

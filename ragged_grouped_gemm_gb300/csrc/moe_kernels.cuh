@@ -18,6 +18,13 @@ struct RouteShape {
 // the unbiased logits, and the expert histogram (counts must be zeroed).
 cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* bias, int32_t* topk_idx,
                         float* topk_w, int32_t* counts, int32_t* status, cudaStream_t st);
+// The whole router of a layer with E <= 32 in one launch: logits (warp-level
+// tensor-core MMA, fp32), top-K and weights as launch_topk, counts and
+// offsets as launch_offsets.  acc: E int32 and ticket: one int32, all zero
+// before the launch (the kernel leaves them zero).  D must be a multiple of 32.
+cudaError_t launch_router_fused(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
+                                float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                int32_t* acc, int32_t* ticket, int32_t* status, cudaStream_t st);
 // offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]; checks the total.
 cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
                            int32_t* status, cudaStream_t st);
@@ -25,12 +32,14 @@ cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_to
 cudaError_t launch_update_bias(const int32_t* counts, int n_exp, float* bias, float gamma, int mode,
                                cudaStream_t st);
 
-// Token chunking of the permute: block_counts/block_base are
-// [num_chunks(n_tok), n_exp] int32 scratch.
+// The stable expert-major permutation maps.  Up to 65536 copies run in one
+// CTA with no scratch (unless `chunked`); otherwise, or with `chunked`, the
+// token-chunked form runs with block_counts/block_base as
+// [num_chunks(n_tok), n_exp] int32 scratch.  Both give the same maps.
 int permute_num_chunks(int n_tok);
 cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
                                 int32_t* block_counts, int32_t* block_base, int32_t* row_of_copy,
-                                int32_t* copy_of_row, int32_t* status, cudaStream_t st);
+                                int32_t* copy_of_row, int32_t* status, cudaStream_t st, bool chunked = false);
 // x_perm[row_of_copy[t*K+k]] = x[t] (bf16 rows of d elements).
 cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, const int32_t* row_of_copy,
                                 void* x_perm, cudaStream_t st);

@@ -64,8 +64,9 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_desc_t* d, const void* x, 
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Both tables are rewritten in full by every call, so nothing needs clearing.
+  // the token-chunked map kernels, with their two chunk tables in the array
   if (moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, scratch, scratch + kScratchInts / 2,
-                               row_of_copy, copy_of_row, nullptr, st) != cudaSuccess)
+                               row_of_copy, copy_of_row, nullptr, st, /*chunked=*/true) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -50,14 +50,18 @@ def test_launch_counts():
     import bench
     from ragged_grouped_gemm_gb300.inputs import CONFIGS
     mix, ds = CONFIGS["mixtral"], CONFIGS["dsv3"]
-    # forward 12 (route 5: dense offsets, logits GEMM in 4 contraction slices, their sum, top-K, scan;
-    # permute 4; GEMM1, GEMM2, combine) + backward 10 (combine bwd, 5 GEMMs, unpermute, router gradient 3)
-    assert bench.route_launches(mix) == 5
-    assert bench.launches_per_step(mix) == 22
+    # forward 6 (fused router; permute: single-CTA maps + rows; GEMM1, GEMM2, combine)
+    # + backward 10 (combine bwd, 5 GEMMs, unpermute, router gradient 3)
+    assert bench.route_launches(mix) == 1
+    assert bench.launches_per_step(mix) == 16
+    # E = 256: dense offsets, logits GEMM in 4 contraction slices, their sum, top-K, scan;
     # + shared expert (3 forward, 6 backward) + route-bias update
-    assert bench.launches_per_step(ds) == 22 + 3 + 6 + 1
-    # enough 128-token tiles to fill the GPU: no slices
-    assert bench.route_launches(mix.replace(n_tok=65536)) == 4
+    assert bench.route_launches(ds) == 5
+    assert bench.launches_per_step(ds) == 5 + 2 + 3 + 10 + 3 + 6 + 1
+    # enough 128-token tiles to fill the GPU: no slices; more than 65536 copies: chunked maps
+    big = ds.replace(n_tok=65536)
+    assert bench.route_launches(big) == 4
+    assert bench.launches_per_step(big) == 4 + 4 + 3 + 10 + 3 + 6 + 1
 
 
 def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):

@@ -85,9 +85,18 @@ def test_route_from_logits_bitexact(name, mode):
     np.testing.assert_array_equal(off.cpu().numpy(), O.exclusive_offsets(counts))
 
 
-@pytest.mark.parametrize("name", SMALL + ["dsv3"])
+# extra router shapes: E = 24 and 32 (fused router with 3 and 4 column
+# tiles of 8 experts, token counts off the 16-token tile), a bias
+ROUTER_EXTRA = {
+    "router_e24": MoEConfig("router_e24", 515, 128, 64, 24, 3),
+    "router_e32": MoEConfig("router_e32", 1001, 192, 64, 32, 4, gate="sigmoid", use_bias=True, bias_beta=0.5,
+                            n_cold=2),
+}
+
+
+@pytest.mark.parametrize("name", SMALL + ["dsv3"] + list(ROUTER_EXTRA))
 def test_route_gate_gemm(name):
-    cfg = CONFIGS[name]
+    cfg = ROUTER_EXTRA.get(name) or CONFIGS[name]
     p_cpu = make_layer(cfg.replace(d_ff=64), "cpu") if name == "dsv3" else make_layer(cfg, "cpu")
     x, wg = p_cpu["x"], p_cpu["w_gate"]
     bias = p_cpu["bias"]
@@ -113,9 +122,14 @@ def test_route_gate_gemm(name):
 
 
 # ------------------------------------------------------------- permutation
-@pytest.mark.parametrize("name", SMALL + ["dsv3"])
+# more than 65536 copies: the token-chunked map kernels (three launches)
+# instead of the single-CTA pass
+LARGE_R = MoEConfig("large_r", 9000, 64, 64, 16, 8)
+
+
+@pytest.mark.parametrize("name", SMALL + ["dsv3", "large_r"])
 def test_permute_bitexact(name):
-    cfg = CONFIGS[name]
+    cfg = LARGE_R if name == "large_r" else CONFIGS[name]
     n, dm, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
     lg = skewed_logits(n, e, "zipf" if e > 8 else "uniform").numpy()
     ridx, _ = O.route(lg, None, k, cfg.gate)
