@@ -177,7 +177,7 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, int32_t* status_host,
  *   logits[N,E] (fp32 out) = x[N,D] (bf16) * w_gate[E,D]^T  (tensor cores,
  *                            fp32 accumulation, deterministic.  E <= 32: the
  *                            whole router is one kernel (warp-level MMA over
- *                            16-token tiles, the contraction cut into 8
+ *                            16-token tiles, the contraction cut into 16
  *                            slices added in slice order, then the selection
  *                            and histogram below).  E > 32: the grouped GEMM
  *                            on 128-token tiles; with few tiles the
@@ -213,6 +213,13 @@ MOE_API moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32
                          int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* The maps of moe_permute alone (row_of_copy, copy_of_row; no row is
+ * copied), for moe_grouped_ffn_gather.  Same arguments, results and errors
+ * as moe_permute without x and x_perm.  Needs the forward workspace. */
+MOE_API moe_status_t moe_permute_maps(const moe_desc_t* d, const int32_t* topk_idx, const int32_t* offsets,
+                                      int32_t* row_of_copy, int32_t* copy_of_row, void* ws, size_t ws_bytes,
+                                      void* stream);
+
 /* Ragged grouped SwiGLU FFN (§9 Expert; grouped GEMM of "Accelerating
  * Dropless MoE Training in JAX with NVIDIA Transformer Engine" ¶5): for every
  * expert e and its rows r in [offsets[e], offsets[e+1]):
@@ -226,6 +233,21 @@ MOE_API moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32
 MOE_API moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
                              const moe_expert_weights_t* w, const moe_ffn_saved_t* saved, void* y_perm,
                              void* y_shared, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_grouped_ffn with the dispatch fused into GEMM1's operand loads
+ * ("LLM Infrastructure Engineering 08: MoE Training Engineering" §9
+ * engineering notes: scatter + grouped GEMM): GEMM1 reads the rows of
+ * expert e straight from the token matrix x [N,D] (bf16), row r being token
+ * copy_of_row[r] / K, by TMA four-row gathers, so no permuted copy of the
+ * tokens is written or read.  copy_of_row and offsets come from
+ * moe_permute_maps (or moe_permute); every other argument, output and saved
+ * activation as moe_grouped_ffn, with bit-identical results.  bf16 layers
+ * only (MOE_ERR_UNSUPPORTED otherwise).  A training step still needs
+ * x_perm for the w1/w3 weight gradients (moe_permute). */
+MOE_API moe_status_t moe_grouped_ffn_gather(const moe_desc_t* d, const void* x, const int32_t* copy_of_row,
+                                            const int32_t* offsets, const moe_expert_weights_t* w,
+                                            const moe_ffn_saved_t* saved, void* y_perm, void* y_shared, void* ws,
+                                            size_t ws_bytes, void* stream);
 
 /* Combine (§9 index_add_ of weighted outputs plus shared expert; §12.5
  * unsort + K-sum): out[t] = sum_{k<K} topk_w[t,k] * y_perm[row_of_copy[t*K+k]]

@@ -97,6 +97,9 @@ SIGNATURES = {
                                 ctypes.POINTER(ctypes.c_int64)]),
     "moe_timing_disable": (c_i32, []),
     "moe_selftest_wait_timeout": (c_i32, [c_vp, ctypes.c_size_t, ctypes.c_uint64, c_i32, c_vp]),
+    "moe_permute_maps": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
+    "moe_grouped_ffn_gather": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, ctypes.POINTER(MoeExpertWeights),
+                                       ctypes.POINTER(MoeFfnSaved), c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
 }
 
 _LIB = None

@@ -136,6 +136,38 @@ def moe_grouped_ffn(desc, x_perm, offsets, x, w1, w3, w2, ws1, ws3, ws2, a1, a3,
         _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
+def moe_permute_maps(desc, topk_idx, offsets, row_of_copy, copy_of_row, ws, stream=None):
+    """The permutation maps of moe_permute without copying any row."""
+    n, e, k = desc.n_tok, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_permute_maps", _lib.load().moe_permute_maps(
+        ctypes.byref(desc), _p(topk_idx, I32, (n, k), "topk_idx"), _p(offsets, I32, (e + 1,), "offsets"),
+        _p(row_of_copy, I32, (r,), "row_of_copy"), _p(copy_of_row, I32, (r,), "copy_of_row"), _p(ws, name="ws"),
+        ws.numel() * ws.element_size(), _s(stream)))
+
+
+def moe_grouped_ffn_gather(desc, x, copy_of_row, offsets, w1, w3, w2, ws1, ws3, ws2, a1, a3, h, a1s, a3s, hs,
+                           y_perm, y_shared, ws, stream=None):
+    """moe_grouped_ffn reading GEMM1's rows from x through copy_of_row (TMA gathers)."""
+    n, d, f, e, k = desc.n_tok, desc.d_model, desc.d_ff, desc.n_exp, desc.top_k
+    r, fs = n * k, desc.d_ff_shared
+    sh = desc.n_shared
+    w = _lib.MoeExpertWeights(_p(w1, BF16, (e, f, d), "w1"), _p(w3, BF16, (e, f, d), "w3"),
+                              _p(w2, BF16, (e, d, f), "w2"),
+                              _p(ws1, BF16, (fs, d), "ws1") if sh else None,
+                              _p(ws3, BF16, (fs, d), "ws3") if sh else None,
+                              _p(ws2, BF16, (d, fs), "ws2") if sh else None)
+    sv = _lib.MoeFfnSaved(_p(a1, BF16, (r, f), "a1"), _p(a3, BF16, (r, f), "a3"), _p(h, BF16, (r, f), "h"),
+                          _p(a1s, BF16, (n, fs), "a1s") if sh else None,
+                          _p(a3s, BF16, (n, fs), "a3s") if sh else None,
+                          _p(hs, BF16, (n, fs), "hs") if sh else None)
+    _check("moe_grouped_ffn_gather", _lib.load().moe_grouped_ffn_gather(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(copy_of_row, I32, (r,), "copy_of_row"),
+        _p(offsets, I32, (e + 1,), "offsets"), ctypes.byref(w), ctypes.byref(sv),
+        _p(y_perm, BF16, (r, d), "y_perm"), _p(y_shared, BF16, (n, d), "y_shared") if sh else None,
+        _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
 def moe_combine(desc, y_perm, row_of_copy, topk_w, y_shared, out, stream=None):
     n, d, k = desc.n_tok, desc.d_model, desc.top_k
     r = n * k
@@ -431,10 +463,14 @@ class MoELayer:
         n, d, f, e, k = cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k
         r, fs = cfg.rows, cfg.d_ff_shared
         z = lambda *s, dt=BF16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+        # an inference layer with bf16 experts and no capacity reads GEMM1's rows
+        # straight from x (moe_permute_maps + moe_grouped_ffn_gather): no x_perm
+        self.gather = (not train) and cfg.precision == "bf16" and cfg.capacity_factor <= 0
         self.buf = {
             "logits": z(n, e, dt=F32), "topk_idx": z(n, k, dt=I32), "topk_w": z(n, k, dt=F32),
             "counts": z(e, dt=I32), "offsets": z(e + 1, dt=I32), "row_of_copy": z(r, dt=I32),
-            "copy_of_row": z(r, dt=I32), "x_perm": z(r, d), "h": z(r, f), "y_perm": z(r, d), "out": z(n, d),
+            "copy_of_row": z(r, dt=I32), "x_perm": None if self.gather else z(r, d), "h": z(r, f),
+            "y_perm": z(r, d), "out": z(n, d),
             "a1": z(r, f) if train else None, "a3": z(r, f) if train else None,
         }
         if cfg.n_shared:
@@ -478,6 +514,15 @@ class MoELayer:
                   b["offsets_full"] if self.cap else b["offsets"], self.ws, stream)
         if self.mx:
             return self._forward_mx(x, stream)
+        if self.gather:
+            b = self.buf
+            moe_permute_maps(self.desc, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], self.ws,
+                             stream)
+            moe_grouped_ffn_gather(self.desc, x, b["copy_of_row"], b["offsets"], p["w1"], p["w3"], p["w2"],
+                                   p.get("ws1"), p.get("ws3"), p.get("ws2"), None, None, b["h"], None, None,
+                                   b["hs"], b["y_perm"], b["y_shared"], self.ws, stream)
+            moe_combine(self.desc, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"], stream)
+            return b["out"]
         self._permute(x, stream)
         return self._ffn_combine(x, stream)
 

@@ -100,10 +100,17 @@ struct KParams {
   const float* wscale[2];
   int32_t ws_cols;       // column tiles per matrix
   int64_t ws_gstride;    // tiles per matrix
+  // GATHER: A row r of the ragged-M problem is row a_gather[r] / gather_k of
+  // the token matrix behind tmA[0] (a 2-D map with one-row boxes)
+  const int32_t* a_gather;
+  int32_t gather_k;
 };
 
 // STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
-template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false, bool STG = false>
+// MAXG / MAXS: the most groups the shared-memory tables hold and the most
+// ring stages
+template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false, bool STG = false, int MAXG = kMaxGroups,
+          int MAXS = 6>
 struct Cfg {
   // FP8 weights (W8): the B codes of a k-block (BN x 64 bytes) land in a
   // two-slot staging ring; converters write the bf16 B tile into the stage
@@ -123,12 +130,12 @@ struct Cfg {
   static constexpr int kStageBytes =
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
   // shared memory left for the stages: 227 KB less the alignment slack, the
-  // staging buffers, the barriers (at most 6 stages) and the group tables
+  // staging buffers, the barriers (at most MAXS stages) and the group tables
   static constexpr int kEpiBytes = STG ? 8 * 2048 : 0;
-  static constexpr int kStageBudget = 232448 - 1024 - kEpiBytes - (3 * 6 + 2 * 2 + 5) * 8 - 16 -
-                                      2 * 4 * (kMaxGroups + 1) - kW8Slots * kW8SlotBytes;
+  static constexpr int kStageBudget = 232448 - 1024 - kEpiBytes - (3 * MAXS + 2 * 2 + 5) * 8 - 16 -
+                                      2 * 4 * (MAXG + 1) - kW8Slots * kW8SlotBytes;
   static constexpr int kStagesRaw = kStageBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  static constexpr int kStages = kStagesRaw > MAXS ? MAXS : kStagesRaw;
   // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
   static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
   static constexpr uint32_t kSfCol = 2 * BN;
@@ -139,13 +146,33 @@ struct Cfg {
   static constexpr int kBarOff = kEpiOff + kEpiBytes;
   static constexpr int kMiscOff = kBarOff + ((QUANT ? 3 : 2) * kStages + 2 * kW8Slots + 5) * 8;
   static constexpr int kOffOff = kMiscOff + 16;
+  static constexpr int kMaxG = MAXG;
   static constexpr size_t smem_bytes(int groups) {
     return 1024 + kOffOff + 2 * 4 * (groups + 1);
   }
   static_assert(kStages >= 2, "shared memory holds fewer than two stages");
-  static_assert(smem_bytes(kMaxGroups) <= 232448, "shared memory above 227 KB");
+  static_assert(smem_bytes(MAXG) <= 232448, "shared memory above 227 KB");
   static_assert(!QUANT || 2 * BN + 16 * kStages <= 512, "accumulators and scale buffers exceed tensor memory");
 };
+
+// The weight gradients on CTA pairs (ragged K, bf16, fp32 out) write their
+// output straight from registers with 256-bit stores instead of staging it
+// for TMA stores: the 16 KB of staging and a group table for at most 64
+// groups leave room for a seventh 32 KB ring stage, which covers more of the
+// operand-load latency this short-contraction form is bound by.
+constexpr int kWgPairMaxGroups = 64;
+template <int BN, bool A_MN, int EPI, bool QUANT, bool PAIR, bool W8>
+struct FormCfg {
+  static constexpr bool kDirectF32 = PAIR && A_MN && !QUANT && !W8 && EPI == EPI_F32;
+  using type = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32 && !kDirectF32, kDirectF32 ? kWgPairMaxGroups : kMaxGroups,
+                   kDirectF32 ? 7 : 6>;
+};
+
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 
 struct Tile {
   int g, mt, nt;
@@ -273,10 +300,16 @@ __device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int
   return nkk;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false>
+// GATHER (ragged M, bf16, one contraction source): A rows are gathered from
+// the token matrix through p.a_gather by TMA tile::gather4, four rows per
+// instruction, every lane of the producer warp taking four of the tile's
+// 128 rows; no permuted copy of the tokens is read.
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 = false, bool GATHER = false>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
     grouped_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
+  static_assert(!GATHER || (!A_MN && !B_MN && !QUANT && !W8), "GATHER: K-major bf16 ragged-M forms");
+  using C = typename FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::type;
+  constexpr bool kDirectF32 = FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::kDirectF32;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
@@ -433,6 +466,71 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           mbar_wait_drain(&full[s], (last / S) & 1u);
         }
       }
+    } else if (GATHER) {
+      // Gathered A: lane l loads the tile's rows 4l..4l+3 (token row
+      // a_gather[r] / gather_k; a row past the group's end loads token row 0,
+      // whose products the epilogue never stores) by one gather4 into its
+      // 512-byte quarter-atom of the stage; lane 0 waits for the stage, arms
+      // the barrier and loads B.
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
+        const Tile t = decode_tile<false, BN, PAIR>(tile, p, s_off, s_pre, rank);
+        const int gend = s_off[t.g + 1];
+        int rr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = t.row0 + 4 * lane + j;
+          rr[j] = r < gend ? __ldg(p.a_gather + r) / p.gather_k : 0;
+        }
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          int okl = 1;
+          if (lane == 0) okl = mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, okl, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + s * C::kStageBytes;
+          uint8_t* sB = sA + kABytes;
+          const int k0 = kb * BK;
+          if (PAIR) {
+            if (leader && lane == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
+            __syncwarp();
+            tma_gather4_pair(sA + lane * 512, &p.tmA[0], bar, k0, rr[0], rr[1], rr[2], rr[3]);
+            if (lane == 0) {
+              if (p.b_dual_n) tma_load_3d_pair(sB, &p.tmB[rank], bar, k0, t.nt * (BN / 2), t.g);
+              else tma_load_3d_pair(sB, &p.tmB[0], bar, k0, t.nt * BN + rank * (BN / 2), t.g);
+            }
+          } else {
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            __syncwarp();
+            tma_gather4(sA + lane * 512, &p.tmA[0], &full[s], k0, rr[0], rr[1], rr[2], rr[3]);
+            if (lane == 0) {
+              if (p.b_dual_n) {
+                const int f0 = t.nt * (BN / 2);
+                tma_load_3d(sB, &p.tmB[0], &full[s], k0, f0, t.g);
+                tma_load_3d(sB + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
+              } else {
+                tma_load_3d(sB, &p.tmB[0], &full[s], k0, t.nt * BN, t.g);
+              }
+            }
+          }
+        }
+      }
+      // every stage's last armed load has landed before the CTA exits (for a
+      // pair the leader's barriers count both CTAs' copies)
+      if (lane == 0 && (!PAIR || leader)) {
+        for (int s = 0; s < S; ++s) {
+          if (it > static_cast<uint32_t>(s)) {
+            const uint32_t last = s + S * ((it - 1 - s) / S);
+            mbar_wait_drain(&full[s], (last / S) & 1u);
+          }
+        }
+      }
+      __syncwarp();
     } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
       uint32_t lph = 0, lused = 0;   // ragged-K pair peer: phases of its own stage barriers
@@ -837,7 +935,40 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         }
         const bool zero = t.num_kb == 0;
         const int c_begin = hf * (BN / 2);
-        if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
+        if (kDirectF32) {
+          // This warp's 32 rows x BN/2 columns straight from registers: TMEM
+          // loads of 32 columns (the next one in flight while this one is
+          // stored), each row's 128 bytes as four 256-bit stores.
+          constexpr int NCH = BN / 64;
+          uint32_t va[32], vb[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) va[j] = 0u;
+          if (!zero) {
+            tmem_ld_32x32b_x32(tb + c_begin, va);
+            tmem_wait_ld(va);
+          }
+          float* drow = reinterpret_cast<float*>(obase) + grow * p.ld_out + t.nt * BN + c_begin;
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            if (i + 1 < NCH) {
+              if (!zero) tmem_ld_32x32b_x32(tb + c_begin + 32 * (i + 1), vb);
+              else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vb[j] = 0u;
+              }
+            }
+            const int col = t.nt * BN + c_begin + 32 * i;
+            if (row_ok && col < p.n_size) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) st_global_v8(drow + 32 * i + 8 * j, va + 8 * j);
+            }
+            if (i + 1 < NCH) {
+              if (!zero) tmem_wait_ld(vb);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) va[j] = vb[j];
+            }
+          }
+        } else if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
           // Stage this warp's 32 rows x 32 columns as two 16-row halves in a
           // 2 KB shared-memory buffer (128-byte swizzle: 16-byte chunk j of
           // row r at chunk j ^ (r & 7)) and write each half with a TMA tensor
@@ -1238,18 +1369,19 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false,
+          bool GATHER = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
-  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
+  using C = typename FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::type;
   constexpr int CN = 2;   // CTAs per cluster (PAIR)
   const size_t smem = C::smem_bytes(kp.num_groups);
-  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8>;
+  auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8, GATHER>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_units = 0;   // co-resident CTAs (or CTA pairs)
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(C::smem_bytes(kMaxGroups)));
+                                    static_cast<int>(C::smem_bytes(C::kMaxG)));
     max_units = PAIR ? num_sms() / CN : num_sms();
     if (attr_err == cudaSuccess && PAIR) {
       cudaLaunchConfig_t cfg{};
@@ -1260,7 +1392,7 @@ cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream
       at[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(CN * max_units);
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = C::smem_bytes(kMaxGroups);
+      cfg.dynamicSmemBytes = C::smem_bytes(C::kMaxG);
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
@@ -1477,9 +1609,41 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (a.epi == EPI_BF16) return launch_impl<256, false, true, EPI_BF16, false, false, true>(kp, tiles_ub, stream);
     return cudaErrorInvalidValue;
   }
+  if (a.a_gather) {
+    // gathered A rows (ragged M, K-major bf16, one contraction source): a 2-D
+    // map of the token matrix with one-row boxes for tile::gather4
+    if (a.ragged_k || a.a_mn || a.b_mn || a.k1 > 0 || BN != 256 || a.gather_k <= 0 ||
+        (a.epi != EPI_SWIGLU_FWD && a.epi != EPI_BF16) || a.max_rows <= 0)
+      return a.max_rows <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    const bool pair = use_cta_pair(a.max_rows, a.num_groups);
+    kp.kblk = BK;
+    kp.kb0 = (a.k0 + BK - 1) / BK;
+    kp.kb1 = 0;
+    if (kp.kb0 <= 0) return cudaErrorInvalidValue;
+    if (!make_map(&kp.tmA[0], a.a[0], 64, 1, false)) return cudaErrorInvalidValue;
+    kp.tmA[1] = kp.tmA[0];
+    const int box_rows = (a.b_dual_n || pair) ? BN / 2 : BN;
+    if (!make_map(&kp.tmB[0], a.b[0], 64, box_rows, true)) return cudaErrorInvalidValue;
+    if (a.b_dual_n) {
+      if (!make_map(&kp.tmB[1], a.b[1], 64, BN / 2, true)) return cudaErrorInvalidValue;
+    } else {
+      kp.tmB[1] = kp.tmB[0];
+    }
+    kp.a_gather = a.a_gather;
+    kp.gather_k = a.gather_k;
+    const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
+    const int64_t ur = pair ? 2 * BM : BM;
+    const int64_t u = ntiles * ((a.max_rows + ur - 1) / ur + a.num_groups);
+    if (a.epi == EPI_SWIGLU_FWD)
+      return pair ? launch_impl<256, false, false, EPI_SWIGLU_FWD, false, true, false, true>(kp, u, stream)
+                  : launch_impl<256, false, false, EPI_SWIGLU_FWD, false, false, false, true>(kp, u, stream);
+    return pair ? launch_impl<256, false, false, EPI_BF16, false, true, false, true>(kp, u, stream)
+                : launch_impl<256, false, false, EPI_BF16, false, false, false, true>(kp, u, stream);
+  }
   // CTA pairs: each CTA loads its own 128 rows of A and half of the B tile
+  // (weight gradients: at most kWgPairMaxGroups groups)
   const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&
-                    (a.ragged_k ? a.epi == EPI_F32
+                    (a.ragged_k ? (a.epi == EPI_F32 && a.num_groups <= kWgPairMaxGroups)
                                 : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));
   kp.kblk = BK;
   if (!a.ragged_k) {
@@ -1524,7 +1688,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (tiles_ub <= 0) return cudaSuccess;
   // fp32 outputs go through TMA stores when every tile's rows either belong to
   // its own output matrix (weight gradients) or end at the tensor's end (one group)
-  if (a.epi == EPI_F32 && (a.ragged_k || a.num_groups == 1)) {
+  if (a.epi == EPI_F32 && ((a.ragged_k && !pair) || (!a.ragged_k && a.num_groups == 1))) {
     const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
     const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
     kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : std::max(1, kp.ksplit),

@@ -88,6 +88,11 @@ struct GemmArgs {
   // [groups][ceil(rows/128)][ceil(cols/128)]; dequantised to bf16 in shared memory
   bool w8 = false;
   const float* w8_scale[2] = {nullptr, nullptr};
+  // Gathered A (ragged M, K-major bf16, one contraction source): row r of the
+  // problem is row a_gather[r] / gather_k of a[0] (the token matrix [N, K0]),
+  // loaded by TMA tile::gather4 instead of a permuted copy
+  const int32_t* a_gather = nullptr;
+  int gather_k = 0;
 };
 
 // Enqueue the grouped GEMM on `stream`.  Returns cudaSuccess or the first

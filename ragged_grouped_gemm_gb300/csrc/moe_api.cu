@@ -181,17 +181,22 @@ Operand wstack(const void* p, int64_t groups, int64_t rows, int64_t cols) {
 // SwiGLU FFN of one "expert set": GEMM1 (fused w1|w3 with SwiGLU epilogue)
 // then GEMM2, over `groups` ragged row groups of `a_in` [rows, D].
 // (w8: w1, w3, w2 are E4M3 codes with fp32 tile scales s1, s3, s2)
+// (gather: GEMM1's row r is row gather[r] / gather_k of a_in [n_src, D], read
+// by TMA gathers instead of a permuted copy)
 moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, const int32_t* offsets,
                       const void* w1, const void* w3, const void* w2, void* h, void* a1, void* a3, void* y,
                       int32_t* status, cudaStream_t st, const float* s1 = nullptr, const float* s3 = nullptr,
-                      const float* s2 = nullptr) {
+                      const float* s2 = nullptr, const int32_t* gather = nullptr, int gather_k = 0,
+                      int64_t n_src = 0) {
   const bool w8 = s1 != nullptr;
   GemmArgs g1;
   g1.w8 = w8;
   g1.w8_scale[0] = s1;
   g1.w8_scale[1] = s3;
   g1.epi = moe::EPI_SWIGLU_FWD;
-  g1.a[0] = act(a_in, rows, D);
+  g1.a[0] = act(a_in, gather ? n_src : rows, D);
+  g1.a_gather = gather;
+  g1.gather_k = gather_k;
   g1.b[0] = wstack(w1, groups, F, D);
   g1.b[1] = wstack(w3, groups, F, D);
   g1.b_dual_n = true;
@@ -457,6 +462,51 @@ moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int3
   const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
   MOE_TRY(ffn_pair(x_perm, R, d->d_model, d->d_ff, d->n_exp, offsets, w->w1, w->w3, w->w2, saved->h, saved->a1,
                    saved->a3, y_perm, status, st));
+  if (d->n_shared) {
+    int32_t* dense = at<int32_t>(ws, L.dense_off);
+    MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
+    MOE_TRY(ffn_pair(x, d->n_tok, d->d_model, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2, saved->hs,
+                     saved->a1s, saved->a3s, y_shared, status, st));
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_permute_maps(const moe_desc_t* d, const int32_t* topk_idx, const int32_t* offsets,
+                              int32_t* row_of_copy, int32_t* copy_of_row, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_permute_maps");
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (!topk_idx || !offsets || !row_of_copy || !copy_of_row) return MOE_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return MOE_OK;
+  const WsLayout L = layout(*d);
+  return cuda_status(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets,
+                                              at<int32_t>(ws, L.blk_counts), at<int32_t>(ws, L.blk_base),
+                                              row_of_copy, copy_of_row, at<int32_t>(ws, L.status),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn_gather(const moe_desc_t* d, const void* x, const int32_t* copy_of_row,
+                                    const int32_t* offsets, const moe_expert_weights_t* w, const moe_ffn_saved_t* saved,
+                                    void* y_perm, void* y_shared, void* ws, size_t ws_bytes, void* stream) {
+  MOE_RANGE("moe_grouped_ffn_gather");
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (d->precision != 0) return MOE_ERR_UNSUPPORTED;
+  if (!w || !saved || !offsets || !copy_of_row) return MOE_ERR_INVALID_ARG;
+  if (!all16({x, w->w1, w->w3, w->w2, saved->h, y_perm})) return MOE_ERR_INVALID_ARG;
+  if ((saved->a1 && !aligned16(saved->a1)) || (saved->a3 && !aligned16(saved->a3))) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared) {
+    if (!all16({w->ws1, w->ws3, w->ws2, saved->hs, y_shared})) return MOE_ERR_INVALID_ARG;
+    if ((saved->a1s && !aligned16(saved->a1s)) || (saved->a3s && !aligned16(saved->a3s)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (d->n_tok == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  MOE_TRY(ffn_pair(x, R, d->d_model, d->d_ff, d->n_exp, offsets, w->w1, w->w3, w->w2, saved->h, saved->a1,
+                   saved->a3, y_perm, status, st, nullptr, nullptr, nullptr, copy_of_row, d->top_k, d->n_tok));
   if (d->n_shared) {
     int32_t* dense = at<int32_t>(ws, L.dense_off);
     MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));

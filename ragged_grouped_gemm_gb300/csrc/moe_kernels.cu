@@ -171,9 +171,10 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __
 // The logits x W_g^T are a skinny contraction (N x D times D x E, E <= 32)
 // bound by the read of x, so they run on the warp-level tensor-core MMA
 // (mma.sync m16n8k16, bf16 in, fp32 accumulate) straight from registers:
-// each CTA takes a tile of 16 tokens, its 8 warps each a contiguous eighth
-// of the contraction, and every lane loads 16 bytes of a token row and of
-// the matching W_g row per 32-column block.  The contraction order inside a
+// each CTA takes a tile of 16 tokens, its 16 warps each a contiguous
+// sixteenth of the contraction, and every lane loads 16 bytes of a token row
+// and of the matching W_g row per 32-column block, four blocks' loads in
+// flight at once.  The contraction order inside a
 // block is a fixed permutation of the columns (the same on both operands),
 // and the warps' partial products are added in warp order, so the result
 // is deterministic.  A warp per token then selects the top K; each CTA adds
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __
 // takes the accumulator (resetting it to zero), writes counts and offsets,
 // checks that they sum to N*K, and resets the ticket.
 constexpr int kRtTok = 16;
-constexpr int kRtWarps = 8;
+constexpr int kRtWarps = 16;
 constexpr int kRtUnroll = 4;
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
     s_acc[warp][g + 8][8 * j + 2 * q + 1] = c[j][3];
   }
   __syncthreads();
-  // two tokens per warp: logits (partials added in warp order), top-K, weights
+  // a token per warp: logits (partials added in warp order), top-K, weights
   for (int tt = warp; tt < kRtTok; tt += kRtWarps) {
     const int t = tok0 + tt;
     if (t >= s.n_tok) break;
