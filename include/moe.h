@@ -163,9 +163,10 @@ MOE_API const char* moe_status_string(moe_status_t s);
  * workspace of bwd_bytes serves every call.  Either output may be NULL. */
 MOE_API moe_status_t moe_workspace_size(const moe_desc_t* d, size_t* fwd_bytes, size_t* bwd_bytes);
 
-/* Clear the 256-byte status block at the start of `ws` (enqueued on
- * stream): the device status words and the router's completion counters,
- * which every call leaves at zero again. */
+/* Clear the whole workspace (ws_bytes, enqueued on stream): the device
+ * status words and the counters and look-back words the router and the
+ * permutation keep there start at zero (every call leaves them ready for
+ * the next one).  Once per workspace, before its first use. */
 MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, then copy the two device status words (bits, site)
@@ -208,7 +209,12 @@ MOE_API moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* log
  * an expert.  row_of_copy[c] (out) is the permuted row of copy c;
  * copy_of_row[r] (out) its inverse; x_perm[r,:] (out, bf16 [R,D]) =
  * x[copy_of_row[r]/K,:].  Rows of expert e are offsets[e]..offsets[e+1]-1.
- * `offsets` comes from moe_route.  Needs the forward workspace. */
+ * `offsets` comes from moe_route.  One launch: each 16-token chunk finds its
+ * first row per expert from the preceding chunks' published counts (bounded
+ * waits; MOE_DEV_TIMEOUT if one ran out) and copies its rows.  A copy whose
+ * row would fall outside its expert's rows or [0, R) gets row -1
+ * (MOE_DEV_BAD_OFFSETS); an expert index outside [0, E) gets row -1
+ * (MOE_DEV_BAD_INDEX).  Needs the forward workspace. */
 MOE_API moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,
                          int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
                          void* stream);

@@ -104,6 +104,14 @@ struct KParams {
   // the token matrix behind tmA[0] (a 2-D map with one-row boxes)
   const int32_t* a_gather;
   int32_t gather_k;
+  // Ragged K (bf16): per-group copies of tmA[0] / tmB[0] whose rows are
+  // exactly the group's rows, one (A, B) pair per ring stage of each CTA,
+  // written by the CTA's producer into this global scratch
+  CUtensorMap* gmaps;
+  const char* ga_ptr;
+  const char* gb_ptr;
+  int64_t ga_ld_bytes;
+  int64_t gb_ld_bytes;
 };
 
 // STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
@@ -154,25 +162,6 @@ struct Cfg {
   static_assert(smem_bytes(MAXG) <= 232448, "shared memory above 227 KB");
   static_assert(!QUANT || 2 * BN + 16 * kStages <= 512, "accumulators and scale buffers exceed tensor memory");
 };
-
-// The weight gradients on CTA pairs (ragged K, bf16, fp32 out) write their
-// output straight from registers with 256-bit stores instead of staging it
-// for TMA stores: the 16 KB of staging and a group table for at most 64
-// groups leave room for a seventh 32 KB ring stage, which covers more of the
-// operand-load latency this short-contraction form is bound by.
-constexpr int kWgPairMaxGroups = 64;
-template <int BN, bool A_MN, int EPI, bool QUANT, bool PAIR, bool W8>
-struct FormCfg {
-  static constexpr bool kDirectF32 = PAIR && A_MN && !QUANT && !W8 && EPI == EPI_F32;
-  using type = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32 && !kDirectF32, kDirectF32 ? kWgPairMaxGroups : kMaxGroups,
-                   kDirectF32 ? 7 : 6>;
-};
-
-__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
-               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
 
 struct Tile {
   int g, mt, nt;
@@ -276,30 +265,6 @@ __device__ __forceinline__ int mx_exponent_of(float amax) {
   return max(-127, min(127, fl - 8));
 }
 
-// Ragged K: rows rv..nkk*16-1 of a k-block's operands belong to the next
-// group; zero them in this CTA's stage (A: 2 MN atoms, B: nb_atoms MN atoms,
-// each 64 K-rows x 128 B) and make the writes visible to the tensor cores.
-// Returns the number of K=16 steps that hold rows of the group.
-__device__ __forceinline__ int zero_k_tail(uint8_t* sA, uint8_t* sB, int rv, int nb_atoms, int lane) {
-  if (rv >= BK) return BK / 16;
-  const int nkk = (rv + 15) / 16;
-  const int zrows = nkk * 16 - rv;
-  if (zrows > 0) {
-    const int nreg = 2 + nb_atoms;
-    const int per_reg = zrows * 8;  // 16-byte chunks
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = lane; i < nreg * per_reg; i += 32) {
-      const int reg = i / per_reg;
-      const int j = i - reg * per_reg;
-      uint8_t* base = (reg < 2) ? (sA + reg * 8192) : (sB + (reg - 2) * 8192);
-      *reinterpret_cast<uint4*>(base + rv * 128 + j * 16) = z;
-    }
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-  return nkk;
-}
-
 // GATHER (ragged M, bf16, one contraction source): A rows are gathered from
 // the token matrix through p.a_gather by TMA tile::gather4, four rows per
 // instruction, every lane of the producer warp taking four of the tile's
@@ -308,8 +273,7 @@ template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
     grouped_gemm_kernel(const __grid_constant__ KParams p) {
   static_assert(!GATHER || (!A_MN && !B_MN && !QUANT && !W8), "GATHER: K-major bf16 ragged-M forms");
-  using C = typename FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::type;
-  constexpr bool kDirectF32 = FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::kDirectF32;
+  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
@@ -345,7 +309,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       // TMA (tx bytes), the converter threads, or (ragged-K pair, rank 0) this
       // CTA's TMA plus the peer's forwarded arrival
       // (FP8 weights: A's TMA bytes plus one arrival per converter warp)
-      mbar_init(&full[s], W8 ? 1 + kConvWarps : ((PAIR && RAGGED_K && leader) ? 2 : 1));
+      mbar_init(&full[s], W8 ? 1 + kConvWarps : 1);
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], kSfWarps);
@@ -533,7 +497,9 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       __syncwarp();
     } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
-      uint32_t lph = 0, lused = 0;   // ragged-K pair peer: phases of its own stage barriers
+      // ragged K: the group (+1) whose maps each stage's slot holds, 10 bits per stage
+      uint64_t slot_g = 0;
+      CUtensorMap* slots = RAGGED_K ? p.gmaps + static_cast<int64_t>(blockIdx.x) * 2 * S : nullptr;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
@@ -573,34 +539,40 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             }
             continue;
           }
-          if (PAIR && RAGGED_K) {
-            // A k-block whose group rows end off a 16-row boundary is loaded
-            // into each CTA's own barrier and zeroed past the group's end
-            // before the MMA (the peer forwards it); any other k-block loads
-            // straight onto the leader's barrier, which also counts one
-            // arrival from the peer's producer.
-            const int rv = t.k_rows - kb * BK;
-            const bool zfix = rv < BK && (rv & 15) != 0;
-            const int r = t.row0 + kb * BK;
-            const int n0 = t.nt * BN + (rank & 1) * (BN / 2);
-            if (!zfix) {
+          if (RAGGED_K) {
+            // The stage's slot holds maps of exactly the group's rows, so the
+            // last k-block of a group reads zeros past the group's end (TMA
+            // fill) instead of the next group's rows; a slot is rewritten
+            // only when its group changes (its previous load has landed: the
+            // stage was released).
+            CUtensorMap* mA = slots + 2 * s;
+            CUtensorMap* mB = mA + 1;
+            if (static_cast<int>((slot_g >> (10 * s)) & 1023u) != t.g + 1) {
+              const uint32_t rows = static_cast<uint32_t>(max(t.k_rows, 1));
+              tensormap_rebase_rows(mA, &p.tmA[0],
+                                    reinterpret_cast<uint64_t>(p.ga_ptr + static_cast<int64_t>(t.row0) * p.ga_ld_bytes),
+                                    rows);
+              tensormap_rebase_rows(mB, &p.tmB[0],
+                                    reinterpret_cast<uint64_t>(p.gb_ptr + static_cast<int64_t>(t.row0) * p.gb_ld_bytes),
+                                    rows);
+              slot_g = (slot_g & ~(1023ull << (10 * s))) | (static_cast<uint64_t>(t.g + 1) << (10 * s));
+            }
+            const int r = kb * BK;   // rows of the group
+            if (PAIR) {
+              // both CTAs' loads complete on the leader's barrier, armed by the leader
+              const int n0 = t.nt * BN + (rank & 1) * (BN / 2);
               if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
-              tma_load_2d_pair(sA, &p.tmA[0], bar, t.m0, r);
-              tma_load_2d_pair(sA + 8192, &p.tmA[0], bar, t.m0 + 64, r);
+              tma_load_2d_pair(sA, mA, bar, t.m0, r);
+              tma_load_2d_pair(sA + 8192, mA, bar, t.m0 + 64, r);
 #pragma unroll
-              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, &p.tmB[0], bar, n0 + 64 * a, r);
-              if (!leader) mbar_arrive_remote(bar);
+              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, mB, bar, n0 + 64 * a, r);
             } else {
               mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-              tma_load_2d(sA, &p.tmA[0], &full[s], t.m0, r);
-              tma_load_2d(sA + 8192, &p.tmA[0], &full[s], t.m0 + 64, r);
+              tma_load_2d(sA, mA, &full[s], t.m0, r);
+              tma_load_2d(sA + 8192, mA, &full[s], t.m0 + 64, r);
 #pragma unroll
-              for (int a = 0; a < BN / 128; ++a) tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], n0 + 64 * a, r);
-              if (!leader) {
-                lph ^= 1u << s;
-                lused |= 1u << s;
-              }
+              for (int a = 0; a < BN / 64; ++a) tma_load_2d(sB + a * 8192, mB, &full[s], t.nt * BN + 64 * a, r);
             }
             continue;
           }
@@ -641,28 +613,18 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
               for (int a = 0; a < BN / 64; ++a)
                 tma_load_3d(sB + a * 8192, &p.tmB[src], &full[s], t.nt * BN + 64 * a, k0, t.g);
             }
-          } else {
-            const int r = t.row0 + kb * BK;
-            tma_load_2d(sA, &p.tmA[0], &full[s], t.m0, r);
-            tma_load_2d(sA + 8192, &p.tmA[0], &full[s], t.m0 + 64, r);
-#pragma unroll
-            for (int a = 0; a < BN / 64; ++a)
-              tma_load_2d(sB + a * 8192, &p.tmB[0], &full[s], t.nt * BN + 64 * a, r);
           }
         }
       }
       // Wait (bounded) for every stage's last armed load so that no copy is
       // still landing in shared memory when the CTA exits (for a pair the
-      // leader's barriers count both CTAs' copies, except the peer's
-      // zero-fixed ragged-K blocks, which land on its own barriers).
+      // leader's barriers count both CTAs' copies).
       for (int s = 0; s < S && (!PAIR || leader); ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = s + S * ((it - 1 - s) / S);
           mbar_wait_drain(&full[s], (last / S) & 1u);
         }
       }
-      for (int s = 0; s < S && PAIR && RAGGED_K && !leader; ++s)
-        if ((lused >> s) & 1u) mbar_wait_drain(&full[s], ((lph >> s) & 1u) ^ 1u);
       for (int s = 0; s < C::kW8Slots; ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = s + C::kW8Slots * ((it - 1 - s) / C::kW8Slots);
@@ -671,28 +633,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       }
     }
   } else if (PAIR && warp == 1 && !leader) {
-    // The leader CTA issues the pair's MMAs.  Ragged K: for each k-block
-    // whose group rows end off a 16-row boundary this warp waits for the
-    // CTA's own copy, zeroes the rows past the group's end and releases the
-    // stage to the leader's barrier.
-    if (RAGGED_K) {
-      uint32_t it = 0, lph = 0;
-      bool ok = true;
-      for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
-        const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
-        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
-          const int rv = t.k_rows - kb * BK;
-          if (rv >= BK || (rv & 15) == 0) continue;
-          const int s = it % S;
-          if (!mbar_wait_bounded(&full[s], (lph >> s) & 1u, s_abort, p.status, 600 + s)) { ok = false; break; }
-          lph ^= 1u << s;
-          uint8_t* sA = smem + s * C::kStageBytes;
-          zero_k_tail(sA, sA + kABytes, rv, BN / 128, lane);
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&full[s]), lead));
-          __syncwarp();
-        }
-      }
-    }
+    // the leader CTA issues the pair's MMAs; this warp has nothing to do
   } else if (warp == 1 && QUANT) {
     // ------------------------------------------------------------ MMA issuer (MXFP8)
     // Per k-block: the scale atoms go to tensor memory by tcgen05.cp, then four
@@ -764,10 +705,11 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         tc_fence_after();
         uint8_t* sA = smem + s * C::kStageBytes;
         uint8_t* sB = sA + kABytes;
-        // Ragged K: rows past the group's end belong to the next expert;
-        // they are zeroed up to the next multiple of 16 and the empty K=16
-        // steps are skipped (a pair's peer zeroes its own stage).
-        const int nkk = RAGGED_K ? zero_k_tail(sA, sB, t.k_rows - kb * BK, PAIR ? BN / 128 : BN / 64, lane) : BK / 16;
+        // Ragged K: rows past the group's end arrive as zeros (the per-group
+        // maps end at the group's last row); K=16 steps holding none of the
+        // group's rows are skipped.
+        const int rv = t.k_rows - kb * BK;
+        const int nkk = (RAGGED_K && rv < BK) ? (rv + 15) / 16 : BK / 16;
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA);
           const uint32_t b_base = smem_u32(sB);
@@ -935,40 +877,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         }
         const bool zero = t.num_kb == 0;
         const int c_begin = hf * (BN / 2);
-        if (kDirectF32) {
-          // This warp's 32 rows x BN/2 columns straight from registers: TMEM
-          // loads of 32 columns (the next one in flight while this one is
-          // stored), each row's 128 bytes as four 256-bit stores.
-          constexpr int NCH = BN / 64;
-          uint32_t va[32], vb[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) va[j] = 0u;
-          if (!zero) {
-            tmem_ld_32x32b_x32(tb + c_begin, va);
-            tmem_wait_ld(va);
-          }
-          float* drow = reinterpret_cast<float*>(obase) + grow * p.ld_out + t.nt * BN + c_begin;
-#pragma unroll
-          for (int i = 0; i < NCH; ++i) {
-            if (i + 1 < NCH) {
-              if (!zero) tmem_ld_32x32b_x32(tb + c_begin + 32 * (i + 1), vb);
-              else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) vb[j] = 0u;
-              }
-            }
-            const int col = t.nt * BN + c_begin + 32 * i;
-            if (row_ok && col < p.n_size) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) st_global_v8(drow + 32 * i + 8 * j, va + 8 * j);
-            }
-            if (i + 1 < NCH) {
-              if (!zero) tmem_wait_ld(vb);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) va[j] = vb[j];
-            }
-          }
-        } else if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
+        if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
           // Stage this warp's 32 rows x 32 columns as two 16-row halves in a
           // 2 KB shared-memory buffer (128-byte swizzle: 16-byte chunk j of
           // row r at chunk j ^ (r & 7)) and write each half with a TMA tensor
@@ -1372,7 +1281,7 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false,
           bool GATHER = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
-  using C = typename FormCfg<BN, A_MN, EPI, QUANT, PAIR, W8>::type;
+  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
   constexpr int CN = 2;   // CTAs per cluster (PAIR)
   const size_t smem = C::smem_bytes(kp.num_groups);
   auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8, GATHER>;
@@ -1641,9 +1550,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
                 : launch_impl<256, false, false, EPI_BF16, false, false, false, true>(kp, u, stream);
   }
   // CTA pairs: each CTA loads its own 128 rows of A and half of the B tile
-  // (weight gradients: at most kWgPairMaxGroups groups)
   const bool pair = BN == 256 && use_cta_pair(a.max_rows, a.num_groups) &&
-                    (a.ragged_k ? (a.epi == EPI_F32 && a.num_groups <= kWgPairMaxGroups)
+                    (a.ragged_k ? a.epi == EPI_F32
                                 : (a.epi == EPI_BF16 || a.epi == EPI_SWIGLU_FWD || a.epi == EPI_SWIGLU_BWD));
   kp.kblk = BK;
   if (!a.ragged_k) {
@@ -1678,17 +1586,24 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
   } else {
     if (a.m_size <= 0) return cudaSuccess;
+    // templates of the per-group maps the producers write (rows rebased per group)
+    if (!a.map_ws || (reinterpret_cast<uintptr_t>(a.map_ws) & 127u) != 0) return cudaErrorInvalidValue;
     if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
       return cudaErrorInvalidValue;
     kp.tmA[1] = kp.tmA[0];
     kp.tmB[1] = kp.tmB[0];
+    kp.gmaps = static_cast<CUtensorMap*>(a.map_ws);
+    kp.ga_ptr = static_cast<const char*>(a.a[0].ptr);
+    kp.gb_ptr = static_cast<const char*>(a.b[0].ptr);
+    kp.ga_ld_bytes = a.a[0].ld * 2;
+    kp.gb_ld_bytes = a.b[0].ld * 2;
     const int64_t ur = pair ? 2 * BM : BM;
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + ur - 1) / ur) * ((a.n_size + BN - 1) / BN);
   }
   if (tiles_ub <= 0) return cudaSuccess;
   // fp32 outputs go through TMA stores when every tile's rows either belong to
   // its own output matrix (weight gradients) or end at the tensor's end (one group)
-  if (a.epi == EPI_F32 && ((a.ragged_k && !pair) || (!a.ragged_k && a.num_groups == 1))) {
+  if (a.epi == EPI_F32 && (a.ragged_k || a.num_groups == 1)) {
     const int64_t m = a.ragged_k ? a.m_size : a.max_rows;
     const int64_t gs = a.ragged_k ? a.group_stride_out : m * a.ld_out;
     kp.c_tma = make_out_map_f32(&kp.tmC, a.out0, a.n_size, m, a.ragged_k ? a.num_groups : std::max(1, kp.ksplit),

@@ -93,7 +93,14 @@ struct GemmArgs {
   // loaded by TMA tile::gather4 instead of a permuted copy
   const int32_t* a_gather = nullptr;
   int gather_k = 0;
+  // Ragged K (bf16): global scratch of kGemmMapScratchBytes, 128-byte
+  // aligned, for the per-group tensor maps the launch's CTAs write
+  void* map_ws = nullptr;
 };
+
+// Scratch the ragged-K bf16 form needs in GemmArgs::map_ws: two 128-byte
+// tensor maps per ring stage (at most 8) of each CTA (at most 256).
+constexpr size_t kGemmMapScratchBytes = 256 * 8 * 2 * 128;
 
 // Enqueue the grouped GEMM on `stream`.  Returns cudaSuccess or the first
 // CUDA error (tensor-map encoding failures map to cudaErrorInvalidValue).

@@ -25,18 +25,24 @@ constexpr size_t kAlign = 256;
 // int32 words of the workspace's status block (256 bytes, cleared by
 // moe_workspace_init): 0 and 1 are the status bits and the failing site;
 // the fused router keeps its completion ticket in word 8 and its histogram
-// accumulator in words 16..47, and leaves both zero.
+// accumulator in words 16..47, and leaves both zero;
 constexpr int kTicketWord = 8;
 constexpr int kRouterAccWord = 16;
+// words 48..50: the single-pass permute's chunk ticket, done counter and
+// generation (it leaves the first two zero and advances the third)
+constexpr int kPermuteCtlWord = 48;
+// Look-back words of the single-pass permute (1 MiB): ceil(N/16) * E of them
+// per call; larger problems take the two-kernel permute.
+constexpr size_t kLookWords = 131072;
 // The router logits GEMM has one 128-token tile per CTA; with few tiles its
 // contraction is cut into up to this many slices (summed in order after).
 constexpr int kGateSlices = 4;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, aux = 0, gpart = 0, fwd_end = 0;
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, look = 0, aux = 0, gpart = 0, fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
-  size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, total = 0;
+  size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, gmaps = 0, total = 0;
   // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
   // padded group starts, and four transposed token-blocked code matrices
   // (weight-gradient operands: two [D, Rp], two [max(F,Fs), Rp]) with scales
@@ -55,6 +61,9 @@ WsLayout layout(const moe_desc_t& d) {
   size_t o = 0;
   L.status = o; o += kAlign;
   L.dense_off = o; o += kAlign;
+  // the single-pass permute's look-back words: a fixed region of the same
+  // place and size for every description, holding nothing else
+  L.look = o; o += kLookWords * 8;
   L.blk_counts = o; o = align_up(o + nch * E * 4);
   L.blk_base = o; o = align_up(o + nch * E * 4);
   L.aux = o; o = align_up(o + moe::aux_partial_floats(d.n_tok > 0 ? d.n_tok : 1, d.n_exp) * 4);
@@ -75,6 +84,7 @@ WsLayout layout(const moe_desc_t& d) {
   L.da3s = o; o = align_up(o + N * Fs * 2);
   L.dxs = o; o = align_up(o + (Fs ? N * D * 2 : 0));
   L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_tok, d.top_k, d.n_exp, d.d_model) * 4);
+  L.gmaps = o; o = align_up(o + moe::kGemmMapScratchBytes);   // per-group maps of the weight gradients
   if (d.precision == 1) {
     const size_t Fm = F > Fs ? F : Fs;
     const size_t ldr = moe::mx_scale_ld(R);
@@ -234,8 +244,8 @@ moe_status_t ffn_pair(const void* a_in, int64_t rows, int D, int F, int groups, 
 moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, const void* a3, const void* h,
                           int64_t rows, int D, int F, int groups, const int32_t* offsets, const void* w1,
                           const void* w3, const void* w2, void* da1, void* da3, void* dx_rows, float* dw1,
-                          float* dw3, float* dw2, int32_t* status, cudaStream_t st, const float* s1 = nullptr,
-                          const float* s3 = nullptr, const float* s2 = nullptr) {
+                          float* dw3, float* dw2, int32_t* status, cudaStream_t st, void* map_ws,
+                          const float* s1 = nullptr, const float* s3 = nullptr, const float* s2 = nullptr) {
   const bool w8 = s1 != nullptr;   // FP8 weights in the data gradients; weight gradients stay bf16
   GemmArgs g;
   g.w8 = w8;
@@ -260,6 +270,7 @@ moe_status_t ffn_pair_bwd(const void* dyw, const void* a_in, const void* a1, con
   GemmArgs w;
   w.epi = moe::EPI_F32;
   w.a_mn = w.b_mn = w.ragged_k = true;
+  w.map_ws = map_ws;
   w.offsets = offsets;
   w.num_groups = groups;
   w.max_rows = rows;
@@ -339,7 +350,8 @@ moe_status_t moe_workspace_size(const moe_desc_t* d, size_t* fwd_bytes, size_t* 
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kAlign || !aligned16(ws)) return MOE_ERR_WORKSPACE;
-  MOE_CUDA(cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)));
+  // all of it: the status block and the permute's look-back words start at zero
+  MOE_CUDA(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -433,11 +445,15 @@ moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk
   if (d->n_tok == 0) return MOE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  if (moe::permute_single_pass_look_words(d->n_tok, d->n_exp) <= static_cast<int64_t>(kLookWords))
+    return cuda_status(moe::launch_permute_single_pass(d->n_tok, d->n_exp, d->top_k, d->d_model, topk_idx, offsets,
+                                                       x, row_of_copy, copy_of_row, x_perm,
+                                                       at<unsigned long long>(ws, L.look),
+                                                       status + kPermuteCtlWord, status, st));
   MOE_CUDA(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, at<int32_t>(ws, L.blk_counts),
-                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row,
-                                    at<int32_t>(ws, L.status), st));
-  MOE_CUDA(moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st));
-  return MOE_OK;
+                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row, status, st));
+  return cuda_status(moe::launch_permute_rows(d->n_tok, d->d_model, d->top_k, x, row_of_copy, x_perm, st));
 }
 
 moe_status_t moe_grouped_ffn(const moe_desc_t* d, const void* x_perm, const int32_t* offsets, const void* x,
@@ -572,7 +588,7 @@ moe_status_t backward_impl(const moe_desc_t* d, const void* w_gate, const moe_ex
   // routed experts; dx_perm overwrites dYw once its last reader is done
   auto sc = [&](const void* p_) { return q ? static_cast<const float*>(p_) : nullptr; };
   MOE_TRY(ffn_pair_bwd(dyw, s->x_perm, s->a1, s->a3, s->h, R, D, F, E, s->offsets, w->w1, w->w3, w->w2, da1, da3,
-                       dyw, g->dw1, g->dw3, g->dw2, status, st, sc(q ? q->w1_scale : nullptr),
+                       dyw, g->dw1, g->dw3, g->dw2, status, st, at<void>(ws, L.gmaps), sc(q ? q->w1_scale : nullptr),
                        sc(q ? q->w3_scale : nullptr), sc(q ? q->w2_scale : nullptr)));
   void* dxs = nullptr;
   if (d->n_shared) {
@@ -581,7 +597,7 @@ moe_status_t backward_impl(const moe_desc_t* d, const void* w_gate, const moe_ex
     dxs = at<void>(ws, L.dxs);
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
                          at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st,
-                         sc(q ? q->ws1_scale : nullptr), sc(q ? q->ws3_scale : nullptr),
+                         at<void>(ws, L.gmaps), sc(q ? q->ws1_scale : nullptr), sc(q ? q->ws3_scale : nullptr),
                          sc(q ? q->ws2_scale : nullptr)));
   }
   if (s->offsets_full && s->copy_of_row_full)   // capacity mode: every copy, x gathered in dropless order

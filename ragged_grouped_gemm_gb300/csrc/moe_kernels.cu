@@ -562,6 +562,189 @@ __global__ void __launch_bounds__(1024, 1) maps_onepass_kernel(int n_tok, int E,
   }
 }
 
+// ------------------------------------------------------------ single-pass permute
+// The whole dispatch of moe_permute in one launch: stable maps and the row
+// copy.  The copies are cut into chunks of kSpTok tokens; a CTA takes the next
+// chunk from a ticket counter (so every chunk before it has a CTA already
+// running), counts its chunk's copies per expert, and publishes per expert a
+// 64-bit word {tag (32 bits), state (1 bit), value (31 bits)}: first the
+// chunk's own count (state "aggregate"), and once known its inclusive row
+// prefix (state "prefix"; chunk 0 publishes offsets[e] + count at once).  A
+// chunk's first row of expert e is found by walking back over the preceding
+// chunks' words, adding aggregates until a prefix is met (decoupled
+// look-back): one warp per expert reads the words of 32 preceding chunks per
+// round trip, the nearest chunk with a prefix ends the walk, and the
+// aggregates before it are added by a warp reduction.  Every wait on a word
+// not yet published this call is bounded and reports MOE_DEV_TIMEOUT.
+// The tag is the call's generation + 1 (the generation counter and the words
+// start at zero after moe_workspace_init; the last CTA of a call advances
+// the generation and resets the ticket).  The words live in a region of the
+// workspace that holds nothing else, so a word is either zero or left by an
+// earlier call, and never reads as this call's (until the 32-bit generation
+// wraps, after 2^32 - 1 calls on one workspace).  Positions inside the chunk follow copy order,
+// exactly as the other map kernels assign them, with the same bound checks;
+// then the chunk's token rows are read once and written to their K rows.
+constexpr int kSpTok = 16;
+constexpr int kSpThreads = 512;
+constexpr uint64_t kSpAggregate = 0, kSpPrefix = 1;
+
+__device__ __forceinline__ uint64_t sp_word(uint32_t tag, uint64_t state, int value) {
+  return (static_cast<uint64_t>(tag) << 32) | (state << 31) | (static_cast<uint32_t>(value) & 0x7FFFFFFFu);
+}
+
+__global__ void __launch_bounds__(kSpThreads) permute_single_pass_kernel(
+    int n_tok, int E, int K, int d8, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+    const uint4* __restrict__ x, int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row,
+    uint4* __restrict__ x_perm, unsigned long long* look, int32_t* ctl, int32_t* status) {
+  extern __shared__ int s_sp[];
+  int* s_h = s_sp;                    // [E] the chunk's copies per expert
+  int* s_base = s_sp + E;             // [E] the chunk's next row per expert
+  int* s_e = s_sp + 2 * E;            // [kSpTok * K] expert of each copy
+  int* s_pos = s_e + kSpTok * K;      // [kSpTok * K] row of each copy (-1: none)
+  __shared__ int s_chunk;
+  __shared__ uint32_t s_tag;
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_chunk = atomicAdd(ctl, 1);
+    s_tag = static_cast<uint32_t>(*reinterpret_cast<volatile int32_t*>(ctl + 2)) + 1u;
+    s_bad = 0;
+  }
+  for (int e = tid; e < E; e += kSpThreads) s_h[e] = 0;
+  __syncthreads();
+  const int chunk = s_chunk;
+  const uint32_t tag = s_tag;
+  const int64_t R = static_cast<int64_t>(n_tok) * K;
+  const int64_t c0 = static_cast<int64_t>(chunk) * kSpTok * K;
+  const int ncp = static_cast<int>(min(R - c0, static_cast<int64_t>(kSpTok) * K));
+  for (int i = tid; i < ncp; i += kSpThreads) {
+    const int e = idx[c0 + i];
+    s_e[i] = e;
+    if (e >= 0 && e < E) atomicAdd(&s_h[e], 1);
+    else atomicOr(&s_bad, DEV_BAD_INDEX);
+  }
+  __syncthreads();
+  volatile unsigned long long* vlook = look;
+  // publish this chunk's aggregates (chunk 0: its prefixes)
+  for (int e = tid; e < E; e += kSpThreads) {
+    unsigned long long* mine = look + static_cast<int64_t>(chunk) * E + e;
+    if (chunk == 0) {
+      s_base[e] = offsets[e];
+      *reinterpret_cast<volatile unsigned long long*>(mine) = sp_word(tag, kSpPrefix, offsets[e] + s_h[e]);
+    } else {
+      *reinterpret_cast<volatile unsigned long long*>(mine) = sp_word(tag, kSpAggregate, s_h[e]);
+    }
+  }
+  if (chunk > 0) {
+    // look-back, a warp per expert: lane l reads chunk j0 - l of the window
+    for (int e = warp; e < E; e += kSpThreads / 32) {
+      int acc = 0;
+      int j0 = chunk - 1;
+      uint64_t t0 = 0;
+      while (true) {
+        const int j = j0 - lane;
+        unsigned long long w = 0;
+        bool ready = true;
+        if (j >= 0) {
+          w = vlook[static_cast<int64_t>(j) * E + e];
+          ready = static_cast<uint32_t>(w >> 32) == tag;
+        }
+        const bool is_prefix = j >= 0 && ready && ((w >> 31) & 1u) == kSpPrefix;
+        const unsigned pm = __ballot_sync(kFull, is_prefix);
+        const int stop = pm ? __ffs(pm) - 1 : 32;                          // nearest chunk with a prefix
+        const unsigned need = stop < 31 ? ((2u << stop) - 1u) : kFull;    // lanes 0..stop
+        const unsigned nr = __ballot_sync(kFull, !ready) & need;
+        if (nr) {   // a chunk before the prefix has not published yet: read the window again (bounded)
+          // (lane 0's clock decides for the whole warp, so the warp leaves together)
+          int out = 0;
+          if (lane == 0) {
+            if (t0 == 0) t0 = globaltimer_ns();
+            else out = globaltimer_ns() - t0 > kSpinTimeoutNs;
+          }
+          if (__shfl_sync(kFull, out, 0)) {
+            if (lane == 0) {
+              atomicOr(&s_bad, DEV_TIMEOUT);
+              if (status) atomicExch(status + 1, 700);
+            }
+            break;
+          }
+          continue;
+        }
+        int v = (((need >> lane) & 1u) && j >= 0) ? static_cast<int>(static_cast<uint32_t>(w) & 0x7FFFFFFFu) : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+        acc += v;
+        if (stop < 32) break;
+        j0 -= 32;
+        t0 = 0;
+      }
+      if (lane == 0) {
+        s_base[e] = acc;
+        *reinterpret_cast<volatile unsigned long long*>(look + static_cast<int64_t>(chunk) * E + e) =
+            sp_word(tag, kSpPrefix, acc + s_h[e]);
+      }
+    }
+  }
+  __syncthreads();
+  // rows of the chunk's copies in copy order (warp 0)
+  if (warp == 0) {
+    for (int b = 0; b < ncp; b += 32) {
+      const int i = b + lane;
+      const bool active = i < ncp;
+      const int e = active ? s_e[i] : -1;
+      const bool ok = active && e >= 0 && e < E;
+      const unsigned am = __ballot_sync(kFull, ok);
+      int pos = -1;
+      if (ok) {
+        const unsigned m = __match_any_sync(am, e);
+        const int leader = __ffs(m) - 1;
+        const int rank = __popc(m & ((1u << lane) - 1u));
+        int base = 0;
+        if (lane == leader) {
+          base = s_base[e];
+          s_base[e] = base + __popc(m);
+        }
+        base = __shfl_sync(am, base, leader);
+        pos = base + rank;
+        if (!(pos >= 0 && pos < offsets[e + 1] && pos < R)) {
+          pos = -1;
+          atomicOr(&s_bad, DEV_BAD_OFFSETS);
+        }
+      }
+      if (active) {
+        s_pos[i] = pos;
+        row_of_copy[c0 + i] = pos;
+        if (pos >= 0) copy_of_row[pos] = static_cast<int32_t>(c0 + i);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // the chunk's token rows, each read once and written to its copies' rows
+  const int t0k = chunk * kSpTok;
+  const int ntk = ncp / K;
+  const int units = ntk * d8;
+#pragma unroll 4
+  for (int u = tid; u < units; u += kSpThreads) {
+    const int tt = u / d8;
+    const int i = u - tt * d8;
+    const uint4 v = x[static_cast<int64_t>(t0k + tt) * d8 + i];
+    for (int k = 0; k < K; ++k) {
+      const int r = s_pos[tt * K + k];
+      if (r >= 0) x_perm[static_cast<int64_t>(r) * d8 + i] = v;
+    }
+  }
+  if (tid == 0) {
+    if (s_bad && status) atomicOr(status, s_bad);
+    __threadfence();
+    if (atomicAdd(ctl + 1, 1) == static_cast<int>(gridDim.x) - 1) {   // last CTA: next call's state
+      ctl[0] = 0;
+      ctl[1] = 0;
+      atomicAdd(ctl + 2, 1);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) permute_rows_kernel(int n_tok, int d8, int K, const uint4* __restrict__ x,
                                                            const int32_t* __restrict__ row_of_copy,
                                                            uint4* __restrict__ x_perm) {
@@ -1112,6 +1295,25 @@ cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* 
   block_base_kernel<<<(n_exp + 255) / 256, 256, 0, st>>>(nch, n_exp, offsets, block_counts, block_base, status);
   scatter_maps_kernel<<<nch, 32, 2 * smem, st>>>(n_tok, n_exp, top_k, topk_idx, offsets, block_base, row_of_copy,
                                                  copy_of_row, status);
+  return cudaGetLastError();
+}
+
+int64_t permute_single_pass_look_words(int n_tok, int n_exp) {
+  return (static_cast<int64_t>(n_tok) + kSpTok - 1) / kSpTok * n_exp;
+}
+
+cudaError_t launch_permute_single_pass(int n_tok, int n_exp, int top_k, int d, const int32_t* topk_idx,
+                                       const int32_t* offsets, const void* x, int32_t* row_of_copy,
+                                       int32_t* copy_of_row, void* x_perm, unsigned long long* look, int32_t* ctl,
+                                       int32_t* status, cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  if (top_k > 32 || d % 8) return cudaErrorInvalidValue;
+  const int chunks = (n_tok + kSpTok - 1) / kSpTok;
+  const size_t smem = (2 * static_cast<size_t>(n_exp) + 2 * kSpTok * top_k) * sizeof(int);
+  permute_single_pass_kernel<<<chunks, kSpThreads, smem, st>>>(n_tok, n_exp, top_k, d / 8, topk_idx, offsets,
+                                                               static_cast<const uint4*>(x), row_of_copy,
+                                                               copy_of_row, static_cast<uint4*>(x_perm), look, ctl,
+                                                               status);
   return cudaGetLastError();
 }
 

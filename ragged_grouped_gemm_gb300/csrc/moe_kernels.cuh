@@ -40,6 +40,15 @@ int permute_num_chunks(int n_tok);
 cudaError_t launch_permute_maps(int n_tok, int n_exp, int top_k, const int32_t* topk_idx, const int32_t* offsets,
                                 int32_t* block_counts, int32_t* block_base, int32_t* row_of_copy,
                                 int32_t* copy_of_row, int32_t* status, cudaStream_t st, bool chunked = false);
+// moe_permute in one launch (maps and rows; decoupled look-back over
+// 16-token chunks).  look: permute_single_pass_look_words() uint64 and ctl:
+// three int32 (chunk ticket, done counter, generation), all zero after
+// moe_workspace_init; the kernel leaves ctl ready for the next call.
+int64_t permute_single_pass_look_words(int n_tok, int n_exp);
+cudaError_t launch_permute_single_pass(int n_tok, int n_exp, int top_k, int d, const int32_t* topk_idx,
+                                       const int32_t* offsets, const void* x, int32_t* row_of_copy,
+                                       int32_t* copy_of_row, void* x_perm, unsigned long long* look, int32_t* ctl,
+                                       int32_t* status, cudaStream_t st);
 // x_perm[row_of_copy[t*K+k]] = x[t] (bf16 rows of d elements).
 cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, const int32_t* row_of_copy,
                                 void* x_perm, cudaStream_t st);

@@ -153,6 +153,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Write into global memory at `dst` (128-byte aligned) a copy of the tensor
+// map `tmpl` whose global address is `addr` and whose second dimension (rows)
+// is `rows`, and make it usable by this thread's following TMA copies (the
+// copy and the field replacements are generic-proxy writes; the release /
+// acquire pair hands them to the tensor-map proxy).
+__device__ __forceinline__ void tensormap_rebase_rows(CUtensorMap* dst, const CUtensorMap* tmpl, uint64_t addr,
+                                                      uint32_t rows) {
+  const uint4* src = reinterpret_cast<const uint4*>(tmpl);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = src[i];
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(addr) : "memory");
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst), "r"(rows) : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(dst) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -144,6 +144,37 @@ def test_permute_bitexact(name):
     np.testing.assert_array_equal(cor.cpu().numpy(), rcor)
     xb = x.view(torch.int16).numpy()
     np.testing.assert_array_equal(xp.cpu().view(torch.int16).numpy(), xb[rcor // k])
+    # the maps alone (one-CTA form up to 65536 copies, token-chunked beyond): the same maps
+    roc2, cor2 = _i32(n * k), _i32(n * k)
+    api.moe_permute_maps(d, torch.from_numpy(ridx).cuda(), torch.from_numpy(off).cuda(), roc2, cor2, ws)
+    _status_ok(ws)
+    np.testing.assert_array_equal(roc2.cpu().numpy(), rroc)
+    np.testing.assert_array_equal(cor2.cpu().numpy(), rcor)
+
+
+def test_permute_twice_in_a_row_and_after_other_sizes():
+    """The single-pass permute keeps a chunk ticket and a generation counter
+    in the workspace between calls: repeated calls, and calls of another
+    size on the same workspace, give the same maps and rows."""
+    cfg = CONFIGS["small_fine"]
+    n, dm, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
+    d, ws = _ws(cfg)
+    x = make_layer(cfg.replace(d_ff=64, n_exp=1, top_k=1, use_bias=False, n_shared=0), "cpu")["x"].cuda()
+    for rep, ntok in enumerate((n, n, 100, n)):
+        c = cfg.replace(n_tok=ntok)
+        lg = skewed_logits(ntok, e, "zipf", seed=20 + rep).numpy()
+        ridx, _ = O.route(lg, None, k, c.gate)
+        off = O.exclusive_offsets(O.histogram(ridx, e))
+        dd = api.make_desc(c)
+        roc, cor, xp = _i32(ntok * k), _i32(ntok * k), _bf(ntok * k, dm)
+        api.moe_permute(dd, x[:ntok].contiguous(), torch.from_numpy(ridx).cuda(), torch.from_numpy(off).cuda(), roc,
+                        cor, xp, ws)
+        _status_ok(ws)
+        rroc, rcor = O.permutation(ridx, e)
+        np.testing.assert_array_equal(roc.cpu().numpy(), rroc)
+        np.testing.assert_array_equal(cor.cpu().numpy(), rcor)
+        np.testing.assert_array_equal(xp.cpu().view(torch.int16).numpy(),
+                                      x[:ntok].cpu().view(torch.int16).numpy()[rcor // k])
 
 
 # ------------------------------------------------------------- grouped FFN
