@@ -149,7 +149,8 @@ def route_launches(cfg, sms: int = 152) -> int:
 def launches_per_step(cfg) -> int:
     """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
     from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
-    maps = 1 if cfg.rows <= 65536 else 3     # single-CTA permutation maps, or the token-chunked kernels
+    # maps of the MXFP8 permute: single-CTA up to 65536 copies, else the token-chunked kernels
+    maps = 1 if cfg.rows <= 65536 else 3
     if cfg.precision == "mxfp8":
         # route; permute: map kernels + row quantiser (+ token quantiser for the shared expert);
         # grouped FFN: GEMM1, GEMM2 (+ dense offsets, GEMM1, GEMM2); combine
@@ -159,10 +160,14 @@ def launches_per_step(cfg) -> int:
         per_set = 2 + 1 + 5 + 5
         bwd = 1 + per_set + (1 + per_set + 1 if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
         return fwd + bwd + (1 if cfg.use_bias else 0)
-    fwd = route_launches(cfg) + maps + 1 + 2 + 1   # route; permute: maps + rows; GEMM1, GEMM2; combine
+    # route; permute (one launch while ceil(N/16) * E <= 131072, else maps + rows); GEMM1, GEMM2; combine
+    sp = -(-cfg.n_tok // 16) * cfg.n_exp <= 131072
+    fwd = route_launches(cfg) + (1 if sp else maps + 1) + 2 + 1
     if cfg.n_shared:
         fwd += 3
-    bwd = 1 + 5 + 1              # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3; unpermute-sum
+    # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3 (each weight gradient over several
+    # experts preceded by the kernel that writes their per-group tensor maps); unpermute-sum
+    bwd = 1 + 5 + (3 if cfg.n_exp > 1 else 0) + 1
     if cfg.n_shared:
         bwd += 6
     bwd += 3                     # router weight gradient: chunk prefix, chunk partials, reduction
@@ -412,6 +417,31 @@ def run_ours(args, cfg, rank, world, local_rank):
     if bits:
         raise RuntimeError(f"device status {bits} at site {site}")
 
+    # --- inference forward (no saved activations), GEMM1 rows gathered from x
+    # (moe_permute_maps + moe_grouped_ffn_gather) against the same layer with a
+    # permuted copy of the tokens (moe_permute + moe_grouped_ffn)
+    inference = None
+    if cfg.precision == "bf16" and cfg.capacity_factor <= 0:
+        del layer
+        torch.cuda.empty_cache()
+        inference = {}
+        for mode in ("gather", "x_perm"):
+            inf = api.MoELayer(cfg, p, train=False, device=dev, gather=mode == "gather")
+            for _ in range(args.warmup):
+                inf.forward(x)
+            i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            i0.record()
+            for _ in range(args.steps):
+                inf.forward(x)
+            i1.record()
+            torch.cuda.synchronize()
+            inference[mode] = cfg.n_tok * args.steps / (i0.elapsed_time(i1) / 1e3)
+            assert inf.device_status()[0] == 0
+            del inf
+            torch.cuda.empty_cache()
+        layer = None
+
     def max_over_ranks(v):
         t = torch.tensor([v], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -420,6 +450,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     nonempty = int((b["counts"] > 0).sum().item())
     counts = b["counts"].float()
     res = {"cfg": cfg, "per_call": per_call, "kernels": kernels, "clocks": clk.summary(), "nonempty": nonempty,
+           "inference_fwd": inference,
            "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
            "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2 + hdx.numel() * 2}
     for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
@@ -574,6 +605,9 @@ def summarize(res, args, peaks) -> dict:
         "e2e": {"value": res["e2e"][0], "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "max_load_over_mean": res["max_load_over_mean"], "clocks": res["clocks"],
+        # forward only, no saved activations: GEMM1 rows gathered from x by TMA
+        # (no permuted copy of the tokens) against the same forward through x_perm
+        "inference_fwd_tokens_per_s": res.get("inference_fwd"),
     }
 
 
@@ -652,6 +686,7 @@ def main():
         "backward_tflops": head["backward_tflops"],
         "per_call_ms": head["per_call_ms"],
         "per_call_gbs": head["per_call_gbs"],
+        "inference_fwd_tokens_per_s": head["inference_fwd_tokens_per_s"],
         "roofline": roof,
         "roofline_by_kind": roofs,
         "e2e": head["e2e"],

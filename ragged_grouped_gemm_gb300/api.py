@@ -455,7 +455,7 @@ class MoELayer:
     (w_gate, w1, w3, w2, bias, and ws1, ws3, ws2 with a shared expert).
     """
 
-    def __init__(self, cfg: MoEConfig, params: dict, train: bool = True, device="cuda"):
+    def __init__(self, cfg: MoEConfig, params: dict, train: bool = True, device="cuda", gather: bool = False):
         self.cfg = cfg
         self.desc = make_desc(cfg)
         self.p = params
@@ -463,9 +463,9 @@ class MoELayer:
         n, d, f, e, k = cfg.n_tok, cfg.d_model, cfg.d_ff, cfg.n_exp, cfg.top_k
         r, fs = cfg.rows, cfg.d_ff_shared
         z = lambda *s, dt=BF16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
-        # an inference layer with bf16 experts and no capacity reads GEMM1's rows
-        # straight from x (moe_permute_maps + moe_grouped_ffn_gather): no x_perm
-        self.gather = (not train) and cfg.precision == "bf16" and cfg.capacity_factor <= 0
+        # gather=True (inference, bf16 experts, no capacity): GEMM1 reads its rows
+        # straight from x (moe_permute_maps + moe_grouped_ffn_gather), no x_perm
+        self.gather = gather and (not train) and cfg.precision == "bf16" and cfg.capacity_factor <= 0
         self.buf = {
             "logits": z(n, e, dt=F32), "topk_idx": z(n, k, dt=I32), "topk_w": z(n, k, dt=F32),
             "counts": z(e, dt=I32), "offsets": z(e + 1, dt=I32), "row_of_copy": z(r, dt=I32),

@@ -104,15 +104,29 @@ struct KParams {
   // the token matrix behind tmA[0] (a 2-D map with one-row boxes)
   const int32_t* a_gather;
   int32_t gather_k;
-  // Ragged K (bf16): per-group copies of tmA[0] / tmB[0] whose rows are
-  // exactly the group's rows, one (A, B) pair per ring stage of each CTA,
-  // written by the CTA's producer into this global scratch
-  CUtensorMap* gmaps;
-  const char* ga_ptr;
-  const char* gb_ptr;
-  int64_t ga_ld_bytes;
-  int64_t gb_ld_bytes;
+  // Ragged K (bf16), several groups: per-group copies of tmA[0] / tmB[0]
+  // whose rows are exactly the group's rows ([0, G) for A, [G, 2G) for B),
+  // written by build_group_maps_kernel before the launch; null with one group
+  // (the whole-tensor maps end at the group's end already)
+  const CUtensorMap* gmaps;
 };
+
+// The per-group maps of a ragged-K launch: thread g writes group g's copy of
+// the A and B maps, rebased to the group's first row with a row extent of
+// the group's row count (at least 1; an empty group is never loaded).
+__global__ void build_group_maps_kernel(CUtensorMap* out, const __grid_constant__ CUtensorMap ta,
+                                        const __grid_constant__ CUtensorMap tb, const int32_t* __restrict__ offsets,
+                                        int G, const char* a_ptr, int64_t a_ld_bytes, const char* b_ptr,
+                                        int64_t b_ld_bytes) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  const int r0 = offsets[g];
+  const uint32_t rows = static_cast<uint32_t>(max(offsets[g + 1] - r0, 1));
+  tensormap_rebase_rows(out + g, &ta, reinterpret_cast<uint64_t>(a_ptr + static_cast<int64_t>(r0) * a_ld_bytes),
+                        rows);
+  tensormap_rebase_rows(out + G + g, &tb, reinterpret_cast<uint64_t>(b_ptr + static_cast<int64_t>(r0) * b_ld_bytes),
+                        rows);
+}
 
 // STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
 // MAXG / MAXS: the most groups the shared-memory tables hold and the most
@@ -497,9 +511,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       __syncwarp();
     } else if (!QUANT && lane == 0) {
       uint32_t it = 0;
-      // ragged K: the group (+1) whose maps each stage's slot holds, 10 bits per stage
-      uint64_t slot_g = 0;
-      CUtensorMap* slots = RAGGED_K ? p.gmaps + static_cast<int64_t>(blockIdx.x) * 2 * S : nullptr;
+      int map_g = -1;   // ragged K: the group whose maps this thread last acquired
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
         const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
@@ -540,24 +552,18 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             continue;
           }
           if (RAGGED_K) {
-            // The stage's slot holds maps of exactly the group's rows, so the
-            // last k-block of a group reads zeros past the group's end (TMA
-            // fill) instead of the next group's rows; a slot is rewritten
-            // only when its group changes (its previous load has landed: the
-            // stage was released).
-            CUtensorMap* mA = slots + 2 * s;
-            CUtensorMap* mB = mA + 1;
-            if (static_cast<int>((slot_g >> (10 * s)) & 1023u) != t.g + 1) {
-              const uint32_t rows = static_cast<uint32_t>(max(t.k_rows, 1));
-              tensormap_rebase_rows(mA, &p.tmA[0],
-                                    reinterpret_cast<uint64_t>(p.ga_ptr + static_cast<int64_t>(t.row0) * p.ga_ld_bytes),
-                                    rows);
-              tensormap_rebase_rows(mB, &p.tmB[0],
-                                    reinterpret_cast<uint64_t>(p.gb_ptr + static_cast<int64_t>(t.row0) * p.gb_ld_bytes),
-                                    rows);
-              slot_g = (slot_g & ~(1023ull << (10 * s))) | (static_cast<uint64_t>(t.g + 1) << (10 * s));
+            // The group's own maps end at its last row, so its last k-block
+            // reads zeros past the group's end (TMA fill) instead of the next
+            // group's rows.  One group: the whole-tensor maps do the same.
+            const bool gm = p.gmaps != nullptr;
+            const CUtensorMap* mA = gm ? p.gmaps + t.g : &p.tmA[0];
+            const CUtensorMap* mB = gm ? p.gmaps + G + t.g : &p.tmB[0];
+            if (gm && t.g != map_g) {
+              tensormap_acquire(mA);
+              tensormap_acquire(mB);
+              map_g = t.g;
             }
-            const int r = kb * BK;   // rows of the group
+            const int r = gm ? kb * BK : t.row0 + kb * BK;   // rows of the group's map
             if (PAIR) {
               // both CTAs' loads complete on the leader's barrier, armed by the leader
               const int n0 = t.nt * BN + (rank & 1) * (BN / 2);
@@ -1586,17 +1592,23 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
   } else {
     if (a.m_size <= 0) return cudaSuccess;
-    // templates of the per-group maps the producers write (rows rebased per group)
-    if (!a.map_ws || (reinterpret_cast<uintptr_t>(a.map_ws) & 127u) != 0) return cudaErrorInvalidValue;
     if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
       return cudaErrorInvalidValue;
     kp.tmA[1] = kp.tmA[0];
     kp.tmB[1] = kp.tmB[0];
-    kp.gmaps = static_cast<CUtensorMap*>(a.map_ws);
-    kp.ga_ptr = static_cast<const char*>(a.a[0].ptr);
-    kp.gb_ptr = static_cast<const char*>(a.b[0].ptr);
-    kp.ga_ld_bytes = a.a[0].ld * 2;
-    kp.gb_ld_bytes = a.b[0].ld * 2;
+    if (a.num_groups > 1) {
+      // every group's own maps (copies of these two, rebased), written just before the GEMM
+      if (!a.map_ws || (reinterpret_cast<uintptr_t>(a.map_ws) & 127u) != 0 ||
+          2 * static_cast<size_t>(a.num_groups) * sizeof(CUtensorMap) > kGemmMapScratchBytes)
+        return cudaErrorInvalidValue;
+      CUtensorMap* maps = static_cast<CUtensorMap*>(a.map_ws);
+      build_group_maps_kernel<<<(a.num_groups + 127) / 128, 128, 0, stream>>>(
+          maps, kp.tmA[0], kp.tmB[0], a.offsets, a.num_groups, static_cast<const char*>(a.a[0].ptr), a.a[0].ld * 2,
+          static_cast<const char*>(a.b[0].ptr), a.b[0].ld * 2);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      kp.gmaps = maps;
+    }
     const int64_t ur = pair ? 2 * BM : BM;
     tiles_ub = static_cast<int64_t>(a.num_groups) * ((a.m_size + ur - 1) / ur) * ((a.n_size + BN - 1) / BN);
   }

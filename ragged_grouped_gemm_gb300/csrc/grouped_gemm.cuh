@@ -93,14 +93,15 @@ struct GemmArgs {
   // loaded by TMA tile::gather4 instead of a permuted copy
   const int32_t* a_gather = nullptr;
   int gather_k = 0;
-  // Ragged K (bf16): global scratch of kGemmMapScratchBytes, 128-byte
-  // aligned, for the per-group tensor maps the launch's CTAs write
+  // Ragged K (bf16) with several groups: global scratch of
+  // kGemmMapScratchBytes, 128-byte aligned, for the per-group tensor maps a
+  // small kernel writes before the GEMM (same stream)
   void* map_ws = nullptr;
 };
 
 // Scratch the ragged-K bf16 form needs in GemmArgs::map_ws: two 128-byte
-// tensor maps per ring stage (at most 8) of each CTA (at most 256).
-constexpr size_t kGemmMapScratchBytes = 256 * 8 * 2 * 128;
+// tensor maps per group (at most 1024 groups).
+constexpr size_t kGemmMapScratchBytes = 2 * 1024 * 128;
 
 // Enqueue the grouped GEMM on `stream`.  Returns cudaSuccess or the first
 // CUDA error (tensor-map encoding failures map to cudaErrorInvalidValue).

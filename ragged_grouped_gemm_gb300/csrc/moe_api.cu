@@ -84,7 +84,9 @@ WsLayout layout(const moe_desc_t& d) {
   L.da3s = o; o = align_up(o + N * Fs * 2);
   L.dxs = o; o = align_up(o + (Fs ? N * D * 2 : 0));
   L.dwg = o; o = align_up(o + moe::dwgate_partial_floats(d.n_tok, d.top_k, d.n_exp, d.d_model) * 4);
-  L.gmaps = o; o = align_up(o + moe::kGemmMapScratchBytes);   // per-group maps of the weight gradients
+  // per-group maps of the weight gradients (+128 bytes: the workspace itself
+  // is only 16-byte aligned, the maps need 128)
+  L.gmaps = o; o = align_up(o + moe::kGemmMapScratchBytes + 128);
   if (d.precision == 1) {
     const size_t Fm = F > Fs ? F : Fs;
     const size_t ldr = moe::mx_scale_ld(R);
@@ -114,6 +116,11 @@ WsLayout layout(const moe_desc_t& d) {
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+// The 128-byte-aligned start of the weight gradients' map scratch.
+void* map_scratch(void* ws, const WsLayout& L) {
+  const uintptr_t p = reinterpret_cast<uintptr_t>(static_cast<char*>(ws) + L.gmaps);
+  return reinterpret_cast<void*>((p + 127) & ~uintptr_t(127));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -588,7 +595,7 @@ moe_status_t backward_impl(const moe_desc_t* d, const void* w_gate, const moe_ex
   // routed experts; dx_perm overwrites dYw once its last reader is done
   auto sc = [&](const void* p_) { return q ? static_cast<const float*>(p_) : nullptr; };
   MOE_TRY(ffn_pair_bwd(dyw, s->x_perm, s->a1, s->a3, s->h, R, D, F, E, s->offsets, w->w1, w->w3, w->w2, da1, da3,
-                       dyw, g->dw1, g->dw3, g->dw2, status, st, at<void>(ws, L.gmaps), sc(q ? q->w1_scale : nullptr),
+                       dyw, g->dw1, g->dw3, g->dw2, status, st, map_scratch(ws, L), sc(q ? q->w1_scale : nullptr),
                        sc(q ? q->w3_scale : nullptr), sc(q ? q->w2_scale : nullptr)));
   void* dxs = nullptr;
   if (d->n_shared) {
@@ -597,7 +604,7 @@ moe_status_t backward_impl(const moe_desc_t* d, const void* w_gate, const moe_ex
     dxs = at<void>(ws, L.dxs);
     MOE_TRY(ffn_pair_bwd(dy, s->x, s->a1s, s->a3s, s->hs, N, D, d->d_ff_shared, 1, dense, w->ws1, w->ws3, w->ws2,
                          at<void>(ws, L.da1s), at<void>(ws, L.da3s), dxs, g->dws1, g->dws3, g->dws2, status, st,
-                         at<void>(ws, L.gmaps), sc(q ? q->ws1_scale : nullptr), sc(q ? q->ws3_scale : nullptr),
+                         map_scratch(ws, L), sc(q ? q->ws1_scale : nullptr), sc(q ? q->ws3_scale : nullptr),
                          sc(q ? q->ws2_scale : nullptr)));
   }
   if (s->offsets_full && s->copy_of_row_full)   // capacity mode: every copy, x gathered in dropless order

@@ -155,9 +155,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // Write into global memory at `dst` (128-byte aligned) a copy of the tensor
 // map `tmpl` whose global address is `addr` and whose second dimension (rows)
-// is `rows`, and make it usable by this thread's following TMA copies (the
-// copy and the field replacements are generic-proxy writes; the release /
-// acquire pair hands them to the tensor-map proxy).
+// is `rows` (generic-proxy writes: the copy, then the two field
+// replacements), and release them to the tensor-map proxy.  A thread that
+// then uses the map acquires it with tensormap_acquire.
 __device__ __forceinline__ void tensormap_rebase_rows(CUtensorMap* dst, const CUtensorMap* tmpl, uint64_t addr,
                                                       uint32_t rows) {
   const uint4* src = reinterpret_cast<const uint4*>(tmpl);
@@ -167,7 +167,9 @@ __device__ __forceinline__ void tensormap_rebase_rows(CUtensorMap* dst, const CU
   asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(addr) : "memory");
   asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst), "r"(rows) : "memory");
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
-  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(dst) : "memory");
+}
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

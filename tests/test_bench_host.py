@@ -50,18 +50,17 @@ def test_launch_counts():
     import bench
     from ragged_grouped_gemm_gb300.inputs import CONFIGS
     mix, ds = CONFIGS["mixtral"], CONFIGS["dsv3"]
-    # forward 6 (fused router; permute: single-CTA maps + rows; GEMM1, GEMM2, combine)
-    # + backward 10 (combine bwd, 5 GEMMs, unpermute, router gradient 3)
+    # forward 5 (fused router; single-pass permute; GEMM1, GEMM2, combine)
+    # + backward 13 (combine bwd, 5 GEMMs, 3 per-group map kernels, unpermute, router gradient 3)
     assert bench.route_launches(mix) == 1
-    assert bench.launches_per_step(mix) == 16
+    assert bench.launches_per_step(mix) == 5 + 13
     # E = 256: dense offsets, logits GEMM in 4 contraction slices, their sum, top-K, scan;
     # + shared expert (3 forward, 6 backward) + route-bias update
     assert bench.route_launches(ds) == 5
-    assert bench.launches_per_step(ds) == 5 + 2 + 3 + 10 + 3 + 6 + 1
-    # enough 128-token tiles to fill the GPU: no slices; more than 65536 copies: chunked maps
+    assert bench.launches_per_step(ds) == 5 + 1 + 3 + 13 + 3 + 6 + 1
+    # enough 128-token tiles to fill the GPU: no slices
     big = ds.replace(n_tok=65536)
     assert bench.route_launches(big) == 4
-    assert bench.launches_per_step(big) == 4 + 4 + 3 + 10 + 3 + 6 + 1
 
 
 def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
@@ -84,7 +83,8 @@ def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
         per_call = {"route": 0.05, "permute": 0.03, "grouped_ffn": 1.86, "combine": 0.02, "backward": 4.4}
         return {"cfg": cfg, "per_call": per_call, "kernels": kernels,
                 "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
-                "nonempty": cfg.n_exp, "max_load_over_mean": 1.1, "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s),
+                "nonempty": cfg.n_exp, "max_load_over_mean": 1.1, "inference_fwd": {"gather": 2.2e6, "x_perm": 2.1e6},
+                "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s),
                 "fwd": (2e6, 2.0 * s), "e2e": (600000.0, 6.8 * s)}
 
     monkeypatch.setattr(bench, "run_ours", fake_run_ours)

@@ -82,7 +82,7 @@ def test_inference_layer_with_gathered_ffn_matches_oracle(name):
     cfg = CONFIGS[name]
     p_cpu = make_layer(cfg, "cpu")
     p, h = to_dev(p_cpu), host_params(p_cpu)
-    layer = api.MoELayer(cfg, p, train=False)
+    layer = api.MoELayer(cfg, p, train=False, gather=True)
     assert layer.gather and layer.buf["x_perm"] is None
     out = layer.forward(p["x"])
     torch.cuda.synchronize()
@@ -106,12 +106,11 @@ def test_gathered_forward_full_size_equals_permuted_forward(name):
     cfg = CONFIGS[name]
     torch.cuda.empty_cache()
     p = make_layer(cfg, "cuda")
-    ref = api.MoELayer(cfg.replace(capacity_factor=0.0), p, train=False)
-    ref.gather = False
-    ref.buf["x_perm"] = torch.empty(cfg.rows, cfg.d_model, dtype=torch.bfloat16, device="cuda")
+    ref = api.MoELayer(cfg, p, train=False)
+    assert not ref.gather and ref.buf["x_perm"] is not None
     out_ref = ref.forward(p["x"]).clone()
     del ref
-    layer = api.MoELayer(cfg, p, train=False)
+    layer = api.MoELayer(cfg, p, train=False, gather=True)
     assert layer.gather
     out = layer.forward(p["x"])
     torch.cuda.synchronize()
