@@ -130,7 +130,9 @@ __global__ void build_group_maps_kernel(CUtensorMap* out, const __grid_constant_
 
 // STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
 // MAXG / MAXS: the most groups the shared-memory tables hold and the most
-// ring stages
+// ring stages.  MAXG = 0: no tables (the bf16 ragged-K form reads the group
+// offsets from global memory), and the room goes to a second fp32 staging
+// buffer per epilogue warp, so one box is written while the last is stored
 template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false, bool STG = false, int MAXG = kMaxGroups,
           int MAXS = 6>
 struct Cfg {
@@ -153,15 +155,17 @@ struct Cfg {
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
   // shared memory left for the stages: 227 KB less the alignment slack, the
   // staging buffers, the barriers (at most MAXS stages) and the group tables
-  static constexpr int kEpiBytes = STG ? 8 * 2048 : 0;
+  static constexpr int kEpiBufs = (STG && MAXG == 0) ? 2 : 1;
+  static constexpr int kEpiBytes = STG ? kEpiBufs * 8 * 2048 : 0;
+  static constexpr int kTableBytes = MAXG > 0 ? 2 * 4 * (MAXG + 1) : 0;
   static constexpr int kStageBudget = 232448 - 1024 - kEpiBytes - (3 * MAXS + 2 * 2 + 5) * 8 - 16 -
-                                      2 * 4 * (MAXG + 1) - kW8Slots * kW8SlotBytes;
+                                      kTableBytes - kW8Slots * kW8SlotBytes;
   static constexpr int kStagesRaw = kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > MAXS ? MAXS : kStagesRaw;
   // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
   static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
   static constexpr uint32_t kSfCol = 2 * BN;
-  // stages | W8 code slots | fp32 staging (8 warps x 2 KB, STG only) |
+  // stages | W8 code slots | fp32 staging (8 warps x kEpiBufs x 2 KB, STG only) |
   // barriers (2S, + S scale-ready for MXFP8, + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
   static constexpr int kW8Off = kStages * kStageBytes;
   static constexpr int kEpiOff = kW8Off + kW8Slots * kW8SlotBytes;
@@ -170,12 +174,17 @@ struct Cfg {
   static constexpr int kOffOff = kMiscOff + 16;
   static constexpr int kMaxG = MAXG;
   static constexpr size_t smem_bytes(int groups) {
-    return 1024 + kOffOff + 2 * 4 * (groups + 1);
+    return 1024 + kOffOff + (MAXG > 0 ? 2 * 4 * (groups + 1) : 0);
   }
   static_assert(kStages >= 2, "shared memory holds fewer than two stages");
   static_assert(smem_bytes(MAXG) <= 232448, "shared memory above 227 KB");
   static_assert(!QUANT || 2 * BN + 16 * kStages <= 512, "accumulators and scale buffers exceed tensor memory");
 };
+
+// The configuration of each kernel form: the bf16 ragged-K (weight-gradient)
+// form keeps no group tables and double-buffers its fp32 staging.
+template <int BN, bool A_MN, int EPI, bool QUANT, bool PAIR, bool W8>
+using KernelCfg = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32, (A_MN && !QUANT && !W8) ? 0 : kMaxGroups>;
 
 struct Tile {
   int g, mt, nt;
@@ -287,7 +296,7 @@ template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT, bool PAIR, bool W8 
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads), 1)
     grouped_gemm_kernel(const __grid_constant__ KParams p) {
   static_assert(!GATHER || (!A_MN && !B_MN && !QUANT && !W8), "GATHER: K-major bf16 ragged-M forms");
-  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
+  using C = KernelCfg<BN, A_MN, EPI, QUANT, PAIR, W8>;
   // bf16: the MN-major-A form is the ragged-K (weight-gradient) form.  MXFP8
   // operands are always K-major; A_MN then only selects the ragged-K form.
   constexpr bool RAGGED_K = A_MN;
@@ -304,8 +313,10 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
   uint64_t* mma_done = tempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
-  int* s_off = reinterpret_cast<int*>(smem + C::kOffOff);
-  int* s_pre = s_off + (p.num_groups + 1);
+  // group offsets: a shared copy, or (no tables) the caller's array itself
+  int* s_tab = reinterpret_cast<int*>(smem + C::kOffOff);
+  const int* s_off = C::kMaxG > 0 ? s_tab : p.offsets;
+  int* s_pre = s_tab + (p.num_groups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -358,7 +369,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
   }
   // group offsets and (ragged M) the prefix of per-group tile counts
   // (128-row M tiles times N tiles)
-  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = p.offsets[i];
+  if (C::kMaxG > 0)
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) s_tab[i] = p.offsets[i];
   __syncthreads();
   if (!RAGGED_K && warp == 0) {
     const int ntiles = (p.n_size + p.tile_n - 1) / p.tile_n;
@@ -864,6 +876,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     const int hf = (warp - 2) >> 2;   // column half of the tile
     const int r = q * 32 + lane;
     uint32_t tcount = 0;
+    uint32_t nstore = 0;   // TMA stores this warp has issued (fp32 staging)
     for (int tile = unit0; tile < total_tiles; tile += ustride, ++tcount) {
       const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
       const uint32_t buf = tcount & 1u;
@@ -890,10 +903,13 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           // store of 16 full 128-byte rows, which clips rows and columns
           // outside the output (evict-first in L2: the fp32 output is written
           // once and not read back).  The TMEM load of the next 32 columns is
-          // in flight while these are staged.
+          // in flight while these are staged.  With two buffers a warp waits
+          // only for the store before the last to have read its buffer; a box
+          // that starts past the output is neither staged nor stored, so the
+          // buffers alternate over the stores actually issued.
           constexpr int NCH = BN / 64;
-          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
-          const uint32_t stg_addr = smem_u32(stg);
+          constexpr int NB = C::kEpiBufs;
+          uint8_t* stg0 = smem + C::kEpiOff + (warp - 2) * (NB * 2048);
           uint32_t va[16], vb[16], vc[16], vd[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) va[j] = vb[j] = vc[j] = vd[j] = 0u;
@@ -912,7 +928,17 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+              // boxes that start past the output's last column or row hold nothing to write
+              const int col = t.nt * BN + c_begin + 32 * i;
+              const int row = (RAGGED_K ? t.m0 : t.row0) + q * 32 + 16 * h;
+              const int rows = RAGGED_K ? p.m_size : p.c_rows;
+              if (!(col < p.n_size && row < rows)) continue;   // uniform across the warp
+              uint8_t* stg = stg0 + (NB == 2 ? (nstore & 1u) * 2048 : 0);
+              const uint32_t stg_addr = smem_u32(stg);
+              if (lane == 0) {   // the store that last used this buffer has read it
+                if (NB == 2) bulk_wait_group_read1();
+                else bulk_wait_group_read0();
+              }
               __syncwarp();
               if ((lane >> 4) == h) {
 #pragma unroll
@@ -927,15 +953,10 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                // boxes that start past the output's last column or row hold nothing to write
-                const int col = t.nt * BN + c_begin + 32 * i;
-                const int row = (RAGGED_K ? t.m0 : t.row0) + q * 32 + 16 * h;
-                const int rows = RAGGED_K ? p.m_size : p.c_rows;
-                if (col < p.n_size && row < rows) {
-                  tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : t.split, policy_evict_first());
-                  bulk_commit_group();
-                }
+                tma_store_3d_hint(&p.tmC, stg, col, row, RAGGED_K ? t.g : t.split, policy_evict_first());
+                bulk_commit_group();
               }
+              ++nstore;
             }
             if (i + 1 < NCH) {
               if (!zero) {
@@ -954,7 +975,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           // a multiple of 32 wide: 32 rows x 16 columns per 2 KB buffer
           // (64-byte swizzle: chunk j of row r at chunk j ^ ((r >> 1) & 3)).
           constexpr int NCH = BN / 32;
-          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * 2048;
+          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * (C::kEpiBufs * 2048);
           const uint32_t stg_addr = smem_u32(stg);
           uint32_t va[16], vb[16];
 #pragma unroll
@@ -1287,7 +1308,7 @@ bool make_map_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 template <int BN, bool A_MN, bool B_MN, int EPI, bool QUANT = false, bool PAIR = false, bool W8 = false,
           bool GATHER = false>
 cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream) {
-  using C = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32>;
+  using C = KernelCfg<BN, A_MN, EPI, QUANT, PAIR, W8>;
   constexpr int CN = 2;   // CTAs per cluster (PAIR)
   const size_t smem = C::smem_bytes(kp.num_groups);
   auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, EPI, QUANT, PAIR, W8, GATHER>;

@@ -572,9 +572,12 @@ __global__ void __launch_bounds__(1024, 1) maps_onepass_kernel(int n_tok, int E,
 // prefix (state "prefix"; chunk 0 publishes offsets[e] + count at once).  A
 // chunk's first row of expert e is found by walking back over the preceding
 // chunks' words, adding aggregates until a prefix is met (decoupled
-// look-back): one warp per expert reads the words of 32 preceding chunks per
-// round trip, the nearest chunk with a prefix ends the walk, and the
-// aggregates before it are added by a warp reduction.  Every wait on a word
+// look-back).  All of a CTA's threads walk at once: S = 32, 16, ... 1 lanes
+// per expert so that every expert has its lanes (S * E <= kSpThreads where it
+// fits), each lane with kSpLook words in flight, so one round trip covers
+// S * kSpLook preceding chunks of every expert; the nearest chunk with a
+// prefix ends the walk, and the values after it are added by a shuffle
+// reduction over the expert's lanes.  Every wait on a word
 // not yet published this call is bounded and reports MOE_DEV_TIMEOUT.
 // The tag is the call's generation + 1 (the generation counter and the words
 // start at zero after moe_workspace_init; the last CTA of a call advances
@@ -585,14 +588,15 @@ __global__ void __launch_bounds__(1024, 1) maps_onepass_kernel(int n_tok, int E,
 // exactly as the other map kernels assign them, with the same bound checks;
 // then the chunk's token rows are read once and written to their K rows.
 constexpr int kSpTok = 16;
-constexpr int kSpThreads = 512;
+constexpr int kSpThreads = 256;
+constexpr int kSpLook = 16;   // look-back words in flight per lane
 constexpr uint64_t kSpAggregate = 0, kSpPrefix = 1;
 
 __device__ __forceinline__ uint64_t sp_word(uint32_t tag, uint64_t state, int value) {
   return (static_cast<uint64_t>(tag) << 32) | (state << 31) | (static_cast<uint32_t>(value) & 0x7FFFFFFFu);
 }
 
-__global__ void __launch_bounds__(kSpThreads) permute_single_pass_kernel(
+__global__ void __launch_bounds__(kSpThreads, 2) permute_single_pass_kernel(
     int n_tok, int E, int K, int d8, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
     const uint4* __restrict__ x, int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row,
     uint4* __restrict__ x_perm, unsigned long long* look, int32_t* ctl, int32_t* status) {
@@ -636,33 +640,55 @@ __global__ void __launch_bounds__(kSpThreads) permute_single_pass_kernel(
     }
   }
   if (chunk > 0) {
-    // look-back, a warp per expert: lane l reads chunk j0 - l of the window
-    for (int e = warp; e < E; e += kSpThreads / 32) {
+    // look-back: S lanes per expert (a power of two; S * experts per pass =
+    // kSpThreads), lane u of an expert's group reads the words of chunks
+    // j0 - u - S*l, l < kSpLook, all in flight together.  The nearest chunk
+    // with a prefix ends the walk; the values from it up to chunk - 1 are
+    // summed over the group.
+    int S = 32;
+    while (S > 1 && S * E > kSpThreads) S >>= 1;
+    const int per_pass = kSpThreads / S;
+    const int u = tid & (S - 1);
+    const unsigned gmask = S == 32 ? kFull : (((1u << S) - 1u) << (lane & ~(S - 1)));
+    for (int e = tid / S; e < E; e += per_pass) {   // uniform within each group of S lanes
       int acc = 0;
       int j0 = chunk - 1;
       uint64_t t0 = 0;
-      while (true) {
-        const int j = j0 - lane;
-        unsigned long long w = 0;
-        bool ready = true;
-        if (j >= 0) {
-          w = vlook[static_cast<int64_t>(j) * E + e];
-          ready = static_cast<uint32_t>(w >> 32) == tag;
+      while (j0 >= 0) {
+        unsigned long long w[kSpLook];
+#pragma unroll
+        for (int l = 0; l < kSpLook; ++l) {
+          const int j = j0 - u - S * l;
+          w[l] = j >= 0 ? vlook[static_cast<int64_t>(j) * E + e] : 0ull;
         }
-        const bool is_prefix = j >= 0 && ready && ((w >> 31) & 1u) == kSpPrefix;
-        const unsigned pm = __ballot_sync(kFull, is_prefix);
-        const int stop = pm ? __ffs(pm) - 1 : 32;                          // nearest chunk with a prefix
-        const unsigned need = stop < 31 ? ((2u << stop) - 1u) : kFull;    // lanes 0..stop
-        const unsigned nr = __ballot_sync(kFull, !ready) & need;
-        if (nr) {   // a chunk before the prefix has not published yet: read the window again (bounded)
-          // (lane 0's clock decides for the whole warp, so the warp leaves together)
+        int jp = -1;   // this lane's nearest chunk with a prefix
+#pragma unroll
+        for (int l = kSpLook - 1; l >= 0; --l) {
+          const int j = j0 - u - S * l;
+          if (j >= 0 && static_cast<uint32_t>(w[l] >> 32) == tag && ((w[l] >> 31) & 1u) == kSpPrefix) jp = j;
+        }
+        for (int o = S >> 1; o; o >>= 1) jp = max(jp, __shfl_xor_sync(gmask, jp, o, S));
+        int nr = 0, v = 0;   // a chunk from the prefix on that has not published yet; the sum
+#pragma unroll
+        for (int l = 0; l < kSpLook; ++l) {
+          const int j = j0 - u - S * l;
+          if (j >= 0 && j >= jp) {
+            if (static_cast<uint32_t>(w[l] >> 32) != tag) nr = 1;
+            else v += static_cast<int>(static_cast<uint32_t>(w[l]) & 0x7FFFFFFFu);
+          }
+        }
+        for (int o = S >> 1; o; o >>= 1) {
+          nr |= __shfl_xor_sync(gmask, nr, o, S);
+          v += __shfl_xor_sync(gmask, v, o, S);
+        }
+        if (nr) {   // read the window again (bounded); lane 0 of the group decides for it
           int out = 0;
-          if (lane == 0) {
+          if (u == 0) {
             if (t0 == 0) t0 = globaltimer_ns();
             else out = globaltimer_ns() - t0 > kSpinTimeoutNs;
           }
-          if (__shfl_sync(kFull, out, 0)) {
-            if (lane == 0) {
+          if (__shfl_sync(gmask, out, 0, S)) {
+            if (u == 0) {
               atomicOr(&s_bad, DEV_TIMEOUT);
               if (status) atomicExch(status + 1, 700);
             }
@@ -670,15 +696,12 @@ __global__ void __launch_bounds__(kSpThreads) permute_single_pass_kernel(
           }
           continue;
         }
-        int v = (((need >> lane) & 1u) && j >= 0) ? static_cast<int>(static_cast<uint32_t>(w) & 0x7FFFFFFFu) : 0;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
         acc += v;
-        if (stop < 32) break;
-        j0 -= 32;
+        if (jp >= 0) break;
+        j0 -= S * kSpLook;
         t0 = 0;
       }
-      if (lane == 0) {
+      if (u == 0) {
         s_base[e] = acc;
         *reinterpret_cast<volatile unsigned long long*>(look + static_cast<int64_t>(chunk) * E + e) =
             sp_word(tag, kSpPrefix, acc + s_h[e]);
@@ -720,18 +743,23 @@ __global__ void __launch_bounds__(kSpThreads) permute_single_pass_kernel(
     }
   }
   __syncthreads();
-  // the chunk's token rows, each read once and written to its copies' rows
+  // the chunk's token rows, each read once and written to its copies' rows:
+  // a thread takes one 16-byte column chunk of all the chunk's tokens (their
+  // loads in flight together), then stores each to its K rows
   const int t0k = chunk * kSpTok;
   const int ntk = ncp / K;
-  const int units = ntk * d8;
-#pragma unroll 4
-  for (int u = tid; u < units; u += kSpThreads) {
-    const int tt = u / d8;
-    const int i = u - tt * d8;
-    const uint4 v = x[static_cast<int64_t>(t0k + tt) * d8 + i];
-    for (int k = 0; k < K; ++k) {
-      const int r = s_pos[tt * K + k];
-      if (r >= 0) x_perm[static_cast<int64_t>(r) * d8 + i] = v;
+  for (int i = tid; i < d8; i += kSpThreads) {
+    uint4 v[kSpTok];
+#pragma unroll
+    for (int tt = 0; tt < kSpTok; ++tt)
+      v[tt] = tt < ntk ? x[static_cast<int64_t>(t0k + tt) * d8 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int tt = 0; tt < kSpTok; ++tt) {
+      if (tt >= ntk) break;
+      for (int k = 0; k < K; ++k) {
+        const int r = s_pos[tt * K + k];
+        if (r >= 0) x_perm[static_cast<int64_t>(r) * d8 + i] = v[tt];
+      }
     }
   }
   if (tid == 0) {
