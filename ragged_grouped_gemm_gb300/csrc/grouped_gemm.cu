@@ -31,9 +31,13 @@
 // rank 0's accumulator-free barrier.  TMEM is allocated and freed by both
 // CTAs together, between cluster barriers.
 //
-// fp32 outputs leave through TMA tensor stores: each epilogue warp stages
-// 16 rows x 32 columns (whole 128-byte rows) at a time in 2 KB of shared
-// memory, or 32 x 16 when a tile's column halves are 16 wide.
+// fp32 outputs of the ragged-M forms leave through TMA tensor stores: each
+// epilogue warp stages 16 rows x 32 columns (whole 128-byte rows) at a time
+// in 2 KB of shared memory, or 32 x 16 when a tile's column halves are 16
+// wide.  The weight gradients (ragged K) have 4 KB per warp: the one-SM form
+// double-buffers its 16 x 32 boxes; the CTA-pair form stages 32 x 32 and
+// writes it with plain coalesced stores, which leaves the TMA unit to the
+// operand loads.
 //
 // Shared-memory operand layouts (both 1024-byte aligned per stage):
 //   K-major : rows of 64 bf16 (128 B), 8-row swizzle atoms of 1024 B;
@@ -131,8 +135,9 @@ __global__ void build_group_maps_kernel(CUtensorMap* out, const __grid_constant_
 // STG: the kernel stages fp32 output blocks for TMA stores (weight gradients)
 // MAXG / MAXS: the most groups the shared-memory tables hold and the most
 // ring stages.  MAXG = 0: no tables (the bf16 ragged-K form reads the group
-// offsets from global memory), and the room goes to a second fp32 staging
-// buffer per epilogue warp, so one box is written while the last is stored
+// offsets from global memory), and the room goes to 4 KB of fp32 staging per
+// epilogue warp: two 2 KB TMA-store buffers (one-SM form) or one 32 x 32 box
+// for plain stores (CTA-pair form)
 template <int BN, bool QUANT = false, bool PAIR = false, bool W8 = false, bool STG = false, int MAXG = kMaxGroups,
           int MAXS = 6>
 struct Cfg {
@@ -155,8 +160,9 @@ struct Cfg {
       QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
   // shared memory left for the stages: 227 KB less the alignment slack, the
   // staging buffers, the barriers (at most MAXS stages) and the group tables
-  static constexpr int kEpiBufs = (STG && MAXG == 0) ? 2 : 1;
-  static constexpr int kEpiBytes = STG ? kEpiBufs * 8 * 2048 : 0;
+  static constexpr bool kWideStaging = STG && MAXG == 0;
+  static constexpr int kEpiWarpBytes = kWideStaging ? 4096 : 2048;
+  static constexpr int kEpiBytes = STG ? 8 * kEpiWarpBytes : 0;
   static constexpr int kTableBytes = MAXG > 0 ? 2 * 4 * (MAXG + 1) : 0;
   static constexpr int kStageBudget = 232448 - 1024 - kEpiBytes - (3 * MAXS + 2 * 2 + 5) * 8 - 16 -
                                       kTableBytes - kW8Slots * kW8SlotBytes;
@@ -165,7 +171,7 @@ struct Cfg {
   // accumulators (2 x BN columns) and, for MXFP8, one 16-column scale buffer per stage
   static constexpr uint32_t kTmemCols = QUANT ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
   static constexpr uint32_t kSfCol = 2 * BN;
-  // stages | W8 code slots | fp32 staging (8 warps x kEpiBufs x 2 KB, STG only) |
+  // stages | W8 code slots | fp32 staging (8 warps x kEpiWarpBytes, STG only) |
   // barriers (2S, + S scale-ready for MXFP8, + 5) | tmem base, abort | offsets[G+1] | prefix[G+1]
   static constexpr int kW8Off = kStages * kStageBytes;
   static constexpr int kEpiOff = kW8Off + kW8Slots * kW8SlotBytes;
@@ -182,7 +188,7 @@ struct Cfg {
 };
 
 // The configuration of each kernel form: the bf16 ragged-K (weight-gradient)
-// form keeps no group tables and double-buffers its fp32 staging.
+// form keeps no group tables and has 4 KB of fp32 staging per epilogue warp.
 template <int BN, bool A_MN, int EPI, bool QUANT, bool PAIR, bool W8>
 using KernelCfg = Cfg<BN, QUANT, PAIR, W8, EPI == EPI_F32, (A_MN && !QUANT && !W8) ? 0 : kMaxGroups>;
 
@@ -896,20 +902,98 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         }
         const bool zero = t.num_kb == 0;
         const int c_begin = hf * (BN / 2);
-        if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
+        if (EPI == EPI_F32 && C::kWideStaging && PAIR && p.c_tma && (BN / 2) % 32 == 0) {
+          // Weight gradients on CTA pairs: the warp's 32 rows x 32 columns go to a 4 KB
+          // shared buffer (one row per lane, 128-byte swizzle: 16-byte chunk j
+          // of row r at chunk j ^ (r & 7)) and leave by plain 16-byte stores,
+          // lane l writing chunk l % 8 of rows l / 8 + 4j, so each store
+          // instruction covers four whole 128-byte lines (L2 evict-first: the
+          // fp32 output is written once).  The TMA unit then carries only the
+          // operand loads: the output is a quarter of the bytes a tile moves,
+          // and as TMA stores it delayed the loads behind them (this form is
+          // tensor-bound; the one-SM form, bound by its output stores, keeps
+          // the TMA stores below).  The TMEM
+          // load of the next 32 columns is in flight meanwhile.  (c_tma: the
+          // output's rows start 16-byte aligned.)
+          constexpr int NCH = BN / 64;
+          const uint32_t stg = smem_u32(smem + C::kEpiOff + (warp - 2) * C::kEpiWarpBytes);
+          const uint64_t pol = policy_evict_first();
+          const int rows = RAGGED_K ? p.m_size : p.c_rows;
+          float* gbase = reinterpret_cast<float*>(obase);
+          const int c8 = lane & 7;
+          uint32_t va[16], vb[16], vc[16], vd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) va[j] = vb[j] = vc[j] = vd[j] = 0u;
+          if (!zero) {
+            tmem_ld_32x32b_x16(tb + c_begin, va);
+            tmem_ld_32x32b_x16(tb + c_begin + 16, vb);
+            tmem_wait_ld(va);
+            reg_fence(vb);
+          }
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            if (!zero && i + 1 < NCH) {
+              tmem_ld_32x32b_x16(tb + c_begin + 32 * (i + 1), vc);
+              tmem_ld_32x32b_x16(tb + c_begin + 32 * (i + 1) + 16, vd);
+            }
+            const int col = t.nt * BN + c_begin + 32 * i;
+            const int row = (RAGGED_K ? t.m0 : t.row0) + q * 32;
+            if (col < p.n_size && row < rows) {   // uniform across the warp
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4), va[4 * j], va[4 * j + 1], va[4 * j + 2],
+                             va[4 * j + 3]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                st_shared_v4(stg + lane * 128 + (((j + 4) ^ (lane & 7)) << 4), vb[4 * j], vb[4 * j + 1],
+                             vb[4 * j + 2], vb[4 * j + 3]);
+              __syncwarp();
+              const int gc = col + 4 * c8;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int r2 = (lane >> 3) + 4 * j;
+                uint32_t x0, x1, x2, x3;
+                ld_shared_v4(stg + r2 * 128 + ((c8 ^ (r2 & 7)) << 4), x0, x1, x2, x3);
+                if (row + r2 < rows && gc < p.n_size) {
+                  float* dst = gbase + static_cast<int64_t>(row + r2) * p.ld_out + gc;
+                  if (gc + 4 <= p.n_size) {
+                    st_global_v4_hint(dst, x0, x1, x2, x3, pol);
+                  } else {   // the output's last columns
+                    dst[0] = __uint_as_float(x0);
+                    if (gc + 1 < p.n_size) dst[1] = __uint_as_float(x1);
+                    if (gc + 2 < p.n_size) dst[2] = __uint_as_float(x2);
+                  }
+                }
+              }
+              __syncwarp();
+            }
+            if (i + 1 < NCH) {
+              if (!zero) {
+                tmem_wait_ld(vc);
+                reg_fence(vd);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                va[j] = vc[j];
+                vb[j] = vd[j];
+              }
+            }
+          }
+        } else if (EPI == EPI_F32 && p.c_tma && (BN / 2) % 32 == 0) {
           // Stage this warp's 32 rows x 32 columns as two 16-row halves in a
           // 2 KB shared-memory buffer (128-byte swizzle: 16-byte chunk j of
           // row r at chunk j ^ (r & 7)) and write each half with a TMA tensor
           // store of 16 full 128-byte rows, which clips rows and columns
           // outside the output (evict-first in L2: the fp32 output is written
           // once and not read back).  The TMEM load of the next 32 columns is
-          // in flight while these are staged.  With two buffers a warp waits
-          // only for the store before the last to have read its buffer; a box
-          // that starts past the output is neither staged nor stored, so the
-          // buffers alternate over the stores actually issued.
+          // in flight while these are staged.  With two buffers (4 KB of
+          // staging) a warp waits only for the store before the last to have
+          // read its buffer; a box that starts past the output is neither
+          // staged nor stored, so the buffers alternate over the stores
+          // actually issued.
           constexpr int NCH = BN / 64;
-          constexpr int NB = C::kEpiBufs;
-          uint8_t* stg0 = smem + C::kEpiOff + (warp - 2) * (NB * 2048);
+          constexpr int NB = C::kWideStaging ? 2 : 1;
+          uint8_t* stg0 = smem + C::kEpiOff + (warp - 2) * C::kEpiWarpBytes;
           uint32_t va[16], vb[16], vc[16], vd[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) va[j] = vb[j] = vc[j] = vd[j] = 0u;
@@ -975,7 +1059,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           // a multiple of 32 wide: 32 rows x 16 columns per 2 KB buffer
           // (64-byte swizzle: chunk j of row r at chunk j ^ ((r >> 1) & 3)).
           constexpr int NCH = BN / 32;
-          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * (C::kEpiBufs * 2048);
+          uint8_t* stg = smem + C::kEpiOff + (warp - 2) * C::kEpiWarpBytes;
           const uint32_t stg_addr = smem_u32(stg);
           uint32_t va[16], vb[16];
 #pragma unroll
