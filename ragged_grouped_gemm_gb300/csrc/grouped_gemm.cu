@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       mbar_init(&full[s], W8 ? 1 + kConvWarps : 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], kSfWarps);
+    for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], 1);   // the scale warp that builds it
     for (int s = 0; s < C::kW8Slots; ++s) {
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], kConvWarps);
@@ -770,8 +770,13 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     // Rearrange the stage's raw scale rows ([block][row]) into the 512-byte
     // atoms tcgen05.cp expects: for row r, byte j (scale block) of 32-bit word
     // (r/32)%4 of 16-byte row r%32; one atom per 128 rows of A or of B.
+    // Warp w of the kSfWarps builds the whole of every stage s with
+    // s % kSfWarps == w, so consecutive stages are built at once; lane l
+    // writes 16-byte row l of each atom (rows l, l+32, l+64, l+96).  A warp
+    // owns whole stages and meets each of their fills in order: a parity
+    // wait must never skip a phase of its barrier.
     if (QUANT) {
-      const int ct = threadIdx.x - 10 * 32;   // 0..127
+      const int sfw = warp - 10;
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < total_tiles; tile += ustride) {
@@ -781,27 +786,35 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         constexpr int AS = RAGGED_K ? 128 : 144;
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           const int s = it % S;
+          if (s % kSfWarps != sfw) continue;
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 500 + s)) { ok = false; break; }
           uint8_t* st = smem + s * C::kStageBytes;
           const uint8_t* ra = st + C::kQARaw;
           const uint8_t* rb = st + C::kQBRaw;
-          uint32_t* atoms = reinterpret_cast<uint32_t*>(st + C::kQAtoms);
-          {
-            const int r = ct;
-            const uint32_t w = static_cast<uint32_t>(ra[a_rem + r]) | (static_cast<uint32_t>(ra[AS + a_rem + r]) << 8) |
-                               (static_cast<uint32_t>(ra[2 * AS + a_rem + r]) << 16) |
-                               (static_cast<uint32_t>(ra[3 * AS + a_rem + r]) << 24);
-            atoms[(r & 31) * 4 + (r >> 5)] = w;
+          const uint32_t atoms = smem_u32(st + C::kQAtoms);
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = a_rem + lane + 32 * i;
+            w[i] = static_cast<uint32_t>(ra[r]) | (static_cast<uint32_t>(ra[AS + r]) << 8) |
+                   (static_cast<uint32_t>(ra[2 * AS + r]) << 16) | (static_cast<uint32_t>(ra[3 * AS + r]) << 24);
           }
-          for (int r = ct; r < BN; r += 128) {
-            // dual N: rows [0, BN/2) from the W1 scale rows, the rest from W3's
-            const int half = p.b_dual_n ? (r >= BN / 2 ? 1 : 0) : 0;
-            const int w_ = p.b_dual_n ? BN / 2 : BN;
-            const uint8_t* src = rb + half * 2 * BN + (r - half * (BN / 2));
-            const uint32_t w = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[w_]) << 8) |
-                               (static_cast<uint32_t>(src[2 * w_]) << 16) | (static_cast<uint32_t>(src[3 * w_]) << 24);
-            atoms[128 + (r >> 7) * 128 + (r & 31) * 4 + ((r >> 5) & 3)] = w;
+          st_shared_v4(atoms + lane * 16, w[0], w[1], w[2], w[3]);
+          // dual N: rows [0, BN/2) from the W1 scale rows, the rest from W3's
+          const int w_ = p.b_dual_n ? BN / 2 : BN;
+#pragma unroll
+          for (int a = 0; a < (BN + 127) / 128; ++a) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 128 * a + lane + 32 * i;
+              const int half = p.b_dual_n ? (r >= BN / 2 ? 1 : 0) : 0;
+              const uint8_t* src = rb + half * 2 * BN + (r - half * (BN / 2));
+              w[i] = r < BN ? (static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[w_]) << 8) |
+                               (static_cast<uint32_t>(src[2 * w_]) << 16) | (static_cast<uint32_t>(src[3 * w_]) << 24))
+                            : 0u;
+            }
+            st_shared_v4(atoms + 512 + a * 512 + lane * 16, w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
