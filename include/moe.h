@@ -390,7 +390,11 @@ MOE_API moe_status_t moe_quantize_mxfp8_t(const void* src, int64_t groups, int64
  * copy_of_row maps, and the permuted rows as codes xq_perm [R,D] with scales
  * xs_perm [D/32, MOE_MX_SCALE_LD(R)]; optionally (xq_tok non-NULL) the
  * token-order rows xq_tok [N,D], xs_tok [D/32, MOE_MX_SCALE_LD(N)] for the
- * shared expert.  d->precision must be 1.  Needs the forward workspace. */
+ * shared expert.  d->precision must be 1.  Needs the forward workspace.
+ * Where moe_permute runs in one launch (ceil(N/16) * E <= 131072), so does
+ * this: each token row is read and quantised once, and its codes and scale
+ * bytes are written to its K rows (and its token row); the codes are those
+ * of moe_quantize_mxfp8 applied to the permuted rows. */
 MOE_API moe_status_t moe_permute_mxfp8(const moe_desc_t* d, const void* x, const int32_t* topk_idx,
                                        const int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row,
                                        void* xq_perm, void* xs_perm, void* xq_tok, void* xs_tok, void* ws,

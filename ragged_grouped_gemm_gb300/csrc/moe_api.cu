@@ -665,9 +665,15 @@ moe_status_t moe_permute_mxfp8(const moe_desc_t* d, const void* x, const int32_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WsLayout L = layout(*d);
   const int64_t R = static_cast<int64_t>(d->n_tok) * d->top_k;
+  int32_t* status = at<int32_t>(ws, L.status);
+  if (moe::permute_single_pass_look_words(d->n_tok, d->n_exp) <= static_cast<int64_t>(kLookWords))
+    return cuda_status(moe::launch_permute_single_pass_mxfp8(
+        d->n_tok, d->n_exp, d->top_k, d->d_model, topk_idx, offsets, x, row_of_copy, copy_of_row,
+        static_cast<uint8_t*>(xq_perm), static_cast<uint8_t*>(xs_perm), moe::mx_scale_ld(R),
+        static_cast<uint8_t*>(xq_tok), static_cast<uint8_t*>(xq_tok ? xs_tok : nullptr), moe::mx_scale_ld(d->n_tok),
+        at<unsigned long long>(ws, L.look), status + kPermuteCtlWord, status, st));
   MOE_CUDA(moe::launch_permute_maps(d->n_tok, d->n_exp, d->top_k, topk_idx, offsets, at<int32_t>(ws, L.blk_counts),
-                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row,
-                                    at<int32_t>(ws, L.status), st));
+                                    at<int32_t>(ws, L.blk_base), row_of_copy, copy_of_row, status, st));
   MOE_CUDA(moe::launch_mx_quant_rows(x, copy_of_row, d->top_k, R, d->d_model, R, moe::mx_scale_ld(R),
                                      static_cast<uint8_t*>(xq_perm), static_cast<uint8_t*>(xs_perm), st));
   if (xq_tok)

@@ -596,10 +596,22 @@ __device__ __forceinline__ uint64_t sp_word(uint32_t tag, uint64_t state, int va
   return (static_cast<uint64_t>(tag) << 32) | (state << 31) | (static_cast<uint32_t>(value) & 0x7FFFFFFFu);
 }
 
+// MXFP8 outputs of the quantising form: codes [rows][d] and E8M0 scales
+// [d/32][ld] of the permuted rows, and (nullable) of the token rows.
+struct SpQuantOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  int64_t ld;
+  uint8_t* tok_codes;
+  uint8_t* tok_scales;
+  int64_t tok_ld;
+};
+
+template <bool QUANT>
 __global__ void __launch_bounds__(kSpThreads, 2) permute_single_pass_kernel(
     int n_tok, int E, int K, int d8, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
     const uint4* __restrict__ x, int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row,
-    uint4* __restrict__ x_perm, unsigned long long* look, int32_t* ctl, int32_t* status) {
+    uint4* __restrict__ x_perm, unsigned long long* look, int32_t* ctl, int32_t* status, SpQuantOut q) {
   extern __shared__ int s_sp[];
   int* s_h = s_sp;                    // [E] the chunk's copies per expert
   int* s_base = s_sp + E;             // [E] the chunk's next row per expert
@@ -629,6 +641,21 @@ __global__ void __launch_bounds__(kSpThreads, 2) permute_single_pass_kernel(
   }
   __syncthreads();
   volatile unsigned long long* vlook = look;
+  // bf16: this thread's first 16-byte column of the chunk's token rows is
+  // loaded now, so the reads are in flight during the look-back
+  const int t0k = chunk * kSpTok;
+  const int ntk = ncp / K;
+  uint4 v[kSpTok];
+  if (!QUANT && tid < d8) {
+#pragma unroll
+    for (int tt = 0; tt < kSpTok; ++tt)
+      v[tt] = tt < ntk ? x[static_cast<int64_t>(t0k + tt) * d8 + tid] : make_uint4(0, 0, 0, 0);
+  }
+  if (QUANT && tid < ntk * (d8 / 4)) {   // QUANT: this thread's first 32-element block
+    const uint4* src = x + static_cast<int64_t>(t0k + tid / (d8 / 4)) * d8 + (tid % (d8 / 4)) * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = src[j];
+  }
   // publish this chunk's aggregates (chunk 0: its prefixes)
   for (int e = tid; e < E; e += kSpThreads) {
     unsigned long long* mine = look + static_cast<int64_t>(chunk) * E + e;
@@ -745,14 +772,51 @@ __global__ void __launch_bounds__(kSpThreads, 2) permute_single_pass_kernel(
   __syncthreads();
   // the chunk's token rows, each read once and written to its copies' rows:
   // a thread takes one 16-byte column chunk of all the chunk's tokens (their
-  // loads in flight together), then stores each to its K rows
-  const int t0k = chunk * kSpTok;
-  const int ntk = ncp / K;
-  for (int i = tid; i < d8; i += kSpThreads) {
-    uint4 v[kSpTok];
+  // loads in flight together; the first chunk was loaded before the
+  // look-back), then stores each to its K rows.  QUANT: a thread takes one
+  // 32-element block of a token, quantises it once (the row quantiser's
+  // arithmetic) and writes its codes and scale byte to the token's K rows
+  // (and to the token row)
+  if (QUANT) {
+    const int nkb = d8 / 4;
+    const int64_t d = static_cast<int64_t>(d8) * 8;    // elements per row = code bytes per row
+    for (int u = tid; u < ntk * nkb; u += kSpThreads) {
+      const int tt = u / nkb;
+      const int kb = u - tt * nkb;
+      const int64_t tok = t0k + tt;
+      uint4 vb[4];
+      if (u == tid) {   // loaded before the look-back
 #pragma unroll
-    for (int tt = 0; tt < kSpTok; ++tt)
-      v[tt] = tt < ntk ? x[static_cast<int64_t>(t0k + tt) * d8 + i] : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; ++j) vb[j] = v[j];
+      } else {
+        const uint4* src = x + tok * d8 + kb * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) vb[j] = src[j];
+      }
+      uint4 c0, c1;
+      const uint8_t sc = mx_quant_block32(vb, c0, c1);
+      for (int k = 0; k < K; ++k) {
+        const int r = s_pos[tt * K + k];
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(q.codes + static_cast<int64_t>(r) * d + kb * 32);
+        dst[0] = c0;
+        dst[1] = c1;
+        q.scales[static_cast<int64_t>(kb) * q.ld + r] = sc;
+      }
+      if (q.tok_codes) {
+        uint4* dst = reinterpret_cast<uint4*>(q.tok_codes + tok * d + kb * 32);
+        dst[0] = c0;
+        dst[1] = c1;
+        q.tok_scales[static_cast<int64_t>(kb) * q.tok_ld + tok] = sc;
+      }
+    }
+  }
+  for (int i = tid; i < (QUANT ? 0 : d8); i += kSpThreads) {
+    if (i != tid) {
+#pragma unroll
+      for (int tt = 0; tt < kSpTok; ++tt)
+        v[tt] = tt < ntk ? x[static_cast<int64_t>(t0k + tt) * d8 + i] : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int tt = 0; tt < kSpTok; ++tt) {
       if (tt >= ntk) break;
@@ -1338,10 +1402,25 @@ cudaError_t launch_permute_single_pass(int n_tok, int n_exp, int top_k, int d, c
   if (top_k > 32 || d % 8) return cudaErrorInvalidValue;
   const int chunks = (n_tok + kSpTok - 1) / kSpTok;
   const size_t smem = (2 * static_cast<size_t>(n_exp) + 2 * kSpTok * top_k) * sizeof(int);
-  permute_single_pass_kernel<<<chunks, kSpThreads, smem, st>>>(n_tok, n_exp, top_k, d / 8, topk_idx, offsets,
-                                                               static_cast<const uint4*>(x), row_of_copy,
-                                                               copy_of_row, static_cast<uint4*>(x_perm), look, ctl,
-                                                               status);
+  permute_single_pass_kernel<false><<<chunks, kSpThreads, smem, st>>>(
+      n_tok, n_exp, top_k, d / 8, topk_idx, offsets, static_cast<const uint4*>(x), row_of_copy, copy_of_row,
+      static_cast<uint4*>(x_perm), look, ctl, status, SpQuantOut{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_single_pass_mxfp8(int n_tok, int n_exp, int top_k, int d, const int32_t* topk_idx,
+                                             const int32_t* offsets, const void* x, int32_t* row_of_copy,
+                                             int32_t* copy_of_row, uint8_t* codes, uint8_t* scales, int64_t ld,
+                                             uint8_t* tok_codes, uint8_t* tok_scales, int64_t tok_ld,
+                                             unsigned long long* look, int32_t* ctl, int32_t* status,
+                                             cudaStream_t st) {
+  if (n_tok <= 0) return cudaSuccess;
+  if (top_k > 32 || d % 32) return cudaErrorInvalidValue;
+  const int chunks = (n_tok + kSpTok - 1) / kSpTok;
+  const size_t smem = (2 * static_cast<size_t>(n_exp) + 2 * kSpTok * top_k) * sizeof(int);
+  permute_single_pass_kernel<true><<<chunks, kSpThreads, smem, st>>>(
+      n_tok, n_exp, top_k, d / 8, topk_idx, offsets, static_cast<const uint4*>(x), row_of_copy, copy_of_row,
+      nullptr, look, ctl, status, SpQuantOut{codes, scales, ld, tok_codes, tok_scales, tok_ld});
   return cudaGetLastError();
 }
 

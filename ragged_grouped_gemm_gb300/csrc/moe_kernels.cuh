@@ -49,6 +49,16 @@ cudaError_t launch_permute_single_pass(int n_tok, int n_exp, int top_k, int d, c
                                        const int32_t* offsets, const void* x, int32_t* row_of_copy,
                                        int32_t* copy_of_row, void* x_perm, unsigned long long* look, int32_t* ctl,
                                        int32_t* status, cudaStream_t st);
+// The same with the rows quantised to MXFP8 on the way (each token row read
+// and quantised once, as launch_mx_quant_rows does): codes [R, d] and scales
+// [d/32][ld] of the permuted rows; tok_codes / tok_scales (nullable): the
+// token rows' codes [n_tok, d] and scales [d/32][tok_ld].  d % 32 == 0.
+cudaError_t launch_permute_single_pass_mxfp8(int n_tok, int n_exp, int top_k, int d, const int32_t* topk_idx,
+                                             const int32_t* offsets, const void* x, int32_t* row_of_copy,
+                                             int32_t* copy_of_row, uint8_t* codes, uint8_t* scales, int64_t ld,
+                                             uint8_t* tok_codes, uint8_t* tok_scales, int64_t tok_ld,
+                                             unsigned long long* look, int32_t* ctl, int32_t* status,
+                                             cudaStream_t st);
 // x_perm[row_of_copy[t*K+k]] = x[t] (bf16 rows of d elements).
 cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, const int32_t* row_of_copy,
                                 void* x_perm, cudaStream_t st);

@@ -33,4 +33,37 @@ __device__ __forceinline__ uint2 mx_encode8(const float (&f)[8], float inv) {
   return make_uint2(w[0], w[1]);
 }
 
+// One 32-element block of bf16 (four 16-byte words, in order): its E8M0
+// scale byte (exponent + 127) and its 32 E4M3 codes (c0: elements 0..15,
+// c1: 16..31), element i encoded as x_i * 2^-e.
+__device__ __forceinline__ uint8_t mx_quant_block32(const uint4 (&v)[4], uint4& c0, uint4& c1) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t ws[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
+      f[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int e = mx_scale_exponent(amax);
+  const float inv = mx_inv_scale(e);
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  c0 = make_uint4(out[0], out[1], out[2], out[3]);
+  c1 = make_uint4(out[4], out[5], out[6], out[7]);
+  return static_cast<uint8_t>(e + 127);
+}
+
 }  // namespace moe

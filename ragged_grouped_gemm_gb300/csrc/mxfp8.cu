@@ -31,37 +31,15 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const __nv_bfloat16*
   if (row >= rows || kb >= nkb) return;
   const int64_t sr = src_row_of ? src_row_of[row] / src_div : row;
   const uint4* p = reinterpret_cast<const uint4*>(src + sr * cols + kb * 32);
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = p[i];
-    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
-      f[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
-    }
-  }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  const int e = mx_scale_exponent(amax);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e in [-127, 119]
-  uint32_t out[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi =
-        __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-    out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
+  const uint4 v[4] = {p[0], p[1], p[2], p[3]};
+  uint4 c0, c1;
+  const uint8_t sc = mx_quant_block32(v, c0, c1);
   uint4* dst = reinterpret_cast<uint4*>(codes + row * cols + kb * 32);
-  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  dst[0] = c0;
+  dst[1] = c1;
   const int64_t g = row / rows_per_group;
   const int64_t n = row - g * rows_per_group;
-  scales[(g * nkb + kb) * ld_s + n] = static_cast<uint8_t>(e + 127);
+  scales[(g * nkb + kb) * ld_s + n] = sc;
 }
 
 // Transposing quantiser.  One CTA: one output block of 32 quantised rows x
