@@ -146,23 +146,32 @@ def route_launches(cfg, sms: int = 152) -> int:
     return 4 + (1 if split else 0)
 
 
+def fused_dispatch(cfg) -> bool:
+    """Whether the layer routes and permutes in one call (moe_route_permute)."""
+    return cfg.n_exp <= 32 and cfg.precision != "mxfp8" and cfg.capacity_factor <= 0
+
+
 def launches_per_step(cfg) -> int:
     """Kernels libmoe launches for one forward + backward (see moe_api.cu)."""
     from ragged_grouped_gemm_gb300 import _lib  # noqa: F401  (ensures the library is the one counted)
-    # maps of the MXFP8 permute: single-CTA up to 65536 copies, else the token-chunked kernels
-    maps = 1 if cfg.rows <= 65536 else 3
+    # permute: one launch while ceil(N/16) * E <= 131072; else the token-chunked map kernels + rows
+    sp = -(-cfg.n_tok // 16) * cfg.n_exp <= 131072
+    maps = 1 if cfg.rows <= 65536 else 3   # map kernels: one CTA up to 65536 copies, else token-chunked
     if cfg.precision == "mxfp8":
-        # route; permute: map kernels + row quantiser (+ token quantiser for the shared expert);
-        # grouped FFN: GEMM1, GEMM2 (+ dense offsets, GEMM1, GEMM2); combine
-        fwd = route_launches(cfg) + maps + 1 + 2 + 1 + (4 if cfg.n_shared else 0)
+        # route; permute (quantising; one launch, else maps + row quantiser + token quantiser for the shared
+        # expert); grouped FFN: GEMM1, GEMM2 (+ token quantiser if the permute did not quantise them,
+        # dense offsets, GEMM1, GEMM2); combine
+        fwd = route_launches(cfg) + (1 if sp else maps + 1 + (1 if cfg.n_shared else 0)) + 2 + 1
+        fwd += 3 if cfg.n_shared else 0
         # per expert set: row-wise quantisers of dYw (fused into the combine backward for the routed
         # experts), da1, da3; pad offsets, 5 transposing quantisers, 5 GEMMs
         per_set = 2 + 1 + 5 + 5
         bwd = 1 + per_set + (1 + per_set + 1 if cfg.n_shared else 0) + 3 + 1   # + combine bwd, router grad, unpermute
         return fwd + bwd + (1 if cfg.use_bias else 0)
-    # route; permute (one launch while ceil(N/16) * E <= 131072, else maps + rows); GEMM1, GEMM2; combine
-    sp = -(-cfg.n_tok // 16) * cfg.n_exp <= 131072
-    fwd = route_launches(cfg) + (1 if sp else maps + 1) + 2 + 1
+    # route and permute (one fused launch for E <= 32; else route, then one permute launch or maps + rows);
+    # GEMM1, GEMM2; combine
+    disp = 1 if fused_dispatch(cfg) else route_launches(cfg) + (1 if sp else maps + 1)
+    fwd = disp + 2 + 1
     if cfg.n_shared:
         fwd += 3
     # combine bwd; dgrad2, wgrad2, dgrad1, wgrad1, wgrad3 (each weight gradient over several
@@ -308,22 +317,29 @@ def run_ours(args, cfg, rank, world, local_rank):
     layer = api.MoELayer(cfg, p, train=True, device=dev)
     b, d, ws = layer.buf, layer.desc, layer.ws
     x = p["x"]
-    names = ["route", "permute", "grouped_ffn", "combine", "backward"]
+    # E <= 32 with bf16 rows: routing and dispatch are one call (moe_route_permute), as the layer runs them
+    fused = layer.fused_dispatch
+    names = (["route_permute"] if fused else ["route", "permute"]) + ["grouped_ffn", "combine", "backward"]
 
     def step(ev=None):
         def mark(i):
             if ev is not None:
-                ev[i].record()
+                ev[names.index(i) if isinstance(i, str) else i].record()
         mark(0)
-        api.moe_route(d, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
-                      b["offsets"], ws)
-        mark(1)
-        if layer.mx:
-            api.moe_permute_mxfp8(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
-                                  b["xq_perm"], b["xs_perm"], b["xq_tok"], b["xs_tok"], ws)
+        if fused:
+            api.moe_route_permute(d, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"],
+                                  b["counts"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], ws)
         else:
-            api.moe_permute(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], ws)
-        mark(2)
+            api.moe_route(d, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
+                          b["offsets"], ws)
+            mark(1)
+            if layer.mx:
+                api.moe_permute_mxfp8(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
+                                      b["xq_perm"], b["xs_perm"], b["xq_tok"], b["xs_tok"], ws)
+            else:
+                api.moe_permute(d, x, b["topk_idx"], b["offsets"], b["row_of_copy"], b["copy_of_row"],
+                                b["x_perm"], ws)
+        mark("grouped_ffn")
         saved = {key: b[key] for key in ("a1", "a3", "h", "a1s", "a3s", "hs") if b.get(key) is not None}
         if layer.mx:
             api.moe_grouped_ffn_mxfp8(d, b["xq_perm"], b["xs_perm"], b["offsets"], b["xq_tok"], b["xs_tok"],
@@ -335,12 +351,12 @@ def run_ours(args, cfg, rank, world, local_rank):
             api.moe_grouped_ffn(d, b["x_perm"], b["offsets"], x, p["w1"], p["w3"], p["w2"], p.get("ws1"),
                                 p.get("ws3"), p.get("ws2"), b["a1"], b["a3"], b["h"], b["a1s"], b["a3s"], b["hs"],
                                 b["y_perm"], b["y_shared"], ws)
-        mark(3)
+        mark("combine")
         api.moe_combine(d, b["y_perm"], b["row_of_copy"], b["topk_w"], b["y_shared"], b["out"])
-        mark(4)
+        mark("backward")
         layer.x = x
         layer.backward(dy)
-        mark(5)
+        mark(len(names))
         if cfg.use_bias:
             layer.update_bias(1e-3, 0)
 
@@ -369,7 +385,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     ms = t0.elapsed_time(t1)
-    per_call = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+    # per call: the median over the timed steps.  The first timed step starts
+    # on an idle GPU, so its first calls also hold the host's time to issue
+    # them; in the later steps the host is ahead and the events see GPU time.
+    per_call = {n: statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                 for j, n in enumerate(names)}
     kernels = {}
     for kind in api.TIMING_KINDS:
@@ -541,9 +560,10 @@ def call_bytes(cfg) -> dict:
     route: x and W_g read, logits, top-K indices and weights, counts and
     offsets written; permute: expert indices and x read, the two maps and
     the permuted rows written (MXFP8: E4M3 codes + one scale byte per 32,
-    plus the token-order copy with a shared expert); combine: the permuted
-    outputs, maps and weights read (+ the shared output), the output
-    written."""
+    plus the token-order copy with a shared expert); route_permute (both in
+    one call): x and W_g read once, every output of both written; combine:
+    the permuted outputs, maps and weights read (+ the shared output), the
+    output written."""
     n, d, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
     r = n * k
     q = 1 + 1 / 32
@@ -553,7 +573,9 @@ def call_bytes(cfg) -> dict:
     else:
         permute = 4 * r + 2 * n * d + 8 * r + 2 * r * d
     combine = 2 * r * d + 8 * r + (2 * n * d if cfg.n_shared else 0) + 2 * n * d
-    return {"route": route, "permute": permute, "combine": combine}
+    # the fused call reads x and the expert indices only once (x again from L2, the indices it wrote itself)
+    route_permute = route + permute - 2 * n * d - 4 * r
+    return {"route": route, "permute": permute, "route_permute": route_permute, "combine": combine}
 
 
 def summarize(res, args, peaks) -> dict:
@@ -595,7 +617,7 @@ def summarize(res, args, peaks) -> dict:
     cb = call_bytes(cfg)
     per_call_gbs = {c: {"gbs": cb[c] / (per_call[c] / 1e3) / 1e9,
                         "frac_of_hbm": cb[c] / (per_call[c] / 1e3) / 1e9 / peaks["hbm_gbs"],
-                        "algorithmic_bytes": cb[c]} for c in cb}
+                        "algorithmic_bytes": cb[c]} for c in cb if c in per_call}
     return {
         "workload": workload_name(cfg), "value": tok_s, "unit": "tokens/s", "ms_per_step": ms / args.steps,
         "fwd_tokens_per_s": res["fwd"][0],

@@ -204,6 +204,24 @@ MOE_API moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* log
                                    int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                    void* ws, size_t ws_bytes, void* stream);
 
+/* Router and dispatch together (§4.1, §4.3, §9 steps 1-4, §12.5 sort by
+ * destination): moe_route followed by moe_permute on the same tokens, in one
+ * launch, for E <= 32 and bf16 rows (precision 0 or 2).  The outputs of both
+ * calls, bit-identical to them (logits, topk_idx, topk_w, counts, offsets as
+ * moe_route; row_of_copy, copy_of_row, x_perm as moe_permute).  A
+ * cooperative launch: each CTA routes its 16-token tiles and
+ * publishes their expert histograms, a grid-wide barrier follows (bounded: a
+ * wait that runs out sets MOE_DEV_TIMEOUT, site 710), then each CTA finds its
+ * tiles' first rows from the histograms and copies its token rows while they
+ * are still in L2.  Needs the forward workspace (its per-tile histograms are
+ * part of it).  Errors: MOE_ERR_INVALID_ARG for E > 32, precision 1 (use
+ * moe_permute_mxfp8), unaligned or missing pointers; the launch's own error
+ * otherwise (for instance when the GPU cannot run a cooperative launch). */
+MOE_API moe_status_t moe_route_permute(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias,
+                                       float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                       int32_t* offsets, int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm,
+                                       void* ws, size_t ws_bytes, void* stream);
+
 /* Dispatch (§12.5 sort by destination; §9 mask/nonzero order): a stable
  * counting sort of the copies c = t*K+k by expert, ascending token inside
  * an expert.  row_of_copy[c] (out) is the permuted row of copy c;

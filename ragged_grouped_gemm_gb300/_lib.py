@@ -59,6 +59,8 @@ SIGNATURES = {
                           ctypes.c_size_t, c_vp]),
     "moe_route_from_logits": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.c_size_t, c_vp]),
+    "moe_route_permute": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                  c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
     "moe_permute": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t,
                             c_vp]),
     "moe_grouped_ffn": (c_i32, [ctypes.POINTER(MoeDesc), c_vp, c_vp, c_vp, ctypes.POINTER(MoeExpertWeights),

@@ -94,6 +94,18 @@ def moe_route_from_logits(desc, logits, bias, topk_idx, topk_w, counts, offsets,
         _p(offsets, I32, (e + 1,), "offsets"), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
 
 
+def moe_route_permute(desc, x, w_gate, bias, logits, topk_idx, topk_w, counts, offsets, row_of_copy, copy_of_row,
+                      x_perm, ws, stream=None):
+    n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
+    r = n * k
+    _check("moe_route_permute", _lib.load().moe_route_permute(
+        ctypes.byref(desc), _p(x, BF16, (n, d), "x"), _p(w_gate, BF16, (e, d), "w_gate"),
+        _p(bias, F32, (e,), "bias"), _p(logits, F32, (n, e), "logits"), _p(topk_idx, I32, (n, k), "topk_idx"),
+        _p(topk_w, F32, (n, k), "topk_w"), _p(counts, I32, (e,), "counts"), _p(offsets, I32, (e + 1,), "offsets"),
+        _p(row_of_copy, I32, (r,), "row_of_copy"), _p(copy_of_row, I32, (r,), "copy_of_row"),
+        _p(x_perm, BF16, (r, d), "x_perm"), _p(ws, name="ws"), ws.numel() * ws.element_size(), _s(stream)))
+
+
 def moe_permute(desc, x, topk_idx, offsets, row_of_copy, copy_of_row, x_perm, ws, stream=None):
     n, d, e, k = desc.n_tok, desc.d_model, desc.n_exp, desc.top_k
     r = n * k
@@ -455,7 +467,8 @@ class MoELayer:
     (w_gate, w1, w3, w2, bias, and ws1, ws3, ws2 with a shared expert).
     """
 
-    def __init__(self, cfg: MoEConfig, params: dict, train: bool = True, device="cuda", gather: bool = False):
+    def __init__(self, cfg: MoEConfig, params: dict, train: bool = True, device="cuda", gather: bool = False,
+                 fused_dispatch: bool = True):
         self.cfg = cfg
         self.desc = make_desc(cfg)
         self.p = params
@@ -488,6 +501,9 @@ class MoELayer:
             self.buf.update(offsets_full=z(e + 1, dt=I32), row_of_copy_full=z(r, dt=I32),
                             copy_of_row_full=z(r, dt=I32), n_dropped=z(1, dt=I32))
         self.mx = cfg.precision == "mxfp8"
+        # E <= 32, bf16 rows, dropless, permuted copy: routing and dispatch in
+        # one launch (moe_route_permute); fused_dispatch=False keeps two calls
+        self.fused_dispatch = (fused_dispatch and e <= 32 and not self.mx and not self.cap and not self.gather)
         if self.mx:
             self.wq = quantize_weights_mxfp8(params)
             self.wqt = quantize_weights_mxfp8_t(params) if train else None
@@ -510,6 +526,12 @@ class MoELayer:
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         b, p = self.buf, self.p
         self.x = x
+        if self.fused_dispatch:
+            # routing and the permuted copy of the tokens in one launch (E <= 32)
+            moe_route_permute(self.desc, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"],
+                              b["counts"], b["offsets"], b["row_of_copy"], b["copy_of_row"], b["x_perm"], self.ws,
+                              stream)
+            return self._ffn_combine(x, stream)
         moe_route(self.desc, x, p["w_gate"], p.get("bias"), b["logits"], b["topk_idx"], b["topk_w"], b["counts"],
                   b["offsets_full"] if self.cap else b["offsets"], self.ws, stream)
         if self.mx:

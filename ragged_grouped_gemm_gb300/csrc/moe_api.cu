@@ -40,7 +40,8 @@ constexpr int kGateSlices = 4;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, look = 0, aux = 0, gpart = 0, fwd_end = 0;
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, look = 0, aux = 0, gpart = 0, rp_hist = 0,
+         fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, gmaps = 0, total = 0;
   // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
@@ -68,6 +69,9 @@ WsLayout layout(const moe_desc_t& d) {
   L.blk_base = o; o = align_up(o + nch * E * 4);
   L.aux = o; o = align_up(o + moe::aux_partial_floats(d.n_tok > 0 ? d.n_tok : 1, d.n_exp) * 4);
   L.gpart = o; o = align_up(o + static_cast<size_t>(kGateSlices) * N * E * 4);   // router logit slices
+  // moe_route_permute's grid-barrier words and per-tile expert histograms (E <= 32)
+  L.rp_hist = o;
+  o = align_up(o + (E <= 32 ? static_cast<size_t>(moe::route_permute_hist_words(d.n_tok, d.n_exp)) * 4 + 128 : 0));
   if (d.precision == 1) {
     L.hq = o; o = align_up(o + R * F);
     L.hs = o; o = align_up(o + F / 32 * moe::mx_scale_ld(R));
@@ -440,6 +444,38 @@ moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, con
   MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
   if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
   return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, at<int32_t>(ws, L.status), st);
+}
+
+// moe_route_permute's scratch words, 128-byte aligned inside their region
+// (the region has 128 bytes to spare; the workspace itself is 16-byte aligned)
+static int32_t* rp_words(void* ws, const WsLayout& L) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(static_cast<char*>(ws) + L.rp_hist);
+  return reinterpret_cast<int32_t*>((a + 127) & ~uintptr_t(127));
+}
+
+moe_status_t moe_route_permute(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias,
+                               float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                               int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, void* ws, size_t ws_bytes,
+                               void* stream) {
+  MOE_RANGE("moe_route_permute");
+  MOE_TRY(check_desc(d));
+  MOE_TRY(check_ws(*d, ws, ws_bytes, false));
+  if (d->n_exp > 32 || d->precision == 1) return MOE_ERR_INVALID_ARG;
+  if (!all16({x, w_gate, logits, x_perm}) || !topk_idx || !topk_w || !counts || !offsets || !row_of_copy ||
+      !copy_of_row)
+    return MOE_ERR_INVALID_ARG;
+  if (d->use_bias && !bias) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d->n_tok == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+  }
+  const WsLayout L = layout(*d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  moe::RouteShape rs{d->n_tok, d->n_exp, d->top_k, d->gate};
+  return cuda_status(moe::launch_route_permute(rs, d->d_model, x, w_gate, d->use_bias ? bias : nullptr, logits,
+                                               topk_idx, topk_w, counts, offsets, row_of_copy, copy_of_row, x_perm,
+                                               rp_words(ws, L), status, st));
 }
 
 moe_status_t moe_permute(const moe_desc_t* d, const void* x, const int32_t* topk_idx, const int32_t* offsets,

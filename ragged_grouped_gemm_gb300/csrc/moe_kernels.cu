@@ -203,25 +203,25 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-template <int NT>   // 8-expert column tiles: E <= 8 * NT
-__global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
-    RouteShape s, int d8, const uint4* __restrict__ x, const uint4* __restrict__ wg, const float* __restrict__ bias,
-    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* acc, int32_t* ticket, int32_t* status) {
-  constexpr int EP = 8 * NT;
-  __shared__ float s_acc[kRtWarps][kRtTok][EP + 1];
-  __shared__ int s_hist[32];
-  __shared__ int s_last;
+// Routing of one tile of at most 16 tokens [tok0, tok_end) by a CTA of
+// kRtWarps warps: logits (each warp a slice of the contraction on the
+// warp-level MMA, the slices added in warp order), then a warp per token:
+// top-K, weights, and the tile's histogram in s_hist (which the caller
+// zeroes).  EP = 8 * NT columns of s_acc.
+template <int NT>
+__device__ __forceinline__ void route_tile(const RouteShape& s, int d8, const uint4* __restrict__ x,
+                                           const uint4* __restrict__ wg, const float* __restrict__ bias,
+                                           float* __restrict__ logits, int32_t* __restrict__ topk_idx,
+                                           float* __restrict__ topk_w, int tok0, int tok_end,
+                                           float (*s_acc)[kRtTok][8 * NT + 1], int* s_hist) {
   const int E = s.n_exp, K = s.top_k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int tok0 = blockIdx.x * kRtTok;
-  if (threadIdx.x < 32) s_hist[threadIdx.x] = 0;
   // this warp's 32-column blocks of the contraction
   const int nblk = d8 / 4;
   const int b0 = nblk * warp / kRtWarps, b1 = nblk * (warp + 1) / kRtWarps;
   const int r0 = tok0 + g, r1 = tok0 + g + 8;
-  const bool v0 = r0 < s.n_tok, v1 = r1 < s.n_tok;
+  const bool v0 = r0 < tok_end, v1 = r1 < tok_end;
   const uint4* x0 = x + static_cast<int64_t>(v0 ? r0 : 0) * d8 + q;
   const uint4* x1 = x + static_cast<int64_t>(v1 ? r1 : 0) * d8 + q;
   const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
   // a token per warp: logits (partials added in warp order), top-K, weights
   for (int tt = warp; tt < kRtTok; tt += kRtWarps) {
     const int t = tok0 + tt;
-    if (t >= s.n_tok) break;
+    if (t >= tok_end) break;
     float lg[1];
     float v = 0.0f;
     if (lane < E) {
@@ -281,6 +281,23 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
       atomicAdd(&s_hist[my_e], 1);
     }
   }
+}
+
+template <int NT>   // 8-expert column tiles: E <= 8 * NT
+__global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
+    RouteShape s, int d8, const uint4* __restrict__ x, const uint4* __restrict__ wg, const float* __restrict__ bias,
+    float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* acc, int32_t* ticket, int32_t* status) {
+  constexpr int EP = 8 * NT;
+  __shared__ float s_acc[kRtWarps][kRtTok][EP + 1];
+  __shared__ int s_hist[32];
+  __shared__ int s_last;
+  const int E = s.n_exp, K = s.top_k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) s_hist[threadIdx.x] = 0;
+  __syncthreads();
+  route_tile<NT>(s, d8, x, wg, bias, logits, topk_idx, topk_w, blockIdx.x * kRtTok,
+                 min(s.n_tok, static_cast<int>(blockIdx.x + 1) * kRtTok), s_acc, s_hist);
   __syncthreads();
   if (threadIdx.x < E && s_hist[threadIdx.x]) atomicAdd(acc + threadIdx.x, s_hist[threadIdx.x]);
   __threadfence();
@@ -310,6 +327,220 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_fused_kernel(
     if (lane == 0 && static_cast<long long>(total) != static_cast<long long>(s.n_tok) * K && status)
       atomicOr(status, DEV_BAD_OFFSETS);
   }
+}
+
+// ------------------------------------------------------------ route + permute
+// moe_route followed by moe_permute in one cooperative launch (E <= 32).
+// Phase 1: each CTA routes its 16-token tiles (route_tile) and publishes each
+// tile's expert histogram th[tile][E].  A bounded grid-wide barrier follows
+// (the launch is cooperative, so every CTA is resident).  Phase 2: each CTA
+// adds up the histograms - the experts' totals give counts and offsets, the
+// tiles before each of its own give that tile's first row per expert - then
+// assigns its copies' rows in copy order (as the permute kernels do) and
+// copies its token rows, which phase 1 has just read (so they come from L2).
+// bar: arrivals in bar[0] and the generation in bar[32] (another 128-byte
+// line, so the waiting CTAs' polls do not contend with the arrivals), zero
+// after moe_workspace_init; the last CTA to arrive resets the arrivals.
+__device__ __forceinline__ bool grid_barrier_bounded(int32_t* bar, int32_t* status, int site) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_ok = 1;
+    volatile int32_t* vgen = bar + 32;
+    const int32_t gen = *vgen;
+    __threadfence();
+    if (atomicAdd(bar, 1) == static_cast<int>(gridDim.x) - 1) {
+      bar[0] = 0;
+      __threadfence();
+      atomicAdd(bar + 32, 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      uint32_t n = 0;
+      while (*vgen == gen) {
+        __nanosleep(32);
+        if ((++n & 63u) == 0 && globaltimer_ns() - t0 > kSpinTimeoutNs) {
+          s_ok = 0;
+          if (status) {
+            atomicOr(status, DEV_TIMEOUT);
+            atomicExch(status + 1, site);
+          }
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+constexpr int kRpCopyBatch = 8;   // token rows a thread's copy loads keep in flight
+
+// Of T tiles, the first N mod T hold q + 1 tokens and the rest q, q = N / T
+// (at most 16 each, in token order); T is a multiple of the grid where that
+// balances the CTAs.  Tile t starts at token t*q + min(t, N mod T).
+__device__ __forceinline__ int rp_tile_begin(int t, int q, int rem) { return t * q + min(t, rem); }
+
+// Per expert, the sum of th[t][e] over tiles t < t_mid (into pre) and over
+// t_mid <= t < t_hi (into post), both zeroed by the caller: the CTA's threads
+// each take entries j = tid, tid + blockDim, ... of th[t_lo..t_hi) (all their
+// loads in flight at once) and add them with shared-memory atomics.
+__device__ __forceinline__ void rp_hist_sums(const int32_t* th, int E, int t_lo, int t_mid, int t_hi, int* pre,
+                                             int* post) {
+  constexpr int kLoads = 4;
+  const int n = (t_hi - t_lo) * E;   // at most (ceil(N/16) + 2048) * 32 entries
+  const int split = (t_mid - t_lo) * E;
+  const int32_t* src = th + static_cast<int64_t>(t_lo) * E;
+  for (int j0 = threadIdx.x; j0 < n; j0 += kLoads * blockDim.x) {
+    int v[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int j = j0 + u * blockDim.x;
+      v[u] = j < n ? __ldcg(src + j) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int j = j0 + u * blockDim.x;
+      if (j < n && v[u]) atomicAdd(j < split ? &pre[j % E] : &post[j % E], v[u]);
+    }
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kRtWarps * 32, 2) route_permute_kernel(
+    RouteShape s, int d8, int ntiles, int tq, int trem, const uint4* __restrict__ x, const uint4* __restrict__ wg,
+    const float* __restrict__ bias, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_of_copy, int32_t* __restrict__ copy_of_row, uint4* __restrict__ x_perm, int32_t* th,
+    int32_t* bar, int32_t* status) {
+  constexpr int EP = 8 * NT;
+  __shared__ float s_acc[kRtWarps][kRtTok][EP + 1];
+  __shared__ int s_hist[32];
+  __shared__ int s_off[33];
+  __shared__ int s_pre[32];
+  __shared__ int s_post[32];
+  __shared__ int s_base[32];
+  __shared__ int s_pos[kRtTok * 32];
+  __shared__ int s_bad;
+  const int E = s.n_exp, K = s.top_k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t R = static_cast<int64_t>(s.n_tok) * K;
+  if (tid == 0) s_bad = 0;
+  // ---- phase 1: routing
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    if (tid < 32) s_hist[tid] = 0;
+    __syncthreads();
+    route_tile<NT>(s, d8, x, wg, bias, logits, topk_idx, topk_w, rp_tile_begin(tile, tq, trem),
+                   rp_tile_begin(tile + 1, tq, trem), s_acc, s_hist);
+    __syncthreads();
+    if (tid < E) {
+      th[static_cast<int64_t>(tile) * E + tid] = s_hist[tid];
+      __threadfence();   // each writer orders its histogram word before the barrier's arrival
+    }
+  }
+  if (tid < 32) {
+    s_pre[tid] = 0;
+    s_post[tid] = 0;
+  }
+  if (!grid_barrier_bounded(bar, status, 710)) return;
+  // ---- phase 2: the experts' totals and the tiles before this CTA's first
+  // tile, in one pass over the histograms
+  rp_hist_sums(th, E, 0, blockIdx.x, ntiles, s_pre, s_post);
+  __syncthreads();
+  if (warp == 0) {
+    int pre = s_pre[lane], tot = pre + s_post[lane];
+    if (lane >= E) tot = pre = 0;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    s_off[lane + 1] = incl;
+    if (lane == 0) s_off[0] = 0;
+    s_pre[lane] = pre;
+    if (blockIdx.x == 0) {
+      if (lane < E) {
+        counts[lane] = tot;
+        offsets[lane + 1] = incl;
+      }
+      if (lane == 0) offsets[0] = 0;
+      const int total = __shfl_sync(kFull, incl, 31);
+      if (lane == 0 && static_cast<long long>(total) != R && status) atomicOr(status, DEV_BAD_OFFSETS);
+    }
+  }
+  __syncthreads();
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    // this tile's first row per expert: offsets plus the copies of the tiles
+    // before it (the running prefix gains the tiles since this CTA's last one)
+    if (tile != static_cast<int>(blockIdx.x)) {
+      rp_hist_sums(th, E, tile - static_cast<int>(gridDim.x), tile, tile, s_pre, s_post);
+    }
+    __syncthreads();
+    if (warp == 0) s_base[lane] = s_off[lane] + s_pre[lane];
+    __syncthreads();
+    // rows of the tile's copies in copy order (warp 0)
+    const int t0k = rp_tile_begin(tile, tq, trem);
+    const int ntk = rp_tile_begin(tile + 1, tq, trem) - t0k;
+    const int64_t c0 = static_cast<int64_t>(t0k) * K;
+    const int ncp = ntk * K;
+    if (warp == 0) {
+      for (int b = 0; b < ncp; b += 32) {
+        const int i = b + lane;
+        const bool active = i < ncp;
+        const int e = active ? __ldcg(topk_idx + c0 + i) : -1;
+        const bool ok = active && e >= 0 && e < E;
+        const unsigned am = __ballot_sync(kFull, ok);
+        int pos = -1;
+        if (ok) {
+          const unsigned m = __match_any_sync(am, e);
+          const int leader = __ffs(m) - 1;
+          const int rank = __popc(m & ((1u << lane) - 1u));
+          int base = 0;
+          if (lane == leader) {
+            base = s_base[e];
+            s_base[e] = base + __popc(m);
+          }
+          base = __shfl_sync(am, base, leader);
+          pos = base + rank;
+          if (!(pos >= 0 && pos < s_off[e + 1] && pos < R)) {
+            pos = -1;
+            atomicOr(&s_bad, DEV_BAD_OFFSETS);
+          }
+        } else if (active) {
+          atomicOr(&s_bad, DEV_BAD_INDEX);
+        }
+        if (active) {
+          s_pos[i] = pos;
+          row_of_copy[c0 + i] = pos;
+          if (pos >= 0) copy_of_row[pos] = static_cast<int32_t>(c0 + i);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    // the tile's token rows (read by phase 1, so from L2), each read once and
+    // written to its copies' rows
+    for (int i = tid; i < d8; i += kRtWarps * 32) {
+#pragma unroll
+      for (int tb = 0; tb < kRtTok; tb += kRpCopyBatch) {
+        uint4 v[kRpCopyBatch];
+#pragma unroll
+        for (int u = 0; u < kRpCopyBatch; ++u)
+          v[u] = tb + u < ntk ? x[static_cast<int64_t>(t0k + tb + u) * d8 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < kRpCopyBatch; ++u) {
+          if (tb + u >= ntk) break;
+          for (int k = 0; k < K; ++k) {
+            const int r = s_pos[(tb + u) * K + k];
+            if (r >= 0) x_perm[static_cast<int64_t>(r) * d8 + i] = v[u];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0 && s_bad && status) atomicOr(status, s_bad);
 }
 
 // ------------------------------------------------------------ offsets scan
@@ -1348,6 +1579,60 @@ cudaError_t launch_router_fused(const RouteShape& s, int d, const void* x, const
   else MOE_ROUTER(4);
 #undef MOE_ROUTER
   return cudaGetLastError();
+}
+
+// At most this many CTAs of route_permute_kernel are resident at once (two
+// per SM by its launch bounds): the tile count may exceed ceil(N/16) by that.
+constexpr int kRpMaxGrid = 2048;
+
+int64_t route_permute_hist_words(int n_tok, int n_exp) {
+  // arrivals and generation words (two 128-byte lines), then T x E histograms
+  return 64 + ((static_cast<int64_t>(n_tok) + kRtTok - 1) / kRtTok + kRpMaxGrid) * n_exp;
+}
+
+cudaError_t launch_route_permute(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
+                                 float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                 int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, int32_t* ws_words,
+                                 int32_t* status, cudaStream_t st) {
+  if (s.n_tok <= 0 || s.n_exp > 32 || s.top_k > 32 || d % 32) return cudaErrorInvalidValue;
+  const int t16 = static_cast<int>((static_cast<int64_t>(s.n_tok) + kRtTok - 1) / kRtTok);
+  const int nt = (s.n_exp + 7) / 8;
+  auto go = [&](auto kern) -> cudaError_t {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRtWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int g = std::min(per_sm * num_sms_kernels(), kRpMaxGrid);
+    // tiles: ceil(N/16) when that is under half the grid (a small batch);
+    // otherwise rounded up to a multiple of the grid, so every CTA routes and
+    // copies the same number of tiles
+    const int ntiles = t16 * 2 < g ? t16 : (t16 + g - 1) / g * g;
+    const int blocks = std::min(ntiles, g);
+    RouteShape sa = s;
+    int d8 = d / 8;
+    int nti = ntiles, tq = s.n_tok / ntiles, trem = s.n_tok % ntiles;
+    const uint4* xa = static_cast<const uint4*>(x);
+    const uint4* wa = static_cast<const uint4*>(w_gate);
+    uint4* xp = static_cast<uint4*>(x_perm);
+    int32_t* bar = ws_words;
+    int32_t* th = ws_words + 64;
+    void* args[] = {&sa, &d8, &nti, &tq, &trem, &xa, &wa, const_cast<float**>(&bias), &logits, &topk_idx, &topk_w, &counts,
+                    &offsets, &row_of_copy, &copy_of_row, &xp, &th, &bar, &status};
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kRtWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+  };
+  if (nt <= 1) return go(route_permute_kernel<1>);
+  if (nt <= 2) return go(route_permute_kernel<2>);
+  return go(route_permute_kernel<4>);
 }
 
 cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,

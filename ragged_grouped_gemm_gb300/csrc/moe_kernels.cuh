@@ -25,6 +25,18 @@ cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* b
 cudaError_t launch_router_fused(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
                                 float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                 int32_t* acc, int32_t* ticket, int32_t* status, cudaStream_t st);
+// launch_router_fused and then the permute of the same tokens in one
+// cooperative launch (E <= 32): the outputs of both (logits, topk_idx,
+// topk_w, counts, offsets, row_of_copy, copy_of_row, x_perm).  ws_words:
+// route_permute_hist_words(n_tok, n_exp) int32 of scratch, 128-byte aligned
+// and zero before the first launch: the grid barrier's words (the kernel
+// leaves them ready for the next launch) and the per-tile expert
+// histograms.  D must be a multiple of 32.
+int64_t route_permute_hist_words(int n_tok, int n_exp);
+cudaError_t launch_route_permute(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
+                                 float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                 int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, int32_t* ws_words,
+                                 int32_t* status, cudaStream_t st);
 // offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]; checks the total.
 cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
                            int32_t* status, cudaStream_t st);

@@ -50,10 +50,12 @@ def test_launch_counts():
     import bench
     from ragged_grouped_gemm_gb300.inputs import CONFIGS
     mix, ds = CONFIGS["mixtral"], CONFIGS["dsv3"]
-    # forward 5 (fused router; single-pass permute; GEMM1, GEMM2, combine)
+    # forward 4 (routing and permute in one launch; GEMM1, GEMM2, combine)
     # + backward 13 (combine bwd, 5 GEMMs, 3 per-group map kernels, unpermute, router gradient 3)
-    assert bench.route_launches(mix) == 1
-    assert bench.launches_per_step(mix) == 5 + 13
+    assert bench.route_launches(mix) == 1 and bench.fused_dispatch(mix)
+    assert bench.launches_per_step(mix) == 4 + 13
+    # MXFP8: the fused router, the quantising single-pass permute, GEMM1, GEMM2, combine
+    assert not bench.fused_dispatch(mix.replace(precision="mxfp8"))
     # E = 256: dense offsets, logits GEMM in 4 contraction slices, their sum, top-K, scan;
     # + shared expert (3 forward, 6 backward) + route-bias update
     assert bench.route_launches(ds) == 5

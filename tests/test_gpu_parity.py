@@ -177,6 +177,63 @@ def test_permute_twice_in_a_row_and_after_other_sizes():
                                       x[:ntok].cpu().view(torch.int16).numpy()[rcor // k])
 
 
+# ------------------------------------------------------------- routing and permute in one launch
+# E <= 32 layers; LARGE_E8: more 16-token tiles (563) than resident CTAs, so
+# every CTA routes and copies several tiles on either side of the barrier
+LARGE_E8 = MoEConfig("large_e8", 9000, 128, 64, 8, 2)
+FUSED = ["tiny", "small_softmax", "small_sigmoid", "router_e24", "router_e32", "large_e8"]
+
+
+@pytest.mark.parametrize("name", FUSED)
+def test_route_permute_equals_route_then_permute(name):
+    """moe_route_permute gives, bit for bit, what moe_route followed by
+    moe_permute give (every output), twice in a row on one workspace (the
+    grid barrier's words are reused), and its maps are the oracle's stable
+    permutation of its own routing."""
+    cfg = {"large_e8": LARGE_E8}.get(name) or ROUTER_EXTRA.get(name) or CONFIGS[name]
+    p_cpu = make_layer(cfg.replace(d_ff=64), "cpu")
+    x, wg, bias = p_cpu["x"].cuda(), p_cpu["w_gate"].cuda(), p_cpu["bias"]
+    bias = None if bias is None else bias.cuda()
+    n, dm, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
+    r = n * k
+    d, ws = _ws(cfg)
+
+    def outs():
+        return dict(lg=_f32(n, e), idx=_i32(n, k), w=_f32(n, k), cnt=_i32(e), off=_i32(e + 1), roc=_i32(r),
+                    cor=_i32(r), xp=_bf(r, dm))
+
+    a = outs()
+    api.moe_route(d, x, wg, bias, a["lg"], a["idx"], a["w"], a["cnt"], a["off"], ws)
+    api.moe_permute(d, x, a["idx"], a["off"], a["roc"], a["cor"], a["xp"], ws)
+    _status_ok(ws)
+    for rep in range(2):
+        b = outs()
+        api.moe_route_permute(d, x, wg, bias, b["lg"], b["idx"], b["w"], b["cnt"], b["off"], b["roc"], b["cor"],
+                              b["xp"], ws)
+        _status_ok(ws)
+        for key in a:
+            ga, gb = a[key].cpu(), b[key].cpu()
+            if ga.dtype == torch.bfloat16:
+                ga, gb = ga.view(torch.int16), gb.view(torch.int16)
+            elif ga.dtype == torch.float32:
+                ga, gb = ga.view(torch.int32), gb.view(torch.int32)
+            assert torch.equal(ga, gb), (key, rep)
+    rroc, rcor = O.permutation(b["idx"].cpu().numpy(), e)
+    np.testing.assert_array_equal(b["roc"].cpu().numpy(), rroc)
+    np.testing.assert_array_equal(b["cor"].cpu().numpy(), rcor)
+
+
+def test_route_permute_rejects_what_it_does_not_cover():
+    """More than 32 experts or MXFP8 rows: an argument error, nothing launched."""
+    for cfg in (CONFIGS["small_fine"], CONFIGS["small_softmax"].replace(precision="mxfp8")):
+        n, dm, e, k = cfg.n_tok, cfg.d_model, cfg.n_exp, cfg.top_k
+        d, ws = _ws(cfg)
+        with pytest.raises(api.MoEError):
+            api.moe_route_permute(d, _bf(n, dm), _bf(e, dm), None, _f32(n, e), _i32(n, k), _f32(n, k), _i32(e),
+                                  _i32(e + 1), _i32(n * k), _i32(n * k), _bf(n * k, dm), ws)
+        _status_ok(ws)
+
+
 # ------------------------------------------------------------- grouped FFN
 def _oracle_route(cfg, h):
     lg = O.gate_logits(h["x"], h["w_gate"])
