@@ -408,26 +408,63 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     ms_fwd = f0.elapsed_time(f1)
 
-    # --- end to end through the public API with pinned host buffers
+    # --- end to end through the public API with pinned host buffers.  Every
+    # step uploads its inputs (x, dY) from pinned host memory and downloads
+    # its results (output, input gradient) to it, all inside the timed region.
+    # The copies run on a copy stream as a training loop's prefetch would:
+    # step i+1's uploads and step i's downloads overlap step i+1's compute.
+    # Inputs and results are double-buffered; the results are first staged
+    # on the device (two 16-byte-row copies) so the next step may overwrite
+    # the layer's own output buffers.
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
-    hout = torch.empty(b["out"].shape, dtype=b["out"].dtype).pin_memory()
-    hdx = torch.empty(x.shape, dtype=x.dtype).pin_memory()
-    x_in, dy_in = torch.empty_like(x), torch.empty_like(dy)
+    hout = [torch.empty(b["out"].shape, dtype=b["out"].dtype).pin_memory() for _ in range(2)]
+    hdx = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for _ in range(2)]
+    x_in = [torch.empty_like(x) for _ in range(2)]
+    dy_in = [torch.empty_like(dy) for _ in range(2)]
+    out_st = [torch.empty_like(b["out"]) for _ in range(2)]
+    dx_st = [torch.empty_like(x) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    up, used, staged, down = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    e0.record()
-    for _ in range(args.steps):
-        x_in.copy_(hx, non_blocking=True)
-        dy_in.copy_(hdy, non_blocking=True)
-        layer.forward(x_in)
-        grads = layer.backward(dy_in)
+    e0.record(comp)
+    cs.wait_event(e0)
+
+    def upload(j):
+        with torch.cuda.stream(cs):
+            x_in[j].copy_(hx, non_blocking=True)
+            dy_in[j].copy_(hdy, non_blocking=True)
+            up[j].record(cs)
+
+    upload(0)
+    for i in range(args.steps):
+        j = i % 2
+        if i + 1 < args.steps:
+            if i >= 1:
+                cs.wait_event(used[1 - j])       # step i-1 is done with the other input buffers
+            upload(1 - j)
+        comp.wait_event(up[j])
+        layer.forward(x_in[j])
+        grads = layer.backward(dy_in[j])
         if cfg.use_bias:
             layer.update_bias(1e-3, 0)
-        hout.copy_(b["out"], non_blocking=True)      # the step's results: output and input gradient
-        hdx.copy_(grads["dx"], non_blocking=True)
-    e1.record()
+        used[j].record(comp)
+        if i >= 2:
+            comp.wait_event(down[j])             # step i-2's download has left this staging buffer
+        out_st[j].copy_(b["out"], non_blocking=True)
+        dx_st[j].copy_(grads["dx"], non_blocking=True)
+        staged[j].record(comp)
+        with torch.cuda.stream(cs):
+            cs.wait_event(staged[j])
+            hout[j].copy_(out_st[j], non_blocking=True)   # the step's results: output and input gradient
+            hdx[j].copy_(dx_st[j], non_blocking=True)
+            down[j].record(cs)
+    comp.wait_stream(cs)
+    e1.record(comp)
     torch.cuda.synchronize()
     clk.__exit__(None, None, None)
     barrier()
@@ -471,7 +508,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     res = {"cfg": cfg, "per_call": per_call, "kernels": kernels, "clocks": clk.summary(), "nonempty": nonempty,
            "inference_fwd": inference,
            "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
-           "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout.numel() * 2 + hdx.numel() * 2}
+           "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout[0].numel() * 2 + hdx[0].numel() * 2}
     for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
         res[key] = aggregate(world, cfg.n_tok, args.steps, v, max_over_ranks)
     del layer, p, dy, b, ws
