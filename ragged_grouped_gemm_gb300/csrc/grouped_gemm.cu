@@ -203,6 +203,36 @@ struct Tile {
   int split;       // ragged M: contraction slice (partial-output index)
 };
 
+// Ragged K: the group of a tile (tiles of a group are consecutive: its M
+// tiles times its N tiles) and the tile from the group's first and
+// one-past-last rows.
+template <int BN, bool PAIR>
+__device__ __forceinline__ int rk_group(int tile, const KParams& p) {
+  constexpr int UR = PAIR ? 2 * BM : BM;
+  return tile / (((p.m_size + UR - 1) / UR) * ((p.n_size + BN - 1) / BN));
+}
+
+template <int BN, bool PAIR>
+__device__ __forceinline__ Tile decode_tile_rk(int tile, const KParams& p, int off0, int off1, int rank) {
+  Tile t;
+  constexpr int UR = PAIR ? 2 * BM : BM;
+  const int prank = rank & 1;
+  const int ntiles = (p.n_size + BN - 1) / BN;
+  const int per_g = ((p.m_size + UR - 1) / UR) * ntiles;
+  t.kbeg = 0;
+  t.split = 0;
+  t.g = tile / per_g;
+  const int rem = tile - t.g * per_g;
+  t.mt = rem / ntiles;
+  t.nt = rem - t.mt * ntiles;
+  t.row0 = off0;
+  t.m0 = t.mt * UR + prank * BM;
+  t.k_rows = off1 - off0;
+  t.rows_valid = min(BM, p.m_size - t.m0);
+  t.num_kb = (t.k_rows + p.kblk - 1) / p.kblk;
+  return t;
+}
+
 // rank: the CTA's rank in its cluster; bit 0 picks its 128 rows of a pair
 // tile.
 template <bool RAGGED_K, int BN, bool PAIR = false>
@@ -243,18 +273,8 @@ __device__ __forceinline__ Tile decode_tile(int tile, const KParams& p, const in
       t.num_kb = max(0, min(kbs, t.num_kb - t.kbeg));
     }
   } else {
-    const int mtiles = (p.m_size + UR - 1) / UR;
-    const int ntiles = (p.n_size + BN - 1) / BN;
-    const int per_g = mtiles * ntiles;
-    t.g = tile / per_g;
-    const int rem = tile - t.g * per_g;
-    t.mt = rem / ntiles;
-    t.nt = rem - t.mt * ntiles;
-    t.row0 = s_off[t.g];
-    t.m0 = t.mt * UR + prank * BM;
-    t.k_rows = s_off[t.g + 1] - s_off[t.g];
-    t.rows_valid = min(BM, p.m_size - t.m0);
-    t.num_kb = (t.k_rows + p.kblk - 1) / p.kblk;
+    t = decode_tile_rk<BN, PAIR>(tile, p, s_off[rk_group<BN, PAIR>(tile, p)], s_off[rk_group<BN, PAIR>(tile, p) + 1],
+                                 rank);
   }
   return t;
 }
@@ -715,8 +735,23 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
     constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
     uint32_t it = 0, tcount = 0;
     bool ok = true;
+    // ragged K: the next tile's group offsets (global memory) are loaded
+    // before this tile's k-blocks are issued and used only after them, so
+    // their latency falls while the MMAs run instead of between tiles
+    int nx0 = 0, nx1 = 0;
+    if (RAGGED_K && unit0 < total_tiles) {
+      const int g = rk_group<BN, PAIR>(unit0, p);
+      nx0 = s_off[g];
+      nx1 = s_off[g + 1];
+    }
     for (int tile = unit0; ok && tile < total_tiles; tile += ustride, ++tcount) {
-      const Tile t = decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
+      const Tile t = RAGGED_K ? decode_tile_rk<BN, PAIR>(tile, p, nx0, nx1, rank)
+                              : decode_tile<RAGGED_K, BN, PAIR>(tile, p, s_off, s_pre, rank);
+      if (RAGGED_K && tile + ustride < total_tiles) {
+        const int g = rk_group<BN, PAIR>(tile + ustride, p);
+        nx0 = s_off[g];
+        nx1 = s_off[g + 1];
+      }
       const uint32_t buf = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, s_abort, p.status, 200)) break;
