@@ -181,7 +181,8 @@ def test_permute_twice_in_a_row_and_after_other_sizes():
 # E <= 32 layers; LARGE_E8: more 16-token tiles (563) than resident CTAs, so
 # every CTA routes and copies several tiles on either side of the barrier
 LARGE_E8 = MoEConfig("large_e8", 9000, 128, 64, 8, 2)
-FUSED = ["tiny", "small_softmax", "small_sigmoid", "router_e24", "router_e32", "large_e8"]
+FUSED = ["tiny", "small_softmax", "small_sigmoid", "router_e24", "router_e32", "large_e8",
+         "single_token", "one_expert", "k_equals_e", "hot_expert"]
 
 
 @pytest.mark.parametrize("name", FUSED)
@@ -190,7 +191,8 @@ def test_route_permute_equals_route_then_permute(name):
     moe_permute give (every output), twice in a row on one workspace (the
     grid barrier's words are reused), and its maps are the oracle's stable
     permutation of its own routing."""
-    cfg = {"large_e8": LARGE_E8}.get(name) or ROUTER_EXTRA.get(name) or CONFIGS[name]
+    cfg = ({"large_e8": LARGE_E8}.get(name) or ROUTER_EXTRA.get(name) or {c.name: c for c in EDGE}.get(name)
+           or CONFIGS[name])
     p_cpu = make_layer(cfg.replace(d_ff=64), "cpu")
     x, wg, bias = p_cpu["x"].cuda(), p_cpu["w_gate"].cuda(), p_cpu["bias"]
     bias = None if bias is None else bias.cuda()
