@@ -209,8 +209,8 @@ MOE_API moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* log
  * launch, for E <= 32 and bf16 rows (precision 0 or 2).  The outputs of both
  * calls, bit-identical to them (logits, topk_idx, topk_w, counts, offsets as
  * moe_route; row_of_copy, copy_of_row, x_perm as moe_permute).  A
- * cooperative launch: each CTA routes its 16-token tiles and
- * publishes their expert histograms, a grid-wide barrier follows (bounded: a
+ * cooperative launch: each CTA routes its tiles (at most 16 tokens each, as
+ * many per CTA as the batch allows) and publishes their expert histograms, a grid-wide barrier follows (bounded: a
  * wait that runs out sets MOE_DEV_TIMEOUT, site 710), then each CTA finds its
  * tiles' first rows from the histograms and copies its token rows while they
  * are still in L2.  Needs the forward workspace (its per-tile histograms are
