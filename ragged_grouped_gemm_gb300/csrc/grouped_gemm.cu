@@ -149,11 +149,14 @@ struct Cfg {
   //   A codes [128][128] | B codes [BN][128] (both 128-byte swizzled) |
   //   A scale rows [4][144] (from a 16-aligned row) | B scale rows [4][BN] |
   //   scale atoms for tcgen05.cp: A 512 B, B 2 x 512 B
+  // (CTA pair, ragged M: this CTA holds half of the B tile's codes, all of
+  // its scale rows)
+  static constexpr int kQBRows = PAIR ? BN / 2 : BN;
   static constexpr int kQBCodes = BM * 128;
-  static constexpr int kQARaw = kQBCodes + BN * 128;
+  static constexpr int kQARaw = kQBCodes + kQBRows * 128;
   static constexpr int kQBRaw = kQARaw + 640;
   static constexpr int kQAtoms = kQBRaw + 4 * BN;
-  static constexpr uint32_t kQTxBytes = BM * 128 + BN * 128 + 4 * 144 + 4 * BN;    // ragged M
+  static constexpr uint32_t kQTxBytes = BM * 128 + kQBRows * 128 + 4 * 144 + 4 * BN;    // ragged M
   static constexpr uint32_t kQTxBytesK = BM * 128 + BN * 128 + 4 * 128 + 4 * BN;   // ragged K
   // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
   static constexpr int kStageBytes =
@@ -363,7 +366,8 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
       mbar_init(&full[s], W8 ? 1 + kConvWarps : 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], 1);   // the scale warp that builds it
+    // the scale warp that builds the stage (CTA pair: that of each CTA, on the leader's barrier)
+    for (int s = 0; s < (QUANT ? S : 0); ++s) mbar_init(&sready[s], PAIR ? 2 : 1);
     for (int s = 0; s < C::kW8Slots; ++s) {
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], kConvWarps);
@@ -464,14 +468,21 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           const int k0 = (src == 0 ? kb : kb - p.kb0) * 128;
           tma_load_2d(st, &p.tmA[src], &full[s], k0, t.row0);
           tma_load_2d(st + C::kQARaw, &p.tmAs[src], &full[s], t.row0 & ~15, k0 / 32);   // 16-byte aligned x
+          // CTA pair: this CTA's half of the B codes (W1 or W3 for the dual-N
+          // tile), and every B scale row (each CTA's tensor memory needs them all)
           if (p.b_dual_n) {
             const int f0 = t.nt * (BN / 2);
-            tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, f0, t.g);
-            tma_load_3d(st + C::kQBCodes + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
+            if (PAIR) {
+              tma_load_3d(st + C::kQBCodes, &p.tmB[rank & 1], &full[s], k0, f0, t.g);
+            } else {
+              tma_load_3d(st + C::kQBCodes, &p.tmB[0], &full[s], k0, f0, t.g);
+              tma_load_3d(st + C::kQBCodes + (BN / 2) * 128, &p.tmB[1], &full[s], k0, f0, t.g);
+            }
             tma_load_3d(st + C::kQBRaw, &p.tmBs[0], &full[s], f0, k0 / 32, t.g);
             tma_load_3d(st + C::kQBRaw + 2 * BN, &p.tmBs[1], &full[s], f0, k0 / 32, t.g);
           } else {
-            tma_load_3d(st + C::kQBCodes, &p.tmB[src], &full[s], k0, t.nt * BN, t.g);
+            tma_load_3d(st + C::kQBCodes, &p.tmB[src], &full[s], k0, t.nt * BN + (PAIR ? (rank & 1) * (BN / 2) : 0),
+                        t.g);
             tma_load_3d(st + C::kQBRaw, &p.tmBs[src], &full[s], t.nt * BN, k0 / 32, t.g);
           }
         }
@@ -703,30 +714,42 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           // rewritten only after the MMAs that read it have completed (stage release)
           const uint32_t sf = tmem_base + C::kSfCol + s * 16;
           const uint32_t atoms = smem_u32(st + C::kQAtoms);
-          tc_cp_32x128b_warpx4(sf, atoms);
-          tc_cp_32x128b_warpx4(sf + 4, atoms + 512);
-          if (BN > 128) tc_cp_32x128b_warpx4(sf + 8, atoms + 1024);
+          if (PAIR) {   // each CTA's atoms to its own tensor memory
+            tc_cp_32x128b_warpx4_pair(sf, atoms);
+            tc_cp_32x128b_warpx4_pair(sf + 4, atoms + 512);
+            if (BN > 128) tc_cp_32x128b_warpx4_pair(sf + 8, atoms + 1024);
+          } else {
+            tc_cp_32x128b_warpx4(sf, atoms);
+            tc_cp_32x128b_warpx4(sf + 4, atoms + 512);
+            if (BN > 128) tc_cp_32x128b_warpx4(sf + 8, atoms + 1024);
+          }
           const uint32_t a_base = smem_u32(st);
           const uint32_t b_base = smem_u32(st + C::kQBCodes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
-            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sf, sf + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+            if (PAIR)
+              tc_mma_mxf8_pair(d_tmem, ad, bd, idesc_mxf8(2 * BM, BN, kk), sf, sf + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sf, sf + 4, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&empty[s]);
+          if (PAIR) tc_commit_pair_mc(&empty[s], 3);
+          else tc_commit(&empty[s]);
         }
         __syncwarp();
       }
       if (!ok) break;
       if (lane == 0) {
-        if (t.num_kb > 0) tc_commit(&tfull[buf]);
+        if (PAIR) tc_commit_pair_mc(&tfull[buf], static_cast<uint16_t>(3u << lead));
+        else if (t.num_kb > 0) tc_commit(&tfull[buf]);
         else mbar_arrive(&tfull[buf]);
       }
       __syncwarp();
     }
     if (lane == 0) {
-      tc_commit(mma_done);
+      if (PAIR) tc_commit_pair_mc(mma_done, static_cast<uint16_t>(1u << lead));
+      else tc_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
     __syncwarp();
@@ -853,7 +876,12 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sready[s]);
+          if (lane == 0) {
+            // CTA pair: the leader copies both CTAs' atoms; the peer's arrival
+            // releases its atom writes at cluster scope
+            if (PAIR && !leader) mbar_arrive_remote_release(mapa_shared(smem_u32(&sready[s]), lead));
+            else mbar_arrive(&sready[s]);
+          }
         }
       }
     }
@@ -1459,7 +1487,7 @@ cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream
       at[0].val.clusterDim.y = 1;
       at[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(CN * max_units);
-      cfg.blockDim = dim3(kThreads);
+      cfg.blockDim = dim3(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads));
       cfg.dynamicSmemBytes = C::smem_bytes(C::kMaxG);
       cfg.attrs = at;
       cfg.numAttrs = 1;
@@ -1481,7 +1509,7 @@ cudaError_t launch_impl(const KParams& kp, int64_t units_ub, cudaStream_t stream
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(CN * units);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThreads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = at;
@@ -1566,7 +1594,14 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       kp.kb1 = static_cast<int>((a.k1 + 127) / 128);
       if (kp.kb0 <= 0) return cudaErrorInvalidValue;
       kp.tile_n = a.b_dual_n ? QBN / 2 : QBN;
+      // CTA pairs (256-row tiles, each CTA half of B): only when forced with
+      // MOE_GEMM_CTA_PAIR=1.  Measured on the Mixtral shape they tie the
+      // one-SM form at best, and the peer's cluster-scope release of its scale
+      // atoms on every stage makes them 15% slower
+      const char* pe = std::getenv("MOE_GEMM_CTA_PAIR");
+      const bool qpair = pe && pe[0] == '1';
       const uint32_t brows = a.b_dual_n ? QBN / 2 : QBN;
+      const uint32_t bcode_rows = (a.b_dual_n || qpair) ? QBN / 2 : QBN;
       for (int src = 0; src < nsrc; ++src) {
         const int64_t K = src == 0 ? a.k0 : a.k1;
         const MxOperand& q = a.qa[src];
@@ -1587,7 +1622,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
         if (b.cols != K) return cudaErrorInvalidValue;
         const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows), static_cast<uint64_t>(b.groups)};
         const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(b.rows * K)};
-        const uint32_t box[3] = {128, brows, 1};
+        const uint32_t box[3] = {128, bcode_rows, 1};
         if (!make_map_u8(&kp.tmB[i], b.codes, 3, dims, str, box, true)) return cudaErrorInvalidValue;
         const uint64_t sd[3] = {static_cast<uint64_t>(b.rows), static_cast<uint64_t>(K / 32), static_cast<uint64_t>(b.groups)};
         const uint64_t ss[2] = {static_cast<uint64_t>(b.scale_ld), static_cast<uint64_t>(b.scale_ld * (K / 32))};
@@ -1595,11 +1630,18 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
         if (!make_map_u8(&kp.tmBs[i], b.scales, 3, sd, ss, sbox)) return cudaErrorInvalidValue;
       }
       const int64_t ntiles = (a.n_size + kp.tile_n - 1) / kp.tile_n;
-      tiles_ub = ntiles * ((a.max_rows + BM - 1) / BM + a.num_groups);
+      const int64_t ur = qpair ? 2 * BM : BM;
+      tiles_ub = ntiles * ((a.max_rows + ur - 1) / ur + a.num_groups);
       switch (a.epi) {
-        case EPI_SWIGLU_FWD_Q: return launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
-        case EPI_SWIGLU_BWD: return launch_impl<QBN, false, false, EPI_SWIGLU_BWD, true>(kp, tiles_ub, stream);
-        default: return launch_impl<QBN, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
+        case EPI_SWIGLU_FWD_Q:
+          return qpair ? launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true, true>(kp, tiles_ub, stream)
+                       : launch_impl<QBN, false, false, EPI_SWIGLU_FWD_Q, true>(kp, tiles_ub, stream);
+        case EPI_SWIGLU_BWD:
+          return qpair ? launch_impl<QBN, false, false, EPI_SWIGLU_BWD, true, true>(kp, tiles_ub, stream)
+                       : launch_impl<QBN, false, false, EPI_SWIGLU_BWD, true>(kp, tiles_ub, stream);
+        default:
+          return qpair ? launch_impl<QBN, false, false, EPI_BF16, true, true>(kp, tiles_ub, stream)
+                       : launch_impl<QBN, false, false, EPI_BF16, true>(kp, tiles_ub, stream);
       }
     }
     // ragged K (weight gradients): offsets are the padded group starts, every

@@ -323,6 +323,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// The same with release semantics at cluster scope: this thread's earlier
+// writes (here: shared memory the peer CTA's async-proxy reads) are visible
+// to whoever observes the arrival.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // TMA tile loads into this CTA's shared memory that complete on an mbarrier
 // of either CTA of the pair (bar = shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
@@ -402,6 +408,18 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) 
 // which is what tcgen05.cp.32x128b.warpx4 produces from a 512-byte shared-memory
 // atom holding, for 128 rows r and 4 scale blocks j, byte j of 32-bit word
 // (r/32)%4 of 16-byte row r%32.
+// CTA pair (M = 256): A rows and D in each CTA, B split between them; the
+// scale factors are read from each CTA's tensor memory at the same address
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
@@ -414,12 +432,19 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
 }
 // Copy 32 rows x 16 bytes of shared memory (no swizzle, rows 16 bytes apart)
 // into 4 columns of tensor memory, row r to lane r of every lane quarter.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint32_t saddr) {
+__device__ __forceinline__ uint64_t cp_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
   d |= static_cast<uint64_t>(128 >> 4) << 32;   // 8-row groups 128 bytes apart
   d |= 1ull << 46;                               // descriptor version; layout 0 = no swizzle
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+  return d;
+}
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc(saddr)) : "memory");
+}
+// CTA pair: each CTA's shared memory at saddr to its own tensor memory at taddr
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc(saddr)) : "memory");
 }
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, E8M0 scales, fp32 D,
 // K-major A and B: bits 4-5 B scale id, 7-9 / 10-12 A / B format (0 = E4M3),

@@ -19,6 +19,15 @@ def _mx(name):
     return CONFIGS[name].replace(precision="mxfp8")
 
 
+@pytest.fixture(params=["1", "0"], ids=["cta_pair", "one_sm"])
+def gemm_form(request, monkeypatch):
+    """Runs a test with the ragged-M MXFP8 GEMMs forced to the CTA-pair form
+    (256-row tiles, each CTA half of B) or to the one-SM form; by default the
+    library picks the form from the group sizes."""
+    monkeypatch.setenv("MOE_GEMM_CTA_PAIR", request.param)
+    return request.param
+
+
 def _quant(src):
     codes = torch.empty(src.shape, dtype=torch.uint8, device="cuda")
     rows, cols = src.shape[-2], src.shape[-1]
@@ -90,7 +99,7 @@ def test_permute_mxfp8_bitexact(name):
 
 
 @pytest.mark.parametrize("name", ["tiny", "small_softmax", "small_sigmoid", "small_fine"])
-def test_forward_mxfp8_matches_quantisation_aware_oracle(name):
+def test_forward_mxfp8_matches_quantisation_aware_oracle(name, gemm_form):
     cfg = _mx(name)
     p_cpu = make_layer(cfg, "cpu")
     p, h = to_dev(p_cpu), host_params(p_cpu)
@@ -147,7 +156,7 @@ EDGE_MX = [
 
 
 @pytest.mark.parametrize("cfg", EDGE_MX, ids=lambda c: c.name)
-def test_backward_mxfp8_matches_quantisation_aware_oracle(cfg):
+def test_backward_mxfp8_matches_quantisation_aware_oracle(cfg, gemm_form):
     """Every gradient of the MXFP8 layer against the oracle's MXFP8 backward
     (each expert GEMM quantised along its contraction, weight-gradient
     operands in group-aware token blocks), normwise 3e-2."""
