@@ -239,6 +239,54 @@ def test_full_size_sampled_mxfp8_dsv3():
     assert empty_ok
 
 
+def test_full_size_sampled_mxfp8_mixtral(monkeypatch):
+    """The Mixtral-shaped layer with MXFP8 expert GEMMs (~1024 rows per
+    expert, contractions of 4096 and 14336), forward and backward at full
+    size, in both GEMM forms (one-SM and CTA pair), against the same
+    quantisation-aware oracle results: a sample of 32 tokens, and the
+    weight gradients of the most loaded expert over its whole row set."""
+    cfg = CONFIGS["mixtral"].replace(precision="mxfp8")
+    torch.cuda.empty_cache()
+    p = make_layer(cfg, "cuda")
+    dy = make_dy(cfg, "cuda")
+    x, wg, dyh = np32(p["x"]), np32(p["w_gate"]), np32(dy)
+    lg = O.gate_logits(x, wg)
+    keys = O.selection_keys(lg, None)
+    idx, g = O.route(lg, None, cfg.top_k, cfg.gate)
+    e_hot = int(np.argmax(O.histogram(idx, cfg.n_exp)))
+    runs = {}
+    for form in ("0", "1"):
+        monkeypatch.setenv("MOE_GEMM_CTA_PAIR", form)
+        layer, gr, res = _mx_layer_run(cfg, p, dy)
+        tol = 2 * float(np.abs(res["logits"] - lg).max()) + 1e-6
+        res["same"] = routing_agreement(keys, res["idx"], idx, tol)
+        res["oracle_idx"] = idx
+        res["hot_dw"] = {k: gr[k][e_hot].cpu().numpy() for k in ("dw1", "dw3", "dw2")}
+        runs[form] = res
+        del layer, gr
+        torch.cuda.empty_cache()
+    same = runs["0"]["same"] & runs["1"]["same"]
+    cand = [t for t in sample_tokens(cfg.n_tok, 1024).numpy() if same[t]]
+    groups = token_groups(idx, cand, max_experts=4, max_tokens=32)
+    assert sum(len(x_) for x_ in groups) == 32
+    hot_ok = bool(same[np.nonzero(idx == e_hot)[0]].all())
+    shm = {k: SharedBf16(_bits(p[k])) for k in ("w1", "w3", "w2")}
+    del p
+    torch.cuda.empty_cache()
+    try:
+        jobs = _jobs(shm, x, dyh, lg, idx, g, groups, wg, cfg.gate, None)
+        hot_job, _ = _expert_job(shm, x, dyh, lg, idx, g, e_hot, wg, cfg.gate)
+        results = run_groups(jobs + ([hot_job] if hot_ok else []))
+    finally:
+        for v in shm.values():
+            v.close()
+    for form, res in runs.items():
+        _compare_groups(res, groups, results[:len(groups)], MX_TOL)
+        if hot_ok:
+            for key in ("dw1", "dw3", "dw2"):
+                assert rel(res["hot_dw"][key], results[-1][key][0]) < MX_TOL, (form, key)
+
+
 @pytest.mark.parametrize("skew", ["uniform", "zipf", "half0"])
 def test_full_size_mxfp8_dsv3_load_skews(skew):
     """The MXFP8 layer (DeepSeek-V3 shapes) forward and backward under the
