@@ -132,18 +132,11 @@ def aggregate(world: int, tokens_per_step: int, steps: int, ms_local: float, red
     return world * tokens_per_step * steps / (ms / 1e3), ms
 
 
-def route_launches(cfg, sms: int = 152) -> int:
+def route_launches(cfg) -> int:
     """moe_route's kernels: one fused router kernel for E <= 32; otherwise
-    dense offsets, the router logits GEMM, top-K, scan, plus the ordered sum
-    of the GEMM's contraction slices when its 128-token tiles are too few to
-    fill the GPU (at most 4 slices of 64-column blocks)."""
-    if cfg.n_exp <= 32:
-        return 1
-    tiles = -(-cfg.n_tok // 128) * -(-cfg.n_exp // (32 if cfg.n_exp <= 32 else 256))
-    want = min(4, sms // max(tiles, 1))
-    kb = -(-cfg.d_model // 64)
-    split = want > 1 and kb > 1 and (cfg.n_tok * cfg.n_exp) % 4 == 0 and -(-kb // -(-kb // want)) > 1
-    return 4 + (1 if split else 0)
+    dense offsets, the router logits GEMM, and one kernel for the ordered sum
+    of the GEMM's contraction slices, top-K, histogram and scan."""
+    return 1 if cfg.n_exp <= 32 else 3
 
 
 def fused_dispatch(cfg) -> bool:

@@ -34,14 +34,17 @@ constexpr int kPermuteCtlWord = 48;
 // Look-back words of the single-pass permute (1 MiB): ceil(N/16) * E of them
 // per call; larger problems take the two-kernel permute.
 constexpr size_t kLookWords = 131072;
+// The router tail's expert histogram accumulator (one int32 per expert, up to
+// 1024), a fixed region like the look-back words; the kernel leaves it zero.
+constexpr size_t kRouteAccWords = 1024;
 // The router logits GEMM has one 128-token tile per CTA; with few tiles its
 // contraction is cut into up to this many slices (summed in order after).
 constexpr int kGateSlices = 4;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, look = 0, aux = 0, gpart = 0, rp_hist = 0,
-         fwd_end = 0;
+  size_t status = 0, dense_off = 0, blk_counts = 0, blk_base = 0, look = 0, racc = 0, aux = 0, gpart = 0,
+         rp_hist = 0, fwd_end = 0;
   size_t hq = 0, hs = 0, hq_sh = 0, hs_sh = 0;   // MXFP8 h between GEMM1 and GEMM2
   size_t dl = 0, dg = 0, dyw = 0, da1 = 0, da3 = 0, da1s = 0, da3s = 0, dxs = 0, dwg = 0, gmaps = 0, total = 0;
   // MXFP8 backward: row-wise codes/scales of dYw, da1, da3 (dgrad operands),
@@ -65,6 +68,7 @@ WsLayout layout(const moe_desc_t& d) {
   // the single-pass permute's look-back words: a fixed region of the same
   // place and size for every description, holding nothing else
   L.look = o; o += kLookWords * 8;
+  L.racc = o; o += kRouteAccWords * 4;
   L.blk_counts = o; o = align_up(o + nch * E * 4);
   L.blk_base = o; o = align_up(o + nch * E * 4);
   L.aux = o; o = align_up(o + moe::aux_partial_floats(d.n_tok > 0 ? d.n_tok : 1, d.n_exp) * 4);
@@ -373,12 +377,16 @@ moe_status_t moe_get_device_status(const void* ws, int32_t* status_host, void* s
   return MOE_OK;
 }
 
-static moe_status_t route_tail(const moe_desc_t* d, const float* logits, const float* bias, int32_t* topk_idx,
-                               float* topk_w, int32_t* counts, int32_t* offsets, int32_t* status, cudaStream_t st) {
+// The ordered sum of the logits' ks contraction slices (ks == 1: part is the
+// logits), top-K, histogram and scan in one launch.
+static moe_status_t route_tail(const moe_desc_t* d, const float* part, int ks, float* logits, const float* bias,
+                               int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, void* ws,
+                               const WsLayout& L, cudaStream_t st) {
   moe::RouteShape rs{d->n_tok, d->n_exp, d->top_k, d->gate};
-  MOE_CUDA(moe::launch_topk(rs, logits, d->use_bias ? bias : nullptr, topk_idx, topk_w, counts, status, st));
-  MOE_CUDA(moe::launch_offsets(counts, d->n_exp, static_cast<int64_t>(d->n_tok) * d->top_k, offsets, status, st));
-  return MOE_OK;
+  int32_t* status = at<int32_t>(ws, L.status);
+  return cuda_status(moe::launch_topk_scan(rs, part, ks, logits, d->use_bias ? bias : nullptr, topk_idx, topk_w,
+                                           counts, offsets, at<int32_t>(ws, L.racc), status + kTicketWord, status,
+                                           st));
 }
 
 moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, const float* bias, float* logits,
@@ -405,7 +413,6 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
                                                 topk_idx, topk_w, counts, offsets, status + kRouterAccWord,
                                                 status + kTicketWord, status, st));
   }
-  MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
   MOE_CUDA(moe::launch_dense_offsets(dense, d->n_tok, st));
   GemmArgs g;
   g.epi = moe::EPI_F32;
@@ -427,8 +434,8 @@ moe_status_t moe_route(const moe_desc_t* d, const void* x, const void* w_gate, c
   float* part = at<float>(ws, L.gpart);
   g.out0 = g.ksplit > 1 ? static_cast<void*>(part) : static_cast<void*>(logits);
   MOE_CUDA(gemm(moe::TIMING_GATE, g, st));
-  if (g.ksplit > 1) MOE_CUDA(moe::launch_sum_slices(part, g.ksplit, ne, logits, st));
-  return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, status, st);
+  if (g.ksplit > 1) return route_tail(d, part, g.ksplit, logits, bias, topk_idx, topk_w, counts, offsets, ws, L, st);
+  return route_tail(d, logits, 1, nullptr, bias, topk_idx, topk_w, counts, offsets, ws, L, st);
 }
 
 moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, const float* bias,
@@ -441,9 +448,11 @@ moe_status_t moe_route_from_logits(const moe_desc_t* d, const float* logits, con
   if (d->use_bias && !bias) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WsLayout L = layout(*d);
-  MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
-  if (d->n_tok == 0) return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
-  return route_tail(d, logits, bias, topk_idx, topk_w, counts, offsets, at<int32_t>(ws, L.status), st);
+  if (d->n_tok == 0) {
+    MOE_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->n_exp, st));
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->n_exp + 1), st));
+  }
+  return route_tail(d, logits, 1, nullptr, bias, topk_idx, topk_w, counts, offsets, ws, L, st);
 }
 
 // moe_route_permute's scratch words, 128-byte aligned inside their region

@@ -131,24 +131,50 @@ __device__ __forceinline__ void topk_token(const float (&lg)[PL], const float* _
   my_w = sel / tot;
 }
 
-// One warp per token; expert e lives in lane e % 32, slot e / 32.
+constexpr int kTopkMaxSlices = 4;
+// One warp per token; expert e lives in lane e % 32, slot e / 32.  Top-K of
+// every token from the router logits' contraction slices (added in slice
+// order, fp32), the logits written, and the expert histogram and its scan
+// in the same launch: each CTA adds its histogram to acc (E int32, zero
+// before the launch), and the CTA that takes the last ticket writes counts
+// and offsets, checks the total and leaves acc and the ticket zero.
+// part: ks slices [N][E] fp32 (ks == 1: the logits themselves, not rewritten).
 template <int PL>
-__global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __restrict__ logits,
-                                                   const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w, int32_t* __restrict__ counts) {
+__global__ void __launch_bounds__(256) topk_scan_kernel(RouteShape s, const float* __restrict__ part, int ks,
+                                                        float* __restrict__ logits, const float* __restrict__ bias,
+                                                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                        int32_t* acc, int32_t* ticket, int32_t* status) {
   extern __shared__ int s_hist[];
+  __shared__ int s_last;
+  __shared__ int s_wsum[8];
   const int E = s.n_exp, K = s.top_k;
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int64_t ne = static_cast<int64_t>(s.n_tok) * E;
   if (t < s.n_tok) {
-    float lg[PL];
-    const float* row = logits + static_cast<int64_t>(t) * E;
+    // every slice of every expert of this lane loaded first (independent
+    // loads), then added in slice order
+    float lg[PL], ps[PL][kTopkMaxSlices - 1];
+    const float* row = part + static_cast<int64_t>(t) * E;
 #pragma unroll
     for (int j = 0; j < PL; ++j) {
       const int e = lane + 32 * j;
       lg[j] = e < E ? row[e] : -INFINITY;
+#pragma unroll
+      for (int sl = 1; sl < kTopkMaxSlices; ++sl) ps[j][sl - 1] = (e < E && sl < ks) ? row[sl * ne + e] : 0.0f;
+    }
+    if (ks > 1) {
+#pragma unroll
+      for (int j = 0; j < PL; ++j) {
+        const int e = lane + 32 * j;
+#pragma unroll
+        for (int sl = 1; sl < kTopkMaxSlices; ++sl)
+          if (sl < ks) lg[j] += ps[j][sl - 1];
+        if (e < E) logits[static_cast<int64_t>(t) * E + e] = lg[j];
+      }
     }
     int my_e;
     float my_w;
@@ -161,7 +187,49 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteShape s, const float* __
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
-    if (s_hist[i]) atomicAdd(&counts[i], s_hist[i]);
+    if (s_hist[i]) atomicAdd(acc + i, s_hist[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last CTA: exclusive scan of the totals, four experts per thread
+  int v[4], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * threadIdx.x + j;
+    v[j] = e < E ? atomicExch(acc + e, 0) : 0;
+    sum += v[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += s_wsum[w];
+  int run = base + incl - sum;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * threadIdx.x + j;
+    if (e < E) {
+      counts[e] = v[j];
+      run += v[j];
+      offsets[e + 1] = run;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[0] = 0;
+    *ticket = 0;
+    int total = 0;
+    for (int w = 0; w < 8; ++w) total += s_wsum[w];
+    if (static_cast<long long>(total) != static_cast<long long>(s.n_tok) * K && status)
+      atomicOr(status, DEV_BAD_OFFSETS);
+  }
 }
 
 // ------------------------------------------------------------ fused router (E <= 32)
@@ -541,38 +609,6 @@ __global__ void __launch_bounds__(kRtWarps * 32, 2) route_permute_kernel(
     __syncthreads();
   }
   if (tid == 0 && s_bad && status) atomicOr(status, s_bad);
-}
-
-// ------------------------------------------------------------ offsets scan
-__global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E, long long expected,
-                                                       int32_t* __restrict__ offsets, int32_t* status) {
-  __shared__ int warp_tot[32];
-  const int i = threadIdx.x;
-  const int lane = i & 31, w = i >> 5;
-  const int c = i < E ? counts[i] : 0;
-  int incl = c;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(kFull, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int v = warp_tot[lane];
-    int inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int u = __shfl_up_sync(kFull, inc, d);
-      if (lane >= d) inc += u;
-    }
-    warp_tot[lane] = inc - v;
-  }
-  __syncthreads();
-  const int val = incl + warp_tot[w];
-  if (i < E) offsets[i + 1] = val;
-  if (i == 0) offsets[0] = 0;
-  if (i == E - 1 && static_cast<long long>(val) != expected && status) atomicOr(status, DEV_BAD_OFFSETS);
 }
 
 // ------------------------------------------------------------ bias update
@@ -1281,23 +1317,6 @@ __global__ void __launch_bounds__(256, 3) combine_bwd_kernel(int n_tok, int d8, 
   }
 }
 
-// out[i] = sum over s of part[s][i], slices added in order (fp32).
-__global__ void __launch_bounds__(256) sum_slices_kernel(const float4* __restrict__ part, int ks, int64_t n4,
-                                                         float4* __restrict__ out) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 a = part[i];
-    for (int s = 1; s < ks; ++s) {
-      const float4 b = part[s * n4 + i];
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
-    }
-    out[i] = a;
-  }
-}
-
 // ------------------------------------------------------------ router weight gradient
 // dW_g[e] = sum over the rows r of expert e of dl[copy_of_row[r]] * x_perm[r].
 // Ragged and deterministic: every expert's rows are cut into 64-row chunks
@@ -1545,22 +1564,24 @@ int grid_for_tokens(int n_tok) {
 
 }  // namespace
 
-cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* bias, int32_t* topk_idx,
-                        float* topk_w, int32_t* counts, int32_t* status, cudaStream_t st) {
-  (void)status;
+cudaError_t launch_topk_scan(const RouteShape& s, const float* part, int ks, float* logits, const float* bias,
+                             int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* acc,
+                             int32_t* ticket, int32_t* status, cudaStream_t st) {
   if (s.n_tok <= 0) return cudaSuccess;
+  if (s.n_exp > 1024 || ks < 1 || ks > kTopkMaxSlices) return cudaErrorInvalidValue;
   const int blocks = (s.n_tok + 7) / 8;
   const size_t smem = static_cast<size_t>(s.n_exp) * sizeof(int);
   const int pl = (s.n_exp + 31) / 32;
-#define MOE_TOPK(P) topk_kernel<P><<<blocks, 256, smem, st>>>(s, logits, bias, topk_idx, topk_w, counts)
-  if (pl <= 1) MOE_TOPK(1);
-  else if (pl <= 2) MOE_TOPK(2);
-  else if (pl <= 4) MOE_TOPK(4);
-  else if (pl <= 8) MOE_TOPK(8);
-  else if (pl <= 16) MOE_TOPK(16);
-  else if (pl <= 32) MOE_TOPK(32);
-  else return cudaErrorInvalidValue;
-#undef MOE_TOPK
+#define MOE_TOPK_SCAN(P)                                                                                          \
+  topk_scan_kernel<P><<<blocks, 256, smem, st>>>(s, part, ks, logits, bias, topk_idx, topk_w, counts, offsets, acc, \
+                                                 ticket, status)
+  if (pl <= 1) MOE_TOPK_SCAN(1);
+  else if (pl <= 2) MOE_TOPK_SCAN(2);
+  else if (pl <= 4) MOE_TOPK_SCAN(4);
+  else if (pl <= 8) MOE_TOPK_SCAN(8);
+  else if (pl <= 16) MOE_TOPK_SCAN(16);
+  else MOE_TOPK_SCAN(32);
+#undef MOE_TOPK_SCAN
   return cudaGetLastError();
 }
 
@@ -1635,13 +1656,6 @@ cudaError_t launch_route_permute(const RouteShape& s, int d, const void* x, cons
   return go(route_permute_kernel<4>);
 }
 
-cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
-                           int32_t* status, cudaStream_t st) {
-  if (n_exp > 1024) return cudaErrorInvalidValue;
-  offsets_kernel<<<1, 1024, 0, st>>>(counts, n_exp, static_cast<long long>(expected_total), offsets, status);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_update_bias(const int32_t* counts, int n_exp, float* bias, float gamma, int mode,
                                cudaStream_t st) {
   const float target = static_cast<float>(1.0 / static_cast<double>(n_exp));
@@ -1714,16 +1728,6 @@ cudaError_t launch_permute_rows(int n_tok, int d, int top_k, const void* x, cons
   if (n_tok <= 0) return cudaSuccess;
   permute_rows_kernel<<<grid_for_tokens(n_tok), 256, 0, st>>>(n_tok, d / 8, top_k, static_cast<const uint4*>(x),
                                                               row_of_copy, static_cast<uint4*>(x_perm));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_sum_slices(const float* part, int ks, int64_t n, float* out, cudaStream_t st) {
-  if (n <= 0) return cudaSuccess;
-  if (ks < 1 || n % 4) return cudaErrorInvalidValue;
-  const int64_t n4 = n / 4;
-  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, 4096));
-  sum_slices_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), ks, n4,
-                                            reinterpret_cast<float4*>(out));
   return cudaGetLastError();
 }
 

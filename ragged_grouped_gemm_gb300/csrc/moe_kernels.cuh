@@ -14,13 +14,9 @@ struct RouteShape {
   int gate;      // 0 softmax, 1 sigmoid
 };
 
-// Per-token top-K over fp32 keys (logits + bias), renormalised weights from
-// the unbiased logits, and the expert histogram (counts must be zeroed).
-cudaError_t launch_topk(const RouteShape& s, const float* logits, const float* bias, int32_t* topk_idx,
-                        float* topk_w, int32_t* counts, int32_t* status, cudaStream_t st);
 // The whole router of a layer with E <= 32 in one launch: logits (warp-level
-// tensor-core MMA, fp32), top-K and weights as launch_topk, counts and
-// offsets as launch_offsets.  acc: E int32 and ticket: one int32, all zero
+// tensor-core MMA, fp32), then top-K, weights, counts and offsets as
+// launch_topk_scan.  acc: E int32 and ticket: one int32, all zero
 // before the launch (the kernel leaves them zero).  D must be a multiple of 32.
 cudaError_t launch_router_fused(const RouteShape& s, int d, const void* x, const void* w_gate, const float* bias,
                                 float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
@@ -37,9 +33,17 @@ cudaError_t launch_route_permute(const RouteShape& s, int d, const void* x, cons
                                  float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                  int32_t* row_of_copy, int32_t* copy_of_row, void* x_perm, int32_t* ws_words,
                                  int32_t* status, cudaStream_t st);
-// offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]; checks the total.
-cudaError_t launch_offsets(const int32_t* counts, int n_exp, int64_t expected_total, int32_t* offsets,
-                           int32_t* status, cudaStream_t st);
+// The router's tail in one launch (E <= 1024): the logits as the ordered fp32
+// sum of their ks contraction slices (1 <= ks <= 4; part: [ks][N][E]; ks ==
+// 1: part is the logits, not rewritten), per-token top-K over fp32 keys (logits + bias),
+// weights renormalised from the unbiased logits, the expert histogram
+// (counts) and its exclusive scan (offsets[0] = 0, offsets[e+1] =
+// offsets[e] + counts[e]; a total other than N*K sets DEV_BAD_OFFSETS).
+// acc: E int32 and ticket: one int32, zero before the launch (the kernel
+// leaves them zero).
+cudaError_t launch_topk_scan(const RouteShape& s, const float* part, int ks, float* logits, const float* bias,
+                             int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* acc,
+                             int32_t* ticket, int32_t* status, cudaStream_t st);
 // Route-bias update from the histogram (mode 0: listing form, 1: +-gamma).
 cudaError_t launch_update_bias(const int32_t* counts, int n_exp, float* bias, float gamma, int mode,
                                cudaStream_t st);
@@ -106,7 +110,5 @@ cudaError_t launch_unpermute_dx(int n_tok, int d, int top_k, const void* dx_perm
                                 const void* dx_shared, void* dx, cudaStream_t st);
 // dst[0] = 0, dst[1] = n (device offsets of a single dense group).
 cudaError_t launch_dense_offsets(int32_t* dst, int n, cudaStream_t st);
-// out[i] = sum_s part[s * n + i] for s = 0..ks-1 in order (fp32; n % 4 == 0, 16-byte aligned).
-cudaError_t launch_sum_slices(const float* part, int ks, int64_t n, float* out, cudaStream_t st);
 
 }  // namespace moe

@@ -56,13 +56,12 @@ def test_launch_counts():
     assert bench.launches_per_step(mix) == 4 + 13
     # MXFP8: the fused router, the quantising single-pass permute, GEMM1, GEMM2, combine
     assert not bench.fused_dispatch(mix.replace(precision="mxfp8"))
-    # E = 256: dense offsets, logits GEMM in 4 contraction slices, their sum, top-K, scan;
-    # + shared expert (3 forward, 6 backward) + route-bias update
-    assert bench.route_launches(ds) == 5
-    assert bench.launches_per_step(ds) == 5 + 1 + 3 + 13 + 3 + 6 + 1
-    # enough 128-token tiles to fill the GPU: no slices
-    big = ds.replace(n_tok=65536)
-    assert bench.route_launches(big) == 4
+    # E = 256: dense offsets, logits GEMM (in contraction slices), one kernel for their sum,
+    # top-K, histogram and scan; + shared expert (3 forward, 6 backward) + route-bias update
+    assert bench.route_launches(ds) == 3
+    assert bench.launches_per_step(ds) == 3 + 1 + 3 + 13 + 3 + 6 + 1
+    # enough 128-token tiles to fill the GPU: no slices, the same three launches
+    assert bench.route_launches(ds.replace(n_tok=65536)) == 3
 
 
 def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
