@@ -184,7 +184,8 @@ MOE_API moe_status_t moe_get_device_status(const void* ws, int32_t* status_host,
  *                            on 128-token tiles; with few tiles the
  *                            contraction runs in up to 4 slices whose fp32
  *                            partial products, kept in the workspace, are
- *                            added in slice order);
+ *                            added in slice order by one more kernel that
+ *                            also does the selection, histogram and scan);
  *   topk_idx[N,K] (out)    = the K experts with the largest
  *                            logits + bias (bias [E] fp32, NULL when the layer
  *                            has none), sorted by rank; equal keys: lower
