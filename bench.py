@@ -466,6 +466,26 @@ def run_ours(args, cfg, rank, world, local_rank):
     if bits:
         raise RuntimeError(f"device status {bits} at site {site}")
 
+    # --- MXFP8: the expert weights' E4M3 codes (rowwise for the forward,
+    # columnwise for the data gradients) are made once per weight update,
+    # outside the layer's forward + backward, so they are not in the step;
+    # their cost is timed here on its own (median of three updates)
+    weight_quant_ms = None
+    if cfg.precision == "mxfp8":
+        wq_ms = []
+        for _ in range(3):
+            q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            q0.record()
+            wq = api.quantize_weights_mxfp8(p)
+            wqt = api.quantize_weights_mxfp8_t(p)
+            q1.record()
+            torch.cuda.synchronize()
+            wq_ms.append(q0.elapsed_time(q1))
+            del wq, wqt
+        weight_quant_ms = sorted(wq_ms)[1]
+        torch.cuda.empty_cache()
+
     # --- inference forward (no saved activations), GEMM1 rows gathered from x
     # (moe_permute_maps + moe_grouped_ffn_gather) against the same layer with a
     # permuted copy of the tokens (moe_permute + moe_grouped_ffn)
@@ -499,7 +519,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     nonempty = int((b["counts"] > 0).sum().item())
     counts = b["counts"].float()
     res = {"cfg": cfg, "per_call": per_call, "kernels": kernels, "clocks": clk.summary(), "nonempty": nonempty,
-           "inference_fwd": inference,
+           "inference_fwd": inference, "weight_quant_ms": weight_quant_ms,
            "max_load_over_mean": float(counts.max()) / (cfg.rows / cfg.n_exp),
            "h2d": hx.numel() * 2 + hdy.numel() * 2, "d2h": hout[0].numel() * 2 + hdx[0].numel() * 2}
     for key, v in (("step", ms), ("fwd", ms_fwd), ("e2e", ms_e2e)):
@@ -660,7 +680,11 @@ def summarize(res, args, peaks) -> dict:
         # forward only, no saved activations: GEMM1 rows gathered from x by TMA
         # (no permuted copy of the tokens) against the same forward through x_perm
         "inference_fwd_tokens_per_s": res.get("inference_fwd"),
-    }
+    } | ({"mxfp8_weight_quantisation": {
+        "ms_per_update": res["weight_quant_ms"], "in_value": False,
+        "what": "rowwise and columnwise E4M3 codes + E8M0 scales of every expert weight, made once per weight "
+                "update (not per forward + backward); amortised over the steps between updates"}}
+        if res.get("weight_quant_ms") is not None else {})
 
 
 # Further configurations timed after the headline one (one GPU only): the
@@ -745,6 +769,8 @@ def main():
         "gpu_launches": launches_per_step(cfg) * args.steps,
         "clocks": head["clocks"],
     }
+    if "mxfp8_weight_quantisation" in head:
+        line["mxfp8_weight_quantisation"] = head["mxfp8_weight_quantisation"]
     if subs:
         line["sub_results"] = [summarize(r, args, peaks) for r in subs]
     if not args.no_cpu_baseline:

@@ -86,7 +86,8 @@ def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
                 "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
                 "nonempty": cfg.n_exp, "max_load_over_mean": 1.1, "inference_fwd": {"gather": 2.2e6, "x_perm": 2.1e6},
                 "h2d": 2, "d2h": 1, "step": (640000.0, 6.4 * s),
-                "fwd": (2e6, 2.0 * s), "e2e": (600000.0, 6.8 * s)}
+                "fwd": (2e6, 2.0 * s), "e2e": (600000.0, 6.8 * s),
+                "weight_quant_ms": 1.7 if cfg.precision == "mxfp8" else None}
 
     monkeypatch.setattr(bench, "run_ours", fake_run_ours)
     monkeypatch.setattr(bench, "measured_peaks", lambda: {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
@@ -117,6 +118,11 @@ def test_gpu_arm_json_line_from_fake_timings(monkeypatch, capsys):
             subs = d["sub_results"]
             assert len(subs) == len(bench.SUB_CONFIGS)
             mx = [x for x in subs if "mxfp8" in x["workload"]]
+            # the MXFP8 weights' quantisation is reported beside the step, not in it
+            assert mx and all(x["mxfp8_weight_quantisation"]["ms_per_update"] == 1.7 and
+                              x["mxfp8_weight_quantisation"]["in_value"] is False for x in mx)
+            assert "mxfp8_weight_quantisation" not in d
+            assert all("mxfp8_weight_quantisation" not in x for x in subs if "mxfp8" not in x["workload"])
             for x in mx:
                 for rk in x["roofline_by_kind"].values():
                     if rk["bound"] == "tensor" and "router" not in rk["kernel"]:
