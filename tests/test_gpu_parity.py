@@ -86,11 +86,16 @@ def test_route_from_logits_bitexact(name, mode):
 
 
 # extra router shapes: E = 24 and 32 (fused router with 3 and 4 column
-# tiles of 8 experts, token counts off the 16-token tile), a bias
+# tiles of 8 experts, token counts off the 16-token tile), a bias; E > 32
+# through the logits GEMM and the one-kernel tail: 79 token tiles fill the
+# GPU, so no contraction slices (the tail reads the logits themselves), and
+# 45 token tiles with six k-blocks, so three slices (E = 96: lanes past E)
 ROUTER_EXTRA = {
     "router_e24": MoEConfig("router_e24", 515, 128, 64, 24, 3),
     "router_e32": MoEConfig("router_e32", 1001, 192, 64, 32, 4, gate="sigmoid", use_bias=True, bias_beta=0.5,
                             n_cold=2),
+    "router_e64_noslice": MoEConfig("router_e64_noslice", 10000, 64, 64, 64, 6),
+    "router_e96_3slices": MoEConfig("router_e96_3slices", 5760, 384, 64, 96, 4, gate="sigmoid"),
 }
 
 
