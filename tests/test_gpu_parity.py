@@ -85,6 +85,25 @@ def test_route_from_logits_bitexact(name, mode):
     np.testing.assert_array_equal(off.cpu().numpy(), O.exclusive_offsets(counts))
 
 
+@pytest.mark.parametrize("e,k,mode", [(1024, 32, "uniform"), (1024, 32, "ties"), (1000, 7, "zipf")])
+def test_route_from_logits_widest(e, k, mode):
+    """The most experts (1024: 32 per lane) and the largest K the selection
+    takes (32: every lane holds a pick), and E off a multiple of 32."""
+    n = 333
+    cfg = MoEConfig("widest", n, 64, 64, e, k)
+    lg = skewed_logits(n, e, mode)
+    d, ws = _ws(cfg)
+    idx, w, cnt, off = _i32(n, k), _f32(n, k), _i32(e), _i32(e + 1)
+    api.moe_route_from_logits(d, lg.cuda(), None, idx, w, cnt, off, ws)
+    _status_ok(ws)
+    ridx, rw = O.route(lg.numpy(), None, k, cfg.gate)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=1e-6)
+    counts = O.histogram(ridx, e)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), counts)
+    np.testing.assert_array_equal(off.cpu().numpy(), O.exclusive_offsets(counts))
+
+
 # extra router shapes: E = 24 and 32 (fused router with 3 and 4 column
 # tiles of 8 experts, token counts off the 16-token tile), a bias; E > 32
 # through the logits GEMM and the one-kernel tail: 79 token tiles fill the
@@ -96,6 +115,8 @@ ROUTER_EXTRA = {
                             n_cold=2),
     "router_e64_noslice": MoEConfig("router_e64_noslice", 10000, 64, 64, 64, 6),
     "router_e96_3slices": MoEConfig("router_e96_3slices", 5760, 384, 64, 96, 4, gate="sigmoid"),
+    # the widest router: 1024 experts (four 256-column tiles of the logits GEMM), top-32
+    "router_e1024": MoEConfig("router_e1024", 700, 128, 64, 1024, 32),
 }
 
 
