@@ -42,9 +42,11 @@
 // Shared-memory operand layouts (both 1024-byte aligned per stage):
 //   K-major : rows of 64 bf16 (128 B), 8-row swizzle atoms of 1024 B;
 //             descriptor SBO = 1024, advance 32 B per K=16 step.
-//   MN-major: per 64-wide MN atom a region of 64 K-rows x 128 B;
-//             descriptor LBO = 8192 (next MN atom), SBO = 1024 (next 8 K-rows),
-//             advance 2048 B per K=16 step.
+//   MN-major: per 64-wide MN atom a region of kb K-rows x 128 B (kb = 64,
+//             or 128 for the weight gradients on CTA pairs: eight K=16 MMAs
+//             per stage barrier, 5-9% faster than four on one expert's dW);
+//             descriptor LBO = kb x 128 (next MN atom), SBO = 1024 (next 8
+//             K-rows), advance 2048 B per K=16 step.
 #include "grouped_gemm.cuh"
 #include "sm100_ptx.cuh"
 
@@ -60,6 +62,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int BKR = 128;   // k-block rows of the bf16 weight gradients on CTA pairs
 constexpr int kThreads = 320;        // producer, MMA, 8 epilogue warps
 constexpr int kThreadsQ = 448;       // + 4 scale-factor warps (MXFP8 operands)
 constexpr int kThreadsW8 = 576;      // + 8 converter warps (FP8 weights)
@@ -159,8 +162,12 @@ struct Cfg {
   static constexpr uint32_t kQTxBytes = BM * 128 + kQBRows * 128 + 4 * 144 + 4 * BN;    // ragged M
   static constexpr uint32_t kQTxBytesK = BM * 128 + BN * 128 + 4 * 128 + 4 * BN;   // ragged K
   // bf16: PAIR = this CTA holds half of the B tile (the pair shares a 256-row tile)
+  // k-block length: 128 rows for the bf16 ragged-K form on CTA pairs (eight
+  // K=16 MMAs per stage barrier instead of four), 64 elsewhere
+  static constexpr int kKb = (MAXG == 0 && PAIR && !QUANT && !W8) ? BKR : BK;
+  static constexpr int kABytesC = BM * kKb * 2;   // A bytes of a bf16 stage
   static constexpr int kStageBytes =
-      QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
+      QUANT ? (kQAtoms + 1536 + 1023) / 1024 * 1024 : (BM + (PAIR ? BN / 2 : BN)) * kKb * 2;
   // shared memory left for the stages: 227 KB less the alignment slack, the
   // staging buffers, the barriers (at most MAXS stages) and the group tables
   static constexpr bool kWideStaging = STG && MAXG == 0;
@@ -520,7 +527,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
             break;
           }
           uint8_t* sA = smem + s * C::kStageBytes;
-          uint8_t* sB = sA + kABytes;
+          uint8_t* sB = sA + (RAGGED_K ? C::kABytesC : kABytes);
           const int k0 = kb * BK;
           if (PAIR) {
             if (leader && lane == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, p.status, 100 + s)) { ok = false; break; }
           uint8_t* sA = smem + s * C::kStageBytes;
-          uint8_t* sB = sA + kABytes;
+          uint8_t* sB = sA + (RAGGED_K ? C::kABytesC : kABytes);
           if (W8) {
             // FP8 weights: A (bf16) straight into the stage; the B codes of the
             // k-block into a staging slot for the converters
@@ -612,16 +619,16 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
               tensormap_acquire(mB);
               map_g = t.g;
             }
-            const int r = gm ? kb * BK : t.row0 + kb * BK;   // rows of the group's map
+            const int r = gm ? kb * C::kKb : t.row0 + kb * C::kKb;   // rows of the group's map
             if (PAIR) {
               // both CTAs' loads complete on the leader's barrier, armed by the leader
               const int n0 = t.nt * BN + (rank & 1) * (BN / 2);
               if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
               const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
               tma_load_2d_pair(sA, mA, bar, t.m0, r);
-              tma_load_2d_pair(sA + 8192, mA, bar, t.m0 + 64, r);
+              tma_load_2d_pair(sA + C::kKb * 128, mA, bar, t.m0 + 64, r);
 #pragma unroll
-              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * 8192, mB, bar, n0 + 64 * a, r);
+              for (int a = 0; a < BN / 128; ++a) tma_load_2d_pair(sB + a * C::kKb * 128, mB, bar, n0 + 64 * a, r);
             } else {
               mbar_arrive_expect_tx(&full[s], C::kStageBytes);
               tma_load_2d(sA, mA, &full[s], t.m0, r);
@@ -786,19 +793,20 @@ __global__ void __launch_bounds__(QUANT ? kThreadsQ : (W8 ? kThreadsW8 : kThread
         if (!mbar_wait_bounded(&full[s], ph, s_abort, p.status, 300 + s)) { ok = false; break; }
         tc_fence_after();
         uint8_t* sA = smem + s * C::kStageBytes;
-        uint8_t* sB = sA + kABytes;
+        uint8_t* sB = sA + (RAGGED_K ? C::kABytesC : kABytes);
         // Ragged K: rows past the group's end arrive as zeros (the per-group
         // maps end at the group's last row); K=16 steps holding none of the
         // group's rows are skipped.
-        const int rv = t.k_rows - kb * BK;
-        const int nkk = (RAGGED_K && rv < BK) ? (rv + 15) / 16 : BK / 16;
+        constexpr int KB = RAGGED_K ? C::kKb : BK;
+        const int rv = t.k_rows - kb * KB;
+        const int nkk = (RAGGED_K && rv < KB) ? (rv + 15) / 16 : KB / 16;
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA);
           const uint32_t b_base = smem_u32(sB);
           for (int kk = 0; kk < nkk; ++kk) {
-            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, 8192, 1024)
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + kk * 2048, KB * 128, 1024)
                                      : smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_base + kk * 2048, KB * 128, 1024)
                                      : smem_desc_sw128(b_base + kk * 32, 16, 1024);
             if (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
             else tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
@@ -1787,7 +1795,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     }
   } else {
     if (a.m_size <= 0) return cudaSuccess;
-    if (!make_map(&kp.tmA[0], a.a[0], 64, 64, false) || !make_map(&kp.tmB[0], a.b[0], 64, 64, false))
+    // k-blocks of BKR rows on CTA pairs (the kernel form's k-block length)
+    const int kbr = pair ? BKR : BK;
+    kp.kblk = kbr;
+    if (!make_map(&kp.tmA[0], a.a[0], 64, kbr, false) || !make_map(&kp.tmB[0], a.b[0], 64, kbr, false))
       return cudaErrorInvalidValue;
     kp.tmA[1] = kp.tmA[0];
     kp.tmB[1] = kp.tmB[0];
